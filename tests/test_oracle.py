@@ -1,0 +1,303 @@
+"""Pins for the fp64 CPU oracle (no GPU).
+
+The pages print no numeric example, so the oracle is pinned to what the
+mathematics fixes: a hand-worked example (tests/golden/hand_worked.json),
+closed forms, invariants, an independent library routine (torch's fp64 CPU
+scaled_dot_product_attention and its autograd) and finite differences.  Each
+pin is chosen so that a plausible slip in the oracle -- a dropped scale, a
+flipped exponent sign, a transposed operand, a wrong GQA head mapping, an
+off-by-one causal mask, a missing normalisation -- fails at least one test.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from tiled_memory_efficient_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rnd(shape, seed, std=1.0):
+    g = np.random.default_rng(seed)
+    return g.standard_normal(shape) * std
+
+
+def sdpa_f64(q, k, v, causal, scale):
+    """torch's own CPU fp64 SDPA; GQA by repeat_interleave of K/V heads."""
+    q, k, v = (torch.as_tensor(np.asarray(x), dtype=torch.float64) for x in (q, k, v))
+    G = q.shape[1] // k.shape[1]
+    k = k.repeat_interleave(G, dim=1)
+    v = v.repeat_interleave(G, dim=1)
+    return F.scaled_dot_product_attention(q, k, v, is_causal=causal, scale=scale).numpy()
+
+
+def lse_f64(q, k, causal, scale):
+    """torch.logsumexp over the scaled scores (library reduction)."""
+    q, k = (torch.as_tensor(np.asarray(x), dtype=torch.float64) for x in (q, k))
+    G = q.shape[1] // k.shape[1]
+    k = k.repeat_interleave(G, dim=1)
+    s = scale * q @ k.transpose(-1, -2)
+    if causal:
+        nq, nk = s.shape[-2:]
+        mask = torch.ones(nq, nk, dtype=torch.bool).tril()
+        s = s.masked_fill(~mask, -math.inf)
+    return torch.logsumexp(s, dim=-1).numpy()
+
+
+# --------------------------------------------------------------------------- golden
+
+def test_hand_worked_example_forward():
+    gd = json.load(open(os.path.join(GOLDEN, "hand_worked.json")))
+    q = np.array(gd["q"])[None, None]
+    k = np.array(gd["k"])[None, None]
+    v = np.array(gd["v"])[None, None]
+    for causal, key in ((False, "noncausal"), (True, "causal")):
+        o, lse = oracle.attention_fwd(q, k, v, causal=causal, scale=gd["scale"])
+        np.testing.assert_allclose(o[0, 0], np.array(gd[key]["o"]), rtol=0, atol=1e-14)
+        np.testing.assert_allclose(lse[0, 0], np.array(gd[key]["lse"]), rtol=0, atol=1e-14)
+
+
+def test_hand_worked_example_backward():
+    gd = json.load(open(os.path.join(GOLDEN, "hand_worked.json")))
+    q = np.array(gd["q"])[None, None]
+    k = np.array(gd["k"])[None, None]
+    v = np.array(gd["v"])[None, None]
+    bw = gd["backward_noncausal"]
+    do = np.array(bw["dout"])[None, None]
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, causal=False, scale=gd["scale"])
+    np.testing.assert_allclose(dq[0, 0], np.array(bw["dq"]), atol=1e-14)
+    np.testing.assert_allclose(dk[0, 0], np.array(bw["dk"]), atol=1e-14)
+    np.testing.assert_allclose(dv[0, 0], np.array(bw["dv"]), atol=1e-14)
+
+
+# --------------------------------------------------------------------------- library routine
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,D,causal", [
+    (1, 2, 2, 37, 37, 16, False),
+    (2, 3, 3, 40, 29, 8, False),
+    (1, 4, 2, 33, 33, 16, True),
+    (1, 6, 2, 20, 31, 8, True),     # Nq != Nk, top-left causal
+    (1, 7, 1, 45, 45, 32, False),   # G = 7 as in the GQA prefill shape
+])
+def test_matches_torch_sdpa_f64(B, Hq, Hkv, Nq, Nk, D, causal):
+    q = rnd((B, Hq, Nq, D), 1)
+    k = rnd((B, Hkv, Nk, D), 2)
+    v = rnd((B, Hkv, Nk, D), 3)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = oracle.attention_fwd(q, k, v, causal=causal)
+    np.testing.assert_allclose(o, sdpa_f64(q, k, v, causal, scale), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_f64(q, k, causal, scale), rtol=0, atol=1e-12)
+
+
+def test_explicit_scale_is_used():
+    q, k, v = rnd((1, 1, 9, 4), 4), rnd((1, 1, 9, 4), 5), rnd((1, 1, 9, 4), 6)
+    o, lse = oracle.attention_fwd(q, k, v, scale=0.37)
+    np.testing.assert_allclose(o, sdpa_f64(q, k, v, False, 0.37), atol=1e-12)
+    np.testing.assert_allclose(lse, lse_f64(q, k, False, 0.37), atol=1e-12)
+
+
+@pytest.mark.parametrize("Hq,Hkv,causal", [(2, 2, False), (4, 2, True), (3, 1, False)])
+def test_backward_matches_torch_autograd(Hq, Hkv, causal):
+    B, N, D = 2, 19, 8
+    q, k, v, do = rnd((B, Hq, N, D), 7), rnd((B, Hkv, N, D), 8), rnd((B, Hkv, N, D), 9), \
+        rnd((B, Hq, N, D), 10)
+    qt, kt, vt = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    G = Hq // Hkv
+    out = F.scaled_dot_product_attention(qt, kt.repeat_interleave(G, 1),
+                                         vt.repeat_interleave(G, 1), is_causal=causal)
+    out.backward(torch.tensor(do))
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, causal=causal)
+    np.testing.assert_allclose(dq, qt.grad.numpy(), atol=1e-11)
+    np.testing.assert_allclose(dk, kt.grad.numpy(), atol=1e-11)
+    np.testing.assert_allclose(dv, vt.grad.numpy(), atol=1e-11)
+
+
+# --------------------------------------------------------------------------- brute force
+
+def test_rows_subset_equals_full():
+    B, Hq, Hkv, N, D = 2, 4, 2, 23, 8
+    q, k, v = rnd((B, Hq, N, D), 11), rnd((B, Hkv, N, D), 12), rnd((B, Hkv, N, D), 13)
+    o, lse = oracle.attention_fwd(q, k, v, causal=True)
+    rows = np.array([0, 5, 22, 23, 60, B * Hq * N - 1])
+    o_r, lse_r = oracle.attention_fwd(q, k, v, causal=True, rows=rows)
+    np.testing.assert_array_equal(o_r, o.reshape(-1, D)[rows])
+    np.testing.assert_array_equal(lse_r, lse.reshape(-1)[rows])
+
+
+def test_finite_differences_backward():
+    B, Hq, Hkv, N, D = 1, 2, 1, 6, 4
+    q, k, v, do = rnd((B, Hq, N, D), 14), rnd((B, Hkv, N, D), 15), rnd((B, Hkv, N, D), 16), \
+        rnd((B, Hq, N, D), 17)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, causal=True)
+
+    def loss(q_, k_, v_):
+        o, _ = oracle.attention_fwd(q_, k_, v_, causal=True)
+        return float((o * do).sum())
+
+    eps = 1e-6
+    for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args = {"q": q, "k": k, "v": v}
+            args[name] = xp
+            fp = loss(args["q"], args["k"], args["v"])
+            args[name] = xm
+            fm = loss(args["q"], args["k"], args["v"])
+            num[idx] = (fp - fm) / (2 * eps)
+        np.testing.assert_allclose(grad, num, rtol=1e-6, atol=1e-8, err_msg=name)
+
+
+# --------------------------------------------------------------------------- closed forms
+
+def test_single_key_returns_its_value_row():
+    q, k, v = rnd((1, 3, 5, 8), 20), rnd((1, 3, 1, 8), 21), rnd((1, 3, 1, 8), 22)
+    o, lse = oracle.attention_fwd(q, k, v)
+    np.testing.assert_allclose(o, np.broadcast_to(v, o.shape), atol=1e-15)
+    expect = (q @ k.transpose(0, 1, 3, 2))[..., 0] / math.sqrt(8)
+    np.testing.assert_allclose(lse, expect, atol=1e-13)
+
+
+def test_identical_keys_give_mean_of_values():
+    N, D = 17, 8
+    q = rnd((1, 2, N, D), 23)
+    k = np.broadcast_to(rnd((1, 2, 1, D), 24), (1, 2, N, D)).copy()
+    v = rnd((1, 2, N, D), 25)
+    o, lse = oracle.attention_fwd(q, k, v)
+    np.testing.assert_allclose(o, np.broadcast_to(v.mean(axis=2, keepdims=True), o.shape),
+                               atol=1e-13)
+    expect = (q @ k[:, :, :1].transpose(0, 1, 3, 2))[..., 0] / math.sqrt(D) + math.log(N)
+    np.testing.assert_allclose(lse, expect, atol=1e-13)
+
+
+def test_zero_query_causal_gives_prefix_means():
+    N, D = 21, 4
+    q = np.zeros((1, 1, N, D))
+    k, v = rnd((1, 1, N, D), 26), rnd((1, 1, N, D), 27)
+    o, lse = oracle.attention_fwd(q, k, v, causal=True)
+    prefix = np.cumsum(v[0, 0], axis=0) / np.arange(1, N + 1)[:, None]
+    np.testing.assert_allclose(o[0, 0], prefix, atol=1e-14)
+    np.testing.assert_allclose(lse[0, 0], np.log(np.arange(1, N + 1)), atol=1e-14)
+    o_nc, lse_nc = oracle.attention_fwd(q, k, v, causal=False)
+    np.testing.assert_allclose(o_nc[0, 0], np.broadcast_to(v[0, 0].mean(0), (N, D)), atol=1e-14)
+    np.testing.assert_allclose(lse_nc, math.log(N), atol=1e-14)
+
+
+def test_causal_row_zero_is_first_value():
+    q, k, v = rnd((2, 2, 9, 8), 28), rnd((2, 2, 9, 8), 29), rnd((2, 2, 9, 8), 30)
+    o, _ = oracle.attention_fwd(q, k, v, causal=True)
+    np.testing.assert_allclose(o[:, :, 0], v[:, :, 0], atol=1e-15)
+
+
+def test_rows_sum_to_one_via_constant_values():
+    q, k = rnd((1, 2, 11, 8), 31, std=3.0), rnd((1, 2, 13, 8), 32, std=3.0)
+    v = np.ones((1, 2, 13, 8))
+    for causal in (False, True):
+        o, _ = oracle.attention_fwd(q, k, v, causal=causal)
+        np.testing.assert_allclose(o, 1.0, atol=1e-14)
+
+
+def test_key_shift_leaves_output_and_moves_lse():
+    D = 8
+    q, k, v = rnd((1, 1, 10, D), 33), rnd((1, 1, 12, D), 34), rnd((1, 1, 12, D), 35)
+    u = rnd((D,), 36)
+    o, lse = oracle.attention_fwd(q, k, v)
+    o2, lse2 = oracle.attention_fwd(q, k + u, v)
+    np.testing.assert_allclose(o2, o, atol=1e-13)
+    np.testing.assert_allclose(lse2, lse + (q @ u) / math.sqrt(D), atol=1e-12)
+
+
+# --------------------------------------------------------------------------- invariants
+
+def test_permuting_keys_and_values_together():
+    q, k, v = rnd((1, 2, 14, 8), 37), rnd((1, 2, 19, 8), 38), rnd((1, 2, 19, 8), 39)
+    perm = np.random.default_rng(40).permutation(19)
+    o, lse = oracle.attention_fwd(q, k, v)
+    o2, lse2 = oracle.attention_fwd(q, k[:, :, perm], v[:, :, perm])
+    np.testing.assert_allclose(o2, o, atol=1e-13)
+    np.testing.assert_allclose(lse2, lse, atol=1e-13)
+
+
+def test_gqa_equals_mha_on_repeated_heads():
+    q, k, v = rnd((1, 6, 15, 8), 41), rnd((1, 2, 15, 8), 42), rnd((1, 2, 15, 8), 43)
+    for causal in (False, True):
+        o, lse = oracle.attention_fwd(q, k, v, causal=causal)
+        o2, lse2 = oracle.attention_fwd(q, np.repeat(k, 3, axis=1), np.repeat(v, 3, axis=1),
+                                        causal=causal)
+        np.testing.assert_array_equal(o, o2)
+        np.testing.assert_array_equal(lse, lse2)
+    # contiguous groups: query heads 0..2 use KV head 0, so changing KV head 1
+    # must leave them alone and change heads 3..5
+    k2 = k.copy()
+    k2[:, 1] = rnd((1, 15, 8), 99)
+    o, _ = oracle.attention_fwd(q, k, v)
+    o3, _ = oracle.attention_fwd(q, k2, v)
+    np.testing.assert_array_equal(o3[:, :3], o[:, :3])
+    assert np.abs(o3[:, 3:] - o[:, 3:]).max() > 1e-3
+
+
+def test_output_is_linear_in_values():
+    q, k = rnd((1, 1, 8, 4), 44), rnd((1, 1, 8, 4), 45)
+    v1, v2 = rnd((1, 1, 8, 4), 46), rnd((1, 1, 8, 4), 47)
+    o1, _ = oracle.attention_fwd(q, k, v1)
+    o2, _ = oracle.attention_fwd(q, k, v2)
+    o3, _ = oracle.attention_fwd(q, k, 2.0 * v1 - 3.0 * v2)
+    np.testing.assert_allclose(o3, 2.0 * o1 - 3.0 * o2, atol=1e-13)
+
+
+def test_backward_invariants():
+    B, Hq, Hkv, N, D = 1, 4, 2, 13, 8
+    q, k = rnd((B, Hq, N, D), 48), rnd((B, Hkv, N, D), 49)
+    do = rnd((B, Hq, N, D), 50)
+    # identical value rows: output is constant in q and k, so dq = dk = 0
+    v_same = np.broadcast_to(rnd((B, Hkv, 1, D), 51), (B, Hkv, N, D)).copy()
+    dq, dk, dv = oracle.attention_bwd(q, k, v_same, do, causal=True)
+    np.testing.assert_allclose(dq, 0.0, atol=1e-13)
+    np.testing.assert_allclose(dk, 0.0, atol=1e-13)
+    # softmax rows sum to one: sum_j dv_j = sum over the group's rows of dout;
+    # shifting every key by u leaves O alone: sum_j dk_j = 0
+    v = rnd((B, Hkv, N, D), 52)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, causal=False)
+    group_do = do.reshape(B, Hkv, Hq // Hkv, N, D).sum(axis=(2, 3))
+    np.testing.assert_allclose(dv.sum(axis=2), group_do, atol=1e-12)
+    np.testing.assert_allclose(dk.sum(axis=2), 0.0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------- inputs and host logic
+
+def test_inputs_are_seeded_and_rounded():
+    w = inputs.WORKLOADS["tiny"]
+    a = inputs.make_inputs(w, 256)
+    b = inputs.make_inputs(w, 256)
+    for key in ("q", "k", "v"):
+        assert a[key].dtype == torch.float16
+        assert torch.equal(a[key], b[key])
+    assert a["q"].shape == (1, 2, 256, 64)
+
+
+def test_outlier_keys_recipe():
+    w = inputs.Workload("t", 9, 1, 2, 2, 16, torch.bfloat16, False, (300,), outlier_keys=True)
+    x = inputs.make_inputs(w, 300)
+    norms = x["k"].float().norm(dim=-1)
+    big = (norms > 3 * norms.median()).sum(dim=-1)
+    assert big.tolist() == [[3, 3]]   # floor(0.01 * 300) rows per KV head
+
+
+def test_sample_rows_cover_edges():
+    rows = inputs.sample_rows(1, 2, 1000, per_head=4, seed=3)
+    r = set(rows.tolist())
+    for base in (0, 1000):
+        assert {base, base + 999, base + 127, base + 128, base + 255, base + 256} <= r
+
+
+def test_flops_formula():
+    w = inputs.WORKLOADS["gqa_prefill"]
+    assert w.flops_fwd(1024) == 4 * 14 * 1024 * 1024 * 64 / 2
