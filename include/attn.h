@@ -1,0 +1,110 @@
+/*
+ * attn.h -- C ABI of the tiled, memory-efficient attention library (sm_103a).
+ *
+ * The operation is scaled-dot-product attention computed the way the
+ * noflash-attention forum post describes it (ai-navigate-news, section "The
+ * DIY approach", list "What worked"): the N x N score matrix is never formed;
+ * Q is tiled along queries and K/V along keys with an online softmax (running
+ * max and sum); the query heads of a GQA group are flattened onto their shared
+ * KV head instead of broadcasting K/V; negligible softmax terms are flushed to
+ * zero; a causal mask is optional.  Its "Other areas where this could be
+ * useful" section adds the autograd tier used for training (attn_bwd).  The
+ * call mirrors the SDPA call the post patches, scaled_dot_product_attention
+ * over [batch, heads, seq_len, dim] tensors (the ai-manual.ru page, section
+ * "2 PyTorch SDPA", and its chunked snippet's default scale 1/sqrt(dim)).
+ *
+ * Conventions for every entry point
+ *   - Pointers named q, k, v, out, dout, dq, dk, dv, lse, workspace are DEVICE
+ *     pointers owned by the caller; the library never allocates, frees or
+ *     retains them past the call.  Layouts are dense row-major:
+ *         q, out, dout, dq : [B, Hq, Nq, D]      (dtype)
+ *         k, v, dk, dv     : [B, Hkv, Nk, D]     (dtype)
+ *         lse              : [B, Hq, Nq]         (fp32, natural log)
+ *     dtype is ATTN_F16 or ATTN_BF16; accumulation is fp32.
+ *   - Query head h uses KV head h / (Hq / Hkv) (contiguous groups).
+ *   - causal != 0 applies the top-left mask: query position i sees keys j <= i.
+ *   - scale multiplies q.k; it must be finite and > 0 (1/sqrt(D) is the usual).
+ *   - Work is enqueued on `stream` (a cudaStream_t; 0 = legacy default) and the
+ *     call returns without synchronising.  The return value reports argument
+ *     validation and launch errors only.  A device-side wait that gives up
+ *     (after about 2 s) sets a status word that attn_sync_status() reports.
+ *   - Requirements: D in {64, 128}; every pointer 16-byte aligned (lse and
+ *     workspace: 16 bytes too); Hq % Hkv == 0; all sizes > 0; the current
+ *     device is an sm_103 GPU.  Violations return an error without launching.
+ */
+#ifndef TME_ATTN_H
+#define TME_ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { ATTN_F16 = 0, ATTN_BF16 = 1 } attn_dtype_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID = 1,     /* null pointer, non-positive size, Hq % Hkv, bad scale/dtype */
+    ATTN_ERR_UNSUPPORTED = 2, /* D not in {64,128}, sizes beyond the kernel's index range, not sm_103 */
+    ATTN_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
+    ATTN_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
+    ATTN_ERR_TIMEOUT = 5,     /* a device wait gave up (reported by attn_sync_status) */
+    ATTN_ERR_WORKSPACE = 6    /* workspace too small */
+} attn_status_t;
+
+/*
+ * Forward: out = softmax(scale * q k^T [masked]) v per query row, and
+ * lse = log(sum_j exp(scale * q.k_j)) over the allowed keys.
+ * (Forum post, "The DIY approach": tiled attention with online softmax.)
+ * Nq and Nk need not be equal nor multiples of 128.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+             int Hkv, int Nq, int Nk, int D, float scale, int causal, int dtype, void* stream);
+
+/*
+ * Bytes of device workspace attn_bwd needs for these sizes (fp32 per-row
+ * statistics).  Returns 0 for invalid sizes.
+ */
+size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int D, int dtype);
+
+/*
+ * Backward of attn_fwd (forum post, "Other areas where this could be useful":
+ * the autograd tier for training).  Inputs: q, k, v, the forward's out and
+ * lse, and the upstream gradient dout.  Outputs dq [B,Hq,Nq,D], and dk, dv
+ * [B,Hkv,Nk,D] summed over the query heads of each group (overwritten, not
+ * accumulated).  workspace: caller-owned device memory of at least
+ * attn_bwd_workspace_size() bytes; its contents on entry do not matter.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv, void* workspace,
+             size_t workspace_bytes, int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale,
+             int causal, int dtype, void* stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device status word of the
+ * current device: ATTN_ERR_TIMEOUT if any kernel's bounded wait gave up since
+ * the last call, ATTN_ERR_CUDA if the synchronisation failed, else ATTN_OK.
+ */
+int attn_sync_status(void* stream);
+
+/*
+ * Self-test of the bounded-wait path: enqueues one tiny kernel that waits on
+ * an mbarrier nothing will ever arrive on, for at most `wait_ns` nanoseconds
+ * (clamped to [1000, 10^8]), then records a timeout in the status word.  A
+ * following attn_sync_status() must return ATTN_ERR_TIMEOUT.  It touches no
+ * caller memory.
+ */
+int attn_selftest_timeout(unsigned long long wait_ns, void* stream);
+
+/* Static, human-readable text for a status code. */
+const char* attn_strerror(int status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TME_ATTN_H */

@@ -1,0 +1,76 @@
+"""C-ABI checks that need no GPU: the library builds, loads, exports every
+symbol include/attn.h declares, and rejects bad arguments before touching the
+device."""
+import ctypes
+import os
+
+import pytest
+
+from tiled_memory_efficient_gb300 import _lib
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build_library()
+    return _lib.load()
+
+
+def test_header_declares_the_boundary():
+    names = _lib.declared_functions()
+    for required in ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_sync_status",
+                     "attn_strerror", "attn_selftest_timeout", "attn_version"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _lib.declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _lib._SIGNATURES, f"binding lacks a signature for {name}"
+
+
+def test_strerror_and_version(lib):
+    assert lib.attn_strerror(0) == b"ok"
+    assert b"aligned" in lib.attn_strerror(3)
+    assert lib.attn_strerror(99) == b"unknown status"
+    assert lib.attn_version() >= 100
+
+
+P = 256  # a fake, 16-byte-aligned "device" address: validation fails before any use
+
+
+@pytest.mark.parametrize("args,code", [
+    # null pointer
+    ((0, P, P, P, P, 1, 2, 2, 128, 128, 64, 0.125, 0, 0), 1),
+    # non-positive sizes
+    ((P, P, P, P, P, 0, 2, 2, 128, 128, 64, 0.125, 0, 0), 1),
+    ((P, P, P, P, P, 1, 2, 2, 128, 0, 64, 0.125, 0, 0), 1),
+    # Hq not a multiple of Hkv
+    ((P, P, P, P, P, 1, 3, 2, 128, 128, 64, 0.125, 0, 0), 1),
+    # bad scale, bad dtype
+    ((P, P, P, P, P, 1, 2, 2, 128, 128, 64, 0.0, 0, 0), 1),
+    ((P, P, P, P, P, 1, 2, 2, 128, 128, 64, float("nan"), 0, 0), 1),
+    ((P, P, P, P, P, 1, 2, 2, 128, 128, 64, 0.125, 0, 7), 1),
+    # unsupported head dim
+    ((P, P, P, P, P, 1, 2, 2, 128, 128, 96, 0.125, 0, 0), 2),
+    # misaligned pointer
+    ((P + 2, P, P, P, P, 1, 2, 2, 128, 128, 64, 0.125, 0, 0), 3),
+    ((P, P, P, P, P + 4, 1, 2, 2, 128, 128, 64, 0.125, 0, 1), 3),
+])
+def test_fwd_rejects_without_launch(lib, args, code):
+    assert lib.attn_fwd(*args, None) == code
+
+
+def test_bwd_validation_and_workspace(lib):
+    ws = lib.attn_bwd_workspace_size(2, 16, 16, 8192, 8192, 128, 1)
+    assert ws >= 2 * 16 * 8192 * 2 * 4 and ws % 256 == 0
+    assert lib.attn_bwd_workspace_size(1, 3, 2, 10, 10, 64, 0) == 0
+    base = [P] * 9
+    # workspace too small
+    assert lib.attn_bwd(*base, P, 16, 2, 16, 16, 8192, 8192, 128, 0.08, 1, 1, None) == 6
+    # null workspace
+    assert lib.attn_bwd(*base, 0, ws, 2, 16, 16, 8192, 8192, 128, 0.08, 1, 1, None) == 1
+    # misaligned dout
+    bad = [P] * 9
+    bad[4] = P + 8
+    assert lib.attn_bwd(*bad, P, ws, 2, 16, 16, 8192, 8192, 128, 0.08, 1, 1, None) == 3

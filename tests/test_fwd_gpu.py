@@ -1,0 +1,143 @@
+"""Forward parity on the GPU: the CUDA path (through the C ABI) against the
+fp64 oracle on the same seeded, rounded inputs.
+
+Small shapes are checked on every row; the full-size workloads on a seeded
+sample of rows (always rows 0, N-1 and the 128-row tile edges of each head),
+since a full fp64 check would cost tens of TFLOP on the CPU.
+"""
+import numpy as np
+import pytest
+import torch
+
+from tests import helpers
+from tiled_memory_efficient_gb300 import _lib, inputs
+
+pytestmark = pytest.mark.gpu
+
+F16, BF16 = torch.float16, torch.bfloat16
+
+
+def run_fwd(x, causal, scale=None):
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    out, lse = _lib.attn_fwd(q, k, v, causal=causal, scale=scale)
+    assert _lib.sync_status() == _lib.ATTN_OK
+    return out, lse
+
+
+def check_full(x, causal, scale=None, what=""):
+    out, lse = run_fwd(x, causal, scale)
+    o_ref, lse_ref = helpers.oracle_rows(x["q"], x["k"], x["v"],
+                                         np.arange(x["q"].shape[0] * x["q"].shape[1] *
+                                                   x["q"].shape[2]), causal, scale)
+    o_gpu, lse_gpu = out.reshape(-1, out.shape[-1]).double().cpu().numpy(), \
+        lse.reshape(-1).double().cpu().numpy()
+    return helpers.assert_fwd_close(o_gpu, lse_gpu, o_ref, lse_ref, x["q"].dtype, what)
+
+
+def test_tiny_workload_every_row(cuda_lib):
+    w = inputs.WORKLOADS["tiny"]
+    x = inputs.make_inputs(w, 256)
+    eo, el = check_full(x, w.causal, what="tiny")
+    print(f"tiny: max|dO|={eo:.2e} max|dLSE|={el:.2e}")
+
+
+SMALL = [
+    # B, Hq, Hkv, Nq, Nk, D, dtype, causal
+    (1, 2, 2, 128, 128, 64, F16, False),
+    (1, 2, 2, 300, 300, 64, F16, True),       # ragged tail, causal
+    (2, 3, 3, 1, 1, 64, F16, False),          # single query and key
+    (1, 3, 3, 1, 517, 128, BF16, False),      # one query row, many keys
+    (1, 4, 4, 200, 333, 128, BF16, False),    # Nq != Nk, both ragged
+    (1, 14, 2, 250, 250, 64, F16, True),      # GQA G=7, tiles cross head boundaries
+    (1, 7, 1, 37, 37, 128, BF16, True),       # tiny heads flattened into one tile
+    (2, 4, 2, 1024, 1024, 128, BF16, True),   # several key tiles, causal skipping
+    (1, 2, 2, 129, 1000, 64, F16, True),      # Nq < Nk, top-left causal
+    (1, 2, 2, 1000, 129, 64, F16, True),      # Nq > Nk: late rows see every key
+    (1, 4, 1, 512, 2048, 128, F16, False),    # GQA G=4, D=128 fp16
+    (1, 2, 2, 640, 640, 64, BF16, False),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,D,dtype,causal", SMALL)
+def test_small_shapes_every_row(cuda_lib, B, Hq, Hkv, Nq, Nk, D, dtype, causal):
+    x = inputs.make_custom(B, Hq, Hkv, Nq, Nk, D, dtype, seed=Nq * 7 + Nk + D)
+    check_full(x, causal, what=f"{(B, Hq, Hkv, Nq, Nk, D, dtype, causal)}")
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+def test_large_scores_stress_ftz_and_rescale(cuda_lib, dtype):
+    # q, k with std 4: scaled scores of std ~16, so rows are nearly one-hot,
+    # the running max moves often and many terms fall under the flush threshold.
+    x = inputs.make_custom(1, 2, 2, 384, 700, 64, dtype, seed=5, std=4.0)
+    check_full(x, False, what="std4")
+    check_full(x, True, what="std4 causal")
+
+
+def test_explicit_scale(cuda_lib):
+    x = inputs.make_custom(1, 2, 2, 256, 256, 128, F16, seed=9)
+    check_full(x, False, scale=0.3, what="scale=0.3")
+
+
+SAMPLED = [("sweep", n) for n in inputs.WORKLOADS["sweep"].seq_lens] + \
+          [("gqa_prefill", n) for n in inputs.WORKLOADS["gqa_prefill"].seq_lens] + \
+          [("video_dit", n) for n in inputs.WORKLOADS["video_dit"].seq_lens] + \
+          [("training", 8192)]
+
+
+@pytest.mark.parametrize("name,n", SAMPLED)
+def test_workloads_sampled_rows(cuda_lib, name, n):
+    w = inputs.WORKLOADS[name]
+    x = inputs.make_inputs(w, n)
+    out, lse = run_fwd(x, w.causal)
+    rows = inputs.sample_rows(w.B, w.Hq, n, per_head=6, seed=n)
+    o_gpu, lse_gpu = helpers.gpu_rows(out, lse, rows)
+    o_ref, lse_ref = helpers.oracle_rows(x["q"], x["k"], x["v"], rows, w.causal)
+    eo, el = helpers.assert_fwd_close(o_gpu, lse_gpu, o_ref, lse_ref, w.dtype, f"{name} N={n}")
+    print(f"{name} N={n}: rows={len(rows)} max|dO|={eo:.2e} max|dLSE|={el:.2e}")
+
+
+def test_output_canaries_untouched(cuda_lib):
+    B, Hq, Hkv, N, D = 1, 3, 3, 200, 64
+    x = inputs.make_custom(B, Hq, Hkv, N, N, D, F16, seed=11)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    pad = 4096
+    o_buf = torch.full((B * Hq * N * D + 2 * pad,), 7.0, device="cuda", dtype=F16)
+    l_buf = torch.full((B * Hq * N + 2 * pad,), 7.0, device="cuda", dtype=torch.float32)
+    out = o_buf[pad:pad + B * Hq * N * D].view(B, Hq, N, D)
+    lse = l_buf[pad:pad + B * Hq * N].view(B, Hq, N)
+    _lib.attn_fwd(q, k, v, causal=True, out=out, lse=lse)
+    assert _lib.sync_status() == _lib.ATTN_OK
+    assert torch.all(o_buf[:pad] == 7.0) and torch.all(o_buf[-pad:] == 7.0)
+    assert torch.all(l_buf[:pad] == 7.0) and torch.all(l_buf[-pad:] == 7.0)
+    assert torch.all(torch.isfinite(out))
+
+
+def test_runs_on_side_stream(cuda_lib):
+    x = inputs.make_custom(1, 2, 2, 256, 256, 64, F16, seed=12)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    ref_out, ref_lse = _lib.attn_fwd(q, k, v)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out, lse = _lib.attn_fwd(q, k, v)
+    s.synchronize()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
+
+
+def test_deterministic(cuda_lib):
+    x = inputs.make_custom(1, 4, 2, 700, 700, 128, BF16, seed=13)
+    o1, l1 = run_fwd(x, True)
+    o2, l2 = run_fwd(x, True)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_bounded_wait_reports_timeout(cuda_lib):
+    lib = cuda_lib
+    stream = torch.cuda.current_stream().cuda_stream
+    assert lib.attn_sync_status(stream) == _lib.ATTN_OK
+    assert lib.attn_selftest_timeout(1_000_000, stream) == _lib.ATTN_OK   # 1 ms
+    assert lib.attn_sync_status(stream) == _lib.ATTN_ERR_TIMEOUT
+    assert lib.attn_sync_status(stream) == _lib.ATTN_OK                  # cleared
+    # the context is still usable afterwards
+    x = inputs.make_custom(1, 2, 2, 128, 128, 64, F16, seed=14)
+    check_full(x, False, what="after timeout")

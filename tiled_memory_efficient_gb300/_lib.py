@@ -1,0 +1,165 @@
+"""ctypes binding of the C ABI in include/attn.h (argument marshalling only).
+
+Every step of the computation runs in libattn.so's CUDA kernels; torch is used
+only to own device memory and to name the current stream.  There is no CPU
+fallback: if the library is missing or the device is not an sm_103 GPU, the
+calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "_build", "libattn.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "attn.h")
+
+ATTN_OK = 0
+ATTN_ERR_INVALID = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_ALIGN = 3
+ATTN_ERR_CUDA = 4
+ATTN_ERR_TIMEOUT = 5
+ATTN_ERR_WORKSPACE = 6
+ATTN_F16 = 0
+ATTN_BF16 = 1
+
+_lock = threading.Lock()
+_lib = None
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_SIGNATURES = {
+    "attn_fwd": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i, _vp],
+                 _i),
+    "attn_bwd_workspace_size": ([_i, _i, _i, _i, _i, _i, _i], ctypes.c_size_t),
+    "attn_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
+                  _i, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i, _vp], _i),
+    "attn_sync_status": ([_vp], _i),
+    "attn_selftest_timeout": ([ctypes.c_ulonglong, _vp], _i),
+    "attn_strerror": ([_i], ctypes.c_char_p),
+    "attn_version": ([], _i),
+}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn} failed: {code} ({strerror(code)})")
+
+
+def declared_functions() -> list:
+    """Names of the functions include/attn.h declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
+
+
+def load(path: str | None = None):
+    """dlopen libattn.so (built by __graft_entry__.build()) and set signatures."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(f"{p} is missing: run __graft_entry__.build() first")
+            lib = ctypes.CDLL(p)
+            for name, (args, res) in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = lib
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return load().attn_strerror(code).decode()
+
+
+def _stream_handle(device) -> int:
+    import torch
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return ATTN_F16
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: use float16 or bfloat16")
+
+
+def _check(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous [B, H, N, D]")
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be 4-D [B, H, N, D]")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    if k.shape != v.shape or k.shape[0] != q.shape[0] or k.shape[3] != q.shape[3]:
+        raise ValueError(f"shapes q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+
+
+def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None):
+    """O, LSE = attention(q, k, v).  q [B,Hq,Nq,D]; k, v [B,Hkv,Nk,D] (CUDA).
+
+    Returns (out [B,Hq,Nq,D] in q's dtype, lse [B,Hq,Nq] fp32 natural log).
+    Enqueued on torch's current stream; no synchronisation.
+    """
+    import torch
+    _check(q, k, v)
+    B, Hq, Nq, D = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), device=q.device, dtype=torch.float32)
+    rc = load().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                         lse.data_ptr(), B, Hq, Hkv, Nq, Nk, D, float(scale), int(bool(causal)),
+                         _dtype_code(q), _stream_handle(q.device))
+    if rc != ATTN_OK:
+        raise AttnError("attn_fwd", rc)
+    return out, lse
+
+
+def attn_bwd(q, k, v, out, dout, lse, causal: bool = False, scale: float | None = None,
+             dq=None, dk=None, dv=None, workspace=None):
+    """dq, dk, dv of attn_fwd (dk, dv summed over each GQA group)."""
+    import torch
+    _check(q, k, v)
+    B, Hq, Nq, D = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dt = _dtype_code(q)
+    lib = load()
+    ws_bytes = lib.attn_bwd_workspace_size(B, Hq, Hkv, Nq, Nk, D, dt)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), device=q.device, dtype=torch.uint8)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    rc = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), dout.data_ptr(),
+                      lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                      workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                      B, Hq, Hkv, Nq, Nk, D, float(scale), int(bool(causal)), dt,
+                      _stream_handle(q.device))
+    if rc != ATTN_OK:
+        raise AttnError("attn_bwd", rc)
+    return dq, dk, dv
+
+
+def sync_status(device=None) -> int:
+    """Synchronise the current stream and return (and clear) the device status."""
+    import torch
+    dev = device if device is not None else torch.cuda.current_device()
+    return load().attn_sync_status(_stream_handle(dev))

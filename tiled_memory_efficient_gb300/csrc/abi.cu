@@ -1,0 +1,228 @@
+// abi.cu -- the extern "C" entry points of include/attn.h: argument
+// validation, TMA tensor-map construction, the device status word, and the
+// kernel launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "attn_internal.h"
+#include "ptx.cuh"
+
+namespace tme {
+
+// One status word per device (a static device variable; nothing is allocated).
+__device__ unsigned int g_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+int g_cc_ok[kMaxDevices] = {};  // 0 unknown, 1 sm_103, -1 other
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Device set-up, once per device with that device current: check the
+// architecture and look up the status word's device address.
+int device_setup(unsigned int** status) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_cc_ok[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        g_cc_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    if (g_cc_ok[dev] != 1) return ATTN_ERR_UNSUPPORTED;
+    if (!g_status_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_status) != cudaSuccess) return ATTN_ERR_CUDA;
+        g_status_ptr[dev] = static_cast<unsigned int*>(ptr);
+    }
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return ATTN_ERR_CUDA;
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    *status = g_status_ptr[dev];
+    return ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 3-D map over a [groups][rows][D] 16-bit tensor, boxes of 64 columns x 128
+// rows x 1 group, 128-byte swizzle, zero fill outside the tensor.
+int make_map(CUtensorMap* map, const void* base, bool bf16, int D, int64_t rows, int64_t groups) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(groups)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                   static_cast<cuuint64_t>(rows) * D * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                                3, const_cast<void*>(base), dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// Shape checks shared by forward and backward.
+int check_shape(int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale, int dtype) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || D <= 0) return ATTN_ERR_INVALID;
+    if (Hq % Hkv != 0) return ATTN_ERR_INVALID;
+    if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID;
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return ATTN_ERR_INVALID;
+    if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+    const int64_t G = Hq / Hkv;
+    const int64_t rows = G * static_cast<int64_t>(Nq);
+    // TMA coordinates and row indices are 32-bit signed inside the kernels.
+    if (rows > (1ll << 31) - 512 || Nk > (1 << 30)) return ATTN_ERR_UNSUPPORTED;
+    const int64_t groups = static_cast<int64_t>(B) * Hkv;
+    const int64_t pairs = (rows + 255) / 256;
+    if (groups * pairs > 0x7fffffffll || groups > 0x7fffffffll) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
+__global__ void selftest_timeout_kernel(unsigned long long wait_ns, unsigned int* status) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    // Nothing ever arrives on `bar`: the wait must give up by itself.
+    const uint32_t a = smem_u32(&bar);
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(a, 0)) return;  // cannot happen
+        if ((it & 63u) == 63u && global_ns() - t0 > wait_ns) {
+            atomicOr(status, kStatusTimeout);
+            return;
+        }
+    }
+}
+
+}  // namespace
+}  // namespace tme
+
+using namespace tme;
+
+extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                        int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal,
+                        int dtype, void* stream) {
+    if (!q || !k || !v || !out || !lse) return ATTN_ERR_INVALID;
+    int rc = check_shape(B, Hq, Hkv, Nq, Nk, D, scale, dtype);
+    if (rc != ATTN_OK) return rc;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+        return ATTN_ERR_ALIGN;
+    unsigned int* status = nullptr;
+    rc = device_setup(&status);
+    if (rc != ATTN_OK) return rc;
+
+    const bool bf16 = dtype == ATTN_BF16;
+    const int64_t G = Hq / Hkv;
+    const int64_t rows = G * Nq;
+    const int64_t groups = static_cast<int64_t>(B) * Hkv;
+    CUtensorMap tmQ, tmK, tmV;
+    if (make_map(&tmQ, q, bf16, D, rows, groups) != ATTN_OK ||
+        make_map(&tmK, k, bf16, D, Nk, groups) != ATTN_OK ||
+        make_map(&tmV, v, bf16, D, Nk, groups) != ATTN_OK)
+        return ATTN_ERR_CUDA;
+
+    FwdParams p{};
+    p.out = out;
+    p.lse = lse;
+    p.status = status;
+    p.rows_per_group = rows;
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.n_groups = static_cast<int>(groups);
+    p.n_pairs = static_cast<int>((rows + 255) / 256);
+    p.scale_log2 = scale * 1.4426950408889634f;
+    const cudaError_t e = launch_fwd(D, bf16, causal != 0, tmQ, tmK, tmV, p,
+                                     static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+extern "C" size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int D,
+                                          int dtype) {
+    if (check_shape(B, Hq, Hkv, Nq, Nk, D, 1.0f, dtype) != ATTN_OK) return 0;
+    // Two fp32 values per query row (log2-domain LSE and Delta), padded to 256 bytes.
+    const size_t rows = static_cast<size_t>(B) * Hq * Nq;
+    return ((rows * 2 * sizeof(float)) + 255) & ~static_cast<size_t>(255);
+}
+
+extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                        void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int Nq,
+                        int Nk, int D, float scale, int causal, int dtype, void* stream) {
+    (void)causal;
+    (void)stream;
+    if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv || !workspace)
+        return ATTN_ERR_INVALID;
+    int rc = check_shape(B, Hq, Hkv, Nq, Nk, D, scale, dtype);
+    if (rc != ATTN_OK) return rc;
+    const void* ptrs[] = {q, k, v, out, dout, lse, dq, dk, dv, workspace};
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return ATTN_ERR_ALIGN;
+    if (workspace_bytes < attn_bwd_workspace_size(B, Hq, Hkv, Nq, Nk, D, dtype))
+        return ATTN_ERR_WORKSPACE;
+    return ATTN_ERR_UNSUPPORTED;
+}
+
+extern "C" int attn_sync_status(void* stream) {
+    unsigned int* status = nullptr;
+    int rc = device_setup(&status);
+    if (rc != ATTN_OK) return rc;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    unsigned int word = 0;
+    if (cudaMemcpy(&word, status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    if (word != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpy(status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+    }
+    return (word & kStatusTimeout) ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+extern "C" int attn_selftest_timeout(unsigned long long wait_ns, void* stream) {
+    unsigned int* status = nullptr;
+    int rc = device_setup(&status);
+    if (rc != ATTN_OK) return rc;
+    if (wait_ns < 1000ull) wait_ns = 1000ull;
+    if (wait_ns > 100000000ull) wait_ns = 100000000ull;
+    selftest_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(wait_ns, status);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+extern "C" const char* attn_strerror(int status) {
+    switch (status) {
+        case ATTN_OK: return "ok";
+        case ATTN_ERR_INVALID: return "invalid argument";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported configuration or device";
+        case ATTN_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case ATTN_ERR_CUDA: return "CUDA runtime or driver error";
+        case ATTN_ERR_TIMEOUT: return "a device-side wait timed out";
+        case ATTN_ERR_WORKSPACE: return "workspace too small";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int attn_version(void) { return 100; }

@@ -1,0 +1,420 @@
+// attn_fwd.cu -- tiled scaled-dot-product attention forward for sm_103a.
+//
+// The method (noflash-attention forum post, ai-navigate-news, section "The DIY
+// approach" and its "What worked" list): never form the N x N score matrix;
+// tile Q along queries and K/V along keys, keep an online-softmax running max
+// and sum per query row, flatten the query heads of a GQA group onto their
+// shared KV head instead of broadcasting K/V, flush negligible softmax terms
+// to zero, and optionally apply a causal mask.
+//
+// GB300 design (one CTA = 256 flattened query rows of one KV group, two
+// 128-row Q tiles ping-ponging on the tensor core):
+//   warp 8      TMA producer: Q tiles once, then K_j / V_j tiles through two
+//               mbarrier-guarded shared-memory rings (128-byte swizzle).
+//   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T with tcgen05.mma
+//               (both operands in shared memory, fp32 accumulator in TMEM),
+//               then O_t += P_t V_j with P_t read from TMEM.
+//   warps 0-7   softmax, one warpgroup per Q tile, one thread per query row:
+//               tcgen05.ld of the S row, masked row max, lazy rescale of the
+//               running state, exp2 with a flush-to-zero threshold, P packed
+//               to fp16/bf16 and written back over S in TMEM; at the end the
+//               epilogue divides O by the row sum and stores O and the
+//               natural-log LSE.
+// TMEM (512 columns): S_0 [0,128) S_1 [128,256) O_0 [256,256+D) O_1 [256+D,256+2D);
+// P_t overwrites the first 64 columns of S_t (two 16-bit values per column).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "attn_internal.h"
+#include "ptx.cuh"
+
+namespace tme {
+namespace {
+
+constexpr int kRows = 128;          // rows of a Q tile, keys of a K/V tile
+constexpr int kThreads = 320;       // 8 softmax warps + producer + MMA
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kLn2 = 0.6931471805599453f;
+// Lazy rescale: the running max used for exponentiation is only moved when
+// the true max exceeds it by more than this many powers of two.
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D>
+struct FwdCfg {
+    static constexpr int kTileBytes = kRows * D * 2;         // one 128 x D tile, 16-bit
+    static constexpr int kKStages = (D == 128) ? 2 : 3;
+    static constexpr int kVStages = (D == 128) ? 2 : 3;
+    static constexpr int kQOff = 0;
+    static constexpr int kKOff = kQOff + 2 * kTileBytes;
+    static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+    static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
+    static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
+    static constexpr int kOCol = 256;                        // first O column in TMEM
+};
+
+// Flush-to-zero threshold in the log2 domain: p = 0 when s*c - m < -T.  For
+// fp16 P, 2^-24 is the smallest subnormal, so anything smaller would round to
+// zero or to that edge anyway; for bf16 the ex2.approx.ftz flush below 2^-126
+// is the threshold itself.
+template <bool BF16>
+__device__ __forceinline__ float softmax_term(float x) {
+    const float p = ex2_ftz(x);
+    if constexpr (BF16) {
+        return p;
+    } else {
+        return x < -24.0f ? 0.0f : p;
+    }
+}
+
+// Number of 128-key tiles a Q tile starting at flattened row `row0` needs.
+__device__ __forceinline__ int kv_tiles_for(int64_t row0, const FwdParams& p, bool causal) {
+    if (row0 >= p.rows_per_group) return 0;
+    if (!causal) return (p.Nk + kRows - 1) / kRows;
+    const int64_t last = min(row0 + kRows - 1, p.rows_per_group - 1);
+    const int64_t max_pos = (row0 / p.Nq == last / p.Nq) ? (last % p.Nq) : (p.Nq - 1);
+    const int64_t keys = (max_pos + 1 < p.Nk) ? (max_pos + 1) : static_cast<int64_t>(p.Nk);
+    return static_cast<int>((keys + kRows - 1) / kRows);
+}
+
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
+                    const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+    using C = FwdCfg<D>;
+    constexpr int KS = C::kKStages, VS = C::kVStages;
+    constexpr int KB = D / 64;  // 64-element (128-byte) column blocks per row
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sQ = smem + C::kQOff;
+    uint8_t* sK = smem + C::kKOff;
+    uint8_t* sV = smem + C::kVOff;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+    uint64_t* q_full = bars;
+    uint64_t* k_full = q_full + 1;
+    uint64_t* k_empty = k_full + KS;
+    uint64_t* v_full = k_empty + KS;
+    uint64_t* v_empty = v_full + VS;
+    uint64_t* s_full = v_empty + VS;   // [2] S_t ready in TMEM
+    uint64_t* p_full = s_full + 2;     // [2] P_t in TMEM and O_t rescaled
+    uint64_t* o_full = p_full + 2;     // [2] last PV of tile t done
+    uint64_t* mma_done = o_full + 2;   // every MMA of this CTA done
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // Work unit: heaviest pair first (for the causal mask the last rows of a
+    // head attend to the most keys).
+    const int group = static_cast<int>(blockIdx.x % p.n_groups);
+    const int pair = p.n_pairs - 1 - static_cast<int>(blockIdx.x / p.n_groups);
+    const int64_t row_base = static_cast<int64_t>(pair) * (2 * kRows);
+    const int n0 = kv_tiles_for(row_base, p, CAUSAL);
+    const int n1 = kv_tiles_for(row_base + kRows, p, CAUSAL);
+    const int nmax = n0 > n1 ? n0 : n1;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int i = 0; i < KS; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
+        for (int i = 0; i < VS; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 1); }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&s_full[t], 1);
+            mbar_init(&p_full[t], 128);
+            mbar_init(&o_full[t], 1);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) tmem_alloc(tmem_slot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            mbar_arrive_expect_tx(q_full, 2 * C::kTileBytes);
+            for (int t = 0; t < 2; ++t)
+                for (int kb = 0; kb < KB; ++kb)
+                    tma_load_3d(&tmQ, q_full, sQ + t * C::kTileBytes + kb * (kRows * 128),
+                                kb * 64, static_cast<int>(row_base + t * kRows), group);
+            int nk = 0, nv = 0;  // loads issued
+            for (int j = 0; j < nmax; ++j) {
+                const int ks = j % KS;
+                if (!mbar_wait(&k_empty[ks], ((j / KS) & 1) ^ 1, abort_flag, p.status)) break;
+                mbar_arrive_expect_tx(&k_full[ks], C::kTileBytes);
+                for (int kb = 0; kb < KB; ++kb)
+                    tma_load_3d(&tmK, &k_full[ks], sK + ks * C::kTileBytes + kb * (kRows * 128),
+                                kb * 64, j * kRows, group);
+                ++nk;
+                const int vs = j % VS;
+                if (!mbar_wait(&v_empty[vs], ((j / VS) & 1) ^ 1, abort_flag, p.status)) break;
+                mbar_arrive_expect_tx(&v_full[vs], C::kTileBytes);
+                for (int kb = 0; kb < KB; ++kb)
+                    tma_load_3d(&tmV, &v_full[vs], sV + vs * C::kTileBytes + kb * (kRows * 128),
+                                kb * 64, j * kRows, group);
+                ++nv;
+            }
+            // Never leave a copy in flight into shared memory we are about to give up.
+            mbar_wait_bounded(q_full, 0, p.status);
+            for (int n = (nk > KS ? nk - KS : 0); n < nk; ++n)
+                mbar_wait_bounded(&k_full[n % KS], (n / KS) & 1, p.status);
+            for (int n = (nv > VS ? nv - VS : 0); n < nv; ++n)
+                mbar_wait_bounded(&v_full[n % VS], (n / VS) & 1, p.status);
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_f16(kRows, kRows, BF16, false);
+            constexpr uint32_t idesc_o = idesc_f16(kRows, D, BF16, true);
+            const uint32_t sq = smem_u32(sQ), sk = smem_u32(sK), sv = smem_u32(sV);
+            const int nt[2] = {n0, n1};
+
+            // S_t = Q_t K^T: D/16 MMAs of K=16; within a 128-byte swizzle row
+            // the K offset advances the start address by 32 bytes.
+            auto issue_s = [&](int t, int kslot) {
+                const uint32_t d = tmem + t * kRows;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * (kRows * 128) + (k & 3) * 32;
+                    const uint64_t a = smem_desc_sw128(sq + t * C::kTileBytes + off, 16, 1024);
+                    const uint64_t b = smem_desc_sw128(sk + kslot * C::kTileBytes + off, 16, 1024);
+                    mma_ss(d, a, b, idesc_s, k > 0 ? 1u : 0u);
+                }
+                mma_commit(&s_full[t]);
+            };
+            // O_t += P_t V: 8 MMAs of 16 keys; P_t from TMEM (8 columns per 16
+            // keys), V MN-major in shared memory (16 key rows = 2048 bytes; the
+            // two 64-column halves of D=128 are one 16 KiB block apart).
+            auto issue_pv = [&](int t, int vslot, int j) {
+                const uint32_t d = tmem + C::kOCol + t * D;
+#pragma unroll
+                for (int k = 0; k < kRows / 16; ++k) {
+                    const uint32_t a = tmem + t * kRows + k * 8;
+                    const uint64_t b =
+                        smem_desc_sw128(sv + vslot * C::kTileBytes + k * 2048, kRows * 128, 1024);
+                    mma_ts(d, a, b, idesc_o, (j > 0 || k > 0) ? 1u : 0u);
+                }
+            };
+
+            bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
+            if (ok && nmax > 0) {
+                ok = mbar_wait(&k_full[0], 0, abort_flag, p.status);
+                if (ok) {
+                    tc_fence_after();
+                    if (n0 > 0) issue_s(0, 0);
+                    if (n1 > 0) issue_s(1, 0);
+                    mma_commit(&k_empty[0]);
+                }
+            }
+            for (int j = 0; ok && j < nmax; ++j) {
+                const int vslot = j % VS;
+                if (!mbar_wait(&v_full[vslot], (j / VS) & 1, abort_flag, p.status)) break;
+                tc_fence_after();
+                const bool more = j + 1 < nmax;
+                const int kslot = (j + 1) % KS;
+                for (int t = 0; t < 2; ++t) {
+                    if (j < nt[t]) {
+                        if (!mbar_wait(&p_full[t], j & 1, abort_flag, p.status)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_pv(t, vslot, j);
+                        if (j == nt[t] - 1) mma_commit(&o_full[t]);
+                    }
+                    if (t == 0 && more) {
+                        // S_0 of the next key tile goes in between the two PVs
+                        // so that softmax of tile 0 overlaps PV of tile 1.
+                        if (!mbar_wait(&k_full[kslot], ((j + 1) / KS) & 1, abort_flag, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        if (j + 1 < nt[0]) issue_s(0, kslot);
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&v_empty[vslot]);
+                if (more) {
+                    if (j + 1 < nt[1]) issue_s(1, kslot);
+                    mma_commit(&k_empty[kslot]);
+                }
+            }
+            mma_commit(mma_done);
+            mbar_wait_bounded(mma_done, 0, p.status);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int t = warp >> 2;         // Q tile of this warpgroup
+        const int quad = warp & 3;       // TMEM lane quadrant = rows quad*32 .. +31
+        const int n_t = t == 0 ? n0 : n1;
+        const int64_t row0 = row_base + t * kRows;
+        const int64_t row = row0 + quad * 32 + lane;
+        const bool row_valid = row < p.rows_per_group;
+        const int pos = static_cast<int>(row % p.Nq);
+        // Smallest query position among this warp's rows: masking is needed on
+        // key tiles that reach past it (or past Nk).
+        const int64_t wr0 = row0 + quad * 32;
+        const int64_t wr1 = min(wr0 + 31, p.rows_per_group - 1);
+        const int warp_min_pos =
+            (wr0 / p.Nq == wr1 / p.Nq) ? static_cast<int>(wr0 % p.Nq) : 0;
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t tS = tmem + lane_base + t * kRows;
+        const uint32_t tO = tmem + lane_base + C::kOCol + t * D;
+        const float sl2 = p.scale_log2;
+
+        float m = -INFINITY;  // running max (log2 domain, scaled) used for exponentiation
+        float l = 0.0f;       // running sum of p
+        bool ok = true;
+        for (int j = 0; j < n_t; ++j) {
+            if (!warp_wait(&s_full[t], j & 1, abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
+
+            const int key0 = j * kRows;
+            const bool need_mask = (key0 + kRows > p.Nk) || (CAUSAL && key0 + kRows - 1 > warp_min_pos);
+            if (need_mask) {
+                const int lim = CAUSAL ? min(p.Nk, pos + 1) : p.Nk;  // keys [0, lim) allowed
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (key0 + c * 32 + i >= lim) sr[c][i] = __float_as_uint(-INFINITY);
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
+            const float m_new = fmaxf(m, mx * sl2);
+            const bool need = m_new > m + kRescaleThreshold;
+            float alpha = 1.0f;
+            if (need) {
+                alpha = ex2_ftz(m - m_new);  // m = -inf gives 0
+                m = m_new;
+            }
+            const float m_sub = (m == -INFINITY) ? 0.0f : m;
+
+            float rs = 0.0f;
+            uint32_t pk[2][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const float p0 = softmax_term<BF16>(fmaf(__uint_as_float(sr[c][i]), sl2, -m_sub));
+                    const float p1 = softmax_term<BF16>(fmaf(__uint_as_float(sr[c][i + 1]), sl2, -m_sub));
+                    rs += p0 + p1;
+                    pk[c >> 1][(c & 1) * 16 + (i >> 1)] = pack2<BF16>(p0, p1);
+                }
+            }
+            tmem_st32(tS, pk[0]);
+            tmem_st32(tS + 32, pk[1]);
+
+            // O_t must be rescaled before the next PV accumulates into it.  PV
+            // of key tile j-1 is complete: S_t of tile j was committed after it.
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c * 32, o);
+                    tmem_wait_ld();
+                    reg_fence(o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st32(tO + c * 32, o);
+                }
+            }
+            l = l * alpha + rs;
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&p_full[t]);
+        }
+
+        if (ok && n_t > 0 && warp_wait(&o_full[t], 0, abort_flag, p.status)) {
+            tc_fence_after();
+            const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+            const int64_t grow = static_cast<int64_t>(group) * p.rows_per_group + row;
+            uint16_t* out = static_cast<uint16_t*>(p.out) + grow * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tO + c * 32, o);
+                tmem_wait_ld();
+                reg_fence(o);
+                if (row_valid) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        w[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l,
+                                           __uint_as_float(o[2 * i + 1]) * inv_l);
+                    uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                }
+            }
+            if (row_valid) {
+                const float m_sub = (m == -INFINITY) ? 0.0f : m;
+                p.lse[grow] = l > 0.0f ? (m_sub + lg2_approx(l)) * kLn2 : -INFINITY;
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D, bool BF16, bool CAUSAL>
+cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                       const FwdParams& p, cudaStream_t stream) {
+    auto kern = attn_fwd_kernel<D, BF16, CAUSAL>;
+    constexpr int smem = FwdCfg<D>::kSmemBytes;
+    // Re-applied on every call: a cheap attribute write that is correct on
+    // whichever device is current.
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const long long ctas = static_cast<long long>(p.n_groups) * p.n_pairs;
+    kern<<<dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, stream>>>(tmQ, tmK, tmV, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(int D, bool bf16, bool causal, const CUtensorMap& tmQ,
+                       const CUtensorMap& tmK, const CUtensorMap& tmV, const FwdParams& p,
+                       cudaStream_t stream) {
+#define TME_CASE(d, b, c) \
+    if (D == d && bf16 == b && causal == c) return launch_one<d, b, c>(tmQ, tmK, tmV, p, stream);
+    TME_CASE(64, false, false)
+    TME_CASE(64, false, true)
+    TME_CASE(64, true, false)
+    TME_CASE(64, true, true)
+    TME_CASE(128, false, false)
+    TME_CASE(128, false, true)
+    TME_CASE(128, true, false)
+    TME_CASE(128, true, true)
+#undef TME_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace tme
