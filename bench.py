@@ -1,0 +1,435 @@
+"""Benchmark: attention forward TFLOP/s on GB300, and its fraction of the dense
+FP16/BF16 tensor peak, across the sequence lengths of the isolated-attention
+benchmark of the noflash-attention forum post (ai-navigate-news, section "It's
+actually faster too!": B=1, H=16, D=64, fp16, non-causal, N = 256 ... 16384).
+
+One step = one forward launch per sequence length of the sweep on synthetic
+seeded inputs already resident in HBM.  Every launch is timed with CUDA events
+on the launching stream; L2 is flushed (a 256 MiB write) before each launch,
+outside the timed events.  value = sum of algorithmic FLOPs / sum of launch
+times.  Prints ONE JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config sweep|gqa_prefill|video_dit|training|tiny]
+
+--impl reference times the fp64 CPU oracle (the reference arm) on the host
+cores: each step is a bounded sample of the same workload.  Under torchrun
+(N > 1) every rank runs its own replica (the path needs no exchange); rank 0
+prints the line, with value = all ranks' FLOPs / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s on 1 GB300 and % of dense FP16/BF16 tensor peak vs seq len"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "fwd_traffic.json")
+
+
+def peaks():
+    """Measured denominators if the driver left MEASURED_PEAKS.json, else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            flat = {}
+
+            def walk(x, pre=""):
+                if isinstance(x, dict):
+                    for k, v in x.items():
+                        walk(v, f"{pre}{k}.")
+                else:
+                    flat[pre[:-1]] = x
+            walk(d)
+
+            def find(*keys):
+                for k, v in flat.items():
+                    kl = k.lower()
+                    if all(s in kl for s in keys) and isinstance(v, (int, float)):
+                        return float(v)
+                return None
+            sus = find("bf16", "sustain")
+            burst = None
+            for k, v in flat.items():
+                kl = k.lower()
+                if "bf16" in kl and "sustain" not in kl and isinstance(v, (int, float)) and v > 100:
+                    burst = float(v)
+                    break
+            hbm = find("hbm")
+            if burst:
+                return {"bf16_tflops": burst, "bf16_tflops_sustained": sus or burst,
+                        "hbm_gbs": hbm or FALLBACK_PEAKS["hbm_gbs"], "source": "measured"}
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("attn_fwd.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "tiled_memory_efficient_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(workload: str, n: int):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    try:
+        d = json.load(open(PROFILE_TRAFFIC))
+    except Exception:
+        return None
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return d.get("per_launch_dram_bytes", {}).get(f"{workload}:{n}")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        return dist, dist.get_rank(), world, local
+    if n_gpus != 1:
+        raise SystemExit("--gpus N > 1 must be launched with torchrun (one rank per GPU)")
+    return None, 0, 1, 0
+
+
+def run_ours(args):
+    import torch
+
+    from tiled_memory_efficient_gb300 import _lib, inputs
+
+    dist, rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = inputs.WORKLOADS[args.config]
+    seq = list(w.seq_lens) if args.n is None else [args.n]
+    _lib.load()
+    pk = peaks()
+    stream = torch.cuda.current_stream(dev)
+
+    # inputs resident in HBM before the timed region
+    bufs = []
+    for n in seq:
+        x = inputs.make_inputs(w, n)
+        q, k, v = (x[m].to(dev) for m in ("q", "k", "v"))
+        out = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], device=dev, dtype=torch.float32)
+        bufs.append((n, q, k, v, out, lse, x))
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def launch(b):
+        n, q, k, v, out, lse, _ = b
+        _lib.attn_fwd(q, k, v, causal=w.causal, out=out, lse=lse)
+
+    for _ in range(args.warmup):
+        for b in bufs:
+            flush.zero_()
+            launch(b)
+    rc = _lib.sync_status(dev)
+    if rc != _lib.ATTN_OK:
+        raise RuntimeError(f"device status after warm-up: {_lib.strerror(rc)}")
+
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in bufs] for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        t_wall = time.perf_counter()
+        for s in range(args.steps):
+            for i, b in enumerate(bufs):
+                flush.zero_()
+                ev[s][i][0].record(stream)
+                launch(b)
+                ev[s][i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    rc = _lib.sync_status(dev)
+    if rc != _lib.ATTN_OK:
+        raise RuntimeError(f"device status after timing: {_lib.strerror(rc)}")
+
+    per_launch_ms = [[ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps)]
+                     for i in range(len(bufs))]
+    ms_each = [statistics.mean(x) for x in per_launch_ms]
+    flops = [w.flops_fwd(n) for n in seq]
+    step_ms = sum(ms_each)
+    if dist:
+        t = torch.tensor([step_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    value = world * sum(flops) / (step_ms * 1e-3) / 1e12
+
+    # roofline of the dominant launch (largest share of the step time)
+    dom = max(range(len(seq)), key=lambda i: ms_each[i])
+    achieved = flops[dom] / (ms_each[dom] * 1e-3) / 1e12
+    peak = pk["bf16_tflops"]
+    traffic = traffic_for(args.config, seq[dom])
+    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                "kernel": "attn_fwd_kernel", "launch": f"N={seq[dom]}",
+                "peak_source": f"{pk['source']} bf16 dense (burst; fp16 runs at the same "
+                               f"tensor rate)"}
+
+    # end to end through the public call with host buffers: H2D of q,k,v from
+    # pinned memory, the forward, D2H of out and lse, every step
+    e2e = None
+    if not args.no_e2e:
+        host = []
+        h2d = d2h = 0
+        for n, q, k, v, out, lse, x in bufs:
+            hq, hk, hv = (x[m].pin_memory() for m in ("q", "k", "v"))
+            ho = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+            hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+            host.append((hq, hk, hv, ho, hl))
+            h2d += sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+            d2h += ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+        e2e_steps = max(1, min(args.steps, 10))
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            for (n, q, k, v, out, lse, _), (hq, hk, hv, ho, hl) in zip(bufs, host):
+                q.copy_(hq, non_blocking=True)
+                k.copy_(hk, non_blocking=True)
+                v.copy_(hv, non_blocking=True)
+                _lib.attn_fwd(q, k, v, causal=w.causal, out=out, lse=lse)
+                ho.copy_(out, non_blocking=True)
+                hl.copy_(lse, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1) / e2e_steps
+        if dist:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": round(world * sum(flops) / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
+
+    clocks = clk.summary()
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline(w, seq, budget_s=args.cpu_budget)
+    sweep = [{"N": n, "ms": round(ms, 4), "tflops": round(f / (ms * 1e-3) / 1e12, 1),
+              "frac_of_peak": round(f / (ms * 1e-3) / 1e12 / peak, 4)}
+             for n, ms, f in zip(seq, ms_each, flops)]
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16" if w.dtype == torch.float16 else "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.note, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                   "causal": w.causal, "seq_lens": seq,
+                   "inputs": "seeded N(0,1) rounded to dtype" +
+                             ("; 1% of key rows x8" if w.outlier_keys else ""),
+                   "l2": "flushed before every launch (256 MiB write, outside the timed events)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": args.steps * len(seq),
+        "clocks": clocks, "sweep": sweep, "wall_s_timed_region": round(t_wall, 3),
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def cpu_baseline(w, seq, budget_s: float = 15.0, n_override=None):
+    """The fp64 oracle, as it stands, on the host cores: a row sample of the
+    largest sequence length, sized to about `budget_s` seconds."""
+    import numpy as np
+
+    import oracle
+    from tiled_memory_efficient_gb300 import inputs
+    n = n_override or max(seq)
+    threads = oracle.default_threads()
+    x = inputs.make_inputs(w, n)
+    G = w.Hq // w.Hkv
+    q, k, v = x["q"][:1, :1], x["k"][:1, :1], x["v"][:1, :1]
+
+    def flops_rows(rows):
+        keys = sum(oracle.attended_keys(int(i), n, w.causal) for i in rows)
+        return 4.0 * w.D * keys
+
+    rng = np.random.default_rng(0)
+    probe = rng.choice(n, size=min(n, 8 * threads), replace=False)
+    t0 = time.perf_counter()
+    oracle.attention_fwd(q, k, v, causal=w.causal, rows=probe, threads=threads)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    per_row = dt / len(probe)
+    n_rows = int(min(n, max(len(probe), budget_s / per_row)))
+    rows = np.sort(rng.choice(n, size=n_rows, replace=False))
+    t0 = time.perf_counter()
+    oracle.attention_fwd(q, k, v, causal=w.causal, rows=rows, threads=threads)
+    dt = time.perf_counter() - t0
+    del G
+    return {"value": round(flops_rows(rows) / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{n_rows} query rows of head (b=0,h=0) at N={n} (all {n} keys"
+                      f"{', causal' if w.causal else ''}), fp64, {dt:.1f} s"}
+
+
+def run_reference(args):
+    """Reference arm: the fp64 oracle on the host cores, bounded sample per step."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from tiled_memory_efficient_gb300 import inputs
+    w = inputs.WORKLOADS[args.config]
+    seq = list(w.seq_lens) if args.n is None else [args.n]
+    threads = oracle.default_threads()
+    data = {}
+    for n in seq:
+        x = inputs.make_inputs(w, n)
+        data[n] = (x["q"][:1, :1], x["k"][:1, :1], x["v"][:1, :1])
+    # rows per N per step, sized so the whole run takes about 60-120 s
+    budget_step = max(0.5, 90.0 / (args.steps + args.warmup))
+    cost = {n: 4.0 * w.D * n for n in seq}          # flops per full row
+    tot = sum(cost.values())
+    rng = np.random.default_rng(0)
+    # calibrate
+    t0 = time.perf_counter()
+    q, k, v = data[seq[-1]]
+    cal = rng.choice(seq[-1], size=min(seq[-1], 4 * threads), replace=False)
+    oracle.attention_fwd(q, k, v, causal=w.causal, rows=cal, threads=threads)
+    rate = cost[seq[-1]] * len(cal) / max(time.perf_counter() - t0, 1e-4)   # flops/s
+    rows_per_n = {n: max(1, min(n, int(budget_step * rate * (cost[n] / tot) / cost[n])))
+                  for n in seq}
+    step_flops = 0.0
+    times = []
+    for s in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        fl = 0.0
+        for n in seq:
+            q, k, v = data[n]
+            rows = rng.choice(n, size=rows_per_n[n], replace=False)
+            oracle.attention_fwd(q, k, v, causal=w.causal, rows=rows, threads=threads)
+            fl += sum(4.0 * w.D * oracle.attended_keys(int(i), n, w.causal) for i in rows)
+        dt = time.perf_counter() - t0
+        if s >= args.warmup:
+            times.append(dt)
+            step_flops += fl
+    total = sum(times)
+    value = step_flops / total / 1e12
+    sample = (f"per step: rows {rows_per_n} of head (b=0,h=0) per N, all keys, fp64 "
+              f"({threads} threads)")
+    line = {
+        "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total / max(1, len(times)), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": w.note, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                   "causal": w.causal, "seq_lens": seq},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="sweep")
+    ap.add_argument("--n", type=int, default=None, help="run one sequence length only")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

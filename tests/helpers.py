@@ -1,9 +1,13 @@
 """Shared helpers for the parity tests: run the oracle on exactly the rows a
 test checks, and compare with the stated tolerances.
 
-Tolerances (max-abs, against the fp64 oracle on the same rounded inputs):
-O <= 2e-3 for fp16 and <= 1e-2 for bf16; LSE <= 1e-3; backward (bf16)
-<= 2e-2, fp16 backward <= 1e-2.
+Tolerances (absolute, per element, against the fp64 oracle on the same
+rounded inputs): O <= 2e-3 for fp16 and <= 1e-2 for bf16; LSE <= 1e-3;
+backward <= 2e-2 (bf16) and <= 1e-2 (fp16).  O and the gradients are stored
+in the 16-bit input dtype, and where one unit in the last place of that dtype
+at the oracle's value is larger than the tolerance (|O| >= 2 in bf16, >= 4 in
+fp16) even the exactly rounded result can miss it; there the bound is that
+one ulp.
 """
 from __future__ import annotations
 
@@ -53,12 +57,32 @@ def max_err(a, b) -> float:
     return float(np.max(np.abs(np.asarray(a) - np.asarray(b)))) if np.size(a) else 0.0
 
 
+_MANT_BITS = {torch.float16: 10, torch.bfloat16: 7}
+
+
+def ulp(ref, dtype):
+    """One unit in the last place of `dtype` at |ref| (normal range)."""
+    a = np.maximum(np.abs(np.asarray(ref, dtype=np.float64)), 2.0 ** -14)
+    return np.exp2(np.floor(np.log2(a)) - _MANT_BITS[dtype])
+
+
+def assert_close_elementwise(got, ref, tol, dtype, what, name):
+    got, ref = np.asarray(got), np.asarray(ref)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite {name}"
+    bound = np.maximum(tol, ulp(ref, dtype))
+    err = np.abs(got - ref)
+    worst = np.unravel_index(np.argmax(err - bound), err.shape) if err.size else None
+    if err.size:
+        assert np.all(err <= bound), (
+            f"{what}: |{name}-oracle| = {err[worst]:.3e} > bound {bound[worst]:.3e} "
+            f"at |ref| = {abs(ref[worst]):.3f} (max err {err.max():.3e})")
+    return float(err.max()) if err.size else 0.0
+
+
 def assert_fwd_close(o_gpu, lse_gpu, o_ref, lse_ref, dtype, what=""):
-    eo = max_err(o_gpu, o_ref)
+    eo = assert_close_elementwise(o_gpu, o_ref, TOL_O[dtype], dtype, what, "O")
     el = max_err(lse_gpu, lse_ref)
-    assert np.all(np.isfinite(o_gpu)), f"{what}: non-finite O"
     assert np.all(np.isfinite(lse_gpu)), f"{what}: non-finite LSE"
-    assert eo <= TOL_O[dtype], f"{what}: max|O-oracle| = {eo:.3e} > {TOL_O[dtype]}"
     assert el <= TOL_LSE, f"{what}: max|LSE-oracle| = {el:.3e} > {TOL_LSE}"
     return eo, el
 

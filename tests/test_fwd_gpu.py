@@ -68,7 +68,9 @@ def test_small_shapes_every_row(cuda_lib, B, Hq, Hkv, Nq, Nk, D, dtype, causal):
 def test_large_scores_stress_ftz_and_rescale(cuda_lib, dtype):
     # q, k with std 4: scaled scores of std ~16, so rows are nearly one-hot,
     # the running max moves often and many terms fall under the flush threshold.
-    x = inputs.make_custom(1, 2, 2, 384, 700, 64, dtype, seed=5, std=4.0)
+    # v has std 0.5 so that |O| stays below 2, where half an fp16 ulp of the
+    # stored output (<= 4.9e-4) leaves room inside the 2e-3 bound.
+    x = inputs.make_custom(1, 2, 2, 384, 700, 64, dtype, seed=5, std=4.0, v_std=0.5)
     check_full(x, False, what="std4")
     check_full(x, True, what="std4 causal")
 

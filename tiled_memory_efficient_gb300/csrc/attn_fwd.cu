@@ -55,18 +55,34 @@ struct FwdCfg {
     static constexpr int kOCol = 256;                        // first O column in TMEM
 };
 
-// Flush-to-zero threshold in the log2 domain: p = 0 when s*c - m < -T.  For
-// fp16 P, 2^-24 is the smallest subnormal, so anything smaller would round to
-// zero or to that edge anyway; for bf16 the ex2.approx.ftz flush below 2^-126
-// is the threshold itself.
-template <bool BF16>
-__device__ __forceinline__ float softmax_term(float x) {
-    const float p = ex2_ftz(x);
-    if constexpr (BF16) {
-        return p;
-    } else {
-        return x < -24.0f ? 0.0f : p;
+// Flush-to-zero threshold in the log2 domain: a softmax term p = 2^x with
+// x = s*c - m is dropped when x < -T.  bf16 P: T = 126, which is exactly the
+// flush of ex2.approx.ftz (results below 2^-126 are zero).  fp16 P: T = 24;
+// the round-to-nearest conversion of P to fp16 is that flush (every p below
+// 2^-25 becomes +0, the smallest fp16 subnormal is 2^-24), so no extra
+// instruction is spent on it; the fp32 row sum still adds those terms, which
+// changes it by less than Nk * 2^-25 (relative, since the sum is >= 1).
+__device__ __forceinline__ float softmax_term(float x) { return ex2_ftz(x); }
+
+// Row maximum of 128 values with three-input max: a 5-level tree (65 ops),
+// fully independent at the first level.
+__device__ __forceinline__ float row_max128(const uint32_t (&s)[4][32]) {
+    float t[43];
+#pragma unroll
+    for (int i = 0; i < 42; ++i) {
+        const int a = 3 * i, b = 3 * i + 1, c = 3 * i + 2;
+        t[i] = fmax3(__uint_as_float(s[a >> 5][a & 31]), __uint_as_float(s[b >> 5][b & 31]),
+                     __uint_as_float(s[c >> 5][c & 31]));
     }
+    t[42] = fmaxf(__uint_as_float(s[3][30]), __uint_as_float(s[3][31]));
+    float u[15];
+#pragma unroll
+    for (int i = 0; i < 14; ++i) u[i] = fmax3(t[3 * i], t[3 * i + 1], t[3 * i + 2]);
+    u[14] = t[42];
+    float w[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) w[i] = fmax3(u[3 * i], u[3 * i + 1], u[3 * i + 2]);
+    return fmaxf(fmax3(w[0], w[1], w[2]), fmaxf(w[3], w[4]));
 }
 
 // Number of 128-key tiles a Q tile starting at flattened row `row0` needs.
@@ -110,10 +126,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Work unit: heaviest pair first (for the causal mask the last rows of a
-    // head attend to the most keys).
-    const int group = static_cast<int>(blockIdx.x % p.n_groups);
-    const int pair = p.n_pairs - 1 - static_cast<int>(blockIdx.x / p.n_groups);
+    // Work unit: consecutive CTAs share a KV group (its K/V stay hot in L2),
+    // and within a group the heaviest pair goes first (under the causal mask
+    // the last rows of a head attend to the most keys).
+    const int group = static_cast<int>(blockIdx.x / p.n_pairs);
+    const int pair = p.n_pairs - 1 - static_cast<int>(blockIdx.x % p.n_pairs);
     const int64_t row_base = static_cast<int64_t>(pair) * (2 * kRows);
     const int n0 = kv_tiles_for(row_base, p, CAUSAL);
     const int n1 = kv_tiles_for(row_base + kRows, p, CAUSAL);
@@ -295,11 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 32; ++i)
                         if (key0 + c * 32 + i >= lim) sr[c][i] = __float_as_uint(-INFINITY);
             }
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
+            const float mx = row_max128(sr);
             const float m_new = fmaxf(m, mx * sl2);
             const bool need = m_new > m + kRescaleThreshold;
             float alpha = 1.0f;
@@ -309,18 +322,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float m_sub = (m == -INFINITY) ? 0.0f : m;
 
-            float rs = 0.0f;
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 partial row sums
             uint32_t pk[2][32];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
-                    const float p0 = softmax_term<BF16>(fmaf(__uint_as_float(sr[c][i]), sl2, -m_sub));
-                    const float p1 = softmax_term<BF16>(fmaf(__uint_as_float(sr[c][i + 1]), sl2, -m_sub));
-                    rs += p0 + p1;
+                    const float p0 = softmax_term(fmaf(__uint_as_float(sr[c][i]), sl2, -m_sub));
+                    const float p1 = softmax_term(fmaf(__uint_as_float(sr[c][i + 1]), sl2, -m_sub));
+                    acc[(i >> 1) & 7] += p0 + p1;
                     pk[c >> 1][(c & 1) * 16 + (i >> 1)] = pack2<BF16>(p0, p1);
                 }
             }
+            const float rs = ((acc[0] + acc[1]) + (acc[2] + acc[3])) +
+                             ((acc[4] + acc[5]) + (acc[6] + acc[7]));
             tmem_st32(tS, pk[0]);
             tmem_st32(tS + 32, pk[1]);
 

@@ -259,6 +259,13 @@ __device__ __forceinline__ float ex2_ftz(float x) {
 
 // Pack two fp32 into one 32-bit word of two 16-bit values (round to nearest
 // even); the first argument goes to the low half.
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ float lg2_approx(float x) {
     float y;
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

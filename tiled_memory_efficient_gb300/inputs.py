@@ -93,13 +93,14 @@ def make_inputs(w: Workload, n: int, nk: int | None = None, seed: int | None = N
 
 
 def make_custom(B, Hq, Hkv, Nq, Nk, D, dtype=torch.float16, seed=0, with_grad=False,
-                std: float = 1.0):
-    """Ad-hoc shapes for parity tests: i.i.d. N(0, std^2) rounded to dtype."""
+                std: float = 1.0, v_std: float = 1.0):
+    """Ad-hoc shapes for parity tests: q, k i.i.d. N(0, std^2), v N(0, v_std^2),
+    rounded to dtype."""
     g = torch.Generator(device="cpu")
     g.manual_seed(seed)
     q = (torch.randn((B, Hq, Nq, D), generator=g) * std).to(dtype)
     k = (torch.randn((B, Hkv, Nk, D), generator=g) * std).to(dtype)
-    v = torch.randn((B, Hkv, Nk, D), generator=g).to(dtype)
+    v = (torch.randn((B, Hkv, Nk, D), generator=g) * v_std).to(dtype)
     out = {"q": q, "k": k, "v": v}
     if with_grad:
         out["do"] = torch.randn((B, Hq, Nq, D), generator=g).to(dtype)
