@@ -192,83 +192,86 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_f16(kRows, kRows, BF16, false);
-            constexpr uint32_t idesc_o = idesc_f16(kRows, D, BF16, true);
-            const uint32_t sq = smem_u32(sQ), sk = smem_u32(sK), sv = smem_u32(sV);
-            const int nt[2] = {n0, n1};
+        // The whole warp runs this loop (converged, warp-uniform values); one
+        // elected lane issues each tcgen05 instruction.
+        constexpr uint32_t idesc_s = idesc_f16(kRows, kRows, BF16, false);
+        constexpr uint32_t idesc_o = idesc_f16(kRows, D, BF16, true);
+        // Descriptor start addresses are in 16-byte units: one tile is
+        // kTileBytes/16, a 64-column block 1024, 32 bytes of K 2, 16 V rows 128.
+        constexpr uint64_t kTileStep = C::kTileBytes >> 4;
+        const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+        const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
+        const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), kRows * 128, 1024);
+        const int nt[2] = {n0, n1};
 
-            // S_t = Q_t K^T: D/16 MMAs of K=16; within a 128-byte swizzle row
-            // the K offset advances the start address by 32 bytes.
-            auto issue_s = [&](int t, int kslot) {
-                const uint32_t d = tmem + t * kRows;
+        // S_t = Q_t K^T: D/16 MMAs of K=16; within a 128-byte swizzle row the
+        // K offset advances the start address by 32 bytes.
+        auto issue_s = [&](int t, int kslot) {
+            const uint32_t d = tmem + t * kRows;
+            const uint64_t a0 = dq0 + t * kTileStep;
+            const uint64_t b0 = dk0 + kslot * kTileStep;
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k >> 2) * (kRows * 128) + (k & 3) * 32;
-                    const uint64_t a = smem_desc_sw128(sq + t * C::kTileBytes + off, 16, 1024);
-                    const uint64_t b = smem_desc_sw128(sk + kslot * C::kTileBytes + off, 16, 1024);
-                    mma_ss(d, a, b, idesc_s, k > 0 ? 1u : 0u);
-                }
-                mma_commit(&s_full[t]);
-            };
-            // O_t += P_t V: 8 MMAs of 16 keys; P_t from TMEM (8 columns per 16
-            // keys), V MN-major in shared memory (16 key rows = 2048 bytes; the
-            // two 64-column halves of D=128 are one 16 KiB block apart).
-            auto issue_pv = [&](int t, int vslot, int j) {
-                const uint32_t d = tmem + C::kOCol + t * D;
-#pragma unroll
-                for (int k = 0; k < kRows / 16; ++k) {
-                    const uint32_t a = tmem + t * kRows + k * 8;
-                    const uint64_t b =
-                        smem_desc_sw128(sv + vslot * C::kTileBytes + k * 2048, kRows * 128, 1024);
-                    mma_ts(d, a, b, idesc_o, (j > 0 || k > 0) ? 1u : 0u);
-                }
-            };
-
-            bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
-            if (ok && nmax > 0) {
-                ok = mbar_wait(&k_full[0], 0, abort_flag, p.status);
-                if (ok) {
-                    tc_fence_after();
-                    if (n0 > 0) issue_s(0, 0);
-                    if (n1 > 0) issue_s(1, 0);
-                    mma_commit(&k_empty[0]);
-                }
+            for (int k = 0; k < D / 16; ++k) {
+                const uint64_t off = (k >> 2) * ((kRows * 128) >> 4) + (k & 3) * 2;
+                mma_ss_elect(d, a0 + off, b0 + off, idesc_s, k > 0 ? 1u : 0u);
             }
-            for (int j = 0; ok && j < nmax; ++j) {
-                const int vslot = j % VS;
-                if (!mbar_wait(&v_full[vslot], (j / VS) & 1, abort_flag, p.status)) break;
+            mma_commit_elect(&s_full[t]);
+        };
+        // O_t += P_t V: 8 MMAs of 16 keys; P_t from TMEM (8 columns per 16
+        // keys), V MN-major in shared memory (16 key rows = 2048 bytes; the two
+        // 64-column halves of D=128 are one 16 KiB block apart).
+        auto issue_pv = [&](int t, int vslot, int j) {
+            const uint32_t d = tmem + C::kOCol + t * D;
+            const uint64_t b0 = dv0 + vslot * kTileStep;
+#pragma unroll
+            for (int k = 0; k < kRows / 16; ++k)
+                mma_ts_elect(d, tmem + t * kRows + k * 8, b0 + k * (2048 >> 4), idesc_o,
+                             (j > 0 || k > 0) ? 1u : 0u);
+        };
+
+        bool ok = warp_wait(q_full, 0, abort_flag, p.status);
+        if (ok && nmax > 0) {
+            ok = warp_wait(&k_full[0], 0, abort_flag, p.status);
+            if (ok) {
                 tc_fence_after();
-                const bool more = j + 1 < nmax;
-                const int kslot = (j + 1) % KS;
-                for (int t = 0; t < 2; ++t) {
-                    if (j < nt[t]) {
-                        if (!mbar_wait(&p_full[t], j & 1, abort_flag, p.status)) { ok = false; break; }
-                        tc_fence_after();
-                        issue_pv(t, vslot, j);
-                        if (j == nt[t] - 1) mma_commit(&o_full[t]);
-                    }
-                    if (t == 0 && more) {
-                        // S_0 of the next key tile goes in between the two PVs
-                        // so that softmax of tile 0 overlaps PV of tile 1.
-                        if (!mbar_wait(&k_full[kslot], ((j + 1) / KS) & 1, abort_flag, p.status)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        if (j + 1 < nt[0]) issue_s(0, kslot);
-                    }
+                if (n0 > 0) issue_s(0, 0);
+                if (n1 > 0) issue_s(1, 0);
+                mma_commit_elect(&k_empty[0]);
+            }
+        }
+        for (int j = 0; ok && j < nmax; ++j) {
+            const int vslot = j % VS;
+            if (!warp_wait(&v_full[vslot], (j / VS) & 1, abort_flag, p.status)) break;
+            tc_fence_after();
+            const bool more = j + 1 < nmax;
+            const int kslot = (j + 1) % KS;
+            for (int t = 0; t < 2; ++t) {
+                if (j < nt[t]) {
+                    if (!warp_wait(&p_full[t], j & 1, abort_flag, p.status)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_pv(t, vslot, j);
+                    if (j == nt[t] - 1) mma_commit_elect(&o_full[t]);
                 }
-                if (!ok) break;
-                mma_commit(&v_empty[vslot]);
-                if (more) {
-                    if (j + 1 < nt[1]) issue_s(1, kslot);
-                    mma_commit(&k_empty[kslot]);
+                if (t == 0 && more) {
+                    // S_0 of the next key tile goes in between the two PVs so
+                    // that softmax of tile 0 overlaps PV of tile 1.
+                    if (!warp_wait(&k_full[kslot], ((j + 1) / KS) & 1, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (j + 1 < nt[0]) issue_s(0, kslot);
                 }
             }
-            mma_commit(mma_done);
-            mbar_wait_bounded(mma_done, 0, p.status);
+            if (!ok) break;
+            mma_commit_elect(&v_empty[vslot]);
+            if (more) {
+                if (j + 1 < nt[1]) issue_s(1, kslot);
+                mma_commit_elect(&k_empty[kslot]);
+            }
         }
+        mma_commit_elect(mma_done);
+        mbar_wait_bounded(mma_done, 0, p.status);
     } else {
         // ------------------------------------------------------------ softmax + epilogue
         const int t = warp >> 2;         // Q tile of this warpgroup
@@ -290,7 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sl2 = p.scale_log2;
 
         float m = -INFINITY;  // running max (log2 domain, scaled) used for exponentiation
-        float l = 0.0f;       // running sum of p
+        float l = 0.0f;       // running sum of p (gives the LSE)
+        float lr = 0.0f;      // bf16: running sum of the rounded p (normalises O)
         bool ok = true;
         for (int j = 0; j < n_t; ++j) {
             if (!warp_wait(&s_full[t], j & 1, abort_flag, p.status)) { ok = false; break; }
@@ -322,7 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float m_sub = (m == -INFINITY) ? 0.0f : m;
 
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 partial row sums
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // partial row sums of p
+            float accr[4] = {0.f, 0.f, 0.f, 0.f};  // bf16: partial sums of the rounded p
             uint32_t pk[2][32];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
@@ -330,12 +335,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 32; i += 2) {
                     const float p0 = softmax_term(fmaf(__uint_as_float(sr[c][i]), sl2, -m_sub));
                     const float p1 = softmax_term(fmaf(__uint_as_float(sr[c][i + 1]), sl2, -m_sub));
+                    const uint32_t w = pack2<BF16>(p0, p1);
+                    pk[c >> 1][(c & 1) * 16 + (i >> 1)] = w;
                     acc[(i >> 1) & 7] += p0 + p1;
-                    pk[c >> 1][(c & 1) * 16 + (i >> 1)] = pack2<BF16>(p0, p1);
+                    if constexpr (BF16) {
+                        // Also sum the weights the PV product actually uses (bf16 P
+                        // has a 2^-8 unit roundoff) and normalise O by that sum:
+                        // O is then an exact weighted mean of the value rows, and a
+                        // row dominated by one key returns that key's value row.
+                        accr[(i >> 1) & 3] += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+                    }
                 }
             }
             const float rs = ((acc[0] + acc[1]) + (acc[2] + acc[3])) +
                              ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+            if constexpr (BF16) lr = lr * alpha + ((accr[0] + accr[1]) + (accr[2] + accr[3]));
             tmem_st32(tS, pk[0]);
             tmem_st32(tS + 32, pk[1]);
 
@@ -362,7 +376,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         if (ok && n_t > 0 && warp_wait(&o_full[t], 0, abort_flag, p.status)) {
             tc_fence_after();
-            const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+            const float l_out = BF16 ? lr : l;
+            const float inv_l = l_out > 0.0f ? 1.0f / l_out : 0.0f;
             const int64_t grow = static_cast<int64_t>(group) * p.rows_per_group + row;
             uint16_t* out = static_cast<uint16_t*>(p.out) + grow * D;
 #pragma unroll
