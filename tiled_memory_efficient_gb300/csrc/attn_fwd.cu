@@ -53,6 +53,11 @@ struct FwdCfg {
     static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
     static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
     static constexpr int kOCol = 256;                        // first O column in TMEM
+    // With D=64 TMEM has room for P next to S and O, so S of the next key tile
+    // can be computed while the softmax still works on this one.  With D=128
+    // the four accumulators fill all 512 columns and P overwrites S.
+    static constexpr bool kSepP = (D == 64);
+    static constexpr int kPCol = 256 + 2 * D;                // P_t at kPCol + 64 t (kSepP)
 };
 
 // Flush-to-zero threshold in the log2 domain: a softmax term p = 2^x with
@@ -119,7 +124,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* s_full = v_empty + VS;   // [2] S_t ready in TMEM
     uint64_t* p_full = s_full + 2;     // [2] P_t in TMEM and O_t rescaled
     uint64_t* o_full = p_full + 2;     // [2] last PV of tile t done
-    uint64_t* mma_done = o_full + 2;   // every MMA of this CTA done
+    uint64_t* s_free = o_full + 2;     // [2] softmax has read S_t (kSepP)
+    uint64_t* pv_done = s_free + 2;    // [2] PV of tile t done (kSepP)
+    uint64_t* mma_done = pv_done + 2;  // every MMA of this CTA done
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -144,6 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&s_full[t], 1);
             mbar_init(&p_full[t], 128);
             mbar_init(&o_full[t], 1);
+            mbar_init(&s_free[t], 128);
+            mbar_init(&pv_done[t], 1);
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -225,8 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t b0 = dv0 + vslot * kTileStep;
 #pragma unroll
             for (int k = 0; k < kRows / 16; ++k)
-                mma_ts_elect(d, tmem + t * kRows + k * 8, b0 + k * (2048 >> 4), idesc_o,
-                             (j > 0 || k > 0) ? 1u : 0u);
+                mma_ts_elect(d, tmem + (C::kSepP ? C::kPCol + t * 64 : t * kRows) + k * 8,
+                             b0 + k * (2048 >> 4), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
         };
 
         bool ok = warp_wait(q_full, 0, abort_flag, p.status);
@@ -239,35 +248,70 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit_elect(&k_empty[0]);
             }
         }
-        for (int j = 0; ok && j < nmax; ++j) {
-            const int vslot = j % VS;
-            if (!warp_wait(&v_full[vslot], (j / VS) & 1, abort_flag, p.status)) break;
-            tc_fence_after();
-            const bool more = j + 1 < nmax;
-            const int kslot = (j + 1) % KS;
-            for (int t = 0; t < 2; ++t) {
-                if (j < nt[t]) {
-                    if (!warp_wait(&p_full[t], j & 1, abort_flag, p.status)) { ok = false; break; }
+        if constexpr (C::kSepP) {
+            // S of key tile j+1 is issued as soon as the softmax has read S of
+            // tile j (s_free), ahead of the PV products of tile j.
+            for (int j = 0; ok && j < nmax; ++j) {
+                if (j + 1 < nmax) {
+                    const int kslot = (j + 1) % KS;
+                    if (!warp_wait(&k_full[kslot], ((j + 1) / KS) & 1, abort_flag, p.status)) break;
                     tc_fence_after();
-                    issue_pv(t, vslot, j);
-                    if (j == nt[t] - 1) mma_commit_elect(&o_full[t]);
-                }
-                if (t == 0 && more) {
-                    // S_0 of the next key tile goes in between the two PVs so
-                    // that softmax of tile 0 overlaps PV of tile 1.
-                    if (!warp_wait(&k_full[kslot], ((j + 1) / KS) & 1, abort_flag, p.status)) {
-                        ok = false;
-                        break;
+                    for (int t = 0; t < 2; ++t) {
+                        if (j + 1 < nt[t]) {
+                            if (!warp_wait(&s_free[t], j & 1, abort_flag, p.status)) { ok = false; break; }
+                            tc_fence_after();
+                            issue_s(t, kslot);
+                        }
                     }
-                    tc_fence_after();
-                    if (j + 1 < nt[0]) issue_s(0, kslot);
+                    if (!ok) break;
+                    mma_commit_elect(&k_empty[kslot]);
                 }
+                const int vslot = j % VS;
+                if (!warp_wait(&v_full[vslot], (j / VS) & 1, abort_flag, p.status)) break;
+                tc_fence_after();
+                for (int t = 0; t < 2; ++t) {
+                    if (j < nt[t]) {
+                        if (!warp_wait(&p_full[t], j & 1, abort_flag, p.status)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_pv(t, vslot, j);
+                        mma_commit_elect(&pv_done[t]);
+                        if (j == nt[t] - 1) mma_commit_elect(&o_full[t]);
+                    }
+                }
+                if (!ok) break;
+                mma_commit_elect(&v_empty[vslot]);
             }
-            if (!ok) break;
-            mma_commit_elect(&v_empty[vslot]);
-            if (more) {
-                if (j + 1 < nt[1]) issue_s(1, kslot);
-                mma_commit_elect(&k_empty[kslot]);
+        } else {
+            for (int j = 0; ok && j < nmax; ++j) {
+                const int vslot = j % VS;
+                if (!warp_wait(&v_full[vslot], (j / VS) & 1, abort_flag, p.status)) break;
+                tc_fence_after();
+                const bool more = j + 1 < nmax;
+                const int kslot = (j + 1) % KS;
+                for (int t = 0; t < 2; ++t) {
+                    if (j < nt[t]) {
+                        if (!warp_wait(&p_full[t], j & 1, abort_flag, p.status)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_pv(t, vslot, j);
+                        if (j == nt[t] - 1) mma_commit_elect(&o_full[t]);
+                    }
+                    if (t == 0 && more) {
+                        // S_0 of the next key tile goes in between the two PVs so
+                        // that softmax of tile 0 overlaps PV of tile 1.
+                        if (!warp_wait(&k_full[kslot], ((j + 1) / KS) & 1, abort_flag, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        if (j + 1 < nt[0]) issue_s(0, kslot);
+                    }
+                }
+                if (!ok) break;
+                mma_commit_elect(&v_empty[vslot]);
+                if (more) {
+                    if (j + 1 < nt[1]) issue_s(1, kslot);
+                    mma_commit_elect(&k_empty[kslot]);
+                }
             }
         }
         mma_commit_elect(mma_done);
@@ -290,6 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t tS = tmem + lane_base + t * kRows;
         const uint32_t tO = tmem + lane_base + C::kOCol + t * D;
+        const uint32_t tP = C::kSepP ? tmem + lane_base + C::kPCol + t * 64 : tS;
         const float sl2 = p.scale_log2;
 
         float m = -INFINITY;  // running max (log2 domain, scaled) used for exponentiation
@@ -305,6 +350,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
+            if constexpr (C::kSepP) {
+                // S_t is in registers: the MMA warp may compute the next S_t.
+                tc_fence_before();
+                mbar_arrive(&s_free[t]);
+            }
 
             const int key0 = j * kRows;
             const bool need_mask = (key0 + kRows > p.Nk) || (CAUSAL && key0 + kRows - 1 > warp_min_pos);
@@ -343,18 +393,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // has a 2^-8 unit roundoff) and normalise O by that sum:
                         // O is then an exact weighted mean of the value rows, and a
                         // row dominated by one key returns that key's value row.
-                        accr[(i >> 1) & 3] += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+                        accr[(i >> 1) & 3] = add_bf16x2_f32(accr[(i >> 1) & 3], w);
                     }
                 }
             }
             const float rs = ((acc[0] + acc[1]) + (acc[2] + acc[3])) +
                              ((acc[4] + acc[5]) + (acc[6] + acc[7]));
             if constexpr (BF16) lr = lr * alpha + ((accr[0] + accr[1]) + (accr[2] + accr[3]));
-            tmem_st32(tS, pk[0]);
-            tmem_st32(tS + 32, pk[1]);
+            if constexpr (C::kSepP) {
+                // P_t and O_t are still in use by the PV product of tile j-1.
+                if (j > 0) {
+                    if (!warp_wait(&pv_done[t], (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+                    tc_fence_after();
+                }
+            }
+            tmem_st32(tP, pk[0]);
+            tmem_st32(tP + 32, pk[1]);
 
             // O_t must be rescaled before the next PV accumulates into it.  PV
-            // of key tile j-1 is complete: S_t of tile j was committed after it.
+            // of key tile j-1 is complete: with P over S, S_t of tile j was
+            // committed after it; with separate P, pv_done was waited above.
             if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {

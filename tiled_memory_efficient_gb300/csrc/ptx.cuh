@@ -307,6 +307,18 @@ __device__ __forceinline__ float lg2_approx(float x) {
     return y;
 }
 
+// acc + lo + hi, where lo/hi are the two bf16 halves of w (mixed-precision
+// adds: the bf16 operand is widened exactly, the sum is rounded in fp32).
+__device__ __forceinline__ float add_bf16x2_f32(float acc, uint32_t w) {
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %1;\n\t"
+        "add.rn.f32.bf16 %0, lo, %0;\n\t"
+        "add.rn.f32.bf16 %0, hi, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(w));
+    return acc;
+}
+
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     uint32_t r;
