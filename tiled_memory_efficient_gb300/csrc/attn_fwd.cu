@@ -220,10 +220,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t a0 = dq0 + t * kTileStep;
             const uint64_t b0 = dk0 + kslot * kTileStep;
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-                const uint64_t off = (k >> 2) * ((kRows * 128) >> 4) + (k & 3) * 2;
-                mma_ss_elect(d, a0 + off, b0 + off, idesc_s, k > 0 ? 1u : 0u);
-            }
+            for (int kb = 0; kb < KB; ++kb)   // 64 columns of D per call
+                mma_ss_k64(d, a0 + kb * ((kRows * 128) >> 4), b0 + kb * ((kRows * 128) >> 4),
+                           idesc_s, kb > 0 ? 1u : 0u);
             mma_commit_elect(&s_full[t]);
         };
         // O_t += P_t V: 8 MMAs of 16 keys; P_t from TMEM (8 columns per 16
@@ -232,10 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto issue_pv = [&](int t, int vslot, int j) {
             const uint32_t d = tmem + C::kOCol + t * D;
             const uint64_t b0 = dv0 + vslot * kTileStep;
-#pragma unroll
-            for (int k = 0; k < kRows / 16; ++k)
-                mma_ts_elect(d, tmem + (C::kSepP ? C::kPCol + t * 64 : t * kRows) + k * 8,
-                             b0 + k * (2048 >> 4), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
+            mma_ts_k128(d, tmem + (C::kSepP ? C::kPCol + t * 64 : t * kRows), b0, idesc_o,
+                        j > 0 ? 1u : 0u);
         };
 
         bool ok = warp_wait(q_full, 0, abort_flag, p.status);

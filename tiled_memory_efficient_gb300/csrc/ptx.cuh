@@ -61,6 +61,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As above, but a thread whose phase is not complete yet is suspended by the
+// hardware until it completes (or about `hint_ns` pass), so waiting warps do
+// not take issue slots from the warps that share their SM sub-partition.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+constexpr uint32_t kSuspendHintNs = 200000;  // 0.2 ms per suspension at most
+
 // Wait until the phase with the given parity has completed.  Bounded: gives up
 // after kWaitLimitNs (or at once when *abort is already set), sets *abort and
 // the device status word, and returns false.
@@ -69,15 +87,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const unsigned long long t0 = global_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(a, parity)) return true;
-        if ((it & 63u) == 0) {
-            if (*abort) return false;
-            if (global_ns() - t0 > kWaitLimitNs) {
-                *abort = 1;
-                atomicOr(status, kStatusTimeout);
-                return false;
-            }
+    for (;;) {
+        if (mbar_try_wait_sleep(a, parity, kSuspendHintNs)) return true;
+        if (*abort) return false;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            atomicOr(status, kStatusTimeout);
+            return false;
         }
     }
 }
@@ -87,9 +103,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
                                                   unsigned int* status) {
     const uint32_t a = smem_u32(bar);
     const unsigned long long t0 = global_ns();
-    for (uint32_t it = 0;; ++it) {
-        if (mbar_try_wait(a, parity)) return true;
-        if ((it & 63u) == 63u && global_ns() - t0 > kWaitLimitNs) {
+    for (;;) {
+        if (mbar_try_wait_sleep(a, parity, kSuspendHintNs)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) {
             atomicOr(status, kStatusTimeout);
             return false;
         }
@@ -189,6 +205,55 @@ __device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, u
         "setp.ne.b32 p, %4, 0;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Groups of MMAs along K from one asm block with a single elect: the K-major
+// operands of a 128-byte-swizzled tile advance by 32 bytes (descriptor +2) per
+// K=16 step and by a 16 KiB block (+1024) every four steps.  `acc` selects
+// accumulate for the first MMA; the others always accumulate.
+__device__ __forceinline__ void mma_ss_k64(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                           uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .b32 lid;\n\t.reg .pred e, p, t;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+        "elect.sync lid|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 t, 0, 0;\n\t"
+        "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
+        "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, t;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// O (+)= P V for 128 keys: 8 MMAs, A = P from TMEM (+8 columns per step), B =
+// V MN-major in shared memory (+16 rows = 2048 bytes = +128 per step).
+__device__ __forceinline__ void mma_ts_k128(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                            uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .b32 lid, a1, a2, a3, a4, a5, a6, a7;\n\t.reg .pred e, p, t;\n\t"
+        ".reg .b64 b1, b2, b3, b4, b5, b6, b7;\n\t"
+        "elect.sync lid|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 t, 0, 0;\n\t"
+        "add.s32 a1, %1, 8;\n\tadd.s32 a2, %1, 16;\n\tadd.s32 a3, %1, 24;\n\t"
+        "add.s32 a4, %1, 32;\n\tadd.s32 a5, %1, 40;\n\tadd.s32 a6, %1, 48;\n\t"
+        "add.s32 a7, %1, 56;\n\t"
+        "add.s64 b1, %2, 128;\n\tadd.s64 b2, %2, 256;\n\tadd.s64 b3, %2, 384;\n\t"
+        "add.s64 b4, %2, 512;\n\tadd.s64 b5, %2, 640;\n\tadd.s64 b6, %2, 768;\n\t"
+        "add.s64 b7, %2, 896;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], b4, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], b5, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], b6, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a7], b7, %3, t;\n\t}" ::"r"(d),
+        "r"(a), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
 
