@@ -180,11 +180,13 @@ int oracle_attn_fwd(const double *q, const double *k, const double *v,
 
 typedef struct {
     const double *q, *k, *v, *dout;
-    double *dq, *dk, *dv;
-    int64_t B, Hq, Hkv, Nq, Nk, D;
+    double *dq;
+    double *dk_part, *dv_part;     /* this thread's private [Nk, D] sums */
+    int64_t b, g;                  /* the KV-head unit */
+    int64_t Hq, Hkv, Nq, Nk, D;
     double scale;
     int causal;
-    int64_t unit_begin, unit_end;  /* units are (b, g) pairs: b*Hkv + g */
+    int64_t row_begin, row_end;    /* slice of the unit's G*Nq rows (head-major) */
     int status;
 } bwd_job_t;
 
@@ -193,54 +195,52 @@ static void *bwd_worker(void *arg)
     bwd_job_t *jb = (bwd_job_t *)arg;
     const int64_t D = jb->D, Nk = jb->Nk, Nq = jb->Nq;
     const int64_t G = jb->Hq / jb->Hkv;
+    const int64_t b = jb->b, g = jb->g;
     double *p = (double *)malloc((size_t)Nk * sizeof(double));
     double *dp = (double *)malloc((size_t)Nk * sizeof(double));
     if (!p || !dp) { free(p); free(dp); jb->status = -2; return NULL; }
-    for (int64_t u = jb->unit_begin; u < jb->unit_end; ++u) {
-        const int64_t b = u / jb->Hkv, g = u % jb->Hkv;
-        const double *k_head = jb->k + u * Nk * D;
-        const double *v_head = jb->v + u * Nk * D;
-        double *dk_head = jb->dk + u * Nk * D;
-        double *dv_head = jb->dv + u * Nk * D;
-        memset(dk_head, 0, (size_t)(Nk * D) * sizeof(double));
-        memset(dv_head, 0, (size_t)(Nk * D) * sizeof(double));
-        for (int64_t hl = 0; hl < G; ++hl) {
-            const int64_t h = g * G + hl;
-            for (int64_t i = 0; i < Nq; ++i) {
-                const int64_t r = (b * jb->Hq + h) * Nq + i;
-                const double *q_row = jb->q + r * D;
-                const double *do_row = jb->dout + r * D;
-                double *dq_row = jb->dq + r * D;
-                const int64_t nkeys = allowed_keys(i, Nk, jb->causal);
-                /* scores and their log-sum-exp, as in the forward definition */
-                double m = -INFINITY;
-                for (int64_t j = 0; j < nkeys; ++j) {
-                    double dot = 0.0;
-                    for (int64_t d = 0; d < D; ++d) dot += q_row[d] * k_head[j * D + d];
-                    p[j] = jb->scale * dot;
-                    if (p[j] > m) m = p[j];
-                }
-                double l = 0.0;
-                for (int64_t j = 0; j < nkeys; ++j) l += exp(p[j] - m);
-                const double lse = m + log(l);
-                /* P, dP and Delta */
-                double delta = 0.0;
-                for (int64_t j = 0; j < nkeys; ++j) {
-                    p[j] = exp(p[j] - lse);
-                    double dot = 0.0;
-                    for (int64_t d = 0; d < D; ++d) dot += do_row[d] * v_head[j * D + d];
-                    dp[j] = dot;
-                    delta += p[j] * dp[j];
-                }
-                for (int64_t d = 0; d < D; ++d) dq_row[d] = 0.0;
-                for (int64_t j = 0; j < nkeys; ++j) {
-                    const double ds = p[j] * (dp[j] - delta);
-                    for (int64_t d = 0; d < D; ++d) {
-                        dq_row[d] += jb->scale * ds * k_head[j * D + d];
-                        dk_head[j * D + d] += jb->scale * ds * q_row[d];
-                        dv_head[j * D + d] += p[j] * do_row[d];
-                    }
-                }
+    const int64_t u = b * jb->Hkv + g;
+    const double *k_head = jb->k + u * Nk * D;
+    const double *v_head = jb->v + u * Nk * D;
+    double *dk_head = jb->dk_part;
+    double *dv_head = jb->dv_part;
+    memset(dk_head, 0, (size_t)(Nk * D) * sizeof(double));
+    memset(dv_head, 0, (size_t)(Nk * D) * sizeof(double));
+    for (int64_t fr = jb->row_begin; fr < jb->row_end; ++fr) {
+        const int64_t hl = fr / Nq, i = fr % Nq;
+        const int64_t h = g * G + hl;
+        const int64_t r = (b * jb->Hq + h) * Nq + i;
+        const double *q_row = jb->q + r * D;
+        const double *do_row = jb->dout + r * D;
+        double *dq_row = jb->dq + r * D;
+        const int64_t nkeys = allowed_keys(i, Nk, jb->causal);
+        /* scores and their log-sum-exp, as in the forward definition */
+        double m = -INFINITY;
+        for (int64_t j = 0; j < nkeys; ++j) {
+            double dot = 0.0;
+            for (int64_t d = 0; d < D; ++d) dot += q_row[d] * k_head[j * D + d];
+            p[j] = jb->scale * dot;
+            if (p[j] > m) m = p[j];
+        }
+        double l = 0.0;
+        for (int64_t j = 0; j < nkeys; ++j) l += exp(p[j] - m);
+        const double lse = m + log(l);
+        /* P, dP and Delta */
+        double delta = 0.0;
+        for (int64_t j = 0; j < nkeys; ++j) {
+            p[j] = exp(p[j] - lse);
+            double dot = 0.0;
+            for (int64_t d = 0; d < D; ++d) dot += do_row[d] * v_head[j * D + d];
+            dp[j] = dot;
+            delta += p[j] * dp[j];
+        }
+        for (int64_t d = 0; d < D; ++d) dq_row[d] = 0.0;
+        for (int64_t j = 0; j < nkeys; ++j) {
+            const double ds = p[j] * (dp[j] - delta);
+            for (int64_t d = 0; d < D; ++d) {
+                dq_row[d] += jb->scale * ds * k_head[j * D + d];
+                dk_head[j * D + d] += jb->scale * ds * q_row[d];
+                dv_head[j * D + d] += p[j] * do_row[d];
             }
         }
     }
@@ -250,8 +250,10 @@ static void *bwd_worker(void *arg)
 }
 
 /*
- * Full backward from the definition.  Threads split the (b, g) KV-head units,
- * so every dk/dv row is written by exactly one thread.
+ * Full backward from the definition.  For each KV-head unit (b, g) the
+ * unit's G*Nq query rows are split among the threads; every thread sums its
+ * rows' contributions to dk/dv in a private buffer, and the buffers are added
+ * up after the join, so no two threads ever write the same element.
  */
 int oracle_attn_bwd(const double *q, const double *k, const double *v, const double *dout,
                     int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t D,
@@ -260,31 +262,50 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v, const dou
 {
     if (check_shape(B, Hq, Hkv, Nq, Nk, D)) return -1;
     if (!q || !k || !v || !dout || !dq || !dk || !dv) return -1;
-    const int64_t units = B * Hkv;
+    const int64_t G = Hq / Hkv;
+    const int64_t unit_rows = G * Nq;
     if (nthreads < 1) nthreads = 1;
-    if (nthreads > units) nthreads = (int)units;
+    if (nthreads > unit_rows) nthreads = (int)unit_rows;
     bwd_job_t *jobs = (bwd_job_t *)calloc((size_t)nthreads, sizeof(bwd_job_t));
     pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
-    if (!jobs || !tids) { free(jobs); free(tids); return -2; }
-    for (int t = 0; t < nthreads; ++t) {
-        bwd_job_t *jb = &jobs[t];
-        jb->q = q; jb->k = k; jb->v = v; jb->dout = dout;
-        jb->dq = dq; jb->dk = dk; jb->dv = dv;
-        jb->B = B; jb->Hq = Hq; jb->Hkv = Hkv; jb->Nq = Nq; jb->Nk = Nk; jb->D = D;
-        jb->scale = scale; jb->causal = causal;
-        jb->unit_begin = units * t / nthreads;
-        jb->unit_end = units * (t + 1) / nthreads;
-        jb->status = -2;
+    double *parts = (double *)malloc((size_t)nthreads * 2 * (size_t)(Nk * D) * sizeof(double));
+    if (!jobs || !tids || !parts) { free(jobs); free(tids); free(parts); return -2; }
+    int rc = 0;
+    for (int64_t b = 0; b < B && rc == 0; ++b) {
+        for (int64_t g = 0; g < Hkv && rc == 0; ++g) {
+            for (int t = 0; t < nthreads; ++t) {
+                bwd_job_t *jb = &jobs[t];
+                jb->q = q; jb->k = k; jb->v = v; jb->dout = dout; jb->dq = dq;
+                jb->dk_part = parts + (size_t)(2 * t) * (size_t)(Nk * D);
+                jb->dv_part = parts + (size_t)(2 * t + 1) * (size_t)(Nk * D);
+                jb->b = b; jb->g = g;
+                jb->Hq = Hq; jb->Hkv = Hkv; jb->Nq = Nq; jb->Nk = Nk; jb->D = D;
+                jb->scale = scale; jb->causal = causal;
+                jb->row_begin = unit_rows * t / nthreads;
+                jb->row_end = unit_rows * (t + 1) / nthreads;
+                jb->status = -2;
+            }
+            for (int t = 1; t < nthreads; ++t)
+                if (pthread_create(&tids[t], NULL, bwd_worker, &jobs[t]) != 0) jobs[t].status = 1;
+            bwd_worker(&jobs[0]);
+            if (jobs[0].status != 0) rc = jobs[0].status;
+            for (int t = 1; t < nthreads; ++t) {
+                if (jobs[t].status == 1) { bwd_worker(&jobs[t]); }
+                else pthread_join(tids[t], NULL);
+                if (jobs[t].status != 0) rc = jobs[t].status;
+            }
+            const int64_t u = b * Hkv + g;
+            for (int64_t e = 0; e < Nk * D; ++e) {
+                double sk = 0.0, sv = 0.0;
+                for (int t = 0; t < nthreads; ++t) {
+                    sk += jobs[t].dk_part[e];
+                    sv += jobs[t].dv_part[e];
+                }
+                dk[u * Nk * D + e] = sk;
+                dv[u * Nk * D + e] = sv;
+            }
+        }
     }
-    for (int t = 1; t < nthreads; ++t)
-        if (pthread_create(&tids[t], NULL, bwd_worker, &jobs[t]) != 0) jobs[t].status = 1;
-    bwd_worker(&jobs[0]);
-    int rc = jobs[0].status;
-    for (int t = 1; t < nthreads; ++t) {
-        if (jobs[t].status == 1) { bwd_worker(&jobs[t]); }
-        else pthread_join(tids[t], NULL);
-        if (jobs[t].status != 0) rc = jobs[t].status;
-    }
-    free(jobs); free(tids);
+    free(jobs); free(tids); free(parts);
     return rc;
 }

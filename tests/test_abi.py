@@ -64,6 +64,8 @@ def test_fwd_rejects_without_launch(lib, args, code):
 def test_bwd_validation_and_workspace(lib):
     ws = lib.attn_bwd_workspace_size(2, 16, 16, 8192, 8192, 128, 1)
     assert ws >= 2 * 16 * 8192 * 2 * 4 and ws % 256 == 0
+    # per-group rows padded to a multiple of 128: G*Nq = 7*37 = 259 -> 384
+    assert lib.attn_bwd_workspace_size(1, 7, 1, 37, 37, 64, 0) == 2 * 384 * 4
     assert lib.attn_bwd_workspace_size(1, 3, 2, 10, 10, 64, 0) == 0
     base = [P] * 9
     # workspace too small

@@ -1,0 +1,100 @@
+"""Backward parity on the GPU: dQ, dK, dV from the CUDA path (forward then
+backward, through the C ABI) against the fp64 oracle's gradients on the same
+seeded, rounded inputs.  Small shapes are checked in full; the training
+workload (B=2, H=16, N=8192, D=128, bf16, causal) on two whole sampled heads,
+each of which is an independent problem (MHA), at the full sequence length.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import helpers
+from tiled_memory_efficient_gb300 import _lib, inputs
+
+pytestmark = pytest.mark.gpu
+
+F16, BF16 = torch.float16, torch.bfloat16
+
+
+def gpu_grads(x, causal, scale=None):
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    out, lse = _lib.attn_fwd(q, k, v, causal=causal, scale=scale)
+    dq, dk, dv = _lib.attn_bwd(q, k, v, out, do, lse, causal=causal, scale=scale)
+    assert _lib.sync_status() == _lib.ATTN_OK
+    return dq, dk, dv
+
+
+def check(got, ref, dtype, what):
+    tol = helpers.TOL_BWD[dtype]
+    errs = []
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        errs.append(helpers.assert_close_elementwise(
+            g.double().cpu().numpy(), r, tol, dtype, what, name))
+    return errs
+
+
+SMALL = [
+    # B, Hq, Hkv, Nq, Nk, D, dtype, causal
+    (1, 2, 2, 128, 128, 64, F16, False),
+    (1, 2, 2, 256, 256, 128, BF16, True),
+    (1, 2, 2, 300, 300, 64, F16, True),      # ragged tail
+    (2, 4, 2, 200, 333, 64, BF16, False),    # GQA G=2, Nq != Nk, ragged
+    (1, 14, 2, 250, 250, 64, F16, True),     # GQA G=7, tiles cross head boundaries
+    (1, 7, 1, 37, 37, 128, BF16, True),      # tiny heads flattened into one tile
+    (1, 2, 2, 129, 700, 128, F16, True),     # Nq < Nk (late key tiles see no query)
+    (1, 3, 3, 1, 1, 64, F16, False),         # single query and key
+    (1, 2, 2, 1024, 1024, 128, BF16, True),  # several tiles each way
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,D,dtype,causal", SMALL)
+def test_backward_small_shapes(cuda_lib, B, Hq, Hkv, Nq, Nk, D, dtype, causal):
+    x = inputs.make_custom(B, Hq, Hkv, Nq, Nk, D, dtype, seed=3 * Nq + Nk + D, with_grad=True)
+    got = gpu_grads(x, causal)
+    ref = oracle.attention_bwd(x["q"], x["k"], x["v"], x["do"], causal=causal)
+    errs = check(got, ref, dtype, f"{(B, Hq, Hkv, Nq, Nk, D, dtype, causal)}")
+    print(f"{(B, Hq, Hkv, Nq, Nk, D, str(dtype), causal)}: max err dq/dk/dv = {errs}")
+
+
+def test_backward_explicit_scale(cuda_lib):
+    x = inputs.make_custom(1, 2, 2, 256, 256, 64, F16, seed=77, with_grad=True)
+    got = gpu_grads(x, False, scale=0.2)
+    ref = oracle.attention_bwd(x["q"], x["k"], x["v"], x["do"], causal=False, scale=0.2)
+    check(got, ref, F16, "scale=0.2")
+
+
+def test_training_workload_sampled_heads(cuda_lib):
+    w = inputs.WORKLOADS["training"]
+    n = w.seq_lens[0]
+    x = inputs.make_inputs(w, n)
+    dq, dk, dv = gpu_grads(x, w.causal)
+    for b, h in ((0, 3), (1, 11)):
+        sl = {m: x[m][b:b + 1, h:h + 1] for m in ("q", "k", "v", "do")}
+        ref = oracle.attention_bwd(sl["q"], sl["k"], sl["v"], sl["do"], causal=w.causal)
+        got = (dq[b:b + 1, h:h + 1], dk[b:b + 1, h:h + 1], dv[b:b + 1, h:h + 1])
+        errs = check(got, ref, w.dtype, f"training head b={b} h={h}")
+        print(f"training N={n} head ({b},{h}): max err dq/dk/dv = {errs}")
+
+
+def test_backward_deterministic(cuda_lib):
+    x = inputs.make_custom(1, 4, 2, 500, 500, 128, BF16, seed=21, with_grad=True)
+    g1 = gpu_grads(x, True)
+    g2 = gpu_grads(x, True)
+    for a, b in zip(g1, g2):
+        assert torch.equal(a, b)
+
+
+def test_backward_workspace_contents_do_not_matter(cuda_lib):
+    x = inputs.make_custom(1, 2, 2, 300, 300, 64, F16, seed=22, with_grad=True)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    out, lse = _lib.attn_fwd(q, k, v, causal=True)
+    lib = _lib.load()
+    ws_bytes = lib.attn_bwd_workspace_size(1, 2, 2, 300, 300, 64, 0)
+    res = []
+    for fill in (0, 255):
+        ws = torch.full((ws_bytes,), fill, device="cuda", dtype=torch.uint8)
+        res.append(_lib.attn_bwd(q, k, v, out, do, lse, causal=True, workspace=ws))
+    assert _lib.sync_status() == _lib.ATTN_OK
+    for a, b in zip(*res):
+        assert torch.equal(a, b)

@@ -162,17 +162,18 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, 
 extern "C" size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int D,
                                           int dtype) {
     if (check_shape(B, Hq, Hkv, Nq, Nk, D, 1.0f, dtype) != ATTN_OK) return 0;
-    // Two fp32 values per query row (log2-domain LSE and Delta), padded to 256 bytes.
-    const size_t rows = static_cast<size_t>(B) * Hq * Nq;
-    return ((rows * 2 * sizeof(float)) + 255) & ~static_cast<size_t>(255);
+    // Two fp32 arrays (LSE * log2(e) and rowsum(dO * O)), each laid out per
+    // KV group with the group's rows padded to a multiple of 128.
+    const size_t groups = static_cast<size_t>(B) * Hkv;
+    const size_t rows = static_cast<size_t>(Hq / Hkv) * Nq;
+    const size_t rows_pad = (rows + 127) / 128 * 128;
+    return (2 * groups * rows_pad * sizeof(float) + 255) & ~static_cast<size_t>(255);
 }
 
 extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* out,
                         const void* dout, const float* lse, void* dq, void* dk, void* dv,
                         void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int Nq,
                         int Nk, int D, float scale, int causal, int dtype, void* stream) {
-    (void)causal;
-    (void)stream;
     if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv || !workspace)
         return ATTN_ERR_INVALID;
     int rc = check_shape(B, Hq, Hkv, Nq, Nk, D, scale, dtype);
@@ -182,7 +183,46 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
         if (!aligned16(ptr)) return ATTN_ERR_ALIGN;
     if (workspace_bytes < attn_bwd_workspace_size(B, Hq, Hkv, Nq, Nk, D, dtype))
         return ATTN_ERR_WORKSPACE;
-    return ATTN_ERR_UNSUPPORTED;
+    unsigned int* status = nullptr;
+    rc = device_setup(&status);
+    if (rc != ATTN_OK) return rc;
+
+    const bool bf16 = dtype == ATTN_BF16;
+    const int64_t G = Hq / Hkv;
+    const int64_t rows = G * Nq;
+    const int64_t groups = static_cast<int64_t>(B) * Hkv;
+    const int64_t n_qtiles = (rows + 127) / 128;
+    CUtensorMap tmQ, tmK, tmV, tmDO;
+    if (make_map(&tmQ, q, bf16, D, rows, groups) != ATTN_OK ||
+        make_map(&tmDO, dout, bf16, D, rows, groups) != ATTN_OK ||
+        make_map(&tmK, k, bf16, D, Nk, groups) != ATTN_OK ||
+        make_map(&tmV, v, bf16, D, Nk, groups) != ATTN_OK)
+        return ATTN_ERR_CUDA;
+    BwdParams p{};
+    p.out = out;
+    p.dout = dout;
+    p.lse = lse;
+    p.lse2 = static_cast<float*>(workspace);
+    p.delta = p.lse2 + groups * n_qtiles * 128;
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.status = status;
+    p.rows_per_group = rows;
+    p.rows_pad = n_qtiles * 128;
+    p.total_rows = rows * groups;
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.n_groups = static_cast<int>(groups);
+    p.n_qtiles = static_cast<int>(n_qtiles);
+    p.n_ktiles = (Nk + 127) / 128;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    if (groups * p.n_ktiles > 0x7fffffffll || groups * n_qtiles > 0x7fffffffll)
+        return ATTN_ERR_UNSUPPORTED;
+    const cudaError_t e = launch_bwd(D, bf16, causal != 0, tmQ, tmK, tmV, tmDO, p,
+                                     static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 extern "C" int attn_sync_status(void* stream) {

@@ -1,0 +1,570 @@
+// attn_bwd.cu -- backward of tiled scaled-dot-product attention for sm_103a.
+//
+// The autograd tier of the method (noflash-attention forum post,
+// ai-navigate-news, section "Other areas where this could be useful": the
+// tiled attention supports autograd, so its memory savings carry over to
+// training).  Like the forward it never forms the N x N matrices: scores and
+// probabilities are recomputed tile by tile from the forward's LSE.
+//
+// With s = scale * q.k, P = exp(s - LSE), dP = dO V^T, Delta = rowsum(dO * O):
+//   dS = P * (dP - Delta),  dV = P^T dO,  dK = scale * dS^T Q,  dQ = scale * dS K.
+// Three kernels, all deterministic (no atomics):
+//   1. statistics: Delta and LSE*log2(e) per query row into the workspace;
+//   2. dK/dV, KV-stationary: one CTA per (KV group, 128-key tile) loops over
+//      the query tiles of every head of the group (so GQA gradients are summed
+//      inside the CTA): S^T = K Q^T and dP^T = V dO^T on the tensor core, P^T
+//      and dS^T elementwise (one thread per key row), then dV += P^T dO and
+//      dK += dS^T Q with P^T / dS^T read from TMEM;
+//   3. dQ, Q-stationary: one CTA per (KV group, 128-row query tile) loops over
+//      key tiles: S = Q K^T, dP = dO V^T, dS elementwise, dQ += dS K.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "attn_internal.h"
+#include "ptx.cuh"
+
+namespace tme {
+namespace {
+
+constexpr int kRows = 128;
+constexpr int kThreads = 192;  // 4 elementwise warps + producer + MMA issuer
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+    if constexpr (BF16) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    } else {
+        __half2 h = *reinterpret_cast<const __half2*>(&w);
+        return __half22float2(h);
+    }
+}
+
+// ---------------------------------------------------------------- statistics
+// One query row per D/8 lanes (16-byte loads): delta = sum_d dO * O in fp32,
+// lse2 = LSE * log2(e).  Output rows go to the per-group padded layout.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) bwd_stats_kernel(const BwdParams p) {
+    constexpr int LPR = D / 8;
+    const int64_t gt = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t row = gt / LPR;
+    const int sub = static_cast<int>(gt % LPR);
+    float acc = 0.0f;
+    if (row < p.total_rows) {
+        const uint4 o = *reinterpret_cast<const uint4*>(
+            static_cast<const uint16_t*>(p.out) + row * D + sub * 8);
+        const uint4 g = *reinterpret_cast<const uint4*>(
+            static_cast<const uint16_t*>(p.dout) + row * D + sub * 8);
+        const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+        const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 a = unpack2<BF16>(ow[i]);
+            const float2 b = unpack2<BF16>(gw[i]);
+            acc = fmaf(a.x, b.x, acc);
+            acc = fmaf(a.y, b.y, acc);
+        }
+    }
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (row < p.total_rows && sub == 0) {
+        const int64_t g = row / p.rows_per_group, r = row % p.rows_per_group;
+        p.delta[g * p.rows_pad + r] = acc;
+        p.lse2[g * p.rows_pad + r] = p.lse[row] * kLog2e;
+    }
+}
+
+// Query position of column q of a 128-row tile whose first row has position
+// `base` (rows are head-major within the group, so positions wrap at Nq).
+__device__ __forceinline__ int tile_pos(int base, int q, int Nq) {
+    const int ps = base + q;
+    if (Nq >= kRows) return ps >= Nq ? ps - Nq : ps;  // at most one wrap per tile
+    return ps % Nq;
+}
+
+// Largest query position in the tile that starts at `row0`.
+__device__ __forceinline__ int tile_max_pos(int64_t row0, const BwdParams& p) {
+    const int64_t last = min(row0 + kRows - 1, p.rows_per_group - 1);
+    return (row0 / p.Nq == last / p.Nq) ? static_cast<int>(last % p.Nq) : p.Nq - 1;
+}
+
+template <int D>
+struct BwdCfg {
+    static constexpr int kTileBytes = kRows * D * 2;
+    static constexpr int kKB = D / 64;
+};
+
+// ---------------------------------------------------------------- dK / dV
+// TMEM: S^T [0,128) (P^T over its first 64 columns), dP^T [128,256) (dS^T over
+// its first 64 columns), dV [256,256+D), dK [256+D,256+2D).
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
+                    const __grid_constant__ CUtensorMap tmDO,
+                    const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const BwdParams p) {
+    using C = BwdCfg<D>;
+    constexpr int TB = C::kTileBytes, KB = C::kKB, QS = 2;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sK = smem;
+    uint8_t* sV = sK + TB;
+    uint8_t* sQ = sV + TB;             // [QS]
+    uint8_t* sDO = sQ + QS * TB;       // [QS]
+    float* sL = reinterpret_cast<float*>(sDO + QS * TB);  // [QS][128] lse2 of the query tile
+    float* sDl = sL + QS * kRows;                          // [QS][128] delta
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sDl + QS * kRows);
+    uint64_t* kv_full = bars;
+    uint64_t* q_full = kv_full + 1;    // [QS]
+    uint64_t* q_empty = q_full + QS;   // [QS]
+    uint64_t* s_full = q_empty + QS;   // S^T and dP^T in TMEM
+    uint64_t* p_full = s_full + 1;     // P^T and dS^T in TMEM (128 arrivals)
+    uint64_t* acc_full = p_full + 1;   // last dV / dK product done
+    uint64_t* mma_done = acc_full + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Heaviest first: under the causal mask low key tiles meet the most queries.
+    const int group = static_cast<int>(blockIdx.x / p.n_ktiles);
+    const int kt = static_cast<int>(blockIdx.x % p.n_ktiles);
+    const int key0 = kt * kRows;
+    auto visit = [&](int qi) {
+        return !CAUSAL || tile_max_pos(static_cast<int64_t>(qi) * kRows, p) >= key0;
+    };
+
+    if (threadIdx.x == 0) {
+        mbar_init(kv_full, 1);
+        for (int i = 0; i < QS; ++i) { mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1); }
+        mbar_init(s_full, 1);
+        mbar_init(p_full, 128);
+        mbar_init(acc_full, 1);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) tmem_alloc(tmem_slot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmDO);
+            mbar_arrive_expect_tx(kv_full, 2 * TB);
+            for (int kb = 0; kb < KB; ++kb) {
+                tma_load_3d(&tmK, kv_full, sK + kb * (kRows * 128), kb * 64, key0, group);
+                tma_load_3d(&tmV, kv_full, sV + kb * (kRows * 128), kb * 64, key0, group);
+            }
+            int n = 0;
+            for (int qi = 0; qi < p.n_qtiles; ++qi) {
+                if (!visit(qi)) continue;
+                const int slot = n % QS;
+                if (!mbar_wait(&q_empty[slot], ((n / QS) & 1) ^ 1, abort_flag, p.status)) break;
+                mbar_arrive_expect_tx(&q_full[slot], 2 * TB + 2 * kRows * 4);
+                for (int kb = 0; kb < KB; ++kb) {
+                    tma_load_3d(&tmQ, &q_full[slot], sQ + slot * TB + kb * (kRows * 128), kb * 64,
+                                qi * kRows, group);
+                    tma_load_3d(&tmDO, &q_full[slot], sDO + slot * TB + kb * (kRows * 128),
+                                kb * 64, qi * kRows, group);
+                }
+                const int64_t w0 = static_cast<int64_t>(group) * p.rows_pad + qi * kRows;
+                bulk_load(sL + slot * kRows, p.lse2 + w0, kRows * 4, &q_full[slot]);
+                bulk_load(sDl + slot * kRows, p.delta + w0, kRows * 4, &q_full[slot]);
+                ++n;
+            }
+            mbar_wait_bounded(kv_full, 0, p.status);
+            for (int m = (n > QS ? n - QS : 0); m < n; ++m)
+                mbar_wait_bounded(&q_full[m % QS], (m / QS) & 1, p.status);
+        }
+    } else if (warp == kMmaWarp) {
+        constexpr uint32_t idesc_s = idesc_f16(kRows, kRows, BF16, false);
+        constexpr uint32_t idesc_g = idesc_f16(kRows, D, BF16, true);
+        constexpr uint64_t kStep = TB >> 4;
+        constexpr uint64_t kBlk = (kRows * 128) >> 4;
+        const uint64_t dK_ = smem_desc_sw128(smem_u32(sK), 16, 1024);
+        const uint64_t dV_ = smem_desc_sw128(smem_u32(sV), 16, 1024);
+        const uint64_t dQk = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+        const uint64_t dDOk = smem_desc_sw128(smem_u32(sDO), 16, 1024);
+        const uint64_t dQm = smem_desc_sw128(smem_u32(sQ), kRows * 128, 1024);
+        const uint64_t dDOm = smem_desc_sw128(smem_u32(sDO), kRows * 128, 1024);
+        warp_wait(kv_full, 0, abort_flag, p.status);
+        int n = 0;
+        for (int qi = 0; qi < p.n_qtiles; ++qi) {
+            if (!visit(qi)) continue;
+            const int slot = n % QS;
+            warp_wait(&q_full[slot], (n / QS) & 1, abort_flag, p.status);
+            tc_fence_after();
+#pragma unroll
+            for (int kb = 0; kb < KB; ++kb)   // S^T = K Q^T
+                mma_ss_k64(tmem, dK_ + kb * kBlk, dQk + slot * kStep + kb * kBlk, idesc_s,
+                           kb > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kb = 0; kb < KB; ++kb)   // dP^T = V dO^T
+                mma_ss_k64(tmem + 128, dV_ + kb * kBlk, dDOk + slot * kStep + kb * kBlk, idesc_s,
+                           kb > 0 ? 1u : 0u);
+            mma_commit_elect(s_full);
+            warp_wait(p_full, n & 1, abort_flag, p.status);
+            tc_fence_after();
+            mma_ts_k128(tmem + 256, tmem, dDOm + slot * kStep, idesc_g, n > 0 ? 1u : 0u);
+            mma_ts_k128(tmem + 256 + D, tmem + 128, dQm + slot * kStep, idesc_g, n > 0 ? 1u : 0u);
+            mma_commit_elect(&q_empty[slot]);
+            ++n;
+        }
+        mma_commit_elect(acc_full);
+        mma_commit_elect(mma_done);
+        mbar_wait_bounded(mma_done, 0, p.status);
+    } else {
+        // one thread per key row of the tile; lanes of warp w are TMEM lanes 32w..32w+31
+        const int key = key0 + warp * 32 + lane;
+        const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t tS = tmem + lb, tDP = tmem + lb + 128;
+        const float sl2 = p.scale_log2;
+        int n = 0;
+        for (int qi = 0; qi < p.n_qtiles; ++qi) {
+            if (!visit(qi)) continue;
+            const int slot = n % QS;
+            warp_wait(&q_full[slot], (n / QS) & 1, abort_flag, p.status);
+            warp_wait(s_full, n & 1, abort_flag, p.status);
+            tc_fence_after();
+            const int64_t row0 = static_cast<int64_t>(qi) * kRows;
+            const int base = static_cast<int>(row0 % p.Nq);
+            const float* L = sL + slot * kRows;
+            const float* Dl = sDl + slot * kRows;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t sv[32], dp[32];
+                tmem_ld32(tS + c * 32, sv);
+                tmem_ld32(tDP + c * 32, dp);
+                tmem_wait_ld();
+                reg_fence(sv);
+                reg_fence(dp);
+                uint32_t pw[16], dw[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    float pp[2], dd[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int q = c * 32 + i + u;
+                        bool ok = (row0 + q < p.rows_per_group) && (key < p.Nk);
+                        if (CAUSAL) ok = ok && key <= tile_pos(base, q, p.Nq);
+                        const float pr = ex2_ftz(fmaf(__uint_as_float(sv[i + u]), sl2, -L[q]));
+                        pp[u] = ok ? pr : 0.0f;
+                        dd[u] = ok ? pr * (__uint_as_float(dp[i + u]) - Dl[q]) : 0.0f;
+                    }
+                    pw[i >> 1] = pack2<BF16>(pp[0], pp[1]);
+                    dw[i >> 1] = pack2<BF16>(dd[0], dd[1]);
+                }
+                // packed P^T / dS^T of query columns 32c.. go to TMEM columns 16c..,
+                // which hold scores already read into registers.
+                tmem_st16(tS + c * 16, pw);
+                tmem_st16(tDP + c * 16, dw);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(p_full);
+            ++n;
+        }
+        // epilogue: dV and scale * dK of this key row
+        const bool ok = *abort_flag == 0;
+        const int64_t grow = static_cast<int64_t>(group) * p.Nk + key;
+        uint16_t* dvp = static_cast<uint16_t*>(p.dv) + grow * D;
+        uint16_t* dkp = static_cast<uint16_t*>(p.dk) + grow * D;
+        if (n > 0) warp_wait(acc_full, 0, abort_flag, p.status);
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t a[32], b[32];
+            if (n > 0) {
+                tmem_ld32(tmem + lb + 256 + c * 32, a);
+                tmem_ld32(tmem + lb + 256 + D + c * 32, b);
+                tmem_wait_ld();
+                reg_fence(a);
+                reg_fence(b);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) a[i] = b[i] = 0u;
+            }
+            if (ok && key < p.Nk) {
+                uint32_t wv[16], wk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    wv[i] = pack2<BF16>(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+                    wk[i] = pack2<BF16>(__uint_as_float(b[2 * i]) * p.scale,
+                                        __uint_as_float(b[2 * i + 1]) * p.scale);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    reinterpret_cast<uint4*>(dvp + c * 32)[i] =
+                        make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
+                    reinterpret_cast<uint4*>(dkp + c * 32)[i] =
+                        make_uint4(wk[4 * i], wk[4 * i + 1], wk[4 * i + 2], wk[4 * i + 3]);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ---------------------------------------------------------------- dQ
+// TMEM: S [0,128), dP [128,256) (dS over its first 64 columns), dQ [256,256+D).
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
+                  const __grid_constant__ CUtensorMap tmDO,
+                  const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const BwdParams p) {
+    using C = BwdCfg<D>;
+    constexpr int TB = C::kTileBytes, KB = C::kKB, KS = 2;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sQ = smem;
+    uint8_t* sDO = sQ + TB;
+    uint8_t* sK = sDO + TB;           // [KS]
+    uint8_t* sV = sK + KS * TB;       // [KS]
+    float* sL = reinterpret_cast<float*>(sV + KS * TB);
+    float* sDl = sL + kRows;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sDl + kRows);
+    uint64_t* q_full = bars;
+    uint64_t* kv_full = q_full + 1;   // [KS]
+    uint64_t* kv_empty = kv_full + KS;  // [KS]
+    uint64_t* s_full = kv_empty + KS;
+    uint64_t* p_full = s_full + 1;
+    uint64_t* acc_full = p_full + 1;
+    uint64_t* mma_done = acc_full + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int group = static_cast<int>(blockIdx.x / p.n_qtiles);
+    const int qi = p.n_qtiles - 1 - static_cast<int>(blockIdx.x % p.n_qtiles);
+    const int64_t row0 = static_cast<int64_t>(qi) * kRows;
+    int nkv = (p.Nk + kRows - 1) / kRows;
+    if (CAUSAL) {
+        const int keys = min(tile_max_pos(row0, p) + 1, p.Nk);
+        nkv = (keys + kRows - 1) / kRows;
+    }
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int i = 0; i < KS; ++i) { mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 1); }
+        mbar_init(s_full, 1);
+        mbar_init(p_full, 128);
+        mbar_init(acc_full, 1);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) tmem_alloc(tmem_slot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            mbar_arrive_expect_tx(q_full, 2 * TB + 2 * kRows * 4);
+            for (int kb = 0; kb < KB; ++kb) {
+                tma_load_3d(&tmQ, q_full, sQ + kb * (kRows * 128), kb * 64, qi * kRows, group);
+                tma_load_3d(&tmDO, q_full, sDO + kb * (kRows * 128), kb * 64, qi * kRows, group);
+            }
+            const int64_t w0 = static_cast<int64_t>(group) * p.rows_pad + row0;
+            bulk_load(sL, p.lse2 + w0, kRows * 4, q_full);
+            bulk_load(sDl, p.delta + w0, kRows * 4, q_full);
+            int n = 0;
+            for (int j = 0; j < nkv; ++j) {
+                const int slot = j % KS;
+                if (!mbar_wait(&kv_empty[slot], ((j / KS) & 1) ^ 1, abort_flag, p.status)) break;
+                mbar_arrive_expect_tx(&kv_full[slot], 2 * TB);
+                for (int kb = 0; kb < KB; ++kb) {
+                    tma_load_3d(&tmK, &kv_full[slot], sK + slot * TB + kb * (kRows * 128), kb * 64,
+                                j * kRows, group);
+                    tma_load_3d(&tmV, &kv_full[slot], sV + slot * TB + kb * (kRows * 128), kb * 64,
+                                j * kRows, group);
+                }
+                ++n;
+            }
+            mbar_wait_bounded(q_full, 0, p.status);
+            for (int m = (n > KS ? n - KS : 0); m < n; ++m)
+                mbar_wait_bounded(&kv_full[m % KS], (m / KS) & 1, p.status);
+        }
+    } else if (warp == kMmaWarp) {
+        constexpr uint32_t idesc_s = idesc_f16(kRows, kRows, BF16, false);
+        constexpr uint32_t idesc_g = idesc_f16(kRows, D, BF16, true);
+        constexpr uint64_t kStep = TB >> 4;
+        constexpr uint64_t kBlk = (kRows * 128) >> 4;
+        const uint64_t dQk = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+        const uint64_t dDOk = smem_desc_sw128(smem_u32(sDO), 16, 1024);
+        const uint64_t dKk = smem_desc_sw128(smem_u32(sK), 16, 1024);
+        const uint64_t dVk = smem_desc_sw128(smem_u32(sV), 16, 1024);
+        const uint64_t dKm = smem_desc_sw128(smem_u32(sK), kRows * 128, 1024);
+        warp_wait(q_full, 0, abort_flag, p.status);
+        for (int j = 0; j < nkv; ++j) {
+            const int slot = j % KS;
+            warp_wait(&kv_full[slot], (j / KS) & 1, abort_flag, p.status);
+            tc_fence_after();
+#pragma unroll
+            for (int kb = 0; kb < KB; ++kb)   // S = Q K^T
+                mma_ss_k64(tmem, dQk + kb * kBlk, dKk + slot * kStep + kb * kBlk, idesc_s,
+                           kb > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kb = 0; kb < KB; ++kb)   // dP = dO V^T
+                mma_ss_k64(tmem + 128, dDOk + kb * kBlk, dVk + slot * kStep + kb * kBlk, idesc_s,
+                           kb > 0 ? 1u : 0u);
+            mma_commit_elect(s_full);
+            warp_wait(p_full, j & 1, abort_flag, p.status);
+            tc_fence_after();
+            mma_ts_k128(tmem + 256, tmem + 128, dKm + slot * kStep, idesc_g, j > 0 ? 1u : 0u);
+            mma_commit_elect(&kv_empty[slot]);
+        }
+        mma_commit_elect(acc_full);
+        mma_commit_elect(mma_done);
+        mbar_wait_bounded(mma_done, 0, p.status);
+    } else {
+        const int64_t row = row0 + warp * 32 + lane;
+        const bool row_ok = row < p.rows_per_group;
+        const int pos = static_cast<int>(row % p.Nq);
+        const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t tS = tmem + lb, tDP = tmem + lb + 128;
+        const float sl2 = p.scale_log2;
+        warp_wait(q_full, 0, abort_flag, p.status);
+        const float lse2 = sL[warp * 32 + lane];
+        const float dl = sDl[warp * 32 + lane];
+        const int lim = CAUSAL ? min(p.Nk, pos + 1) : p.Nk;  // keys [0, lim) allowed
+        for (int j = 0; j < nkv; ++j) {
+            warp_wait(s_full, j & 1, abort_flag, p.status);
+            tc_fence_after();
+            const int k0 = j * kRows;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t sv[32], dp[32];
+                tmem_ld32(tS + c * 32, sv);
+                tmem_ld32(tDP + c * 32, dp);
+                tmem_wait_ld();
+                reg_fence(sv);
+                reg_fence(dp);
+                uint32_t dw[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    float dd[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const bool ok = row_ok && (k0 + c * 32 + i + u < lim);
+                        const float pr = ex2_ftz(fmaf(__uint_as_float(sv[i + u]), sl2, -lse2));
+                        dd[u] = ok ? pr * (__uint_as_float(dp[i + u]) - dl) : 0.0f;
+                    }
+                    dw[i >> 1] = pack2<BF16>(dd[0], dd[1]);
+                }
+                tmem_st16(tDP + c * 16, dw);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(p_full);
+        }
+        const bool ok = *abort_flag == 0;
+        if (nkv > 0) warp_wait(acc_full, 0, abort_flag, p.status);
+        tc_fence_after();
+        uint16_t* dqp = static_cast<uint16_t*>(p.dq) + (static_cast<int64_t>(group) * p.rows_per_group + row) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t a[32];
+            tmem_ld32(tmem + lb + 256 + c * 32, a);
+            tmem_wait_ld();
+            reg_fence(a);
+            if (ok && row_ok) {
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    w[i] = pack2<BF16>(__uint_as_float(a[2 * i]) * p.scale,
+                                       __uint_as_float(a[2 * i + 1]) * p.scale);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    reinterpret_cast<uint4*>(dqp + c * 32)[i] =
+                        make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D>
+constexpr int dkdv_smem() { return 2 * BwdCfg<D>::kTileBytes + 4 * BwdCfg<D>::kTileBytes + 2 * 2 * kRows * 4 + 256 + 1024; }
+template <int D>
+constexpr int dq_smem() { return 2 * BwdCfg<D>::kTileBytes + 4 * BwdCfg<D>::kTileBytes + 2 * kRows * 4 + 256 + 1024; }
+
+template <int D, bool BF16, bool CAUSAL>
+cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                       const CUtensorMap& tmDO, const BwdParams& p, cudaStream_t stream) {
+    {
+        const int64_t threads = p.total_rows * (D / 8);
+        const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
+        bwd_stats_kernel<D, BF16><<<blocks, 256, 0, stream>>>(p);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    {
+        auto kern = bwd_dkdv_kernel<D, BF16, CAUSAL>;
+        constexpr int smem = dkdv_smem<D>();
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        const long long ctas = static_cast<long long>(p.n_groups) * p.n_ktiles;
+        kern<<<dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, stream>>>(tmQ, tmDO, tmK, tmV, p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    {
+        auto kern = bwd_dq_kernel<D, BF16, CAUSAL>;
+        constexpr int smem = dq_smem<D>();
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        const long long ctas = static_cast<long long>(p.n_groups) * p.n_qtiles;
+        kern<<<dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, stream>>>(tmQ, tmDO, tmK, tmV, p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(int D, bool bf16, bool causal, const CUtensorMap& tmQ,
+                       const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmDO,
+                       const BwdParams& p, cudaStream_t stream) {
+#define TME_CASE(d, b, c)                   \
+    if (D == d && bf16 == b && causal == c) \
+        return launch_one<d, b, c>(tmQ, tmK, tmV, tmDO, p, stream);
+    TME_CASE(64, false, false)
+    TME_CASE(64, false, true)
+    TME_CASE(64, true, false)
+    TME_CASE(64, true, true)
+    TME_CASE(128, false, false)
+    TME_CASE(128, false, true)
+    TME_CASE(128, true, false)
+    TME_CASE(128, true, true)
+#undef TME_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace tme

@@ -27,4 +27,34 @@ cudaError_t launch_fwd(int D, bool bf16, bool causal, const CUtensorMap& tmQ,
                        const CUtensorMap& tmK, const CUtensorMap& tmV, const FwdParams& p,
                        cudaStream_t stream);
 
+// Backward launch parameters.  The workspace holds two fp32 arrays laid out
+// per KV group with rows_pad = n_qtiles * 128 rows each (so every 128-row
+// tile of per-row statistics is one aligned 512-byte block): lse2 = LSE *
+// log2(e) and delta = rowsum(dO * O).
+struct BwdParams {
+    const void* out;         // forward output O, [B, Hq, Nq, D]
+    const void* dout;        // upstream gradient dO, [B, Hq, Nq, D]
+    const float* lse;        // forward LSE, [B, Hq, Nq]
+    float* lse2;             // workspace [n_groups][rows_pad]
+    float* delta;            // workspace [n_groups][rows_pad]
+    void* dq;                // [B, Hq, Nq, D]
+    void* dk;                // [B, Hkv, Nk, D]
+    void* dv;                // [B, Hkv, Nk, D]
+    unsigned int* status;
+    int64_t rows_per_group;  // G * Nq
+    int64_t rows_pad;        // n_qtiles * 128
+    int64_t total_rows;      // B * Hq * Nq
+    int Nq, Nk;
+    int n_groups;            // B * Hkv
+    int n_qtiles;            // ceil(rows_per_group / 128)
+    int n_ktiles;            // ceil(Nk / 128)
+    float scale;
+    float scale_log2;
+};
+
+// Launches the three backward kernels (statistics, dK/dV, dQ) in order.
+cudaError_t launch_bwd(int D, bool bf16, bool causal, const CUtensorMap& tmQ,
+                       const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmDO,
+                       const BwdParams& p, cudaStream_t stream);
+
 }  // namespace tme
