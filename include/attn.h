@@ -82,6 +82,30 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
              int causal, int dtype, void* stream);
 
 /*
+ * attn_bwd without a workspace argument, for callers that cannot allocate
+ * device memory (for example an operator handed its buffers by a framework
+ * that owns every device allocation, or code that must not call cudaMalloc /
+ * cudaFree because they can synchronise the device).  The pages have no
+ * counterpart: this is a packaging convenience of this library.
+ *
+ * The scratch comes from one fixed 4 MiB array inside the library's device
+ * image (present on every GPU that loads the library until the process
+ * exits); nothing is allocated per call.  Problems whose
+ * attn_bwd_workspace_size() exceeds 4 MiB return ATTN_ERR_WORKSPACE without
+ * launching; invalid or unsupported sizes return ATTN_ERR_INVALID.  All calls
+ * on a device share the array, so calls that may run on the GPU at the same
+ * time (e.g. unordered streams) race and must be ordered by the caller.  The
+ * array keeps the last call's contents; nothing in it needs to start at zero.
+ * The first call on each device looks up the array's address; make that first
+ * call before any stream capture.  Other arguments, layouts and errors are
+ * those of attn_bwd.
+ */
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* out,
+                     const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                     int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal, int dtype,
+                     void* stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device status word of the
  * current device: ATTN_ERR_TIMEOUT if any kernel's bounded wait gave up since
  * the last call, ATTN_ERR_CUDA if the synchronisation failed, else ATTN_OK.

@@ -38,6 +38,8 @@ _SIGNATURES = {
     "attn_bwd_workspace_size": ([_i, _i, _i, _i, _i, _i, _i], ctypes.c_size_t),
     "attn_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
                   _i, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i, _vp], _i),
+    "attn_bwd_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                          _i, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i, _vp], _i),
     "attn_sync_status": ([_vp], _i),
     "attn_selftest_timeout": ([ctypes.c_ulonglong, _vp], _i),
     "attn_strerror": ([_i], ctypes.c_char_p),
