@@ -34,6 +34,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd TFLOP/s on 1 GB300 and % of dense FP16/BF16 tensor peak vs seq len"
+METRIC_BWD = "attention bwd TFLOP/s on 1 GB300 (5 products of the forward's size, halved for causal)"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "fwd_traffic.json")
 
@@ -181,19 +182,36 @@ def run_ours(args):
     pk = peaks()
     stream = torch.cuda.current_stream(dev)
 
+    bwd = args.pass_ == "bwd"
     # inputs resident in HBM before the timed region
     bufs = []
     for n in seq:
         x = inputs.make_inputs(w, n)
+        if bwd and "do" not in x:
+            g = torch.Generator().manual_seed(inputs.seed_for(w, n) + 1)
+            x["do"] = torch.randn(x["q"].shape, generator=g).to(w.dtype)
         q, k, v = (x[m].to(dev) for m in ("q", "k", "v"))
         out = torch.empty_like(q)
         lse = torch.empty(q.shape[:3], device=dev, dtype=torch.float32)
-        bufs.append((n, q, k, v, out, lse, x))
+        extra = None
+        if bwd:
+            _lib.attn_fwd(q, k, v, causal=w.causal, out=out, lse=lse)
+            do = x["do"].to(dev)
+            ws = torch.empty(max(16, _lib.load().attn_bwd_workspace_size(
+                w.B, w.Hq, w.Hkv, n, n, w.D, 1 if w.dtype == torch.bfloat16 else 0)),
+                device=dev, dtype=torch.uint8)
+            extra = (do, torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), ws)
+        bufs.append((n, q, k, v, out, lse, x, extra))
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
     def launch(b):
-        n, q, k, v, out, lse, _ = b
-        _lib.attn_fwd(q, k, v, causal=w.causal, out=out, lse=lse)
+        n, q, k, v, out, lse, _, extra = b
+        if bwd:
+            do, dq, dk, dv, ws = extra
+            _lib.attn_bwd(q, k, v, out, do, lse, causal=w.causal, dq=dq, dk=dk, dv=dv,
+                          workspace=ws)
+        else:
+            _lib.attn_fwd(q, k, v, causal=w.causal, out=out, lse=lse)
 
     for _ in range(args.warmup):
         for b in bufs:
@@ -227,7 +245,8 @@ def run_ours(args):
     per_launch_ms = [[ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps)]
                      for i in range(len(bufs))]
     ms_each = [statistics.mean(x) for x in per_launch_ms]
-    flops = [w.flops_fwd(n) for n in seq]
+    # backward: 5 products of the forward's size (S recomputed, dP, dV, dK, dQ)
+    flops = [(2.5 if bwd else 1.0) * w.flops_fwd(n) for n in seq]
     step_ms = sum(ms_each)
     if dist:
         t = torch.tensor([step_ms], device=dev)
@@ -240,19 +259,22 @@ def run_ours(args):
     achieved = flops[dom] / (ms_each[dom] * 1e-3) / 1e12
     peak = pk["bf16_tflops"]
     traffic = traffic_for(args.config, seq[dom])
+    if bwd:
+        traffic = None
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                "kernel": "attn_fwd_kernel", "launch": f"N={seq[dom]}",
+                "kernel": "attn_bwd (stats + dK/dV + dQ kernels)" if bwd else "attn_fwd_kernel",
+                "launch": f"N={seq[dom]}",
                 "peak_source": f"{pk['source']} bf16 dense (burst; fp16 runs at the same "
                                f"tensor rate)"}
 
     # end to end through the public call with host buffers: H2D of q,k,v from
     # pinned memory, the forward, D2H of out and lse, every step
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not bwd:
         host = []
         h2d = d2h = 0
-        for n, q, k, v, out, lse, x in bufs:
+        for n, q, k, v, out, lse, x, _ in bufs:
             hq, hk, hv = (x[m].pin_memory() for m in ("q", "k", "v"))
             ho = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
             hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
@@ -264,7 +286,7 @@ def run_ours(args):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(e2e_steps):
-            for (n, q, k, v, out, lse, _), (hq, hk, hv, ho, hl) in zip(bufs, host):
+            for (n, q, k, v, out, lse, _, _e), (hq, hk, hv, ho, hl) in zip(bufs, host):
                 q.copy_(hq, non_blocking=True)
                 k.copy_(hk, non_blocking=True)
                 v.copy_(hv, non_blocking=True)
@@ -287,12 +309,14 @@ def run_ours(args):
             dist.destroy_process_group()
         return
 
-    cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline(w, seq, budget_s=args.cpu_budget)
+    cpu = None if (args.no_cpu_baseline or world > 1 or bwd) else \
+        cpu_baseline(w, seq, budget_s=args.cpu_budget)
     sweep = [{"N": n, "ms": round(ms, 4), "tflops": round(f / (ms * 1e-3) / 1e12, 1),
               "frac_of_peak": round(f / (ms * 1e-3) / 1e12 / peak, 4)}
              for n, ms, f in zip(seq, ms_each, flops)]
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "metric": METRIC_BWD if bwd else METRIC, "value": round(value, 2), "unit": "TFLOP/s",
+        "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16" if w.dtype == torch.float16 else "bf16",
@@ -304,7 +328,7 @@ def run_ours(args):
                    "l2": "flushed before every launch (256 MiB write, outside the timed events)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": args.steps * len(seq),
+        "gpu_launches": args.steps * len(seq) * (3 if bwd else 1),
         "clocks": clocks, "sweep": sweep, "wall_s_timed_region": round(t_wall, 3),
     }
     print(json.dumps(line), flush=True)
@@ -419,6 +443,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="sweep")
     ap.add_argument("--n", type=int, default=None, help="run one sequence length only")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
+                    help="time the forward (default) or the backward")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)

@@ -202,8 +202,8 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
     p.out = out;
     p.dout = dout;
     p.lse = lse;
-    p.lse2 = static_cast<float*>(workspace);
-    p.delta = p.lse2 + groups * n_qtiles * 128;
+    p.nlse2 = static_cast<float*>(workspace);
+    p.ndelta = p.nlse2 + groups * n_qtiles * 128;
     p.dq = dq;
     p.dk = dk;
     p.dv = dv;

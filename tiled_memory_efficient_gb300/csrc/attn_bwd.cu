@@ -9,7 +9,7 @@
 // With s = scale * q.k, P = exp(s - LSE), dP = dO V^T, Delta = rowsum(dO * O):
 //   dS = P * (dP - Delta),  dV = P^T dO,  dK = scale * dS^T Q,  dQ = scale * dS K.
 // Three kernels, all deterministic (no atomics):
-//   1. statistics: Delta and LSE*log2(e) per query row into the workspace;
+//   1. statistics: -Delta and -LSE*log2(e) per query row into the workspace;
 //   2. dK/dV, KV-stationary: one CTA per (KV group, 128-key tile) loops over
 //      the query tiles of every head of the group (so GQA gradients are summed
 //      inside the CTA): S^T = K Q^T and dP^T = V dO^T on the tensor core, P^T
@@ -47,8 +47,8 @@ __device__ __forceinline__ float2 unpack2(uint32_t w) {
 }
 
 // ---------------------------------------------------------------- statistics
-// One query row per D/8 lanes (16-byte loads): delta = sum_d dO * O in fp32,
-// lse2 = LSE * log2(e).  Output rows go to the per-group padded layout.
+// One query row per D/8 lanes (16-byte loads): ndelta = -sum_d dO * O in fp32,
+// nlse2 = -LSE * log2(e).  Output rows go to the per-group padded layout.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_stats_kernel(const BwdParams p) {
     constexpr int LPR = D / 8;
@@ -75,8 +75,8 @@ __global__ void __launch_bounds__(256) bwd_stats_kernel(const BwdParams p) {
     for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (row < p.total_rows && sub == 0) {
         const int64_t g = row / p.rows_per_group, r = row % p.rows_per_group;
-        p.delta[g * p.rows_pad + r] = acc;
-        p.lse2[g * p.rows_pad + r] = p.lse[row] * kLog2e;
+        p.ndelta[g * p.rows_pad + r] = -acc;
+        p.nlse2[g * p.rows_pad + r] = -p.lse[row] * kLog2e;
     }
 }
 
@@ -118,8 +118,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sV = sK + TB;
     uint8_t* sQ = sV + TB;             // [QS]
     uint8_t* sDO = sQ + QS * TB;       // [QS]
-    float* sL = reinterpret_cast<float*>(sDO + QS * TB);  // [QS][128] lse2 of the query tile
-    float* sDl = sL + QS * kRows;                          // [QS][128] delta
+    float* sL = reinterpret_cast<float*>(sDO + QS * TB);  // [QS][128] -lse2 of the query tile
+    float* sDl = sL + QS * kRows;                          // [QS][128] -delta
     uint64_t* bars = reinterpret_cast<uint64_t*>(sDl + QS * kRows);
     uint64_t* kv_full = bars;
     uint64_t* q_full = kv_full + 1;    // [QS]
@@ -178,8 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 kb * 64, qi * kRows, group);
                 }
                 const int64_t w0 = static_cast<int64_t>(group) * p.rows_pad + qi * kRows;
-                bulk_load(sL + slot * kRows, p.lse2 + w0, kRows * 4, &q_full[slot]);
-                bulk_load(sDl + slot * kRows, p.delta + w0, kRows * 4, &q_full[slot]);
+                bulk_load(sL + slot * kRows, p.nlse2 + w0, kRows * 4, &q_full[slot]);
+                bulk_load(sDl + slot * kRows, p.ndelta + w0, kRows * 4, &q_full[slot]);
                 ++n;
             }
             mbar_wait_bounded(kv_full, 0, p.status);
@@ -240,6 +240,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int base = static_cast<int>(row0 % p.Nq);
             const float* L = sL + slot * kRows;
             const float* Dl = sDl + slot * kRows;
+            // No mask anywhere in this warp's 32 x 128 block: every column is a
+            // real row of the group, every key exists, and (causal) the warp's
+            // last key is at or before the tile's first query position.
+            const int wkey_last = key0 + warp * 32 + 31;
+            bool fast = (row0 + kRows <= p.rows_per_group) && (wkey_last < p.Nk);
+            if (CAUSAL) fast = fast && (base + kRows <= p.Nq) && (wkey_last <= base);
+            const uint64_t sl22 = f2(sl2, sl2);
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 uint32_t sv[32], dp[32];
@@ -249,20 +256,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                 reg_fence(sv);
                 reg_fence(dp);
                 uint32_t pw[16], dw[16];
+                if (fast) {
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    float pp[2], dd[2];
+                    for (int i = 0; i < 32; i += 4) {
+                        const float4 l4 = *reinterpret_cast<const float4*>(L + c * 32 + i);
+                        const float4 d4 = *reinterpret_cast<const float4*>(Dl + c * 32 + i);
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int q = c * 32 + i + u;
-                        bool ok = (row0 + q < p.rows_per_group) && (key < p.Nk);
-                        if (CAUSAL) ok = ok && key <= tile_pos(base, q, p.Nq);
-                        const float pr = ex2_ftz(fmaf(__uint_as_float(sv[i + u]), sl2, -L[q]));
-                        pp[u] = ok ? pr : 0.0f;
-                        dd[u] = ok ? pr * (__uint_as_float(dp[i + u]) - Dl[q]) : 0.0f;
+                        for (int h = 0; h < 2; ++h) {
+                            const int e = i + 2 * h;
+                            const uint64_t x = ffma2(f2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                                     sl22, h ? f2(l4.z, l4.w) : f2(l4.x, l4.y));
+                            const float p0 = ex2_ftz(f2lo(x)), p1 = ex2_ftz(f2hi(x));
+                            const uint64_t dd = fmul2(
+                                f2(p0, p1),
+                                fadd2(f2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
+                                      h ? f2(d4.z, d4.w) : f2(d4.x, d4.y)));
+                            pw[e >> 1] = pack2<BF16>(p0, p1);
+                            dw[e >> 1] = pack2<BF16>(f2lo(dd), f2hi(dd));
+                        }
                     }
-                    pw[i >> 1] = pack2<BF16>(pp[0], pp[1]);
-                    dw[i >> 1] = pack2<BF16>(dd[0], dd[1]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        float pp[2], dd[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int q = c * 32 + i + u;
+                            bool ok = (row0 + q < p.rows_per_group) && (key < p.Nk);
+                            if (CAUSAL) ok = ok && key <= tile_pos(base, q, p.Nq);
+                            const float pr = ex2_ftz(fmaf(__uint_as_float(sv[i + u]), sl2, L[q]));
+                            pp[u] = ok ? pr : 0.0f;
+                            dd[u] = ok ? pr * (__uint_as_float(dp[i + u]) + Dl[q]) : 0.0f;
+                        }
+                        pw[i >> 1] = pack2<BF16>(pp[0], pp[1]);
+                        dw[i >> 1] = pack2<BF16>(dd[0], dd[1]);
+                    }
                 }
                 // packed P^T / dS^T of query columns 32c.. go to TMEM columns 16c..,
                 // which hold scores already read into registers.
@@ -386,8 +414,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(&tmDO, q_full, sDO + kb * (kRows * 128), kb * 64, qi * kRows, group);
             }
             const int64_t w0 = static_cast<int64_t>(group) * p.rows_pad + row0;
-            bulk_load(sL, p.lse2 + w0, kRows * 4, q_full);
-            bulk_load(sDl, p.delta + w0, kRows * 4, q_full);
+            bulk_load(sL, p.nlse2 + w0, kRows * 4, q_full);
+            bulk_load(sDl, p.ndelta + w0, kRows * 4, q_full);
             int n = 0;
             for (int j = 0; j < nkv; ++j) {
                 const int slot = j % KS;
@@ -445,13 +473,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tS = tmem + lb, tDP = tmem + lb + 128;
         const float sl2 = p.scale_log2;
         warp_wait(q_full, 0, abort_flag, p.status);
-        const float lse2 = sL[warp * 32 + lane];
-        const float dl = sDl[warp * 32 + lane];
+        const float nl = sL[warp * 32 + lane];   // -lse2 of this row
+        const float nd = sDl[warp * 32 + lane];  // -delta of this row
         const int lim = CAUSAL ? min(p.Nk, pos + 1) : p.Nk;  // keys [0, lim) allowed
+        // Smallest position among this warp's rows: key tiles past it (or past
+        // Nk) need the mask.  Rows past the group only feed their own dQ rows,
+        // which are never stored, so they need none.
+        const int64_t wr0 = row0 + warp * 32;
+        const int64_t wr1 = min(wr0 + 31, p.rows_per_group - 1);
+        const int warp_min_pos = (wr0 / p.Nq == wr1 / p.Nq) ? static_cast<int>(wr0 % p.Nq) : 0;
+        const uint64_t sl22 = f2(sl2, sl2), nl2 = f2(nl, nl), nd2 = f2(nd, nd);
         for (int j = 0; j < nkv; ++j) {
             warp_wait(s_full, j & 1, abort_flag, p.status);
             tc_fence_after();
             const int k0 = j * kRows;
+            const bool need_mask = (k0 + kRows > p.Nk) || (CAUSAL && k0 + kRows - 1 > warp_min_pos);
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 uint32_t sv[32], dp[32];
@@ -463,14 +499,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t dw[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
-                    float dd[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const bool ok = row_ok && (k0 + c * 32 + i + u < lim);
-                        const float pr = ex2_ftz(fmaf(__uint_as_float(sv[i + u]), sl2, -lse2));
-                        dd[u] = ok ? pr * (__uint_as_float(dp[i + u]) - dl) : 0.0f;
+                    const uint64_t x = ffma2(f2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])),
+                                             sl22, nl2);
+                    float p0 = ex2_ftz(f2lo(x)), p1 = ex2_ftz(f2hi(x));
+                    if (need_mask) {
+                        const int kk = k0 + c * 32 + i;
+                        p0 = kk < lim ? p0 : 0.0f;
+                        p1 = kk + 1 < lim ? p1 : 0.0f;
                     }
-                    dw[i >> 1] = pack2<BF16>(dd[0], dd[1]);
+                    const uint64_t dd = fmul2(
+                        f2(p0, p1), fadd2(f2(__uint_as_float(dp[i]), __uint_as_float(dp[i + 1])), nd2));
+                    dw[i >> 1] = pack2<BF16>(f2lo(dd), f2hi(dd));
                 }
                 tmem_st16(tDP + c * 16, dw);
             }

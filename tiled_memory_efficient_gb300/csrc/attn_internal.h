@@ -29,14 +29,15 @@ cudaError_t launch_fwd(int D, bool bf16, bool causal, const CUtensorMap& tmQ,
 
 // Backward launch parameters.  The workspace holds two fp32 arrays laid out
 // per KV group with rows_pad = n_qtiles * 128 rows each (so every 128-row
-// tile of per-row statistics is one aligned 512-byte block): lse2 = LSE *
-// log2(e) and delta = rowsum(dO * O).
+// tile of per-row statistics is one aligned 512-byte block), stored negated
+// so each enters its use as a single fused add: nlse2 = -LSE * log2(e) and
+// ndelta = -rowsum(dO * O).
 struct BwdParams {
     const void* out;         // forward output O, [B, Hq, Nq, D]
     const void* dout;        // upstream gradient dO, [B, Hq, Nq, D]
     const float* lse;        // forward LSE, [B, Hq, Nq]
-    float* lse2;             // workspace [n_groups][rows_pad]
-    float* delta;            // workspace [n_groups][rows_pad]
+    float* nlse2;            // workspace [n_groups][rows_pad]
+    float* ndelta;           // workspace [n_groups][rows_pad]
     void* dq;                // [B, Hq, Nq, D]
     void* dk;                // [B, Hkv, Nk, D]
     void* dv;                // [B, Hkv, Nk, D]

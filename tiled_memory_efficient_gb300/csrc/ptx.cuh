@@ -393,6 +393,31 @@ __device__ __forceinline__ float lg2_approx(float x) {
     return y;
 }
 
+// Packed fp32 pairs (one 64-bit register holds two floats, low = first).
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+    return static_cast<uint64_t>(__float_as_uint(lo)) |
+           (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
+}
+__device__ __forceinline__ float f2lo(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float f2hi(uint64_t v) {
+    return __uint_as_float(static_cast<uint32_t>(v >> 32));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // acc + lo + hi, where lo/hi are the two bf16 halves of w (mixed-precision
 // adds: the bf16 operand is widened exactly, the sum is rounded in fp32).
 __device__ __forceinline__ float add_bf16x2_f32(float acc, uint32_t w) {
