@@ -154,6 +154,21 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """Largest value of x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tflops(world: int, flops_per_rank: float, slowest_ms: float) -> float:
+    """Whole-job throughput: every rank's FLOPs over the slowest rank's time."""
+    return world * flops_per_rank / (slowest_ms * 1e-3) / 1e12
+
+
 def dist_setup(n_gpus):
     import torch
     import torch.distributed as dist
@@ -247,12 +262,8 @@ def run_ours(args):
     ms_each = [statistics.mean(x) for x in per_launch_ms]
     # backward: 5 products of the forward's size (S recomputed, dP, dV, dK, dQ)
     flops = [(2.5 if bwd else 1.0) * w.flops_fwd(n) for n in seq]
-    step_ms = sum(ms_each)
-    if dist:
-        t = torch.tensor([step_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
-    value = world * sum(flops) / (step_ms * 1e-3) / 1e12
+    step_ms = max_over_ranks(sum(ms_each), dist, dev)
+    value = aggregate_tflops(world, sum(flops), step_ms)
 
     # roofline of the dominant launch (largest share of the step time)
     dom = max(range(len(seq)), key=lambda i: ms_each[i])
@@ -295,12 +306,8 @@ def run_ours(args):
                 hl.copy_(lse, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = e0.elapsed_time(e1) / e2e_steps
-        if dist:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": round(world * sum(flops) / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
+        e2e = {"value": round(aggregate_tflops(world, sum(flops), e2e_ms), 2), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
 
     clocks = clk.summary()
@@ -337,8 +344,9 @@ def run_ours(args):
 
 
 def cpu_baseline(w, seq, budget_s: float = 15.0, n_override=None):
-    """The fp64 oracle, as it stands, on the host cores: a row sample of the
-    largest sequence length, sized to about `budget_s` seconds."""
+    """The fp64 oracle, as it stands, on the host cores: a sample of query rows
+    (spread over the heads of batch 0) of the largest sequence length, sized
+    to about `budget_s` seconds."""
     import numpy as np
 
     import oracle
@@ -346,29 +354,32 @@ def cpu_baseline(w, seq, budget_s: float = 15.0, n_override=None):
     n = n_override or max(seq)
     threads = oracle.default_threads()
     x = inputs.make_inputs(w, n)
-    G = w.Hq // w.Hkv
-    q, k, v = x["q"][:1, :1], x["k"][:1, :1], x["v"][:1, :1]
+    q, k, v = x["q"][:1], x["k"][:1], x["v"][:1]
+    total_rows = w.Hq * n
 
     def flops_rows(rows):
-        keys = sum(oracle.attended_keys(int(i), n, w.causal) for i in rows)
+        keys = sum(oracle.attended_keys(int(r) % n, n, w.causal) for r in rows)
         return 4.0 * w.D * keys
 
     rng = np.random.default_rng(0)
-    probe = rng.choice(n, size=min(n, 8 * threads), replace=False)
+    probe = np.sort(rng.choice(total_rows, size=min(total_rows, 8 * threads), replace=False))
     t0 = time.perf_counter()
     oracle.attention_fwd(q, k, v, causal=w.causal, rows=probe, threads=threads)
-    dt = max(time.perf_counter() - t0, 1e-4)
-    per_row = dt / len(probe)
-    n_rows = int(min(n, max(len(probe), budget_s / per_row)))
-    rows = np.sort(rng.choice(n, size=n_rows, replace=False))
-    t0 = time.perf_counter()
-    oracle.attention_fwd(q, k, v, causal=w.causal, rows=rows, threads=threads)
-    dt = time.perf_counter() - t0
-    del G
+    per_row = max(time.perf_counter() - t0, 1e-4) / len(probe)
+    for _ in range(3):  # re-size from the last run until it fills about the budget
+        n_rows = int(min(total_rows, max(len(probe), budget_s / per_row)))
+        rows = np.sort(rng.choice(total_rows, size=n_rows, replace=False))
+        t0 = time.perf_counter()
+        oracle.attention_fwd(q, k, v, causal=w.causal, rows=rows, threads=threads)
+        dt = time.perf_counter() - t0
+        per_row = dt / n_rows
+        if dt >= 0.5 * budget_s or n_rows == total_rows:
+            break
     return {"value": round(flops_rows(rows) / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
             "kind": "oracle",
-            "sample": f"{n_rows} query rows of head (b=0,h=0) at N={n} (all {n} keys"
-                      f"{', causal' if w.causal else ''}), fp64, {dt:.1f} s"}
+            "sample": f"{n_rows} of the {total_rows} query rows of batch 0 at N={n} (seeded, "
+                      f"all heads; each row over all {n} keys{', causal' if w.causal else ''}), "
+                      f"fp64, {dt:.1f} s"}
 
 
 def run_reference(args):
