@@ -34,9 +34,9 @@ namespace tme {
 namespace {
 
 constexpr int kRows = 128;          // rows of a Q tile, keys of a K/V tile
-constexpr int kThreads = 320;       // 8 softmax warps + producer + MMA
+constexpr int kThreads = 352;       // 8 softmax warps + producer + 2 MMA issuers
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp0 = 9;        // issues the tensor-core work of Q tile 0; warp 10 of tile 1
 constexpr float kLn2 = 0.6931471805599453f;
 // Lazy rescale: the running max used for exponentiation is only moved when
 // the true max exceeds it by more than this many powers of two.
@@ -51,7 +51,7 @@ struct FwdCfg {
     static constexpr int kKOff = kQOff + 2 * kTileBytes;
     static constexpr int kVOff = kKOff + kKStages * kTileBytes;
     static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
-    static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
+    static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // barriers + alignment slack
     static constexpr int kOCol = 256;                        // first O column in TMEM
     // With D=64 TMEM has room for P next to S and O, so S of the next key tile
     // can be computed while the softmax still works on this one.  With D=128
@@ -117,17 +117,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sV = smem + C::kVOff;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
     uint64_t* q_full = bars;
-    uint64_t* k_full = q_full + 1;
-    uint64_t* k_empty = k_full + KS;
-    uint64_t* v_full = k_empty + KS;
-    uint64_t* v_empty = v_full + VS;
-    uint64_t* s_full = v_empty + VS;   // [2] S_t ready in TMEM
+    uint64_t* k_full = q_full + 1;       // [KS]
+    uint64_t* k_empty = k_full + KS;     // [KS][2]: tile t is done with the K in slot s
+    uint64_t* v_full = k_empty + 2 * KS; // [VS]
+    uint64_t* v_empty = v_full + VS;     // [VS][2]
+    uint64_t* s_full = v_empty + 2 * VS; // [2] S_t ready in TMEM
     uint64_t* p_full = s_full + 2;     // [2] P_t in TMEM and O_t rescaled
     uint64_t* o_full = p_full + 2;     // [2] last PV of tile t done
     uint64_t* s_free = o_full + 2;     // [2] softmax has read S_t (kSepP)
     uint64_t* pv_done = s_free + 2;    // [2] PV of tile t done (kSepP)
-    uint64_t* mma_done = pv_done + 2;  // every MMA of this CTA done
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    uint64_t* mma_done = pv_done + 2;  // [2] every MMA of tile t done
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -145,20 +145,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int i = 0; i < KS; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
-        for (int i = 0; i < VS; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 1); }
+        for (int i = 0; i < KS; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[2 * i], 1);
+            mbar_init(&k_empty[2 * i + 1], 1);
+        }
+        for (int i = 0; i < VS; ++i) {
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[2 * i], 1);
+            mbar_init(&v_empty[2 * i + 1], 1);
+        }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&s_full[t], 1);
             mbar_init(&p_full[t], 128);
             mbar_init(&o_full[t], 1);
             mbar_init(&s_free[t], 128);
             mbar_init(&pv_done[t], 1);
+            mbar_init(&mma_done[t], 1);
         }
-        mbar_init(mma_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == kMmaWarp) tmem_alloc(tmem_slot, 512);
+    if (warp == kMmaWarp0) tmem_alloc(tmem_slot, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -175,17 +183,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = 0; kb < KB; ++kb)
                     tma_load_3d(&tmQ, q_full, sQ + t * C::kTileBytes + kb * (kRows * 128),
                                 kb * 64, static_cast<int>(row_base + t * kRows), group);
+            const int nt[2] = {n0, n1};
             int nk = 0, nv = 0;  // loads issued
-            for (int j = 0; j < nmax; ++j) {
+            bool okp = true;
+            for (int j = 0; okp && j < nmax; ++j) {
+                // A slot is free once every tile that used its previous tile
+                // (the one KS loads back) has released it.
                 const int ks = j % KS;
-                if (!mbar_wait(&k_empty[ks], ((j / KS) & 1) ^ 1, abort_flag, p.status)) break;
+                for (int t = 0; okp && t < 2; ++t)
+                    if (j >= KS && j - KS < nt[t])
+                        okp = mbar_wait(&k_empty[2 * ks + t], ((j - KS) / KS) & 1, abort_flag, p.status);
+                if (!okp) break;
                 mbar_arrive_expect_tx(&k_full[ks], C::kTileBytes);
                 for (int kb = 0; kb < KB; ++kb)
                     tma_load_3d(&tmK, &k_full[ks], sK + ks * C::kTileBytes + kb * (kRows * 128),
                                 kb * 64, j * kRows, group);
                 ++nk;
                 const int vs = j % VS;
-                if (!mbar_wait(&v_empty[vs], ((j / VS) & 1) ^ 1, abort_flag, p.status)) break;
+                for (int t = 0; okp && t < 2; ++t)
+                    if (j >= VS && j - VS < nt[t])
+                        okp = mbar_wait(&v_empty[2 * vs + t], ((j - VS) / VS) & 1, abort_flag, p.status);
+                if (!okp) break;
                 mbar_arrive_expect_tx(&v_full[vs], C::kTileBytes);
                 for (int kb = 0; kb < KB; ++kb)
                     tma_load_3d(&tmV, &v_full[vs], sV + vs * C::kTileBytes + kb * (kRows * 128),
@@ -199,120 +217,85 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int n = (nv > VS ? nv - VS : 0); n < nv; ++n)
                 mbar_wait_bounded(&v_full[n % VS], (n / VS) & 1, p.status);
         }
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
-        // The whole warp runs this loop (converged, warp-uniform values); one
-        // elected lane issues each tcgen05 instruction.
+    } else if (warp == kMmaWarp0 || warp == kMmaWarp0 + 1) {
+        // ------------------------------------------------------------ MMA issue
+        // Converged warps; one elected lane issues each MMA group.  An issuing
+        // thread waits while its previous group drains, so everything else it
+        // does leaves the tensor pipe idle unless another issuer fills it.
         constexpr uint32_t idesc_s = idesc_f16(kRows, kRows, BF16, false);
         constexpr uint32_t idesc_o = idesc_f16(kRows, D, BF16, true);
         // Descriptor start addresses are in 16-byte units: one tile is
-        // kTileBytes/16, a 64-column block 1024, 32 bytes of K 2, 16 V rows 128.
+        // kTileBytes/16, a 64-column block 1024.
         constexpr uint64_t kTileStep = C::kTileBytes >> 4;
+        constexpr uint64_t kBlk = (kRows * 128) >> 4;
         const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ), 16, 1024);
         const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
         const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), kRows * 128, 1024);
-        const int nt[2] = {n0, n1};
+        auto nt = [&](int t) { return t == 0 ? n0 : n1; };
 
-        // S_t = Q_t K^T: D/16 MMAs of K=16; within a 128-byte swizzle row the
-        // K offset advances the start address by 32 bytes.
-        auto issue_s = [&](int t, int kslot) {
-            const uint32_t d = tmem + t * kRows;
-            const uint64_t a0 = dq0 + t * kTileStep;
+        // S_t = Q_t K_j^T (64 columns of D per call), then release K_j for tile t.
+        auto issue_s = [&](int t, int j) {
+            const int kslot = j % KS;
+            warp_wait(&k_full[kslot], (j / KS) & 1, abort_flag, p.status);
+            tc_fence_after();
             const uint64_t b0 = dk0 + kslot * kTileStep;
 #pragma unroll
-            for (int kb = 0; kb < KB; ++kb)   // 64 columns of D per call
-                mma_ss_k64(d, a0 + kb * ((kRows * 128) >> 4), b0 + kb * ((kRows * 128) >> 4),
+            for (int kb = 0; kb < KB; ++kb)
+                mma_ss_k64(tmem + t * kRows, dq0 + t * kTileStep + kb * kBlk, b0 + kb * kBlk,
                            idesc_s, kb > 0 ? 1u : 0u);
             mma_commit_elect(&s_full[t]);
+            mma_commit_elect(&k_empty[2 * kslot + t]);
         };
-        // O_t += P_t V: 8 MMAs of 16 keys; P_t from TMEM (8 columns per 16
-        // keys), V MN-major in shared memory (16 key rows = 2048 bytes; the two
-        // 64-column halves of D=128 are one 16 KiB block apart).
-        auto issue_pv = [&](int t, int vslot, int j) {
-            const uint32_t d = tmem + C::kOCol + t * D;
-            const uint64_t b0 = dv0 + vslot * kTileStep;
-            mma_ts_k128(d, tmem + (C::kSepP ? C::kPCol + t * 64 : t * kRows), b0, idesc_o,
-                        j > 0 ? 1u : 0u);
+        // O_t += P_t V_j with P_t from TMEM, then release V_j for tile t.
+        auto issue_pv = [&](int t, int j) {
+            const int vslot = j % VS;
+            warp_wait(&v_full[vslot], (j / VS) & 1, abort_flag, p.status);
+            warp_wait(&p_full[t], j & 1, abort_flag, p.status);
+            tc_fence_after();
+            mma_ts_k128(tmem + C::kOCol + t * D,
+                        tmem + (C::kSepP ? C::kPCol + t * 64 : t * kRows),
+                        dv0 + vslot * kTileStep, idesc_o, j > 0 ? 1u : 0u);
+            if constexpr (C::kSepP) mma_commit_elect(&pv_done[t]);
+            mma_commit_elect(&v_empty[2 * vslot + t]);
+            if (j == nt(t) - 1) mma_commit_elect(&o_full[t]);
         };
 
-        bool ok = warp_wait(q_full, 0, abort_flag, p.status);
-        if (ok && nmax > 0) {
-            ok = warp_wait(&k_full[0], 0, abort_flag, p.status);
-            if (ok) {
-                tc_fence_after();
-                if (n0 > 0) issue_s(0, 0);
-                if (n1 > 0) issue_s(1, 0);
-                mma_commit_elect(&k_empty[0]);
-            }
-        }
+        // A wait that times out sets the abort flag and later waits return at
+        // once, so every loop below runs to its end without blocking.
         if constexpr (C::kSepP) {
-            // S of key tile j+1 is issued as soon as the softmax has read S of
-            // tile j (s_free), ahead of the PV products of tile j.
-            for (int j = 0; ok && j < nmax; ++j) {
-                if (j + 1 < nmax) {
-                    const int kslot = (j + 1) % KS;
-                    if (!warp_wait(&k_full[kslot], ((j + 1) / KS) & 1, abort_flag, p.status)) break;
-                    tc_fence_after();
-                    for (int t = 0; t < 2; ++t) {
-                        if (j + 1 < nt[t]) {
-                            if (!warp_wait(&s_free[t], j & 1, abort_flag, p.status)) { ok = false; break; }
-                            tc_fence_after();
-                            issue_s(t, kslot);
-                        }
-                    }
-                    if (!ok) break;
-                    mma_commit_elect(&k_empty[kslot]);
-                }
-                const int vslot = j % VS;
-                if (!warp_wait(&v_full[vslot], (j / VS) & 1, abort_flag, p.status)) break;
-                tc_fence_after();
-                for (int t = 0; t < 2; ++t) {
-                    if (j < nt[t]) {
-                        if (!warp_wait(&p_full[t], j & 1, abort_flag, p.status)) { ok = false; break; }
-                        tc_fence_after();
-                        issue_pv(t, vslot, j);
-                        mma_commit_elect(&pv_done[t]);
-                        if (j == nt[t] - 1) mma_commit_elect(&o_full[t]);
-                    }
-                }
-                if (!ok) break;
-                mma_commit_elect(&v_empty[vslot]);
+            // Separate P: one issuer per Q tile.  S of key tile j+1 goes as soon
+            // as the softmax has read S of tile j, then PV of tile j.
+            const int t = warp - kMmaWarp0;
+            const int n_t = nt(t);
+            if (n_t > 0) {
+                warp_wait(q_full, 0, abort_flag, p.status);
+                issue_s(t, 0);
             }
-        } else {
-            for (int j = 0; ok && j < nmax; ++j) {
-                const int vslot = j % VS;
-                if (!warp_wait(&v_full[vslot], (j / VS) & 1, abort_flag, p.status)) break;
-                tc_fence_after();
-                const bool more = j + 1 < nmax;
-                const int kslot = (j + 1) % KS;
-                for (int t = 0; t < 2; ++t) {
-                    if (j < nt[t]) {
-                        if (!warp_wait(&p_full[t], j & 1, abort_flag, p.status)) { ok = false; break; }
-                        tc_fence_after();
-                        issue_pv(t, vslot, j);
-                        if (j == nt[t] - 1) mma_commit_elect(&o_full[t]);
-                    }
-                    if (t == 0 && more) {
-                        // S_0 of the next key tile goes in between the two PVs so
-                        // that softmax of tile 0 overlaps PV of tile 1.
-                        if (!warp_wait(&k_full[kslot], ((j + 1) / KS) & 1, abort_flag, p.status)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        if (j + 1 < nt[0]) issue_s(0, kslot);
-                    }
+            for (int j = 0; j < n_t; ++j) {
+                if (j + 1 < n_t) {
+                    warp_wait(&s_free[t], j & 1, abort_flag, p.status);
+                    issue_s(t, j + 1);
                 }
-                if (!ok) break;
-                mma_commit_elect(&v_empty[vslot]);
-                if (more) {
-                    if (j + 1 < nt[1]) issue_s(1, kslot);
-                    mma_commit_elect(&k_empty[kslot]);
-                }
+                issue_pv(t, j);
             }
+            mma_commit_elect(&mma_done[t]);
+            mbar_wait_bounded(&mma_done[t], 0, p.status);
+        } else if (warp == kMmaWarp0) {
+            // P over S: one issuer for both tiles in the order PV_0, S_0', PV_1,
+            // S_1', which keeps the two tiles half a period apart so one tile's
+            // softmax runs under the other tile's products.
+            warp_wait(q_full, 0, abort_flag, p.status);
+            if (n0 > 0) issue_s(0, 0);
+            if (n1 > 0) issue_s(1, 0);
+            for (int j = 0; j < nmax; ++j) {
+                if (j < n0) issue_pv(0, j);
+                if (j + 1 < n0) issue_s(0, j + 1);
+                if (j < n1) issue_pv(1, j);
+                if (j + 1 < n1) issue_s(1, j + 1);
+            }
+            mma_commit_elect(&mma_done[0]);
+            mbar_wait_bounded(&mma_done[0], 0, p.status);
         }
-        mma_commit_elect(mma_done);
-        mbar_wait_bounded(mma_done, 0, p.status);
     } else {
         // ------------------------------------------------------------ softmax + epilogue
         const int t = warp >> 2;         // Q tile of this warpgroup
@@ -463,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == kMmaWarp0) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
