@@ -31,9 +31,11 @@ namespace tme {
 namespace {
 
 constexpr int kRows = 128;
-constexpr int kThreads = 192;  // 4 elementwise warps + producer + MMA issuer
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+// 8 elementwise warps (two warpgroups, each owning 64 of the 128 columns of a
+// tile) + producer + MMA issuer.
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <bool BF16>
@@ -101,8 +103,10 @@ struct BwdCfg {
 };
 
 // ---------------------------------------------------------------- dK / dV
-// TMEM: S^T [0,128) (P^T over its first 64 columns), dP^T [128,256) (dS^T over
-// its first 64 columns), dV [256,256+D), dK [256+D,256+2D).
+// TMEM: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D,256+2D).
+// Warpgroup h owns query columns [64h, 64h+64) of S^T and dP^T and packs its
+// P^T / dS^T into the first 32 of its own 64 columns, so the PV-type products
+// read A from columns [0,32) and [64,96) (P^T), [128,160) and [192,224) (dS^T).
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -125,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* q_full = kv_full + 1;    // [QS]
     uint64_t* q_empty = q_full + QS;   // [QS]
     uint64_t* s_full = q_empty + QS;   // S^T and dP^T in TMEM
-    uint64_t* p_full = s_full + 1;     // P^T and dS^T in TMEM (128 arrivals)
+    uint64_t* p_full = s_full + 1;     // P^T and dS^T in TMEM (256 arrivals)
     uint64_t* acc_full = p_full + 1;   // last dV / dK product done
     uint64_t* mma_done = acc_full + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
@@ -144,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(kv_full, 1);
         for (int i = 0; i < QS; ++i) { mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1); }
         mbar_init(s_full, 1);
-        mbar_init(p_full, 128);
+        mbar_init(p_full, 256);
         mbar_init(acc_full, 1);
         mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -215,8 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit_elect(s_full);
             warp_wait(p_full, n & 1, abort_flag, p.status);
             tc_fence_after();
-            mma_ts_k128(tmem + 256, tmem, dDOm + slot * kStep, idesc_g, n > 0 ? 1u : 0u);
-            mma_ts_k128(tmem + 256 + D, tmem + 128, dQm + slot * kStep, idesc_g, n > 0 ? 1u : 0u);
+            mma_ts_k128_split(tmem + 256, tmem, tmem + 64, dDOm + slot * kStep, idesc_g,
+                              n > 0 ? 1u : 0u);
+            mma_ts_k128_split(tmem + 256 + D, tmem + 128, tmem + 192, dQm + slot * kStep, idesc_g,
+                              n > 0 ? 1u : 0u);
             mma_commit_elect(&q_empty[slot]);
             ++n;
         }
@@ -224,9 +230,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit_elect(mma_done);
         mbar_wait_bounded(mma_done, 0, p.status);
     } else {
-        // one thread per key row of the tile; lanes of warp w are TMEM lanes 32w..32w+31
-        const int key = key0 + warp * 32 + lane;
-        const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+        // one thread per key row and column half; warp w reads TMEM lanes
+        // 32(w%4) .. 32(w%4)+31 and columns of half w/4
+        const int hq = warp >> 2, quad = warp & 3;
+        const int key = key0 + quad * 32 + lane;
+        const uint32_t lb = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t tS = tmem + lb, tDP = tmem + lb + 128;
         const float sl2 = p.scale_log2;
         int n = 0;
@@ -243,12 +251,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // No mask anywhere in this warp's 32 x 128 block: every column is a
             // real row of the group, every key exists, and (causal) the warp's
             // last key is at or before the tile's first query position.
-            const int wkey_last = key0 + warp * 32 + 31;
+            const int wkey_last = key0 + quad * 32 + 31;
             bool fast = (row0 + kRows <= p.rows_per_group) && (wkey_last < p.Nk);
             if (CAUSAL) fast = fast && (base + kRows <= p.Nq) && (wkey_last <= base);
             const uint64_t sl22 = f2(sl2, sl2);
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = 2 * hq + cc;   // 32-column chunk of the tile
                 uint32_t sv[32], dp[32];
                 tmem_ld32(tS + c * 32, sv);
                 tmem_ld32(tDP + c * 32, dp);
@@ -292,10 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         dw[i >> 1] = pack2<BF16>(dd[0], dd[1]);
                     }
                 }
-                // packed P^T / dS^T of query columns 32c.. go to TMEM columns 16c..,
-                // which hold scores already read into registers.
-                tmem_st16(tS + c * 16, pw);
-                tmem_st16(tDP + c * 16, dw);
+                // packed P^T / dS^T of chunk c go to columns 64h + 16cc, which
+                // hold this half's scores already read into registers.
+                tmem_st16(tS + 64 * hq + 16 * cc, pw);
+                tmem_st16(tDP + 64 * hq + 16 * cc, dw);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -310,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n > 0) warp_wait(acc_full, 0, abort_flag, p.status);
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = hq * (D / 64); c < (hq + 1) * (D / 64); ++c) {   // this half's columns
             uint32_t a[32], b[32];
             if (n > 0) {
                 tmem_ld32(tmem + lb + 256 + c * 32, a);
@@ -349,7 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- dQ
-// TMEM: S [0,128), dP [128,256) (dS over its first 64 columns), dQ [256,256+D).
+// TMEM: S [0,128), dP [128,256), dQ [256,256+D).  Warpgroup h owns key
+// columns [64h, 64h+64) and packs its dS into dP columns [128+64h, 128+64h+32).
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -392,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(q_full, 1);
         for (int i = 0; i < KS; ++i) { mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 1); }
         mbar_init(s_full, 1);
-        mbar_init(p_full, 128);
+        mbar_init(p_full, 256);
         mbar_init(acc_full, 1);
         mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -459,27 +469,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit_elect(s_full);
             warp_wait(p_full, j & 1, abort_flag, p.status);
             tc_fence_after();
-            mma_ts_k128(tmem + 256, tmem + 128, dKm + slot * kStep, idesc_g, j > 0 ? 1u : 0u);
+            mma_ts_k128_split(tmem + 256, tmem + 128, tmem + 192, dKm + slot * kStep, idesc_g,
+                              j > 0 ? 1u : 0u);
             mma_commit_elect(&kv_empty[slot]);
         }
         mma_commit_elect(acc_full);
         mma_commit_elect(mma_done);
         mbar_wait_bounded(mma_done, 0, p.status);
     } else {
-        const int64_t row = row0 + warp * 32 + lane;
+        const int hq = warp >> 2, quad = warp & 3;   // column half, TMEM lane quadrant
+        const int64_t row = row0 + quad * 32 + lane;
         const bool row_ok = row < p.rows_per_group;
         const int pos = static_cast<int>(row % p.Nq);
-        const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t lb = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t tS = tmem + lb, tDP = tmem + lb + 128;
         const float sl2 = p.scale_log2;
         warp_wait(q_full, 0, abort_flag, p.status);
-        const float nl = sL[warp * 32 + lane];   // -lse2 of this row
-        const float nd = sDl[warp * 32 + lane];  // -delta of this row
+        const float nl = sL[quad * 32 + lane];   // -lse2 of this row
+        const float nd = sDl[quad * 32 + lane];  // -delta of this row
         const int lim = CAUSAL ? min(p.Nk, pos + 1) : p.Nk;  // keys [0, lim) allowed
         // Smallest position among this warp's rows: key tiles past it (or past
         // Nk) need the mask.  Rows past the group only feed their own dQ rows,
         // which are never stored, so they need none.
-        const int64_t wr0 = row0 + warp * 32;
+        const int64_t wr0 = row0 + quad * 32;
         const int64_t wr1 = min(wr0 + 31, p.rows_per_group - 1);
         const int warp_min_pos = (wr0 / p.Nq == wr1 / p.Nq) ? static_cast<int>(wr0 % p.Nq) : 0;
         const uint64_t sl22 = f2(sl2, sl2), nl2 = f2(nl, nl), nd2 = f2(nd, nd);
@@ -489,7 +501,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int k0 = j * kRows;
             const bool need_mask = (k0 + kRows > p.Nk) || (CAUSAL && k0 + kRows - 1 > warp_min_pos);
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = 2 * hq + cc;   // 32-column chunk of the tile
                 uint32_t sv[32], dp[32];
                 tmem_ld32(tS + c * 32, sv);
                 tmem_ld32(tDP + c * 32, dp);
@@ -511,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         f2(p0, p1), fadd2(f2(__uint_as_float(dp[i]), __uint_as_float(dp[i + 1])), nd2));
                     dw[i >> 1] = pack2<BF16>(f2lo(dd), f2hi(dd));
                 }
-                tmem_st16(tDP + c * 16, dw);
+                tmem_st16(tDP + 64 * hq + 16 * cc, dw);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -522,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         uint16_t* dqp = static_cast<uint16_t*>(p.dq) + (static_cast<int64_t>(group) * p.rows_per_group + row) * D;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = hq * (D / 64); c < (hq + 1) * (D / 64); ++c) {   // this half's columns
             uint32_t a[32];
             tmem_ld32(tmem + lb + 256 + c * 32, a);
             tmem_wait_ld();
