@@ -34,9 +34,13 @@ namespace tme {
 namespace {
 
 constexpr int kRows = 128;          // rows of a Q tile, keys of a K/V tile
-constexpr int kThreads = 352;       // 8 softmax warps + producer + 2 MMA issuers
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp0 = 9;        // issues the tensor-core work of Q tile 0; warp 10 of tile 1
+// Warps 0-7 softmax (warp w reads TMEM lane quadrant w%4 and runs on SM
+// sub-partition w%4); warp 8 only waits at the teardown, so that the three
+// light roles land on sub-partitions 1-3: warps 9/10 issue the tensor-core work
+// of Q tiles 0/1 and warp 11 is the TMA producer.
+constexpr int kThreads = 384;
+constexpr int kProducerWarp = 11;
+constexpr int kMmaWarp0 = 9;
 constexpr float kLn2 = 0.6931471805599453f;
 // Lazy rescale: the running max used for exponentiation is only moved when
 // the true max exceeds it by more than this many powers of two.
@@ -296,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit_elect(&mma_done[0]);
             mbar_wait_bounded(&mma_done[0], 0, p.status);
         }
-    } else {
+    } else if (warp < 8) {
         // ------------------------------------------------------------ softmax + epilogue
         const int t = warp >> 2;         // Q tile of this warpgroup
         const int quad = warp & 3;       // TMEM lane quadrant = rows quad*32 .. +31
@@ -356,18 +360,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float m_sub = (m == -INFINITY) ? 0.0f : m;
 
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // partial row sums of p
-            float accr[4] = {0.f, 0.f, 0.f, 0.f};  // bf16: partial sums of the rounded p
-            uint32_t pk[2][32];
+            if constexpr (C::kSepP) {
+                // P_t and O_t are still in use by the PV product of tile j-1.
+                if (j > 0) {
+                    if (!warp_wait(&pv_done[t], (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+                    tc_fence_after();
+                }
+            }
+            // partial row sums of p, as packed pairs; bf16: of the rounded p
+            uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+            float accr[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint64_t sl22 = f2(sl2, sl2), nm2 = f2(-m_sub, -m_sub);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
+                // P of keys 32c..32c+31 goes to TMEM columns 16c..16c+15 as soon
+                // as it is packed (with P over S those scores are already read).
+                uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
-                    const float p0 = softmax_term(fmaf(__uint_as_float(sr[c][i]), sl2, -m_sub));
-                    const float p1 = softmax_term(fmaf(__uint_as_float(sr[c][i + 1]), sl2, -m_sub));
+                    const uint64_t x = ffma2(f2(__uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1])),
+                                             sl22, nm2);
+                    const float p0 = softmax_term(f2lo(x));
+                    const float p1 = softmax_term(f2hi(x));
                     const uint32_t w = pack2<BF16>(p0, p1);
-                    pk[c >> 1][(c & 1) * 16 + (i >> 1)] = w;
-                    acc[(i >> 1) & 7] += p0 + p1;
+                    pk[i >> 1] = w;
+                    acc2[(i >> 1) & 3] = fadd2(acc2[(i >> 1) & 3], f2(p0, p1));
                     if constexpr (BF16) {
                         // Also sum the weights the PV product actually uses (bf16 P
                         // has a 2^-8 unit roundoff) and normalise O by that sum:
@@ -376,19 +393,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         accr[(i >> 1) & 3] = add_bf16x2_f32(accr[(i >> 1) & 3], w);
                     }
                 }
+                tmem_st16(tP + c * 16, pk);
             }
-            const float rs = ((acc[0] + acc[1]) + (acc[2] + acc[3])) +
-                             ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+            const uint64_t a2 = fadd2(fadd2(acc2[0], acc2[1]), fadd2(acc2[2], acc2[3]));
+            const float rs = f2lo(a2) + f2hi(a2);
             if constexpr (BF16) lr = lr * alpha + ((accr[0] + accr[1]) + (accr[2] + accr[3]));
-            if constexpr (C::kSepP) {
-                // P_t and O_t are still in use by the PV product of tile j-1.
-                if (j > 0) {
-                    if (!warp_wait(&pv_done[t], (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-                    tc_fence_after();
-                }
-            }
-            tmem_st32(tP, pk[0]);
-            tmem_st32(tP + 32, pk[1]);
 
             // O_t must be rescaled before the next PV accumulates into it.  PV
             // of key tile j-1 is complete: with P over S, S_t of tile j was
