@@ -126,6 +126,34 @@ def test_runs_on_side_stream(cuda_lib):
     assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
 
 
+def test_calls_from_a_fresh_host_thread(cuda_lib):
+    # A new host thread has no current CUDA context until something makes one
+    # current; the library must still encode its tensor maps and launch.
+    import threading
+    x = inputs.make_custom(1, 2, 2, 200, 200, 64, F16, seed=15, with_grad=True)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    ref_out, ref_lse = _lib.attn_fwd(q, k, v, causal=True)
+    ref_g = _lib.attn_bwd(q, k, v, ref_out, do, ref_lse, causal=True)
+    torch.cuda.synchronize()
+    res = {}
+
+    def worker():
+        try:
+            out, lse = _lib.attn_fwd(q, k, v, causal=True)
+            g = _lib.attn_bwd(q, k, v, out, do, lse, causal=True)
+            torch.cuda.synchronize()
+            res["v"] = (out, lse) + tuple(g)
+        except Exception as e:  # reported below
+            res["e"] = e
+
+    t = threading.Thread(target=worker)
+    t.start()
+    t.join()
+    assert "e" not in res, res.get("e")
+    for a, b in zip(res["v"], (ref_out, ref_lse) + tuple(ref_g)):
+        assert torch.equal(a, b)
+
+
 def test_deterministic(cuda_lib):
     x = inputs.make_custom(1, 4, 2, 700, 700, 128, BF16, seed=13)
     o1, l1 = run_fwd(x, True)

@@ -36,6 +36,15 @@ int device_setup(unsigned int** status) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+    // The tensor-map encoder is a driver call and needs a current context; a
+    // thread whose only runtime call so far was cudaGetDevice (autograd's
+    // worker thread, for one) has none.  Make the device's primary context
+    // current once per thread and device.
+    thread_local int tl_current_dev = -1;
+    if (tl_current_dev != dev) {
+        if (cudaSetDevice(dev) != cudaSuccess) return ATTN_ERR_CUDA;
+        tl_current_dev = dev;
+    }
     std::lock_guard<std::mutex> lk(g_mu);
     if (g_cc_ok[dev] == 0) {
         int major = 0, minor = 0;
@@ -248,8 +257,10 @@ extern "C" int attn_selftest_timeout(unsigned long long wait_ns, void* stream) {
     if (rc != ATTN_OK) return rc;
     if (wait_ns < 1000ull) wait_ns = 1000ull;
     if (wait_ns > 100000000ull) wait_ns = 100000000ull;
-    selftest_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(wait_ns, status);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    return launch_kernel(selftest_timeout_kernel, dim3(1), dim3(32), 0,
+                         static_cast<cudaStream_t>(stream), wait_ns, status) == cudaSuccess
+               ? ATTN_OK
+               : ATTN_ERR_CUDA;
 }
 
 extern "C" const char* attn_strerror(int status) {

@@ -96,6 +96,9 @@ __device__ __forceinline__ int tile_max_pos(int64_t row0, const BwdParams& p) {
     return (row0 / p.Nq == last / p.Nq) ? static_cast<int>(last % p.Nq) : p.Nq - 1;
 }
 
+constexpr int kDqKStages = 3;  // dQ kernel: K ring (live from S_j to dQ_j)
+constexpr int kDqVStages = 2;  // dQ kernel: V ring (live until dP_j)
+
 template <int D>
 struct BwdCfg {
     static constexpr int kTileBytes = kRows * D * 2;
@@ -358,8 +361,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- dQ
-// TMEM: S [0,128), dP [128,256), dQ [256,256+D).  Warpgroup h owns key
-// columns [64h, 64h+64) and packs its dS into dP columns [128+64h, 128+64h+32).
+// TMEM: S [0,128), dP [128,256), dQ [256,256+D), dS [384,448) (packed 16-bit).
+// Warpgroup h owns key columns [64h, 64h+64).  dS has its own columns, so once
+// both warpgroups have read S_j and dP_j into registers (s_free) the tensor
+// core computes S_{j+1} and dP_{j+1} while the elementwise work on j runs.
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -367,23 +372,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const BwdParams p) {
     using C = BwdCfg<D>;
-    constexpr int TB = C::kTileBytes, KB = C::kKB, KS = 2;
+    // K lives from S_j to dQ_j, V only until dP_j: separate rings, K deeper.
+    constexpr int TB = C::kTileBytes, KB = C::kKB, KS = kDqKStages, VS = kDqVStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sQ = smem;
     uint8_t* sDO = sQ + TB;
     uint8_t* sK = sDO + TB;           // [KS]
-    uint8_t* sV = sK + KS * TB;       // [KS]
-    float* sL = reinterpret_cast<float*>(sV + KS * TB);
+    uint8_t* sV = sK + KS * TB;       // [VS]
+    float* sL = reinterpret_cast<float*>(sV + VS * TB);
     float* sDl = sL + kRows;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sDl + kRows);
     uint64_t* q_full = bars;
-    uint64_t* kv_full = q_full + 1;   // [KS]
-    uint64_t* kv_empty = kv_full + KS;  // [KS]
-    uint64_t* s_full = kv_empty + KS;
-    uint64_t* p_full = s_full + 1;
-    uint64_t* acc_full = p_full + 1;
+    uint64_t* k_full = q_full + 1;    // [KS]
+    uint64_t* k_empty = k_full + KS;  // [KS]
+    uint64_t* v_full = k_empty + KS;  // [VS]
+    uint64_t* v_empty = v_full + VS;  // [VS]
+    uint64_t* s_full = v_empty + VS;  // S_j and dP_j in TMEM
+    uint64_t* s_free = s_full + 1;     // S_j and dP_j read by all 256 threads
+    uint64_t* p_full = s_free + 1;     // dS_j in TMEM (256 arrivals)
+    uint64_t* dq_done = p_full + 1;    // dQ += dS_j K_j done (dS columns free)
+    uint64_t* acc_full = dq_done + 1;
     uint64_t* mma_done = acc_full + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -400,9 +410,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int i = 0; i < KS; ++i) { mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 1); }
+        for (int i = 0; i < KS; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
+        for (int i = 0; i < VS; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 1); }
         mbar_init(s_full, 1);
+        mbar_init(s_free, 256);
         mbar_init(p_full, 256);
+        mbar_init(dq_done, 1);
         mbar_init(acc_full, 1);
         mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -426,22 +439,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t w0 = static_cast<int64_t>(group) * p.rows_pad + row0;
             bulk_load(sL, p.nlse2 + w0, kRows * 4, q_full);
             bulk_load(sDl, p.ndelta + w0, kRows * 4, q_full);
-            int n = 0;
+            int nk = 0, nv = 0;
             for (int j = 0; j < nkv; ++j) {
-                const int slot = j % KS;
-                if (!mbar_wait(&kv_empty[slot], ((j / KS) & 1) ^ 1, abort_flag, p.status)) break;
-                mbar_arrive_expect_tx(&kv_full[slot], 2 * TB);
-                for (int kb = 0; kb < KB; ++kb) {
-                    tma_load_3d(&tmK, &kv_full[slot], sK + slot * TB + kb * (kRows * 128), kb * 64,
+                const int ks = j % KS, vs = j % VS;
+                if (!mbar_wait(&k_empty[ks], ((j / KS) & 1) ^ 1, abort_flag, p.status)) break;
+                mbar_arrive_expect_tx(&k_full[ks], TB);
+                for (int kb = 0; kb < KB; ++kb)
+                    tma_load_3d(&tmK, &k_full[ks], sK + ks * TB + kb * (kRows * 128), kb * 64,
                                 j * kRows, group);
-                    tma_load_3d(&tmV, &kv_full[slot], sV + slot * TB + kb * (kRows * 128), kb * 64,
+                ++nk;
+                if (!mbar_wait(&v_empty[vs], ((j / VS) & 1) ^ 1, abort_flag, p.status)) break;
+                mbar_arrive_expect_tx(&v_full[vs], TB);
+                for (int kb = 0; kb < KB; ++kb)
+                    tma_load_3d(&tmV, &v_full[vs], sV + vs * TB + kb * (kRows * 128), kb * 64,
                                 j * kRows, group);
-                }
-                ++n;
+                ++nv;
             }
             mbar_wait_bounded(q_full, 0, p.status);
-            for (int m = (n > KS ? n - KS : 0); m < n; ++m)
-                mbar_wait_bounded(&kv_full[m % KS], (m / KS) & 1, p.status);
+            for (int m = (nk > KS ? nk - KS : 0); m < nk; ++m)
+                mbar_wait_bounded(&k_full[m % KS], (m / KS) & 1, p.status);
+            for (int m = (nv > VS ? nv - VS : 0); m < nv; ++m)
+                mbar_wait_bounded(&v_full[m % VS], (m / VS) & 1, p.status);
         }
     } else if (warp == kMmaWarp) {
         constexpr uint32_t idesc_s = idesc_f16(kRows, kRows, BF16, false);
@@ -453,25 +471,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dKk = smem_desc_sw128(smem_u32(sK), 16, 1024);
         const uint64_t dVk = smem_desc_sw128(smem_u32(sV), 16, 1024);
         const uint64_t dKm = smem_desc_sw128(smem_u32(sK), kRows * 128, 1024);
-        warp_wait(q_full, 0, abort_flag, p.status);
-        for (int j = 0; j < nkv; ++j) {
-            const int slot = j % KS;
-            warp_wait(&kv_full[slot], (j / KS) & 1, abort_flag, p.status);
+        // S_j = Q K_j^T and dP_j = dO V_j^T, one commit for both.
+        auto issue_s_dp = [&](int j) {
+            const int ks = j % KS, vs = j % VS;
+            warp_wait(&k_full[ks], (j / KS) & 1, abort_flag, p.status);
+            warp_wait(&v_full[vs], (j / VS) & 1, abort_flag, p.status);
             tc_fence_after();
 #pragma unroll
-            for (int kb = 0; kb < KB; ++kb)   // S = Q K^T
-                mma_ss_k64(tmem, dQk + kb * kBlk, dKk + slot * kStep + kb * kBlk, idesc_s,
+            for (int kb = 0; kb < KB; ++kb)
+                mma_ss_k64(tmem, dQk + kb * kBlk, dKk + ks * kStep + kb * kBlk, idesc_s,
                            kb > 0 ? 1u : 0u);
 #pragma unroll
-            for (int kb = 0; kb < KB; ++kb)   // dP = dO V^T
-                mma_ss_k64(tmem + 128, dDOk + kb * kBlk, dVk + slot * kStep + kb * kBlk, idesc_s,
+            for (int kb = 0; kb < KB; ++kb)
+                mma_ss_k64(tmem + 128, dDOk + kb * kBlk, dVk + vs * kStep + kb * kBlk, idesc_s,
                            kb > 0 ? 1u : 0u);
             mma_commit_elect(s_full);
+            mma_commit_elect(&v_empty[vs]);   // V_j is only read by dP_j
+        };
+        warp_wait(q_full, 0, abort_flag, p.status);
+        if (nkv > 0) issue_s_dp(0);
+        for (int j = 0; j < nkv; ++j) {
+            const int ks = j % KS;
+            if (j + 1 < nkv) {
+                warp_wait(s_free, j & 1, abort_flag, p.status);
+                issue_s_dp(j + 1);
+            }
             warp_wait(p_full, j & 1, abort_flag, p.status);
             tc_fence_after();
-            mma_ts_k128_split(tmem + 256, tmem + 128, tmem + 192, dKm + slot * kStep, idesc_g,
-                              j > 0 ? 1u : 0u);
-            mma_commit_elect(&kv_empty[slot]);
+            mma_ts_k128(tmem + 256, tmem + 384, dKm + ks * kStep, idesc_g, j > 0 ? 1u : 0u);
+            mma_commit_elect(dq_done);
+            mma_commit_elect(&k_empty[ks]);
         }
         mma_commit_elect(acc_full);
         mma_commit_elect(mma_done);
@@ -495,24 +524,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t wr1 = min(wr0 + 31, p.rows_per_group - 1);
         const int warp_min_pos = (wr0 / p.Nq == wr1 / p.Nq) ? static_cast<int>(wr0 % p.Nq) : 0;
         const uint64_t sl22 = f2(sl2, sl2), nl2 = f2(nl, nl), nd2 = f2(nd, nd);
+        const uint32_t tDS = tmem + lb + 384;
         for (int j = 0; j < nkv; ++j) {
             warp_wait(s_full, j & 1, abort_flag, p.status);
             tc_fence_after();
             const int k0 = j * kRows;
             const bool need_mask = (k0 + kRows > p.Nk) || (CAUSAL && k0 + kRows - 1 > warp_min_pos);
-#pragma unroll 1
+            uint32_t sv[2][32], dp[2][32];
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                tmem_ld32(tS + (2 * hq + cc) * 32, sv[cc]);
+                tmem_ld32(tDP + (2 * hq + cc) * 32, dp[cc]);
+            }
+            tmem_wait_ld();
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                reg_fence(sv[cc]);
+                reg_fence(dp[cc]);
+            }
+            // S_j and dP_j are in registers: the next S and dP may overwrite them.
+            tc_fence_before();
+            mbar_arrive(s_free);
+            // dS columns still feed dQ += dS_{j-1} K_{j-1}.
+            if (j > 0) {
+                warp_wait(dq_done, (j - 1) & 1, abort_flag, p.status);
+                tc_fence_after();
+            }
+#pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 const int c = 2 * hq + cc;   // 32-column chunk of the tile
-                uint32_t sv[32], dp[32];
-                tmem_ld32(tS + c * 32, sv);
-                tmem_ld32(tDP + c * 32, dp);
-                tmem_wait_ld();
-                reg_fence(sv);
-                reg_fence(dp);
                 uint32_t dw[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
-                    const uint64_t x = ffma2(f2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])),
+                    const uint64_t x = ffma2(f2(__uint_as_float(sv[cc][i]), __uint_as_float(sv[cc][i + 1])),
                                              sl22, nl2);
                     float p0 = ex2_ftz(f2lo(x)), p1 = ex2_ftz(f2hi(x));
                     if (need_mask) {
@@ -521,10 +565,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         p1 = kk + 1 < lim ? p1 : 0.0f;
                     }
                     const uint64_t dd = fmul2(
-                        f2(p0, p1), fadd2(f2(__uint_as_float(dp[i]), __uint_as_float(dp[i + 1])), nd2));
+                        f2(p0, p1),
+                        fadd2(f2(__uint_as_float(dp[cc][i]), __uint_as_float(dp[cc][i + 1])), nd2));
                     dw[i >> 1] = pack2<BF16>(f2lo(dd), f2hi(dd));
                 }
-                tmem_st16(tDP + 64 * hq + 16 * cc, dw);
+                tmem_st16(tDS + 16 * c, dw);   // keys 32c.. -> dS columns 16c..
             }
             tmem_wait_st();
             tc_fence_before();
@@ -564,7 +609,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 constexpr int dkdv_smem() { return 2 * BwdCfg<D>::kTileBytes + 4 * BwdCfg<D>::kTileBytes + 2 * 2 * kRows * 4 + 256 + 1024; }
 template <int D>
-constexpr int dq_smem() { return 2 * BwdCfg<D>::kTileBytes + 4 * BwdCfg<D>::kTileBytes + 2 * kRows * 4 + 256 + 1024; }
+constexpr int dq_smem() {
+    return (2 + kDqKStages + kDqVStages) * BwdCfg<D>::kTileBytes + 2 * kRows * 4 + 256 + 1024;
+}
 
 template <int D, bool BF16, bool CAUSAL>
 cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
@@ -572,8 +619,7 @@ cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
     {
         const int64_t threads = p.total_rows * (D / 8);
         const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
-        bwd_stats_kernel<D, BF16><<<blocks, 256, 0, stream>>>(p);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_kernel(bwd_stats_kernel<D, BF16>, dim3(blocks), dim3(256), 0, stream, p);
         if (e != cudaSuccess) return e;
     }
     {
@@ -582,8 +628,8 @@ cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         const long long ctas = static_cast<long long>(p.n_groups) * p.n_ktiles;
-        kern<<<dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, stream>>>(tmQ, tmDO, tmK, tmV, p);
-        e = cudaGetLastError();
+        e = launch_kernel(kern, dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, stream,
+                          tmQ, tmDO, tmK, tmV, p);
         if (e != cudaSuccess) return e;
     }
     {
@@ -592,8 +638,8 @@ cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         const long long ctas = static_cast<long long>(p.n_groups) * p.n_qtiles;
-        kern<<<dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, stream>>>(tmQ, tmDO, tmK, tmV, p);
-        e = cudaGetLastError();
+        e = launch_kernel(kern, dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, stream,
+                          tmQ, tmDO, tmK, tmV, p);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

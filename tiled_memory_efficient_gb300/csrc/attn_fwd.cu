@@ -471,8 +471,8 @@ cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const long long ctas = static_cast<long long>(p.n_groups) * p.n_pairs;
-    kern<<<dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, stream>>>(tmQ, tmK, tmV, p);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, stream,
+                         tmQ, tmK, tmV, p);
 }
 
 }  // namespace

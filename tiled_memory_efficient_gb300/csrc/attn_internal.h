@@ -8,6 +8,16 @@
 
 namespace tme {
 
+// Launches `kern` and returns the status of this launch itself (unlike
+// cudaGetLastError, which would also report an unrelated earlier error left
+// in the calling thread).
+template <typename... Params, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t stream, Args... args) {
+    void* ptrs[] = {static_cast<void*>(&args)...};
+    return cudaLaunchKernel(reinterpret_cast<const void*>(kern), grid, block, ptrs, smem, stream);
+}
+
 // Forward launch parameters (everything the kernel needs besides the three
 // tensor maps).  Row indices are "flattened": within KV group g of batch b the
 // G query heads that share that KV head form G*Nq consecutive rows, head-major.
