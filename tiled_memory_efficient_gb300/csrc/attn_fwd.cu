@@ -34,13 +34,6 @@ namespace tme {
 namespace {
 
 constexpr int kRows = 128;          // rows of a Q tile, keys of a K/V tile
-// Warps 0-7 softmax (warp w reads TMEM lane quadrant w%4 and runs on SM
-// sub-partition w%4); warp 8 only waits at the teardown, so that the three
-// light roles land on sub-partitions 1-3: warps 9/10 issue the tensor-core work
-// of Q tiles 0/1 and warp 11 is the TMA producer.
-constexpr int kThreads = 384;
-constexpr int kProducerWarp = 11;
-constexpr int kMmaWarp0 = 9;
 constexpr float kLn2 = 0.6931471805599453f;
 // Lazy rescale: the running max used for exponentiation is only moved when
 // the true max exceeds it by more than this many powers of two.
@@ -55,13 +48,33 @@ struct FwdCfg {
     static constexpr int kKOff = kQOff + 2 * kTileBytes;
     static constexpr int kVOff = kKOff + kKStages * kTileBytes;
     static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
-    static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // barriers + alignment slack
     static constexpr int kOCol = 256;                        // first O column in TMEM
     // With D=64 TMEM has room for P next to S and O, so S of the next key tile
     // can be computed while the softmax still works on this one.  With D=128
     // the four accumulators fill all 512 columns and P overwrites S.
     static constexpr bool kSepP = (D == 64);
     static constexpr int kPCol = 256 + 2 * D;                // P_t at kPCol + 64 t (kSepP)
+    // Warp roles.  A softmax warp w reads TMEM lane quadrant w%4 and runs on
+    // SM sub-partition w%4.
+    //  D=128: warps 0-7 softmax, one thread per 128-key row; warp 8 only waits
+    //         at the teardown, so the light roles land on sub-partitions 1-3:
+    //         warps 9/10 issue the tensor-core work of Q tiles 0/1, warp 11 is
+    //         the TMA producer.
+    //  D=64:  the softmax is the bottleneck, so every row is split over two
+    //         warps of 64 keys each: warps 0-15 softmax (Q tile (w/4)%2, key
+    //         half w/8), warp 16 producer, warps 17/18 MMA issuers.
+    static constexpr bool kSplit = (D == 64);
+    static constexpr int kSoftmaxWarps = kSplit ? 16 : 8;
+    static constexpr int kProducerWarp = kSplit ? 16 : 11;
+    static constexpr int kMmaWarp0 = kSplit ? 17 : 9;
+    static constexpr int kThreads = kSplit ? 19 * 32 : 12 * 32;
+    static constexpr int kTileThreads = kSplit ? 256 : 128;  // softmax threads per Q tile
+    // Split rows exchange partial maxima (double-buffered by key-tile parity)
+    // and, at the end, partial sums: xm[2][2 tiles][128 rows][2 halves],
+    // xl[2 tiles][128][2], xr[2 tiles][128][2] (floats).
+    static constexpr int kXOff = kBarOff + 512;
+    static constexpr int kXBytes = kSplit ? (4096 + 2048 + 2048) : 0;
+    static constexpr int kSmemBytes = kBarOff + 512 + kXBytes + 1024;
 };
 
 // Flush-to-zero threshold in the log2 domain: a softmax term p = 2^x with
@@ -71,7 +84,7 @@ struct FwdCfg {
 // 2^-25 becomes +0, the smallest fp16 subnormal is 2^-24), so no extra
 // instruction is spent on it; the fp32 row sum still adds those terms, which
 // changes it by less than Nk * 2^-25 (relative, since the sum is >= 1).
-__device__ __forceinline__ float softmax_term(float x) { return ex2_ftz(x); }
+// The terms are computed two at a time by softmax_pair (ptx.cuh).
 
 // Row maximum of 128 values with three-input max: a 5-level tree (65 ops),
 // fully independent at the first level.
@@ -104,13 +117,32 @@ __device__ __forceinline__ int kv_tiles_for(int64_t row0, const FwdParams& p, bo
     return static_cast<int>((keys + kRows - 1) / kRows);
 }
 
+// Maximum of 64 values (three-input max tree).
+__device__ __forceinline__ float row_max64(const uint32_t (&s)[2][32]) {
+    float t[22];
+#pragma unroll
+    for (int i = 0; i < 21; ++i) {
+        const int a = 3 * i, b = 3 * i + 1, c = 3 * i + 2;
+        t[i] = fmax3(__uint_as_float(s[a >> 5][a & 31]), __uint_as_float(s[b >> 5][b & 31]),
+                     __uint_as_float(s[c >> 5][c & 31]));
+    }
+    t[21] = __uint_as_float(s[1][31]);
+    float u[8];
+#pragma unroll
+    for (int i = 0; i < 7; ++i) u[i] = fmax3(t[3 * i], t[3 * i + 1], t[3 * i + 2]);
+    u[7] = t[21];
+    return fmaxf(fmax3(u[0], u[1], u[2]), fmax3(u[3], u[4], fmax3(u[5], u[6], u[7])));
+}
+
 template <int D, bool BF16, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
     using C = FwdCfg<D>;
     constexpr int KS = C::kKStages, VS = C::kVStages;
+    constexpr int kProducerWarp = C::kProducerWarp;
+    constexpr int kMmaWarp0 = C::kMmaWarp0;
     constexpr int KB = D / 64;  // 64-element (128-byte) column blocks per row
 
     extern __shared__ uint8_t smem_raw[];
@@ -161,9 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&s_full[t], 1);
-            mbar_init(&p_full[t], 128);
+            mbar_init(&p_full[t], C::kTileThreads);
             mbar_init(&o_full[t], 1);
-            mbar_init(&s_free[t], 128);
+            mbar_init(&s_free[t], C::kTileThreads);
             mbar_init(&pv_done[t], 1);
             mbar_init(&mma_done[t], 1);
         }
@@ -300,7 +332,156 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit_elect(&mma_done[0]);
             mbar_wait_bounded(&mma_done[0], 0, p.status);
         }
-    } else if (warp < 8) {
+    } else if (C::kSplit && warp < C::kSoftmaxWarps) {
+        // ------------------------------------------------------------ split softmax (D=64)
+        // Thread = (row, half of the key tile).  The two warps of a row pair
+        // share the row max through shared memory; a wait that times out sets
+        // the abort flag and later waits return at once, so both warps of a
+        // pair always meet at every pair barrier.
+        const int t = (warp >> 2) & 1;   // Q tile
+        const int quad = warp & 3;       // TMEM lane quadrant = rows quad*32 .. +31
+        const int h = warp >> 3;         // key half: keys [64h, 64h+64) of each key tile
+        const int n_t = t == 0 ? n0 : n1;
+        const int rl = quad * 32 + lane;              // row within the Q tile
+        const int64_t row0 = row_base + t * kRows;
+        const int64_t row = row0 + rl;
+        const bool row_valid = row < p.rows_per_group;
+        const int pos = static_cast<int>(row % p.Nq);
+        const int64_t wr0 = row0 + quad * 32;
+        const int64_t wr1 = min(wr0 + 31, p.rows_per_group - 1);
+        const int warp_min_pos =
+            (wr0 / p.Nq == wr1 / p.Nq) ? static_cast<int>(wr0 % p.Nq) : 0;
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t tS = tmem + lane_base + t * kRows + 64 * h;
+        const uint32_t tO = tmem + lane_base + C::kOCol + t * D;
+        const uint32_t tP = tmem + lane_base + C::kPCol + t * 64 + 32 * h;
+        // Shared-window byte addresses of this thread's exchange slots:
+        // xm[2 buffers][2 tiles][128 rows][2 halves] (buffer stride 2048 B),
+        // then xl[2][128][2] and xr[2][128][2].  The partner's slot is at
+        // address ^ 4 (the half is the lowest index bit).
+        const uint32_t x_slot = smem_u32(smem + C::kXOff) + ((t * 128 + rl) * 2 + h) * 4;
+        const uint32_t xl_slot = x_slot + 4096;
+        const uint32_t xr_slot = x_slot + 6144;
+        const uint32_t pair_bar = 1 + t * 4 + quad;  // named barrier of the warp pair
+        uint32_t xbuf = 0;                           // 0 / 2048: buffer of key tile j
+        const float sl2 = p.scale_log2;
+
+        float m = -INFINITY;  // running max (log2 domain, scaled), same in both halves
+        float l = 0.0f;       // this half's running sum of p
+        float lr = 0.0f;      // bf16: this half's running sum of the rounded p
+        for (int j = 0; j < n_t; ++j) {
+            warp_wait(&s_full[t], j & 1, abort_flag, p.status);
+            tc_fence_after();
+            uint32_t sr[2][32];
+            tmem_ld32(tS, sr[0]);
+            tmem_ld32(tS + 32, sr[1]);
+            tmem_wait_ld();
+            reg_fence(sr[0]);
+            reg_fence(sr[1]);
+            // S_t is in registers: the MMA warp may compute the next S_t.
+            tc_fence_before();
+            mbar_arrive(&s_free[t]);
+
+            const int key0 = j * kRows + 64 * h;
+            const bool need_mask = (key0 + 64 > p.Nk) || (CAUSAL && key0 + 63 > warp_min_pos);
+            if (need_mask) {
+                const int lim = CAUSAL ? min(p.Nk, pos + 1) : p.Nk;  // keys [0, lim) allowed
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (key0 + c * 32 + i >= lim) sr[c][i] = __float_as_uint(-INFINITY);
+            }
+            const float pm = row_max64(sr);
+            st_shared_f32(x_slot + xbuf, pm);
+            named_bar_sync(pair_bar, 64);
+            const float mx = fmaxf(pm, ld_shared_f32((x_slot ^ 4u) + xbuf));
+            xbuf ^= 2048u;
+            const float m_new = fmaxf(m, mx * sl2);
+            const bool need = m_new > m + kRescaleThreshold;
+            // Branch-free: alpha is only used when need (m = -inf gives 0).
+            const float alpha = need ? ex2_ftz(m - m_new) : 1.0f;
+            m = need ? m_new : m;
+            const float m_sub = (m == -INFINITY) ? 0.0f : m;
+
+            uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+            float accr[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint64_t sl22 = f2(sl2, sl2), nm2 = f2(-m_sub, -m_sub);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2)
+                    pk[i >> 1] = softmax_pair<BF16>(sr[c][i], sr[c][i + 1], sl22, nm2,
+                                                    acc2[(i >> 1) & 3], accr[(i >> 1) & 3]);
+                if (c == 0 && j > 0) {
+                    // P_t and O_t are still in use by the PV product of tile j-1.
+                    warp_wait(&pv_done[t], (j - 1) & 1, abort_flag, p.status);
+                    tc_fence_after();
+                }
+                tmem_st16(tP + c * 16, pk);   // keys 64h + 32c.. -> P columns 32h + 16c..
+            }
+            const uint64_t a2 = fadd2(fadd2(acc2[0], acc2[1]), fadd2(acc2[2], acc2[3]));
+            const float rs = f2lo(a2) + f2hi(a2);
+            if constexpr (BF16) lr = lr * alpha + ((accr[0] + accr[1]) + (accr[2] + accr[3]));
+            // Each half rescales its half of O's columns (the decision is the
+            // same in both halves).
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+                for (int c = h * (D / 64); c < (h + 1) * (D / 64); ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c * 32, o);
+                    tmem_wait_ld();
+                    reg_fence(o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st32(tO + c * 32, o);
+                }
+            }
+            l = l * alpha + rs;
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&p_full[t]);
+        }
+
+        if (n_t > 0) {
+            warp_wait(&o_full[t], 0, abort_flag, p.status);
+            tc_fence_after();
+            st_shared_f32(xl_slot, l);
+            st_shared_f32(xr_slot, lr);
+            named_bar_sync(pair_bar, 64);
+            const float lt = l + ld_shared_f32(xl_slot ^ 4u);
+            const float lrt = lr + ld_shared_f32(xr_slot ^ 4u);
+            const bool ok = *abort_flag == 0;
+            const float l_out = BF16 ? lrt : lt;
+            const float inv_l = l_out > 0.0f ? 1.0f / l_out : 0.0f;
+            const int64_t grow = static_cast<int64_t>(group) * p.rows_per_group + row;
+            uint16_t* out = static_cast<uint16_t*>(p.out) + grow * D;
+#pragma unroll
+            for (int c = h * (D / 64); c < (h + 1) * (D / 64); ++c) {
+                uint32_t o[32];
+                tmem_ld32(tO + c * 32, o);
+                tmem_wait_ld();
+                reg_fence(o);
+                if (ok && row_valid) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        w[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l,
+                                           __uint_as_float(o[2 * i + 1]) * inv_l);
+                    uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                }
+            }
+            if (ok && row_valid && h == 0) {
+                const float m_sub = (m == -INFINITY) ? 0.0f : m;
+                p.lse[grow] = lt > 0.0f ? (m_sub + lg2_approx(lt)) * kLn2 : -INFINITY;
+            }
+        }
+    } else if (!C::kSplit && warp < C::kSoftmaxWarps) {
         // ------------------------------------------------------------ softmax + epilogue
         const int t = warp >> 2;         // Q tile of this warpgroup
         const int quad = warp & 3;       // TMEM lane quadrant = rows quad*32 .. +31
@@ -353,11 +534,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float mx = row_max128(sr);
             const float m_new = fmaxf(m, mx * sl2);
             const bool need = m_new > m + kRescaleThreshold;
-            float alpha = 1.0f;
-            if (need) {
-                alpha = ex2_ftz(m - m_new);  // m = -inf gives 0
-                m = m_new;
-            }
+            // Branch-free: alpha is only used when need (m = -inf gives 0).
+            const float alpha = need ? ex2_ftz(m - m_new) : 1.0f;
+            m = need ? m_new : m;
             const float m_sub = (m == -INFINITY) ? 0.0f : m;
 
             if constexpr (C::kSepP) {
@@ -377,22 +556,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // as it is packed (with P over S those scores are already read).
                 uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const uint64_t x = ffma2(f2(__uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1])),
-                                             sl22, nm2);
-                    const float p0 = softmax_term(f2lo(x));
-                    const float p1 = softmax_term(f2hi(x));
-                    const uint32_t w = pack2<BF16>(p0, p1);
-                    pk[i >> 1] = w;
-                    acc2[(i >> 1) & 3] = fadd2(acc2[(i >> 1) & 3], f2(p0, p1));
-                    if constexpr (BF16) {
-                        // Also sum the weights the PV product actually uses (bf16 P
-                        // has a 2^-8 unit roundoff) and normalise O by that sum:
-                        // O is then an exact weighted mean of the value rows, and a
-                        // row dominated by one key returns that key's value row.
-                        accr[(i >> 1) & 3] = add_bf16x2_f32(accr[(i >> 1) & 3], w);
-                    }
-                }
+                // bf16 also sums the weights the PV product actually uses (bf16 P
+                // has a 2^-8 unit roundoff) and normalises O by that sum: O is
+                // then an exact weighted mean of the value rows, and a row
+                // dominated by one key returns that key's value row.
+                for (int i = 0; i < 32; i += 2)
+                    pk[i >> 1] = softmax_pair<BF16>(sr[c][i], sr[c][i + 1], sl22, nm2,
+                                                    acc2[(i >> 1) & 3], accr[(i >> 1) & 3]);
                 tmem_st16(tP + c * 16, pk);
             }
             const uint64_t a2 = fadd2(fadd2(acc2[0], acc2[1]), fadd2(acc2[2], acc2[3]));
@@ -466,6 +636,7 @@ cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
                        const FwdParams& p, cudaStream_t stream) {
     auto kern = attn_fwd_kernel<D, BF16, CAUSAL>;
     constexpr int smem = FwdCfg<D>::kSmemBytes;
+    constexpr int kThreads = FwdCfg<D>::kThreads;
     // Re-applied on every call: a cheap attribute write that is correct on
     // whichever device is current.
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

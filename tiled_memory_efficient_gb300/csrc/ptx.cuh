@@ -445,6 +445,59 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
     return d;
 }
 
+// 32-bit shared-memory store / load at a shared-window address (smem_u32).
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+// Named barrier `id` (1..15) over `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Two softmax terms in one step: x = s * scale2 + negm2 (packed pair),
+// p = 2^x per lane (flush-to-zero), acc += p (packed pair), and p rounded to a
+// 16-bit pair (low half = first term).  BF16 also adds the two ROUNDED terms
+// to accr.  Written as one asm block so the 64-bit pairs stay register pairs.
+template <bool BF16>
+__device__ __forceinline__ uint32_t softmax_pair(uint32_t s0, uint32_t s1, uint64_t scale2,
+                                                 uint64_t negm2, uint64_t& acc, float& accr) {
+    uint32_t w;
+    if constexpr (BF16) {
+        asm("{\n\t.reg .b64 x, p;\n\t.reg .f32 a, b;\n\t.reg .b16 lo, hi;\n\t"
+            "mov.b64 x, {%3, %4};\n\t"
+            "fma.rn.f32x2 x, x, %5, %6;\n\t"
+            "mov.b64 {a, b}, x;\n\t"
+            "ex2.approx.ftz.f32 a, a;\n\t"
+            "ex2.approx.ftz.f32 b, b;\n\t"
+            "mov.b64 p, {a, b};\n\t"
+            "add.rn.f32x2 %1, %1, p;\n\t"
+            "cvt.rn.bf16x2.f32 %0, b, a;\n\t"
+            "mov.b32 {lo, hi}, %0;\n\t"
+            "add.rn.f32.bf16 %2, lo, %2;\n\t"
+            "add.rn.f32.bf16 %2, hi, %2;\n\t}"
+            : "=r"(w), "+l"(acc), "+f"(accr)
+            : "r"(s0), "r"(s1), "l"(scale2), "l"(negm2));
+    } else {
+        asm("{\n\t.reg .b64 x, p;\n\t.reg .f32 a, b;\n\t"
+            "mov.b64 x, {%2, %3};\n\t"
+            "fma.rn.f32x2 x, x, %4, %5;\n\t"
+            "mov.b64 {a, b}, x;\n\t"
+            "ex2.approx.ftz.f32 a, a;\n\t"
+            "ex2.approx.ftz.f32 b, b;\n\t"
+            "mov.b64 p, {a, b};\n\t"
+            "add.rn.f32x2 %1, %1, p;\n\t"
+            "cvt.rn.f16x2.f32 %0, b, a;\n\t}"
+            : "=r"(w), "+l"(acc)
+            : "r"(s0), "r"(s1), "l"(scale2), "l"(negm2));
+    }
+    return w;
+}
+
 // acc + lo + hi, where lo/hi are the two bf16 halves of w (mixed-precision
 // adds: the bf16 operand is widened exactly, the sum is rounded in fp32).
 __device__ __forceinline__ float add_bf16x2_f32(float acc, uint32_t w) {
