@@ -10,7 +10,10 @@ outside the timed events.  value = sum of algorithmic FLOPs / sum of launch
 times.  Prints ONE JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config sweep|gqa_prefill|video_dit|training|tiny]
+                    [--config sweep|gqa_prefill|video_dit|training|tiny|gqa_decode]
+
+--config gqa_decode times the split-key forward (attn_fwd_splitkv) on decode
+shapes and reports GB/s against the HBM copy bandwidth instead of TFLOP/s.
 
 --impl reference times the fp64 CPU oracle (the reference arm) on the host
 cores: each step is a bounded sample of the same workload.  Under torchrun
@@ -35,6 +38,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd TFLOP/s on 1 GB300 and % of dense FP16/BF16 tensor peak vs seq len"
 METRIC_BWD = "attention bwd TFLOP/s on 1 GB300 (5 products of the forward's size, halved for causal)"
+METRIC_DECODE = ("attention decode GB/s on 1 GB300 (split-key forward against a KV cache: "
+                 "Q, K, V read once, O and LSE written)")
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "fwd_traffic.json")
 
@@ -198,6 +203,10 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     bwd = args.pass_ == "bwd"
+    decode = w.nq is not None
+    if decode and bwd:
+        raise SystemExit("the decode workload has no backward pass")
+    splits = {n: _lib.num_splits(w.B, w.Hq, w.Hkv, w.queries(n), n, w.D) for n in seq}
     # inputs resident in HBM before the timed region
     bufs = []
     for n in seq:
@@ -216,6 +225,9 @@ def run_ours(args):
                 w.B, w.Hq, w.Hkv, n, n, w.D, 1 if w.dtype == torch.bfloat16 else 0)),
                 device=dev, dtype=torch.uint8)
             extra = (do, torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), ws)
+        elif decode:
+            extra = torch.empty(max(16, _lib.splitkv_workspace_size(
+                w.B, w.Hq, w.Hkv, w.queries(n), n, w.D, splits[n])), device=dev, dtype=torch.uint8)
         bufs.append((n, q, k, v, out, lse, x, extra))
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
@@ -225,6 +237,9 @@ def run_ours(args):
             do, dq, dk, dv, ws = extra
             _lib.attn_bwd(q, k, v, out, do, lse, causal=w.causal, dq=dq, dk=dk, dv=dv,
                           workspace=ws)
+        elif decode:
+            _lib.attn_fwd_splitkv(q, k, v, causal=w.causal, splits=splits[n], out=out, lse=lse,
+                                  workspace=extra)
         else:
             _lib.attn_fwd(q, k, v, causal=w.causal, out=out, lse=lse)
 
@@ -260,27 +275,37 @@ def run_ours(args):
     per_launch_ms = [[ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps)]
                      for i in range(len(bufs))]
     ms_each = [statistics.mean(x) for x in per_launch_ms]
-    # backward: 5 products of the forward's size (S recomputed, dP, dV, dK, dQ)
+    # backward: 5 products of the forward's size (S recomputed, dP, dV, dK, dQ);
+    # decode: algorithmic bytes instead of FLOPs (the work is HBM-bound)
     flops = [(2.5 if bwd else 1.0) * w.flops_fwd(n) for n in seq]
+    work = [w.bytes_fwd(n) for n in seq] if decode else flops
+    scale = 1e9 if decode else 1e12
+    unit = "GB/s" if decode else "TFLOP/s"
     step_ms = max_over_ranks(sum(ms_each), dist, dev)
-    value = aggregate_tflops(world, sum(flops), step_ms)
+    value = world * sum(work) / (step_ms * 1e-3) / scale
 
     # roofline of the dominant launch (largest share of the step time)
     dom = max(range(len(seq)), key=lambda i: ms_each[i])
-    achieved = flops[dom] / (ms_each[dom] * 1e-3) / 1e12
-    peak = pk["bf16_tflops"]
+    achieved = work[dom] / (ms_each[dom] * 1e-3) / scale
+    peak = pk["hbm_gbs"] if decode else pk["bf16_tflops"]
     traffic = traffic_for(args.config, seq[dom])
     if bwd:
         traffic = None
-    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
-                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                "kernel": "attn_bwd (stats + dK/dV + dQ kernels)" if bwd else "attn_fwd_kernel",
-                "launch": f"N={seq[dom]}",
-                "peak_source": f"{pk['source']} bf16 dense (burst; fp16 runs at the same "
-                               f"tensor rate)"}
+    if decode:
+        kernel = ("attn_fwd_kernel over key ranges + splitkv_merge_kernel (one call)"
+                  if splits[seq[dom]] > 1 else "attn_fwd_kernel")
+        peak_source = f"{pk['source']} HBM copy bandwidth"
+    else:
+        kernel = "attn_bwd (stats + dK/dV + dQ kernels)" if bwd else "attn_fwd_kernel"
+        peak_source = f"{pk['source']} bf16 dense (burst; fp16 runs at the same tensor rate)"
+    roofline = {"bound": "hbm" if decode else "tensor", "achieved": round(achieved, 1),
+                "peak": peak, "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
+                "kernel": kernel, "launch": f"N={seq[dom]}", "peak_source": peak_source}
 
     # end to end through the public call with host buffers: H2D of q,k,v from
     # pinned memory, the forward, D2H of out and lse, every step
+    # (decode: the KV cache lives on the device, as in serving; only the new
+    # queries go up and the outputs come back)
     e2e = None
     if not args.no_e2e and not bwd:
         host = []
@@ -290,24 +315,26 @@ def run_ours(args):
             ho = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
             hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
             host.append((hq, hk, hv, ho, hl))
-            h2d += sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+            h2d += sum(t.numel() * t.element_size() for t in ((hq,) if decode else (hq, hk, hv)))
             d2h += ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
         e2e_steps = max(1, min(args.steps, 10))
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(e2e_steps):
-            for (n, q, k, v, out, lse, _, _e), (hq, hk, hv, ho, hl) in zip(bufs, host):
+            for b, (hq, hk, hv, ho, hl) in zip(bufs, host):
+                n, q, k, v, out, lse = b[:6]
                 q.copy_(hq, non_blocking=True)
-                k.copy_(hk, non_blocking=True)
-                v.copy_(hv, non_blocking=True)
-                _lib.attn_fwd(q, k, v, causal=w.causal, out=out, lse=lse)
+                if not decode:
+                    k.copy_(hk, non_blocking=True)
+                    v.copy_(hv, non_blocking=True)
+                launch(b)
                 ho.copy_(out, non_blocking=True)
                 hl.copy_(lse, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
-        e2e = {"value": round(aggregate_tflops(world, sum(flops), e2e_ms), 2), "unit": "TFLOP/s",
+        e2e = {"value": round(world * sum(work) / (e2e_ms * 1e-3) / scale, 2), "unit": unit,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
 
     clocks = clk.summary()
@@ -318,24 +345,33 @@ def run_ours(args):
 
     cpu = None if (args.no_cpu_baseline or world > 1 or bwd) else \
         cpu_baseline(w, seq, budget_s=args.cpu_budget)
-    sweep = [{"N": n, "ms": round(ms, 4), "tflops": round(f / (ms * 1e-3) / 1e12, 1),
-              "frac_of_peak": round(f / (ms * 1e-3) / 1e12 / peak, 4)}
-             for n, ms, f in zip(seq, ms_each, flops)]
+    if decode:
+        sweep = [{"Nk": n, "ms": round(ms, 4), "splits": splits[n],
+                  "gbs": round(b / (ms * 1e-3) / 1e9, 1),
+                  "frac_of_peak": round(b / (ms * 1e-3) / 1e9 / peak, 4)}
+                 for n, ms, b in zip(seq, ms_each, work)]
+    else:
+        sweep = [{"N": n, "ms": round(ms, 4), "tflops": round(f / (ms * 1e-3) / 1e12, 1),
+                  "frac_of_peak": round(f / (ms * 1e-3) / 1e12 / peak, 4)}
+                 for n, ms, f in zip(seq, ms_each, flops)]
+    launches_per_step = sum((2 if splits[n] > 1 else 1) if decode else (3 if bwd else 1)
+                            for n in seq)
+    metric = METRIC_DECODE if decode else (METRIC_BWD if bwd else METRIC)
     line = {
-        "metric": METRIC_BWD if bwd else METRIC, "value": round(value, 2), "unit": "TFLOP/s",
+        "metric": metric, "value": round(value, 2), "unit": unit,
         "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16" if w.dtype == torch.float16 else "bf16",
         "data": "synthetic",
         "config": {"workload": w.note, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
-                   "causal": w.causal, "seq_lens": seq,
+                   "causal": w.causal, "seq_lens": seq, "Nq": w.nq if decode else "= N",
                    "inputs": "seeded N(0,1) rounded to dtype" +
                              ("; 1% of key rows x8" if w.outlier_keys else ""),
                    "l2": "flushed before every launch (256 MiB write, outside the timed events)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": args.steps * len(seq) * (3 if bwd else 1),
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks, "sweep": sweep, "wall_s_timed_region": round(t_wall, 3),
     }
     print(json.dumps(line), flush=True)
@@ -345,20 +381,24 @@ def run_ours(args):
 
 def cpu_baseline(w, seq, budget_s: float = 15.0, n_override=None):
     """The fp64 oracle, as it stands, on the host cores: a sample of query rows
-    (spread over the heads of batch 0) of the largest sequence length, sized
-    to about `budget_s` seconds."""
+    (spread over the heads of batch 0; every batch for decode shapes) of the
+    largest sequence length, sized to about `budget_s` seconds.  Decode shapes
+    report GB/s: the sampled rows' share of the workload's algorithmic bytes."""
     import numpy as np
 
     import oracle
     from tiled_memory_efficient_gb300 import inputs
     n = n_override or max(seq)
+    nq = w.queries(n)
+    decode = w.nq is not None
     threads = oracle.default_threads()
     x = inputs.make_inputs(w, n)
-    q, k, v = x["q"][:1], x["k"][:1], x["v"][:1]
-    total_rows = w.Hq * n
+    nb = w.B if decode else 1
+    q, k, v = x["q"][:nb], x["k"][:nb], x["v"][:nb]
+    total_rows = nb * w.Hq * nq
 
     def flops_rows(rows):
-        keys = sum(oracle.attended_keys(int(r) % n, n, w.causal) for r in rows)
+        keys = sum(oracle.attended_keys(int(r) % nq, n, w.causal, nq) for r in rows)
         return 4.0 * w.D * keys
 
     rng = np.random.default_rng(0)
@@ -375,11 +415,16 @@ def cpu_baseline(w, seq, budget_s: float = 15.0, n_override=None):
         per_row = dt / n_rows
         if dt >= 0.5 * budget_s or n_rows == total_rows:
             break
-    return {"value": round(flops_rows(rows) / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
-            "kind": "oracle",
-            "sample": f"{n_rows} of the {total_rows} query rows of batch 0 at N={n} (seeded, "
-                      f"all heads; each row over all {n} keys{', causal' if w.causal else ''}), "
-                      f"fp64, {dt:.1f} s"}
+    if decode:
+        value, unit = n_rows / (w.B * w.Hq * nq) * w.bytes_fwd(n) / dt / 1e9, "GB/s"
+        where = f"all {w.B} sequences, Nk={n}"
+    else:
+        value, unit = flops_rows(rows) / dt / 1e12, "TFLOP/s"
+        where = f"batch 0 at N={n}"
+    return {"value": round(value, 6), "unit": unit, "cores": threads, "kind": "oracle",
+            "sample": f"{n_rows} of the {total_rows} query rows of {where} (seeded, all heads; "
+                      f"each row over its visible keys{', causal ' + str(w.causal) if w.causal else ''}),"
+                      f" fp64, {dt:.3f} s"}
 
 
 def run_reference(args):
@@ -394,11 +439,13 @@ def run_reference(args):
     from tiled_memory_efficient_gb300 import inputs
     w = inputs.WORKLOADS[args.config]
     seq = list(w.seq_lens) if args.n is None else [args.n]
+    decode = w.nq is not None
     threads = oracle.default_threads()
     data = {}
     for n in seq:
         x = inputs.make_inputs(w, n)
         data[n] = (x["q"][:1, :1], x["k"][:1, :1], x["v"][:1, :1])
+    nqs = {n: w.queries(n) for n in seq}
     # rows per N per step, sized so the whole run takes about 60-120 s
     budget_step = max(0.5, 90.0 / (args.steps + args.warmup))
     cost = {n: 4.0 * w.D * n for n in seq}          # flops per full row
@@ -407,40 +454,46 @@ def run_reference(args):
     # calibrate
     t0 = time.perf_counter()
     q, k, v = data[seq[-1]]
-    cal = rng.choice(seq[-1], size=min(seq[-1], 4 * threads), replace=False)
+    cal = rng.choice(nqs[seq[-1]], size=min(nqs[seq[-1]], 4 * threads), replace=False)
     oracle.attention_fwd(q, k, v, causal=w.causal, rows=cal, threads=threads)
     rate = cost[seq[-1]] * len(cal) / max(time.perf_counter() - t0, 1e-4)   # flops/s
-    rows_per_n = {n: max(1, min(n, int(budget_step * rate * (cost[n] / tot) / cost[n])))
+    rows_per_n = {n: max(1, min(nqs[n], int(budget_step * rate * (cost[n] / tot) / cost[n])))
                   for n in seq}
-    step_flops = 0.0
+    step_work = 0.0
     times = []
     for s in range(args.warmup + args.steps):
         t0 = time.perf_counter()
         fl = 0.0
         for n in seq:
             q, k, v = data[n]
-            rows = rng.choice(n, size=rows_per_n[n], replace=False)
+            rows = rng.choice(nqs[n], size=rows_per_n[n], replace=False)
             oracle.attention_fwd(q, k, v, causal=w.causal, rows=rows, threads=threads)
-            fl += sum(4.0 * w.D * oracle.attended_keys(int(i), n, w.causal) for i in rows)
+            if decode:   # the rows' share of the workload's algorithmic bytes
+                fl += len(rows) / (w.B * w.Hq * nqs[n]) * w.bytes_fwd(n)
+            else:
+                fl += sum(4.0 * w.D * oracle.attended_keys(int(i), n, w.causal, nqs[n])
+                          for i in rows)
         dt = time.perf_counter() - t0
         if s >= args.warmup:
             times.append(dt)
-            step_flops += fl
+            step_work += fl
     total = sum(times)
-    value = step_flops / total / 1e12
-    sample = (f"per step: rows {rows_per_n} of head (b=0,h=0) per N, all keys, fp64 "
+    value = step_work / total / (1e9 if decode else 1e12)
+    unit = "GB/s" if decode else "TFLOP/s"
+    sample = (f"per step: rows {rows_per_n} of head (b=0,h=0) per N, all visible keys, fp64 "
               f"({threads} threads)")
     line = {
-        "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "metric": METRIC_DECODE if decode else METRIC, "value": round(value, 6), "unit": unit,
+        "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * total / max(1, len(times)), 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic", "impl": "reference",
         "config": {"workload": w.note, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
                    "causal": w.causal, "seq_lens": seq},
-        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
+        "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": threads,
                          "kind": "oracle", "sample": sample},
-        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

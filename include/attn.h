@@ -22,7 +22,12 @@
  *         lse              : [B, Hq, Nq]         (fp32, natural log)
  *     dtype is ATTN_F16 or ATTN_BF16; accumulation is fp32.
  *   - Query head h uses KV head h / (Hq / Hkv) (contiguous groups).
- *   - causal != 0 applies the top-left mask: query position i sees keys j <= i.
+ *   - causal selects the mask (attn_causal_t): ATTN_CAUSAL_NONE, or
+ *     ATTN_CAUSAL_TOP_LEFT (query position i sees keys j <= i; the is_causal
+ *     convention of the SDPA call), or, forward only, ATTN_CAUSAL_BOTTOM_RIGHT
+ *     (i sees j <= i + Nk - Nq: the Nq queries are the last Nq positions of a
+ *     sequence whose first Nk positions are in K/V, as when decoding against
+ *     a KV cache; requires Nq <= Nk).  Other values are ATTN_ERR_INVALID.
  *   - scale multiplies q.k; it must be finite and > 0 (1/sqrt(D) is the usual).
  *   - Work is enqueued on `stream` (a cudaStream_t; 0 = legacy default) and the
  *     call returns without synchronising.  The return value reports argument
@@ -44,6 +49,12 @@ extern "C" {
 typedef enum { ATTN_F16 = 0, ATTN_BF16 = 1 } attn_dtype_t;
 
 typedef enum {
+    ATTN_CAUSAL_NONE = 0,
+    ATTN_CAUSAL_TOP_LEFT = 1,
+    ATTN_CAUSAL_BOTTOM_RIGHT = 2
+} attn_causal_t;
+
+typedef enum {
     ATTN_OK = 0,
     ATTN_ERR_INVALID = 1,     /* null pointer, non-positive size, Hq % Hkv, bad scale/dtype */
     ATTN_ERR_UNSUPPORTED = 2, /* D not in {64,128}, sizes beyond the kernel's index range, not sm_103 */
@@ -63,6 +74,49 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
              int Hkv, int Nq, int Nk, int D, float scale, int causal, int dtype, void* stream);
 
 /*
+ * Split-key forward for short query blocks against long key sequences (LLM
+ * decode against a KV cache, the workload of the forum post's table "PyTorch
+ * LLM Inference -- Qwen 2.5 0.5B (GQA, FP16)").  attn_fwd runs one CTA per KV
+ * group and pair of 128-row query tiles, which leaves most of the GPU idle
+ * when B * Hkv * ceil(G * Nq / 256) is small.  This call also cuts the keys
+ * into num_splits ranges of whole 128-key tiles (fewer if the keys run out:
+ * every range gets ceil(tiles / num_splits) tiles), runs one CTA per range,
+ * writes each range's normalised partial output and log-sum-exp to the
+ * workspace in fp32, and merges them into out / lse with a second kernel:
+ *     lse = M + ln sum_r e^(lse_r - M),  out = sum_r e^(lse_r - lse) out_r,
+ * M = max_r lse_r.  The result is the attention of attn_fwd up to rounding
+ * (out is rounded once, from fp32).
+ *
+ * num_splits: 1..256.  With one effective range the call is attn_fwd (no
+ * workspace is touched and it may be NULL).  Otherwise workspace must be a
+ * 16-byte-aligned device buffer of at least
+ * attn_fwd_splitkv_workspace_size(..., num_splits) bytes (ATTN_ERR_WORKSPACE
+ * if smaller); its contents on entry do not matter.  Other arguments, layouts
+ * and errors are those of attn_fwd.
+ */
+int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* out, float* lse,
+                     void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int Nq,
+                     int Nk, int D, float scale, int causal, int dtype, int num_splits,
+                     void* stream);
+
+/*
+ * Workspace bytes attn_fwd_splitkv needs: fp32 partial outputs and LSEs of
+ * every range, each array padded to 256 bytes.  0 when one range results, or
+ * for invalid sizes / num_splits outside 1..256.  Host-only.
+ */
+size_t attn_fwd_splitkv_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int D,
+                                       int num_splits);
+
+/*
+ * A range count for attn_fwd_splitkv: 1 when the unsplit grid already has at
+ * least one CTA per SM, else enough ranges to fill one wave of num_sms CTAs,
+ * keeping at least two key tiles per range.  num_sms <= 0 asks the current
+ * device for its SM count.  Returns 1 for invalid sizes.  Host-only apart
+ * from that query.
+ */
+int attn_fwd_num_splits(int B, int Hq, int Hkv, int Nq, int Nk, int D, int num_sms);
+
+/*
  * Bytes of device workspace attn_bwd needs for these sizes (fp32 per-row
  * statistics).  Returns 0 for invalid sizes.
  */
@@ -75,6 +129,8 @@ size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int D, in
  * [B,Hkv,Nk,D] summed over the query heads of each group (overwritten, not
  * accumulated).  workspace: caller-owned device memory of at least
  * attn_bwd_workspace_size() bytes; its contents on entry do not matter.
+ * causal: ATTN_CAUSAL_NONE or ATTN_CAUSAL_TOP_LEFT (bottom-right returns
+ * ATTN_ERR_UNSUPPORTED).
  */
 int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
              const float* lse, void* dq, void* dk, void* dv, void* workspace,

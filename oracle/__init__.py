@@ -10,8 +10,10 @@ What it computes is the plain definition of attention that the tiled method
 reaches by a faster route (noflash-attention forum post, ai-navigate-news,
 section "The DIY approach": tiling gives the same math with O(N) memory):
 ``O = softmax(scale * Q K^T) V`` per row, ``LSE = log sum_j exp(scale q.k_j)``,
-GQA by ``h_kv = h_q // (Hq // Hkv)``, optional top-left causal mask, and the
-gradients of that map.
+GQA by ``h_kv = h_q // (Hq // Hkv)``, an optional causal mask (top-left, or
+for the forward also bottom-right: the queries are the last Nq positions of
+the key sequence, as in KV-cache decoding), and the gradients of that map
+(no mask or top-left).
 """
 from __future__ import annotations
 
@@ -99,7 +101,7 @@ def _shapes(q, k, v):
     return B, Hq, Hkv, Nq, Nk, D
 
 
-def attention_fwd(q, k, v, causal: bool = False, scale: float | None = None,
+def attention_fwd(q, k, v, causal=False, scale: float | None = None,
                   rows=None, threads: int | None = None):
     """Forward definition in fp64.
 
@@ -125,7 +127,7 @@ def attention_fwd(q, k, v, causal: bool = False, scale: float | None = None,
         if n == 0:
             return o, lse
     rc = _load().oracle_attn_fwd_rows(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nk, D,
-                                      float(scale), int(bool(causal)), rows_p, n,
+                                      float(scale), causal_code(causal), rows_p, n,
                                       _ptr(o), _ptr(lse), int(threads or default_threads()))
     if rc != 0:
         raise RuntimeError(f"oracle_attn_fwd_rows failed with {rc}")
@@ -145,13 +147,29 @@ def attention_bwd(q, k, v, dout, causal: bool = False, scale: float | None = Non
     dk = np.empty_like(k)
     dv = np.empty_like(v)
     rc = _load().oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B, Hq, Hkv, Nq, Nk, D,
-                                 float(scale), int(bool(causal)), _ptr(dq), _ptr(dk), _ptr(dv),
+                                 float(scale), causal_code(causal), _ptr(dq), _ptr(dk), _ptr(dv),
                                  int(threads or default_threads()))
     if rc != 0:
         raise RuntimeError(f"oracle_attn_bwd failed with {rc}")
     return dq, dk, dv
 
 
-def attended_keys(i: int, nk: int, causal: bool) -> int:
-    """How many keys query position i attends to (top-left causal)."""
-    return min(i + 1, nk) if causal else nk
+def causal_code(causal) -> int:
+    """0 none, 1 top-left (True), 2 bottom-right ("bottom_right")."""
+    if causal is None or causal is False:
+        return 0
+    if causal is True:
+        return 1
+    if isinstance(causal, str):
+        return {"none": 0, "top_left": 1, "bottom_right": 2}[causal]
+    return int(causal)
+
+
+def attended_keys(i: int, nk: int, causal, nq: int | None = None) -> int:
+    """How many keys query i attends to: all, j <= i (top-left), or
+    j <= i + nk - nq (bottom-right; needs nq)."""
+    c = causal_code(causal)
+    if c == 0:
+        return nk
+    pos = i + (nk - nq) if c == 2 else i
+    return max(0, min(pos + 1, nk))

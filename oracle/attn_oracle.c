@@ -21,7 +21,10 @@
  *
  *   "Allowed" is every key, or with the causal mask the keys j <= i
  *   (top-left alignment, the is_causal convention of the SDPA call the forum
- *   post patches).  The default scale 1/sqrt(D) is the one the ai-manual.ru
+ *   post patches).  The forward also takes causal = 2, bottom-right
+ *   alignment: the Nq queries are the LAST Nq positions of a sequence whose
+ *   first Nk positions are the keys, so query i sees keys j <= i + (Nk - Nq)
+ *   (the KV-cache decode of the post's LLM-inference table; Nq <= Nk).  The default scale 1/sqrt(D) is the one the ai-manual.ru
  *   page's chunked snippet divides by (section "3 Samopisnyi memory-efficient
  *   attention"); the caller passes it explicitly.  No flush-to-zero and no
  *   epsilon: this is the exact result the tiled method approximates.
@@ -108,7 +111,9 @@ static void *fwd_worker(void *arg)
         const double *q_row = jb->q + r * jb->D;
         const double *k_head = jb->k + (b * jb->Hkv + g) * jb->Nk * jb->D;
         const double *v_head = jb->v + (b * jb->Hkv + g) * jb->Nk * jb->D;
-        fwd_one_row(q_row, k_head, v_head, allowed_keys(i, jb->Nk, jb->causal), jb->D,
+        /* bottom-right: query i sits at sequence position i + (Nk - Nq) */
+        const int64_t seq_pos = (jb->causal == 2) ? i + (jb->Nk - jb->Nq) : i;
+        fwd_one_row(q_row, k_head, v_head, allowed_keys(seq_pos, jb->Nk, jb->causal), jb->D,
                     jb->scale, s, jb->o + t * jb->D, jb->lse + t);
     }
     free(s);
@@ -136,6 +141,7 @@ int oracle_attn_fwd_rows(const double *q, const double *k, const double *v,
 {
     if (check_shape(B, Hq, Hkv, Nq, Nk, D)) return -1;
     if (!q || !k || !v || !o || !lse) return -1;
+    if (causal < 0 || causal > 2 || (causal == 2 && Nq > Nk)) return -1;
     const int64_t total = rows ? n_rows : B * Hq * Nq;
     if (rows) {
         for (int64_t t = 0; t < n_rows; ++t)
@@ -262,6 +268,7 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v, const dou
 {
     if (check_shape(B, Hq, Hkv, Nq, Nk, D)) return -1;
     if (!q || !k || !v || !dout || !dq || !dk || !dv) return -1;
+    if (causal < 0 || causal > 1) return -1;   /* the backward covers none / top-left */
     const int64_t G = Hq / Hkv;
     const int64_t unit_rows = G * Nq;
     if (nthreads < 1) nthreads = 1;

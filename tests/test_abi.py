@@ -19,7 +19,8 @@ def lib():
 def test_header_declares_the_boundary():
     names = _lib.declared_functions()
     for required in ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_sync_status",
-                     "attn_strerror", "attn_selftest_timeout", "attn_version"):
+                     "attn_strerror", "attn_selftest_timeout", "attn_version", "attn_fwd_splitkv",
+                     "attn_fwd_splitkv_workspace_size", "attn_fwd_num_splits"):
         assert required in names
 
 
@@ -56,6 +57,9 @@ P = 256  # a fake, 16-byte-aligned "device" address: validation fails before any
     # misaligned pointer
     ((P + 2, P, P, P, P, 1, 2, 2, 128, 128, 64, 0.125, 0, 0), 3),
     ((P, P, P, P, P + 4, 1, 2, 2, 128, 128, 64, 0.125, 0, 1), 3),
+    # unknown causal mode; bottom-right with more queries than keys
+    ((P, P, P, P, P, 1, 2, 2, 128, 128, 64, 0.125, 3, 0), 1),
+    ((P, P, P, P, P, 1, 2, 2, 129, 128, 64, 0.125, 2, 0), 1),
 ])
 def test_fwd_rejects_without_launch(lib, args, code):
     assert lib.attn_fwd(*args, None) == code
@@ -76,3 +80,41 @@ def test_bwd_validation_and_workspace(lib):
     bad = [P] * 9
     bad[4] = P + 8
     assert lib.attn_bwd(*bad, P, ws, 2, 16, 16, 8192, 8192, 128, 0.08, 1, 1, None) == 3
+
+
+def test_bwd_rejects_bottom_right(lib):
+    ws = lib.attn_bwd_workspace_size(1, 2, 2, 128, 256, 64, 0)
+    assert lib.attn_bwd(*([P] * 9), P, ws, 1, 2, 2, 128, 256, 64, 0.125, 2, 0, None) == 2
+    assert lib.attn_bwd(*([P] * 9), P, ws, 1, 2, 2, 128, 256, 64, 0.125, 5, 0, None) == 1
+
+
+def test_num_splits_heuristic(lib):
+    """Host-only: one wave of CTAs on num_sms SMs, >= 2 key tiles per range,
+    and no empty range."""
+    # decode, 8 sequences, Qwen-like GQA (14:2): 16 units -> 9 wanted on 152
+    # SMs; 32 key tiles in ranges of 4 -> 8 ranges
+    assert lib.attn_fwd_num_splits(8, 14, 2, 1, 4096, 64, 152) == 8
+    # a grid that already fills the GPU is not split
+    assert lib.attn_fwd_num_splits(1, 16, 16, 16384, 16384, 64, 152) == 1
+    # two key tiles: at most one range
+    assert lib.attn_fwd_num_splits(1, 2, 2, 1, 200, 64, 152) == 1
+    # one unit, long keys: 152 ranges of 7 tiles cover 1024 tiles in 147
+    assert lib.attn_fwd_num_splits(1, 1, 1, 1, 131072, 128, 152) == 147
+    assert lib.attn_fwd_num_splits(1, 3, 2, 1, 4096, 64, 152) == 1   # invalid sizes
+
+
+def test_splitkv_workspace_and_validation(lib):
+    ws = lib.attn_fwd_splitkv_workspace_size(8, 14, 2, 1, 4096, 64, 8)
+    rows = 8 * 14 * 1
+    assert ws == 8 * rows * 64 * 4 + ((8 * rows * 4 + 255) // 256) * 256
+    # 9 requested on 32 tiles is ranges of 4 tiles: 8 ranges
+    assert lib.attn_fwd_splitkv_workspace_size(8, 14, 2, 1, 4096, 64, 9) == ws
+    assert lib.attn_fwd_splitkv_workspace_size(8, 14, 2, 1, 4096, 64, 1) == 0
+    assert lib.attn_fwd_splitkv_workspace_size(8, 14, 2, 1, 4096, 64, 257) == 0
+    assert lib.attn_fwd_splitkv_workspace_size(8, 14, 3, 1, 4096, 64, 8) == 0
+    args = (8, 14, 2, 1, 4096, 64, 0.125, 0, 0)
+    # bad range count, null / misaligned / short workspace: all before any device call
+    assert lib.attn_fwd_splitkv(P, P, P, P, P, P, ws, *args, 0, None) == 1
+    assert lib.attn_fwd_splitkv(P, P, P, P, P, 0, ws, *args, 8, None) == 1
+    assert lib.attn_fwd_splitkv(P, P, P, P, P, P + 8, ws, *args, 8, None) == 3
+    assert lib.attn_fwd_splitkv(P, P, P, P, P, P, ws - 16, *args, 8, None) == 6

@@ -191,6 +191,66 @@ def test_zero_query_causal_gives_prefix_means():
     np.testing.assert_allclose(lse_nc, math.log(N), atol=1e-14)
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,D", [
+    (1, 2, 2, 5, 19, 8),      # Nq < Nk
+    (2, 4, 2, 1, 23, 16),     # one query (decode) with GQA
+    (1, 7, 1, 12, 40, 8),     # G = 7
+    (1, 2, 1, 17, 17, 8),     # Nq = Nk
+])
+def test_bottom_right_matches_torch_causal_lower_right(B, Hq, Hkv, Nq, Nk, D):
+    """Bottom-right causal against torch's own lower-right causal bias (an
+    independent library routine) and torch.logsumexp over a tril mask."""
+    from torch.nn.attention.bias import causal_lower_right
+    q, k, v = rnd((B, Hq, Nq, D), 81), rnd((B, Hkv, Nk, D), 82), rnd((B, Hkv, Nk, D), 83)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = oracle.attention_fwd(q, k, v, causal="bottom_right")
+    G = Hq // Hkv
+    qt, kt, vt = (torch.as_tensor(x) for x in (q, k, v))
+    kt, vt = kt.repeat_interleave(G, dim=1), vt.repeat_interleave(G, dim=1)
+    ref = F.scaled_dot_product_attention(qt, kt, vt, attn_mask=causal_lower_right(Nq, Nk))
+    np.testing.assert_allclose(o, ref.numpy(), rtol=0, atol=1e-12)
+    s = scale * qt @ kt.transpose(-1, -2)
+    mask = torch.ones(Nq, Nk, dtype=torch.bool).tril(diagonal=Nk - Nq)
+    ref_lse = torch.logsumexp(s.masked_fill(~mask, -math.inf), dim=-1)
+    np.testing.assert_allclose(lse, ref_lse.numpy(), rtol=0, atol=1e-12)
+
+
+def test_zero_query_bottom_right_gives_prefix_means():
+    """Q = 0, bottom-right: query i averages V[0 .. i + Nk - Nq] and its LSE
+    is ln(i + Nk - Nq + 1) (closed form)."""
+    Nq, Nk, D = 6, 15, 4
+    q = np.zeros((1, 1, Nq, D))
+    k, v = rnd((1, 1, Nk, D), 84), rnd((1, 1, Nk, D), 85)
+    o, lse = oracle.attention_fwd(q, k, v, causal="bottom_right")
+    n = np.arange(Nq) + (Nk - Nq) + 1
+    prefix = np.cumsum(v[0, 0], axis=0)[n - 1] / n[:, None]
+    np.testing.assert_allclose(o[0, 0], prefix, atol=1e-14)
+    np.testing.assert_allclose(lse[0, 0], np.log(n), atol=1e-14)
+    assert [oracle.attended_keys(i, Nk, "bottom_right", Nq) for i in range(Nq)] == list(n)
+
+
+def test_bottom_right_special_cases():
+    """Square: bottom-right is top-left.  The last query sees every key."""
+    q, k, v = rnd((1, 2, 11, 8), 86), rnd((1, 2, 11, 8), 87), rnd((1, 2, 11, 8), 88)
+    a = oracle.attention_fwd(q, k, v, causal="bottom_right")
+    b = oracle.attention_fwd(q, k, v, causal=True)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+    k2, v2 = rnd((1, 2, 30, 8), 89), rnd((1, 2, 30, 8), 90)
+    o, lse = oracle.attention_fwd(q, k2, v2, causal="bottom_right")
+    o_nc, lse_nc = oracle.attention_fwd(q[:, :, -1:], k2, v2)
+    np.testing.assert_allclose(o[:, :, -1:], o_nc, atol=1e-15)
+    np.testing.assert_allclose(lse[:, :, -1:], lse_nc, atol=1e-15)
+
+
+def test_bottom_right_argument_checks():
+    q, k = rnd((1, 1, 9, 4), 91), rnd((1, 1, 5, 4), 92)
+    with pytest.raises(RuntimeError):
+        oracle.attention_fwd(q, k, k, causal="bottom_right")   # Nq > Nk
+    with pytest.raises(RuntimeError):
+        oracle.attention_bwd(q[:, :, :5], k, k, q[:, :, :5], causal="bottom_right")
+
+
 def test_causal_row_zero_is_first_value():
     q, k, v = rnd((2, 2, 9, 8), 28), rnd((2, 2, 9, 8), 29), rnd((2, 2, 9, 8), 30)
     o, _ = oracle.attention_fwd(q, k, v, causal=True)

@@ -2,7 +2,7 @@
 
 A mutant is the oracle's own source with one plausible slip written into it
 (a dropped scale, a flipped exponent, a wrong GQA head, an off-by-one causal
-mask, a missing normalisation, V swapped for K, a log2 for a log, a missing
+mask (top-left or bottom-right), a missing normalisation, V swapped for K, a log2 for a log, a missing
 Delta or scale in the backward).  Each is compiled with gcc into a temporary
 library, swapped in for the real one, and run through a battery of the pins
 in test_oracle.py; the test passes only if the battery rejects it.  All on the
@@ -34,6 +34,8 @@ MUTANTS = {
                         "dk_head[j * D + d] += ds * q_row[d];"),
     "bwd_dv_transposed": ("dv_head[j * D + d] += p[j] * do_row[d];",
                           "dv_head[j * D + d] += p[j] * q_row[d];"),
+    "bottom_right_off_by_one": ("? i + (jb->Nk - jb->Nq) : i;", "? i + (jb->Nk - jb->Nq) - 1 : i;"),
+    "bottom_right_as_top_left": ("? i + (jb->Nk - jb->Nq) : i;", "? i : i;"),
 }
 
 
@@ -47,6 +49,9 @@ def battery():
         ("autograd_gqa", pins.test_backward_matches_torch_autograd, (4, 2, True)),
         ("prefix_means", pins.test_zero_query_causal_gives_prefix_means, ()),
         ("single_key", pins.test_single_key_returns_its_value_row, ()),
+        ("bottom_right", pins.test_bottom_right_matches_torch_causal_lower_right,
+         (2, 4, 2, 1, 23, 16)),
+        ("bottom_right_prefix", pins.test_zero_query_bottom_right_gives_prefix_means, ()),
     ]
     failed = []
     for name, fn, args in checks:

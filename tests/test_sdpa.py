@@ -66,3 +66,24 @@ def test_patched_torch_sdpa_runs_on_the_tiled_kernels(cuda_lib):
     o_ref, _ = oracle.attention_fwd(x["q"], x["k"], x["v"], causal=True)
     helpers.assert_close_elementwise(out.double().cpu().numpy(), o_ref, 1e-2, torch.bfloat16,
                                      "patched sdpa", "O")
+
+
+@pytest.mark.gpu
+def test_decode_shape_takes_the_split_path_and_trains(cuda_lib):
+    """One query per head against 5000 keys: the forward runs split (the
+    library picks several key ranges for this grid) and the backward uses its
+    LSE; both against the oracle."""
+    from tiled_memory_efficient_gb300 import _lib
+    assert _lib.num_splits(2, 14, 2, 1, 5000, 64) > 1
+    x = inputs.make_custom(2, 14, 2, 1, 5000, 64, torch.float16, seed=43, with_grad=True)
+    q, k, v = (x[n].cuda().requires_grad_(True) for n in ("q", "k", "v"))
+    out = sdpa.scaled_dot_product_attention(q, k, v, enable_gqa=True)
+    out.backward(x["do"].cuda())
+    o_ref, _ = oracle.attention_fwd(x["q"], x["k"], x["v"])
+    helpers.assert_close_elementwise(out.detach().double().cpu().numpy(), o_ref,
+                                     helpers.TOL_O[torch.float16], torch.float16, "decode", "O")
+    ref = oracle.attention_bwd(x["q"], x["k"], x["v"], x["do"])
+    for name, t, r in zip(("dq", "dk", "dv"), (q, k, v), ref):
+        helpers.assert_close_elementwise(t.grad.double().cpu().numpy(), r,
+                                         helpers.TOL_BWD[torch.float16], torch.float16,
+                                         "decode bwd", name)

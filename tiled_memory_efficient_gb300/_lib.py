@@ -26,6 +26,11 @@ ATTN_ERR_TIMEOUT = 5
 ATTN_ERR_WORKSPACE = 6
 ATTN_F16 = 0
 ATTN_BF16 = 1
+ATTN_CAUSAL_NONE = 0
+ATTN_CAUSAL_TOP_LEFT = 1
+ATTN_CAUSAL_BOTTOM_RIGHT = 2
+_CAUSAL_NAMES = {"none": ATTN_CAUSAL_NONE, "top_left": ATTN_CAUSAL_TOP_LEFT,
+                 "bottom_right": ATTN_CAUSAL_BOTTOM_RIGHT}
 
 _lock = threading.Lock()
 _lib = None
@@ -35,6 +40,10 @@ _i = ctypes.c_int
 _SIGNATURES = {
     "attn_fwd": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i, _vp],
                  _i),
+    "attn_fwd_splitkv": ([_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _i, _i, _i, _i, _i, _i,
+                          ctypes.c_float, _i, _i, _i, _vp], _i),
+    "attn_fwd_splitkv_workspace_size": ([_i, _i, _i, _i, _i, _i, _i], ctypes.c_size_t),
+    "attn_fwd_num_splits": ([_i, _i, _i, _i, _i, _i, _i], _i),
     "attn_bwd_workspace_size": ([_i, _i, _i, _i, _i, _i, _i], ctypes.c_size_t),
     "attn_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
                   _i, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i, _vp], _i),
@@ -95,6 +104,21 @@ def _dtype_code(t) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}: use float16 or bfloat16")
 
 
+def causal_code(causal) -> int:
+    """Mask code of the C ABI: False/None -> none, True -> top-left (the SDPA
+    is_causal convention), or one of "none", "top_left", "bottom_right", or
+    the integer code itself."""
+    if causal is None or causal is False:
+        return ATTN_CAUSAL_NONE
+    if causal is True:
+        return ATTN_CAUSAL_TOP_LEFT
+    if isinstance(causal, str):
+        if causal not in _CAUSAL_NAMES:
+            raise ValueError(f"causal must be one of {sorted(_CAUSAL_NAMES)}, got {causal!r}")
+        return _CAUSAL_NAMES[causal]
+    return int(causal)
+
+
 def _check(q, k, v):
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not t.is_cuda:
@@ -109,11 +133,12 @@ def _check(q, k, v):
         raise ValueError(f"shapes q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
 
 
-def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None):
+def attn_fwd(q, k, v, causal=False, scale: float | None = None, out=None, lse=None):
     """O, LSE = attention(q, k, v).  q [B,Hq,Nq,D]; k, v [B,Hkv,Nk,D] (CUDA).
 
     Returns (out [B,Hq,Nq,D] in q's dtype, lse [B,Hq,Nq] fp32 natural log).
-    Enqueued on torch's current stream; no synchronisation.
+    causal: see causal_code.  Enqueued on torch's current stream; no
+    synchronisation.
     """
     import torch
     _check(q, k, v)
@@ -126,10 +151,53 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None
     if lse is None:
         lse = torch.empty((B, Hq, Nq), device=q.device, dtype=torch.float32)
     rc = load().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                         lse.data_ptr(), B, Hq, Hkv, Nq, Nk, D, float(scale), int(bool(causal)),
+                         lse.data_ptr(), B, Hq, Hkv, Nq, Nk, D, float(scale), causal_code(causal),
                          _dtype_code(q), _stream_handle(q.device))
     if rc != ATTN_OK:
         raise AttnError("attn_fwd", rc)
+    return out, lse
+
+
+def num_splits(B, Hq, Hkv, Nq, Nk, D, num_sms: int = 0) -> int:
+    """The library's key-range count for attn_fwd_splitkv (num_sms 0: ask the
+    current device)."""
+    return load().attn_fwd_num_splits(B, Hq, Hkv, Nq, Nk, D, int(num_sms))
+
+
+def splitkv_workspace_size(B, Hq, Hkv, Nq, Nk, D, splits: int) -> int:
+    return load().attn_fwd_splitkv_workspace_size(B, Hq, Hkv, Nq, Nk, D, int(splits))
+
+
+def attn_fwd_splitkv(q, k, v, causal=False, scale: float | None = None, splits: int | None = None,
+                     out=None, lse=None, workspace=None):
+    """attn_fwd with the keys cut into ``splits`` ranges (None: the library's
+    choice for this device) and the partial results merged; for short query
+    blocks against long keys, e.g. decoding against a KV cache (use
+    causal="bottom_right" when the queries are the newest positions)."""
+    import torch
+    _check(q, k, v)
+    B, Hq, Nq, D = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    lib = load()
+    if splits is None:
+        splits = lib.attn_fwd_num_splits(B, Hq, Hkv, Nq, Nk, D, 0)
+    ws_bytes = lib.attn_fwd_splitkv_workspace_size(B, Hq, Hkv, Nq, Nk, D, int(splits))
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes, device=q.device, dtype=torch.uint8)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), device=q.device, dtype=torch.float32)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib.attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                              lse.data_ptr(), ws_ptr, ws_len, B, Hq, Hkv, Nq, Nk, D, float(scale),
+                              causal_code(causal), _dtype_code(q), int(splits),
+                              _stream_handle(q.device))
+    if rc != ATTN_OK:
+        raise AttnError("attn_fwd_splitkv", rc)
     return out, lse
 
 
@@ -153,7 +221,7 @@ def attn_bwd(q, k, v, out, dout, lse, causal: bool = False, scale: float | None 
     rc = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), dout.data_ptr(),
                       lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                       workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                      B, Hq, Hkv, Nq, Nk, D, float(scale), int(bool(causal)), dt,
+                      B, Hq, Hkv, Nq, Nk, D, float(scale), causal_code(causal), dt,
                       _stream_handle(q.device))
     if rc != ATTN_OK:
         raise AttnError("attn_bwd", rc)

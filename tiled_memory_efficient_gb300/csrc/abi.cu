@@ -20,6 +20,7 @@ __device__ unsigned int g_status;
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr int kMaxSplits = 256;  // key ranges of one split forward, at most
 std::mutex g_mu;
 unsigned int* g_status_ptr[kMaxDevices] = {};
 int g_cc_ok[kMaxDevices] = {};  // 0 unknown, 1 sm_103, -1 other
@@ -131,12 +132,31 @@ __global__ void selftest_timeout_kernel(unsigned long long wait_ns, unsigned int
 
 using namespace tme;
 
-extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
-                        int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal,
-                        int dtype, void* stream) {
+namespace tme {
+namespace {
+
+int64_t key_tiles(int Nk) { return (static_cast<int64_t>(Nk) + 127) / 128; }
+
+// Ranges actually used for a requested count: every range gets
+// ceil(tiles / requested) key tiles, and no range is left empty.
+int effective_splits(int Nk, int requested) {
+    const int64_t tiles = key_tiles(Nk);
+    if (requested <= 1) return 1;
+    if (requested > tiles) requested = static_cast<int>(tiles);
+    const int64_t per = (tiles + requested - 1) / requested;
+    return static_cast<int>((tiles + per - 1) / per);
+}
+
+// Checks shared by the forward entry points; fills everything in FwdParams
+// but the split fields.
+int fwd_prepare(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal, int dtype,
+                CUtensorMap* tmQ, CUtensorMap* tmK, CUtensorMap* tmV, FwdParams* p) {
     if (!q || !k || !v || !out || !lse) return ATTN_ERR_INVALID;
     int rc = check_shape(B, Hq, Hkv, Nq, Nk, D, scale, dtype);
     if (rc != ATTN_OK) return rc;
+    if (causal < ATTN_CAUSAL_NONE || causal > ATTN_CAUSAL_BOTTOM_RIGHT) return ATTN_ERR_INVALID;
+    if (causal == ATTN_CAUSAL_BOTTOM_RIGHT && Nq > Nk) return ATTN_ERR_INVALID;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
         return ATTN_ERR_ALIGN;
     unsigned int* status = nullptr;
@@ -147,24 +167,112 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, 
     const int64_t G = Hq / Hkv;
     const int64_t rows = G * Nq;
     const int64_t groups = static_cast<int64_t>(B) * Hkv;
-    CUtensorMap tmQ, tmK, tmV;
-    if (make_map(&tmQ, q, bf16, D, rows, groups) != ATTN_OK ||
-        make_map(&tmK, k, bf16, D, Nk, groups) != ATTN_OK ||
-        make_map(&tmV, v, bf16, D, Nk, groups) != ATTN_OK)
+    if (make_map(tmQ, q, bf16, D, rows, groups) != ATTN_OK ||
+        make_map(tmK, k, bf16, D, Nk, groups) != ATTN_OK ||
+        make_map(tmV, v, bf16, D, Nk, groups) != ATTN_OK)
         return ATTN_ERR_CUDA;
 
-    FwdParams p{};
-    p.out = out;
-    p.lse = lse;
-    p.status = status;
-    p.rows_per_group = rows;
-    p.Nq = Nq;
-    p.Nk = Nk;
-    p.n_groups = static_cast<int>(groups);
-    p.n_pairs = static_cast<int>((rows + 255) / 256);
-    p.scale_log2 = scale * 1.4426950408889634f;
-    const cudaError_t e = launch_fwd(D, bf16, causal != 0, tmQ, tmK, tmV, p,
-                                     static_cast<cudaStream_t>(stream));
+    *p = FwdParams{};
+    p->out = out;
+    p->lse = lse;
+    p->status = status;
+    p->rows_per_group = rows;
+    p->total_rows = rows * groups;
+    p->Nq = Nq;
+    p->Nk = Nk;
+    p->causal_off = causal == ATTN_CAUSAL_BOTTOM_RIGHT ? Nk - Nq : 0;
+    p->n_groups = static_cast<int>(groups);
+    p->n_pairs = static_cast<int>((rows + 255) / 256);
+    p->n_splits = 1;
+    p->tiles_per_split = static_cast<int>(key_tiles(Nk));
+    p->scale_log2 = scale * 1.4426950408889634f;
+    return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace tme
+
+extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                        int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal,
+                        int dtype, void* stream) {
+    CUtensorMap tmQ, tmK, tmV;
+    FwdParams p;
+    const int rc = fwd_prepare(q, k, v, out, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype,
+                               &tmQ, &tmK, &tmV, &p);
+    if (rc != ATTN_OK) return rc;
+    const cudaError_t e = launch_fwd(D, dtype == ATTN_BF16, causal != ATTN_CAUSAL_NONE, tmQ, tmK,
+                                     tmV, p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+extern "C" int attn_fwd_num_splits(int B, int Hq, int Hkv, int Nq, int Nk, int D, int num_sms) {
+    if (check_shape(B, Hq, Hkv, Nq, Nk, D, 1.0f, ATTN_F16) != ATTN_OK) return 1;
+    if (num_sms <= 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            num_sms <= 0)
+            return 1;
+    }
+    // One CTA per SM (shared memory and the 512 TMEM columns): fill one wave
+    // of CTAs, keeping at least two key tiles per range.
+    const int64_t rows = static_cast<int64_t>(Hq / Hkv) * Nq;
+    const int64_t units = static_cast<int64_t>(B) * Hkv * ((rows + 255) / 256);
+    if (units >= num_sms) return 1;
+    int64_t want = num_sms / units;
+    const int64_t by_len = key_tiles(Nk) / 2;
+    if (want > by_len) want = by_len;
+    if (want > kMaxSplits) want = kMaxSplits;
+    return effective_splits(Nk, static_cast<int>(want < 1 ? 1 : want));
+}
+
+extern "C" size_t attn_fwd_splitkv_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int D,
+                                                  int num_splits) {
+    if (check_shape(B, Hq, Hkv, Nq, Nk, D, 1.0f, ATTN_F16) != ATTN_OK) return 0;
+    if (num_splits < 1 || num_splits > kMaxSplits) return 0;
+    const int splits = effective_splits(Nk, num_splits);
+    if (splits == 1) return 0;
+    const size_t rows = static_cast<size_t>(B) * Hq * Nq;
+    const size_t o_bytes = (static_cast<size_t>(splits) * rows * D * sizeof(float) + 255) & ~size_t(255);
+    const size_t l_bytes = (static_cast<size_t>(splits) * rows * sizeof(float) + 255) & ~size_t(255);
+    return o_bytes + l_bytes;
+}
+
+extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* out, float* lse,
+                                void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+                                int Nq, int Nk, int D, float scale, int causal, int dtype,
+                                int num_splits, void* stream) {
+    if (num_splits < 1 || num_splits > kMaxSplits) return ATTN_ERR_INVALID;
+    int rc = check_shape(B, Hq, Hkv, Nq, Nk, D, scale, dtype);
+    if (rc != ATTN_OK) return rc;
+    const int splits = effective_splits(Nk, num_splits);
+    if (splits > 1) {
+        // Workspace checks come before any device call.
+        if (!workspace) return ATTN_ERR_INVALID;
+        if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
+        if (workspace_bytes < attn_fwd_splitkv_workspace_size(B, Hq, Hkv, Nq, Nk, D, num_splits))
+            return ATTN_ERR_WORKSPACE;
+    }
+    CUtensorMap tmQ, tmK, tmV;
+    FwdParams p;
+    rc = fwd_prepare(q, k, v, out, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype, &tmQ, &tmK,
+                     &tmV, &p);
+    if (rc != ATTN_OK) return rc;
+    const bool bf16 = dtype == ATTN_BF16;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (splits > 1) {
+        if (static_cast<long long>(p.n_groups) * p.n_pairs * splits > 0x7fffffffll)
+            return ATTN_ERR_UNSUPPORTED;
+        const int64_t tiles = key_tiles(Nk);
+        p.n_splits = splits;
+        p.tiles_per_split = static_cast<int>((tiles + num_splits - 1) / num_splits);
+        const size_t o_bytes =
+            (static_cast<size_t>(splits) * p.total_rows * D * sizeof(float) + 255) & ~size_t(255);
+        p.o_part = static_cast<float*>(workspace);
+        p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes);
+    }
+    cudaError_t e = launch_fwd(D, bf16, causal != ATTN_CAUSAL_NONE, tmQ, tmK, tmV, p, st);
+    if (e == cudaSuccess && splits > 1) e = launch_splitkv_merge(D, bf16, p, st);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -187,6 +295,8 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
         return ATTN_ERR_INVALID;
     int rc = check_shape(B, Hq, Hkv, Nq, Nk, D, scale, dtype);
     if (rc != ATTN_OK) return rc;
+    if (causal == ATTN_CAUSAL_BOTTOM_RIGHT) return ATTN_ERR_UNSUPPORTED;
+    if (causal != ATTN_CAUSAL_NONE && causal != ATTN_CAUSAL_TOP_LEFT) return ATTN_ERR_INVALID;
     const void* ptrs[] = {q, k, v, out, dout, lse, dq, dk, dv, workspace};
     for (const void* ptr : ptrs)
         if (!aligned16(ptr)) return ATTN_ERR_ALIGN;

@@ -113,8 +113,50 @@ __device__ __forceinline__ int kv_tiles_for(int64_t row0, const FwdParams& p, bo
     if (!causal) return (p.Nk + kRows - 1) / kRows;
     const int64_t last = min(row0 + kRows - 1, p.rows_per_group - 1);
     const int64_t max_pos = (row0 / p.Nq == last / p.Nq) ? (last % p.Nq) : (p.Nq - 1);
-    const int64_t keys = (max_pos + 1 < p.Nk) ? (max_pos + 1) : static_cast<int64_t>(p.Nk);
+    // keys [0, max_pos + causal_off] are visible to the tile's last row
+    int64_t keys = max_pos + p.causal_off + 1;
+    if (keys > p.Nk) keys = p.Nk;
+    if (keys <= 0) return 0;
     return static_cast<int>((keys + kRows - 1) / kRows);
+}
+
+// Key tiles of [kt0, kt0 + tiles_per_split) below a tile's limit n_full.
+__device__ __forceinline__ int tiles_in_range(int n_full, int kt0, const FwdParams& p) {
+    const int end = n_full < kt0 + p.tiles_per_split ? n_full : kt0 + p.tiles_per_split;
+    return end > kt0 ? end - kt0 : 0;
+}
+
+// Epilogue stores.  Normal mode: 32 output columns of row `grow` rounded to
+// the 16-bit dtype (4 x 16-byte stores) and the row's LSE.  Split mode: the
+// same values in fp32 to this key range's partial arrays.
+template <int D, bool BF16>
+__device__ __forceinline__ void store_o32(const FwdParams& p, int split, int64_t grow, int c,
+                                          const uint32_t (&o)[32], float inv_l) {
+    if (p.n_splits > 1) {
+        float4* dst = reinterpret_cast<float4*>(
+            p.o_part + (static_cast<int64_t>(split) * p.total_rows + grow) * D + c * 32);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                                 __uint_as_float(o[4 * i + 2]) * inv_l,
+                                 __uint_as_float(o[4 * i + 3]) * inv_l);
+    } else {
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            w[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + grow * D + c * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    }
+}
+
+__device__ __forceinline__ void store_lse(const FwdParams& p, int split, int64_t grow, float v) {
+    if (p.n_splits > 1)
+        p.lse_part[static_cast<int64_t>(split) * p.total_rows + grow] = v;
+    else
+        p.lse[grow] = v;
 }
 
 // Maximum of 64 values (three-input max tree).
@@ -172,11 +214,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     // Work unit: consecutive CTAs share a KV group (its K/V stay hot in L2),
     // and within a group the heaviest pair goes first (under the causal mask
     // the last rows of a head attend to the most keys).
-    const int group = static_cast<int>(blockIdx.x / p.n_pairs);
-    const int pair = p.n_pairs - 1 - static_cast<int>(blockIdx.x % p.n_pairs);
+    // With split keys, the CTAs of one (group, pair) are adjacent and each
+    // takes the key tiles [kt0, kt0 + tiles_per_split).
+    const int split = static_cast<int>(blockIdx.x % p.n_splits);
+    const int unit = static_cast<int>(blockIdx.x / p.n_splits);
+    const int group = unit / p.n_pairs;
+    const int pair = p.n_pairs - 1 - unit % p.n_pairs;
     const int64_t row_base = static_cast<int64_t>(pair) * (2 * kRows);
-    const int n0 = kv_tiles_for(row_base, p, CAUSAL);
-    const int n1 = kv_tiles_for(row_base + kRows, p, CAUSAL);
+    const int kt0 = split * p.tiles_per_split;
+    const int n0 = tiles_in_range(kv_tiles_for(row_base, p, CAUSAL), kt0, p);
+    const int n1 = tiles_in_range(kv_tiles_for(row_base + kRows, p, CAUSAL), kt0, p);
     const int nmax = n0 > n1 ? n0 : n1;
 
     if (threadIdx.x == 0) {
@@ -233,7 +280,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
                 mbar_arrive_expect_tx(&k_full[ks], C::kTileBytes);
                 for (int kb = 0; kb < KB; ++kb)
                     tma_load_3d(&tmK, &k_full[ks], sK + ks * C::kTileBytes + kb * (kRows * 128),
-                                kb * 64, j * kRows, group);
+                                kb * 64, (kt0 + j) * kRows, group);
                 ++nk;
                 const int vs = j % VS;
                 for (int t = 0; okp && t < 2; ++t)
@@ -243,7 +290,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
                 mbar_arrive_expect_tx(&v_full[vs], C::kTileBytes);
                 for (int kb = 0; kb < KB; ++kb)
                     tma_load_3d(&tmV, &v_full[vs], sV + vs * C::kTileBytes + kb * (kRows * 128),
-                                kb * 64, j * kRows, group);
+                                kb * 64, (kt0 + j) * kRows, group);
                 ++nv;
             }
             // Never leave a copy in flight into shared memory we are about to give up.
@@ -382,10 +429,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             tc_fence_before();
             mbar_arrive(&s_free[t]);
 
-            const int key0 = j * kRows + 64 * h;
-            const bool need_mask = (key0 + 64 > p.Nk) || (CAUSAL && key0 + 63 > warp_min_pos);
+            const int key0 = (kt0 + j) * kRows + 64 * h;
+            const bool need_mask =
+                (key0 + 64 > p.Nk) || (CAUSAL && key0 + 63 > warp_min_pos + p.causal_off);
             if (need_mask) {
-                const int lim = CAUSAL ? min(p.Nk, pos + 1) : p.Nk;  // keys [0, lim) allowed
+                // keys [0, lim) allowed
+                const int lim = CAUSAL ? min(p.Nk, pos + p.causal_off + 1) : p.Nk;
 #pragma unroll
                 for (int c = 0; c < 2; ++c)
 #pragma unroll
@@ -457,29 +506,26 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             const float l_out = BF16 ? lrt : lt;
             const float inv_l = l_out > 0.0f ? 1.0f / l_out : 0.0f;
             const int64_t grow = static_cast<int64_t>(group) * p.rows_per_group + row;
-            uint16_t* out = static_cast<uint16_t*>(p.out) + grow * D;
 #pragma unroll
             for (int c = h * (D / 64); c < (h + 1) * (D / 64); ++c) {
                 uint32_t o[32];
                 tmem_ld32(tO + c * 32, o);
                 tmem_wait_ld();
                 reg_fence(o);
-                if (ok && row_valid) {
-                    uint32_t w[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        w[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l,
-                                           __uint_as_float(o[2 * i + 1]) * inv_l);
-                    uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-                }
+                if (ok && row_valid) store_o32<D, BF16>(p, split, grow, c, o, inv_l);
             }
             if (ok && row_valid && h == 0) {
                 const float m_sub = (m == -INFINITY) ? 0.0f : m;
-                p.lse[grow] = lt > 0.0f ? (m_sub + lg2_approx(lt)) * kLn2 : -INFINITY;
+                store_lse(p, split, grow, lt > 0.0f ? (m_sub + lg2_approx(lt)) * kLn2 : -INFINITY);
             }
+        } else if (p.n_splits > 1 && row_valid) {
+            // No key of this range is visible to the tile: an empty partial.
+            const int64_t grow = static_cast<int64_t>(group) * p.rows_per_group + row;
+            const uint32_t z[32] = {};
+#pragma unroll
+            for (int c = h * (D / 64); c < (h + 1) * (D / 64); ++c)
+                store_o32<D, BF16>(p, split, grow, c, z, 0.0f);
+            if (h == 0) store_lse(p, split, grow, -INFINITY);
         }
     } else if (!C::kSplit && warp < C::kSoftmaxWarps) {
         // ------------------------------------------------------------ softmax + epilogue
@@ -521,10 +567,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
                 mbar_arrive(&s_free[t]);
             }
 
-            const int key0 = j * kRows;
-            const bool need_mask = (key0 + kRows > p.Nk) || (CAUSAL && key0 + kRows - 1 > warp_min_pos);
+            const int key0 = (kt0 + j) * kRows;
+            const bool need_mask =
+                (key0 + kRows > p.Nk) || (CAUSAL && key0 + kRows - 1 > warp_min_pos + p.causal_off);
             if (need_mask) {
-                const int lim = CAUSAL ? min(p.Nk, pos + 1) : p.Nk;  // keys [0, lim) allowed
+                // keys [0, lim) allowed
+                const int lim = CAUSAL ? min(p.Nk, pos + p.causal_off + 1) : p.Nk;
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -596,29 +644,25 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             const float l_out = BF16 ? lr : l;
             const float inv_l = l_out > 0.0f ? 1.0f / l_out : 0.0f;
             const int64_t grow = static_cast<int64_t>(group) * p.rows_per_group + row;
-            uint16_t* out = static_cast<uint16_t*>(p.out) + grow * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
                 tmem_ld32(tO + c * 32, o);
                 tmem_wait_ld();
                 reg_fence(o);
-                if (row_valid) {
-                    uint32_t w[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        w[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l,
-                                           __uint_as_float(o[2 * i + 1]) * inv_l);
-                    uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-                }
+                if (row_valid) store_o32<D, BF16>(p, split, grow, c, o, inv_l);
             }
             if (row_valid) {
                 const float m_sub = (m == -INFINITY) ? 0.0f : m;
-                p.lse[grow] = l > 0.0f ? (m_sub + lg2_approx(l)) * kLn2 : -INFINITY;
+                store_lse(p, split, grow, l > 0.0f ? (m_sub + lg2_approx(l)) * kLn2 : -INFINITY);
             }
+        } else if (n_t == 0 && p.n_splits > 1 && row_valid) {
+            // No key of this range is visible to the tile: an empty partial.
+            const int64_t grow = static_cast<int64_t>(group) * p.rows_per_group + row;
+            const uint32_t z[32] = {};
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) store_o32<D, BF16>(p, split, grow, c, z, 0.0f);
+            store_lse(p, split, grow, -INFINITY);
         }
     }
 
@@ -641,7 +685,7 @@ cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
     // whichever device is current.
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const long long ctas = static_cast<long long>(p.n_groups) * p.n_pairs;
+    const long long ctas = static_cast<long long>(p.n_groups) * p.n_pairs * p.n_splits;
     return launch_kernel(kern, dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, stream,
                          tmQ, tmK, tmV, p);
 }

@@ -21,14 +21,25 @@ inline cudaError_t launch_kernel(void (*kern)(Params...), dim3 grid, dim3 block,
 // Forward launch parameters (everything the kernel needs besides the three
 // tensor maps).  Row indices are "flattened": within KV group g of batch b the
 // G query heads that share that KV head form G*Nq consecutive rows, head-major.
+// With n_splits > 1 the keys are cut into n_splits ranges of tiles_per_split
+// 128-key tiles, one CTA per (group, pair of Q tiles, range); each CTA writes
+// its range's normalised partial output and LSE in fp32 to o_part / lse_part
+// ([n_splits][n_groups * rows_per_group][D] and [n_splits][...]) instead of
+// out / lse, and splitkv_merge combines them.
 struct FwdParams {
     void* out;               // [B, Hq, Nq, D] fp16/bf16
     float* lse;              // [B, Hq, Nq] fp32, natural log
+    float* o_part;           // split mode: partial outputs (fp32)
+    float* lse_part;         // split mode: partial LSEs (fp32)
     unsigned int* status;    // device status word
     int64_t rows_per_group;  // G * Nq
+    int64_t total_rows;      // n_groups * rows_per_group
     int Nq, Nk;
+    int causal_off;          // causal: position i sees keys j <= i + causal_off
     int n_groups;            // B * Hkv
-    int n_pairs;             // ceil(rows_per_group / 256): CTAs per group
+    int n_pairs;             // ceil(rows_per_group / 256): CTAs per group and key range
+    int n_splits;            // key ranges (1: no split)
+    int tiles_per_split;     // 128-key tiles per range
     float scale_log2;        // scale * log2(e)
 };
 
@@ -36,6 +47,9 @@ struct FwdParams {
 cudaError_t launch_fwd(int D, bool bf16, bool causal, const CUtensorMap& tmQ,
                        const CUtensorMap& tmK, const CUtensorMap& tmV, const FwdParams& p,
                        cudaStream_t stream);
+
+// Combines the n_splits partial results of a split forward into out / lse.
+cudaError_t launch_splitkv_merge(int D, bool bf16, const FwdParams& p, cudaStream_t stream);
 
 // Backward launch parameters.  The workspace holds two fp32 arrays laid out
 // per KV group with rows_pad = n_qtiles * 128 rows each (so every 128-row

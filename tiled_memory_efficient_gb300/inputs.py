@@ -15,7 +15,10 @@ Workload shapes follow the pages:
     self-attention, 24 heads): D=128, bf16, non-causal, with 1% of key rows
     scaled by 8 so that the softmax sees a wide range of scores;
   * the autograd tier's training use (section "Other areas where this could
-    be useful"): B=2, H=16, D=128, bf16, causal, plus an upstream gradient.
+    be useful"): B=2, H=16, D=128, bf16, causal, plus an upstream gradient;
+  * decoding with that GQA model against a KV cache (the inference side of
+    the LLM table): one new query per head, contexts of 1K to 64K cached keys,
+    8 sequences at once, bottom-right causal.
 Every tensor is drawn as fp32 N(0,1) from a torch CPU generator and rounded
 once to the workload's dtype.
 """
@@ -35,16 +38,38 @@ class Workload:
     Hkv: int
     D: int
     dtype: torch.dtype
-    causal: bool
-    seq_lens: tuple
+    causal: object        # False, True (top-left) or "bottom_right"
+    seq_lens: tuple       # key counts Nk (and query counts, unless nq is set)
     outlier_keys: bool = False   # scale 1% of key rows by 8
     with_grad: bool = False      # also draw an upstream gradient dO
+    nq: int | None = None        # fixed query count (decode); None: Nq = Nk = n
     note: str = ""
 
+    def queries(self, n: int) -> int:
+        return n if self.nq is None else self.nq
+
     def flops_fwd(self, n: int) -> float:
-        """Algorithmic forward FLOPs 4*B*Hq*Nq*Nk*D, halved under the causal mask."""
-        f = 4.0 * self.B * self.Hq * n * n * self.D
-        return f / 2 if self.causal else f
+        """Algorithmic forward FLOPs 4*B*Hq*Nq*Nk*D, halved under the causal
+        mask when Nq = Nk; with a fixed query count, 4*D per visible
+        (query, key) pair."""
+        if self.nq is None:
+            f = 4.0 * self.B * self.Hq * n * n * self.D
+            return f / 2 if self.causal else f
+        nq = self.nq
+        if self.causal == "bottom_right":   # query i sees n - nq + i + 1 keys
+            pairs = nq * (n - nq) + nq * (nq + 1) / 2
+        elif self.causal:                   # top-left: query i sees min(i + 1, n)
+            pairs = sum(min(i + 1, n) for i in range(nq))
+        else:
+            pairs = nq * n
+        return 4.0 * self.B * self.Hq * pairs * self.D
+
+    def bytes_fwd(self, n: int) -> float:
+        """Algorithmic forward bytes: read Q, K, V once, write O and LSE."""
+        e = 2  # fp16 / bf16
+        nq = self.queries(n)
+        return (2.0 * self.B * self.Hq * nq * self.D * e + 2.0 * self.B * self.Hkv * n * self.D * e
+                + 4.0 * self.B * self.Hq * nq)
 
 
 WORKLOADS = {
@@ -61,6 +86,10 @@ WORKLOADS = {
                           note="video-DiT self-attention H=24 D=128 bf16, 1% keys x8"),
     "training": Workload("training", 4, 2, 16, 16, 128, torch.bfloat16, True, (8192,),
                          with_grad=True, note="training fwd+bwd B=2 H=16 D=128 bf16 causal"),
+    "gqa_decode": Workload("gqa_decode", 5, 8, 14, 2, 64, torch.float16, "bottom_right",
+                           (1024, 4096, 16384, 65536), nq=1,
+                           note="GQA KV-cache decode B=8 Hq=14 Hkv=2 D=64 fp16, 1 query, "
+                                "bottom-right causal"),
 }
 
 
@@ -71,12 +100,13 @@ def seed_for(w: Workload, n: int) -> int:
 def make_inputs(w: Workload, n: int, nk: int | None = None, seed: int | None = None):
     """Return dict(q, k, v[, do]) as CPU tensors of the workload's dtype.
 
-    q: [B,Hq,n,D]; k, v: [B,Hkv,nk,D] (nk defaults to n).
+    q: [B,Hq,nq,D] with nq = w.nq or n; k, v: [B,Hkv,nk,D] (nk defaults to n).
     """
     nk = n if nk is None else nk
+    nq = w.queries(n)
     g = torch.Generator(device="cpu")
     g.manual_seed(seed_for(w, n) if seed is None else seed)
-    q = torch.randn((w.B, w.Hq, n, w.D), generator=g, dtype=torch.float32)
+    q = torch.randn((w.B, w.Hq, nq, w.D), generator=g, dtype=torch.float32)
     k = torch.randn((w.B, w.Hkv, nk, w.D), generator=g, dtype=torch.float32)
     v = torch.randn((w.B, w.Hkv, nk, w.D), generator=g, dtype=torch.float32)
     if w.outlier_keys:
@@ -87,7 +117,7 @@ def make_inputs(w: Workload, n: int, nk: int | None = None, seed: int | None = N
                 k[b, h, idx, :] *= 8.0
     out = {"q": q.to(w.dtype), "k": k.to(w.dtype), "v": v.to(w.dtype)}
     if w.with_grad:
-        out["do"] = torch.randn((w.B, w.Hq, n, w.D), generator=g,
+        out["do"] = torch.randn((w.B, w.Hq, nq, w.D), generator=g,
                                 dtype=torch.float32).to(w.dtype)
     return out
 

@@ -35,7 +35,16 @@ class _TiledAttention(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, is_causal, scale):
         q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
-        out, lse = _lib.attn_fwd(q, k, v, causal=is_causal, scale=scale)
+        B, Hq, Nq, D = q.shape
+        Hkv, Nk = k.shape[1], k.shape[2]
+        # Short query blocks against long keys (decode) leave most SMs idle
+        # in one CTA per query-tile pair: cut the keys into ranges then.
+        splits = _lib.num_splits(B, Hq, Hkv, Nq, Nk, D)
+        if splits > 1:
+            out, lse = _lib.attn_fwd_splitkv(q, k, v, causal=is_causal, scale=scale,
+                                             splits=splits)
+        else:
+            out, lse = _lib.attn_fwd(q, k, v, causal=is_causal, scale=scale)
         ctx.save_for_backward(q, k, v, out, lse)
         ctx.is_causal = is_causal
         ctx.scale = scale
