@@ -106,10 +106,16 @@ struct BwdCfg {
 };
 
 // ---------------------------------------------------------------- dK / dV
-// TMEM: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D,256+2D).
-// Warpgroup h owns query columns [64h, 64h+64) of S^T and dP^T and packs its
-// P^T / dS^T into the first 32 of its own 64 columns, so the PV-type products
-// read A from columns [0,32) and [64,96) (P^T), [128,160) and [192,224) (dS^T).
+// Each 128-query tile is processed as two halves of 64 queries, one per
+// elementwise warpgroup, so that the tensor core works on one half while the
+// other half's P^T / dS^T are computed.  TMEM: half u holds S^T_u at
+// [128u, 128u+64) and dP^T_u at [128u+64, 128u+128) (M = 128 keys, N = 64
+// queries); its warpgroup packs P^T_u / dS^T_u into the first 32 columns of
+// each.  dV at [256, 256+D), dK at [256+D, 256+2D).
+// MMA order per tile n: for u = 0, 1: dV/dK += (half u of tile n) as soon as
+// its P^T / dS^T are in TMEM, then S^T / dP^T of half u of tile n+1 into the
+// same columns (the tensor pipe runs in order, so the products of tile n have
+// read them first).
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -131,9 +137,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* kv_full = bars;
     uint64_t* q_full = kv_full + 1;    // [QS]
     uint64_t* q_empty = q_full + QS;   // [QS]
-    uint64_t* s_full = q_empty + QS;   // S^T and dP^T in TMEM
-    uint64_t* p_full = s_full + 1;     // P^T and dS^T in TMEM (256 arrivals)
-    uint64_t* acc_full = p_full + 1;   // last dV / dK product done
+    uint64_t* s_full = q_empty + QS;   // [2] S^T_u and dP^T_u in TMEM
+    uint64_t* p_full = s_full + 2;     // [2] P^T_u and dS^T_u in TMEM (128 arrivals)
+    uint64_t* acc_full = p_full + 2;   // last dV / dK product done
     uint64_t* mma_done = acc_full + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -150,8 +156,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
         for (int i = 0; i < QS; ++i) { mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1); }
-        mbar_init(s_full, 1);
-        mbar_init(p_full, 256);
+        for (int u = 0; u < 2; ++u) {
+            mbar_init(&s_full[u], 1);
+            mbar_init(&p_full[u], 128);
+        }
         mbar_init(acc_full, 1);
         mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -194,58 +202,82 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait_bounded(&q_full[m % QS], (m / QS) & 1, p.status);
         }
     } else if (warp == kMmaWarp) {
-        constexpr uint32_t idesc_s = idesc_f16(kRows, kRows, BF16, false);
+        constexpr uint32_t idesc_s = idesc_f16(kRows, 64, BF16, false);  // 128 keys x 64 queries
         constexpr uint32_t idesc_g = idesc_f16(kRows, D, BF16, true);
         constexpr uint64_t kStep = TB >> 4;
         constexpr uint64_t kBlk = (kRows * 128) >> 4;
+        // 64 rows of a 128-byte-swizzled tile, in 16-byte descriptor units:
+        // query half u starts 64u rows into the Q / dO tiles (the N rows of
+        // the K-major view, the K rows of the MN-major view).
+        constexpr uint64_t kHalf = (64 * 128) >> 4;
         const uint64_t dK_ = smem_desc_sw128(smem_u32(sK), 16, 1024);
         const uint64_t dV_ = smem_desc_sw128(smem_u32(sV), 16, 1024);
         const uint64_t dQk = smem_desc_sw128(smem_u32(sQ), 16, 1024);
         const uint64_t dDOk = smem_desc_sw128(smem_u32(sDO), 16, 1024);
         const uint64_t dQm = smem_desc_sw128(smem_u32(sQ), kRows * 128, 1024);
         const uint64_t dDOm = smem_desc_sw128(smem_u32(sDO), kRows * 128, 1024);
+        // S^T_u = K Q_u^T and dP^T_u = V dO_u^T of the tile in `slot`.
+        auto issue_sdp = [&](int slot, int u) {
+            const uint32_t d = tmem + 128 * u;
+#pragma unroll
+            for (int kb = 0; kb < KB; ++kb)
+                mma_ss_k64(d, dK_ + kb * kBlk, dQk + slot * kStep + kb * kBlk + u * kHalf, idesc_s,
+                           kb > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kb = 0; kb < KB; ++kb)
+                mma_ss_k64(d + 64, dV_ + kb * kBlk, dDOk + slot * kStep + kb * kBlk + u * kHalf,
+                           idesc_s, kb > 0 ? 1u : 0u);
+            mma_commit_elect(&s_full[u]);
+        };
+        int n_vis = 0;   // query tiles this key tile meets (the producer loads them in order)
+        for (int qi = 0; qi < p.n_qtiles; ++qi) n_vis += visit(qi) ? 1 : 0;
         warp_wait(kv_full, 0, abort_flag, p.status);
-        int n = 0;
-        for (int qi = 0; qi < p.n_qtiles; ++qi) {
-            if (!visit(qi)) continue;
-            const int slot = n % QS;
-            warp_wait(&q_full[slot], (n / QS) & 1, abort_flag, p.status);
+        if (n_vis > 0) {
+            warp_wait(&q_full[0], 0, abort_flag, p.status);
             tc_fence_after();
-#pragma unroll
-            for (int kb = 0; kb < KB; ++kb)   // S^T = K Q^T
-                mma_ss_k64(tmem, dK_ + kb * kBlk, dQk + slot * kStep + kb * kBlk, idesc_s,
-                           kb > 0 ? 1u : 0u);
-#pragma unroll
-            for (int kb = 0; kb < KB; ++kb)   // dP^T = V dO^T
-                mma_ss_k64(tmem + 128, dV_ + kb * kBlk, dDOk + slot * kStep + kb * kBlk, idesc_s,
-                           kb > 0 ? 1u : 0u);
-            mma_commit_elect(s_full);
-            warp_wait(p_full, n & 1, abort_flag, p.status);
-            tc_fence_after();
-            mma_ts_k128_split(tmem + 256, tmem, tmem + 64, dDOm + slot * kStep, idesc_g,
-                              n > 0 ? 1u : 0u);
-            mma_ts_k128_split(tmem + 256 + D, tmem + 128, tmem + 192, dQm + slot * kStep, idesc_g,
-                              n > 0 ? 1u : 0u);
-            mma_commit_elect(&q_empty[slot]);
-            ++n;
+            issue_sdp(0, 0);
+            issue_sdp(0, 1);
+        }
+        // A wait that times out sets the abort flag and later waits return at
+        // once, so the loop runs to its end without blocking.
+        for (int n = 0; n < n_vis; ++n) {
+            const int slot = n % QS, nslot = (n + 1) % QS;
+#pragma unroll 1
+            for (int u = 0; u < 2; ++u) {
+                warp_wait(&p_full[u], n & 1, abort_flag, p.status);
+                tc_fence_after();
+                const uint32_t acc = (n > 0 || u > 0) ? 1u : 0u;
+                // dV += P^T_u dO_u, dK += dS^T_u Q_u (K = the 64 queries of half u)
+                mma_ts_k64(tmem + 256, tmem + 128 * u, dDOm + slot * kStep + u * kHalf, idesc_g, acc);
+                mma_ts_k64(tmem + 256 + D, tmem + 128 * u + 64, dQm + slot * kStep + u * kHalf,
+                           idesc_g, acc);
+                if (u == 1) mma_commit_elect(&q_empty[slot]);
+                if (n + 1 < n_vis) {
+                    if (u == 0) {
+                        warp_wait(&q_full[nslot], ((n + 1) / QS) & 1, abort_flag, p.status);
+                        tc_fence_after();
+                    }
+                    issue_sdp(nslot, u);
+                }
+            }
         }
         mma_commit_elect(acc_full);
         mma_commit_elect(mma_done);
         mbar_wait_bounded(mma_done, 0, p.status);
     } else {
-        // one thread per key row and column half; warp w reads TMEM lanes
-        // 32(w%4) .. 32(w%4)+31 and columns of half w/4
+        // one thread per key row and query half; warp w reads TMEM lanes
+        // 32(w%4) .. 32(w%4)+31 and the columns of query half w/4
         const int hq = warp >> 2, quad = warp & 3;
         const int key = key0 + quad * 32 + lane;
         const uint32_t lb = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t tS = tmem + lb, tDP = tmem + lb + 128;
+        const uint32_t tS = tmem + lb + 128 * hq, tDP = tS + 64;
         const float sl2 = p.scale_log2;
         int n = 0;
         for (int qi = 0; qi < p.n_qtiles; ++qi) {
             if (!visit(qi)) continue;
             const int slot = n % QS;
             warp_wait(&q_full[slot], (n / QS) & 1, abort_flag, p.status);
-            warp_wait(s_full, n & 1, abort_flag, p.status);
+            warp_wait(&s_full[hq], n & 1, abort_flag, p.status);
             tc_fence_after();
             const int64_t row0 = static_cast<int64_t>(qi) * kRows;
             const int base = static_cast<int>(row0 % p.Nq);
@@ -260,10 +292,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t sl22 = f2(sl2, sl2);
 #pragma unroll 1
             for (int cc = 0; cc < 2; ++cc) {
-                const int c = 2 * hq + cc;   // 32-column chunk of the tile
+                const int c = 2 * hq + cc;   // 32-query chunk of the tile
                 uint32_t sv[32], dp[32];
-                tmem_ld32(tS + c * 32, sv);
-                tmem_ld32(tDP + c * 32, dp);
+                tmem_ld32(tS + cc * 32, sv);
+                tmem_ld32(tDP + cc * 32, dp);
                 tmem_wait_ld();
                 reg_fence(sv);
                 reg_fence(dp);
@@ -304,14 +336,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         dw[i >> 1] = pack2<BF16>(dd[0], dd[1]);
                     }
                 }
-                // packed P^T / dS^T of chunk c go to columns 64h + 16cc, which
-                // hold this half's scores already read into registers.
-                tmem_st16(tS + 64 * hq + 16 * cc, pw);
-                tmem_st16(tDP + 64 * hq + 16 * cc, dw);
+                // packed P^T / dS^T of chunk cc go to columns 16cc of this half's
+                // S^T / dP^T, which are already read into registers.
+                tmem_st16(tS + 16 * cc, pw);
+                tmem_st16(tDP + 16 * cc, dw);
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(p_full);
+            mbar_arrive(&p_full[hq]);
             ++n;
         }
         // epilogue: dV and scale * dK of this key row

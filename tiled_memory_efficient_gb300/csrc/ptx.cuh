@@ -268,6 +268,27 @@ __device__ __forceinline__ void mma_ts_k128(uint32_t d, uint32_t a, uint64_t b, 
         : "memory");
 }
 
+// Four MMAs along K (64 values): A from TMEM columns a, a+8, a+16, a+24
+// (packed 16-bit pairs), B descriptor advanced by 128 (2048 bytes: 16 rows of
+// an MN-major 128-byte-swizzled tile) per step.
+__device__ __forceinline__ void mma_ts_k64(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                           uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .b32 lid, a1, a2, a3;\n\t.reg .pred e, p, t;\n\t"
+        ".reg .b64 b1, b2, b3;\n\t"
+        "elect.sync lid|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 t, 0, 0;\n\t"
+        "add.s32 a1, %1, 8;\n\tadd.s32 a2, %1, 16;\n\tadd.s32 a3, %1, 24;\n\t"
+        "add.s64 b1, %2, 128;\n\tadd.s64 b2, %2, 256;\n\tadd.s64 b3, %2, 384;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, t;\n\t}" ::"r"(d),
+        "r"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
 // As mma_ts_k128, but the 128 K values of A come from two TMEM column ranges:
 // steps 0-3 from a_lo (+8 per step), steps 4-7 from a_hi (+8 per step).
 __device__ __forceinline__ void mma_ts_k128_split(uint32_t d, uint32_t a_lo, uint32_t a_hi,
