@@ -31,11 +31,16 @@ namespace tme {
 namespace {
 
 constexpr int kRows = 128;
-// 8 elementwise warps (two warpgroups, each owning 64 of the 128 columns of a
-// tile) + producer + MMA issuer.
+// dQ kernel: 8 elementwise warps (two warpgroups, each owning 64 of the 128
+// columns of a tile) + producer + MMA issuer.
 constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+// dK/dV kernel: 16 elementwise warps (warp w: key rows 32(w%4).., query half
+// (w/4)%2, 32-query chunk w/8 of that half) + producer + MMA issuer.
+constexpr int kKvThreads = 18 * 32;
+constexpr int kKvProducerWarp = 16;
+constexpr int kKvMmaWarp = 17;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <bool BF16>
@@ -106,18 +111,20 @@ struct BwdCfg {
 };
 
 // ---------------------------------------------------------------- dK / dV
-// Each 128-query tile is processed as two halves of 64 queries, one per
-// elementwise warpgroup, so that the tensor core works on one half while the
-// other half's P^T / dS^T are computed.  TMEM: half u holds S^T_u at
+// Each 128-query tile is processed as two halves of 64 queries, one per pair
+// of elementwise warpgroups, so that the tensor core works on one half while
+// the other half's P^T / dS^T are computed.  TMEM: half u holds S^T_u at
 // [128u, 128u+64) and dP^T_u at [128u+64, 128u+128) (M = 128 keys, N = 64
-// queries); its warpgroup packs P^T_u / dS^T_u into the first 32 columns of
-// each.  dV at [256, 256+D), dK at [256+D, 256+2D).
+// queries).  The warp of 32-query chunk c of the half packs its P^T / dS^T
+// into the first 16 of its own 32 columns ([128u+32c, +16) and
+// [128u+64+32c, +16)), which it has already read, so the products read A
+// from two column ranges.  dV at [256, 256+D), dK at [256+D, 256+2D).
 // MMA order per tile n: for u = 0, 1: dV/dK += (half u of tile n) as soon as
 // its P^T / dS^T are in TMEM, then S^T / dP^T of half u of tile n+1 into the
 // same columns (the tensor pipe runs in order, so the products of tile n have
 // read them first).
 template <int D, bool BF16, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kKvThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmDO,
                     const __grid_constant__ CUtensorMap tmK,
@@ -158,20 +165,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < QS; ++i) { mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1); }
         for (int u = 0; u < 2; ++u) {
             mbar_init(&s_full[u], 1);
-            mbar_init(&p_full[u], 128);
+            mbar_init(&p_full[u], 256);
         }
         mbar_init(acc_full, 1);
         mbar_init(mma_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == kMmaWarp) tmem_alloc(tmem_slot, 512);
+    if (warp == kKvMmaWarp) tmem_alloc(tmem_slot, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == kProducerWarp) {
+    if (warp == kKvProducerWarp) {
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmDO);
@@ -201,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int m = (n > QS ? n - QS : 0); m < n; ++m)
                 mbar_wait_bounded(&q_full[m % QS], (m / QS) & 1, p.status);
         }
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kKvMmaWarp) {
         constexpr uint32_t idesc_s = idesc_f16(kRows, 64, BF16, false);  // 128 keys x 64 queries
         constexpr uint32_t idesc_g = idesc_f16(kRows, D, BF16, true);
         constexpr uint64_t kStep = TB >> 4;
@@ -248,9 +255,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t acc = (n > 0 || u > 0) ? 1u : 0u;
                 // dV += P^T_u dO_u, dK += dS^T_u Q_u (K = the 64 queries of half u)
-                mma_ts_k64(tmem + 256, tmem + 128 * u, dDOm + slot * kStep + u * kHalf, idesc_g, acc);
-                mma_ts_k64(tmem + 256 + D, tmem + 128 * u + 64, dQm + slot * kStep + u * kHalf,
-                           idesc_g, acc);
+                const uint32_t pu = tmem + 128 * u;
+                mma_ts_k64_split(tmem + 256, pu, pu + 32, dDOm + slot * kStep + u * kHalf, idesc_g,
+                                 acc);
+                mma_ts_k64_split(tmem + 256 + D, pu + 64, pu + 96, dQm + slot * kStep + u * kHalf,
+                                 idesc_g, acc);
                 if (u == 1) mma_commit_elect(&q_empty[slot]);
                 if (n + 1 < n_vis) {
                     if (u == 0) {
@@ -265,12 +274,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit_elect(mma_done);
         mbar_wait_bounded(mma_done, 0, p.status);
     } else {
-        // one thread per key row and query half; warp w reads TMEM lanes
-        // 32(w%4) .. 32(w%4)+31 and the columns of query half w/4
-        const int hq = warp >> 2, quad = warp & 3;
+        // One thread per key row and 32-query chunk: warp w reads TMEM lanes
+        // 32(w%4) .. 32(w%4)+31, query half hq = (w/4)%2, chunk cc = w/8 of it.
+        const int quad = warp & 3, hq = (warp >> 2) & 1, cc = warp >> 3;
+        const int c = 2 * hq + cc;   // 32-query chunk of the tile
         const int key = key0 + quad * 32 + lane;
         const uint32_t lb = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t tS = tmem + lb + 128 * hq, tDP = tS + 64;
+        const uint32_t tS = tmem + lb + 128 * hq + 32 * cc, tDP = tS + 64;
         const float sl2 = p.scale_log2;
         int n = 0;
         for (int qi = 0; qi < p.n_qtiles; ++qi) {
@@ -279,114 +289,110 @@ __global__ void __launch_bounds__(kThreads, 1)
             warp_wait(&q_full[slot], (n / QS) & 1, abort_flag, p.status);
             warp_wait(&s_full[hq], n & 1, abort_flag, p.status);
             tc_fence_after();
+            uint32_t sv[32], dp[32];
+            tmem_ld32(tS, sv);
+            tmem_ld32(tDP, dp);
             const int64_t row0 = static_cast<int64_t>(qi) * kRows;
             const int base = static_cast<int>(row0 % p.Nq);
-            const float* L = sL + slot * kRows;
-            const float* Dl = sDl + slot * kRows;
-            // No mask anywhere in this warp's 32 x 128 block: every column is a
+            const float* L = sL + slot * kRows + c * 32;
+            const float* Dl = sDl + slot * kRows + c * 32;
+            // No mask anywhere in this warp's 32 x 32 block: every column is a
             // real row of the group, every key exists, and (causal) the warp's
-            // last key is at or before the tile's first query position.
+            // last key is at or before the chunk's first query position.
             const int wkey_last = key0 + quad * 32 + 31;
-            bool fast = (row0 + kRows <= p.rows_per_group) && (wkey_last < p.Nk);
-            if (CAUSAL) fast = fast && (base + kRows <= p.Nq) && (wkey_last <= base);
+            const int q_first = c * 32;
+            bool fast = (row0 + q_first + 32 <= p.rows_per_group) && (wkey_last < p.Nk);
+            if (CAUSAL)
+                fast = fast && (base + q_first + 32 <= p.Nq) && (wkey_last <= base + q_first);
             const uint64_t sl22 = f2(sl2, sl2);
-#pragma unroll 1
-            for (int cc = 0; cc < 2; ++cc) {
-                const int c = 2 * hq + cc;   // 32-query chunk of the tile
-                uint32_t sv[32], dp[32];
-                tmem_ld32(tS + cc * 32, sv);
-                tmem_ld32(tDP + cc * 32, dp);
-                tmem_wait_ld();
-                reg_fence(sv);
-                reg_fence(dp);
-                uint32_t pw[16], dw[16];
-                if (fast) {
+            tmem_wait_ld();
+            reg_fence(sv);
+            reg_fence(dp);
+            uint32_t pw[16], dw[16];
+            if (fast) {
 #pragma unroll
-                    for (int i = 0; i < 32; i += 4) {
-                        const float4 l4 = *reinterpret_cast<const float4*>(L + c * 32 + i);
-                        const float4 d4 = *reinterpret_cast<const float4*>(Dl + c * 32 + i);
+                for (int i = 0; i < 32; i += 4) {
+                    const float4 l4 = *reinterpret_cast<const float4*>(L + i);
+                    const float4 d4 = *reinterpret_cast<const float4*>(Dl + i);
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int e = i + 2 * h;
-                            const uint64_t x = ffma2(f2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
-                                                     sl22, h ? f2(l4.z, l4.w) : f2(l4.x, l4.y));
-                            const float p0 = ex2_ftz(f2lo(x)), p1 = ex2_ftz(f2hi(x));
-                            const uint64_t dd = fmul2(
-                                f2(p0, p1),
-                                fadd2(f2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
-                                      h ? f2(d4.z, d4.w) : f2(d4.x, d4.y)));
-                            pw[e >> 1] = pack2<BF16>(p0, p1);
-                            dw[e >> 1] = pack2<BF16>(f2lo(dd), f2hi(dd));
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        float pp[2], dd[2];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int q = c * 32 + i + u;
-                            bool ok = (row0 + q < p.rows_per_group) && (key < p.Nk);
-                            if (CAUSAL) ok = ok && key <= tile_pos(base, q, p.Nq);
-                            const float pr = ex2_ftz(fmaf(__uint_as_float(sv[i + u]), sl2, L[q]));
-                            pp[u] = ok ? pr : 0.0f;
-                            dd[u] = ok ? pr * (__uint_as_float(dp[i + u]) + Dl[q]) : 0.0f;
-                        }
-                        pw[i >> 1] = pack2<BF16>(pp[0], pp[1]);
-                        dw[i >> 1] = pack2<BF16>(dd[0], dd[1]);
+                    for (int h = 0; h < 2; ++h) {
+                        const int e = i + 2 * h;
+                        const uint64_t x = ffma2(f2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                                 sl22, h ? f2(l4.z, l4.w) : f2(l4.x, l4.y));
+                        const float p0 = ex2_ftz(f2lo(x)), p1 = ex2_ftz(f2hi(x));
+                        const uint64_t dd = fmul2(
+                            f2(p0, p1),
+                            fadd2(f2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
+                                  h ? f2(d4.z, d4.w) : f2(d4.x, d4.y)));
+                        pw[e >> 1] = pack2<BF16>(p0, p1);
+                        dw[e >> 1] = pack2<BF16>(f2lo(dd), f2hi(dd));
                     }
                 }
-                // packed P^T / dS^T of chunk cc go to columns 16cc of this half's
-                // S^T / dP^T, which are already read into registers.
-                tmem_st16(tS + 16 * cc, pw);
-                tmem_st16(tDP + 16 * cc, dw);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    float pp[2], dd[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int q = q_first + i + u;
+                        bool ok = (row0 + q < p.rows_per_group) && (key < p.Nk);
+                        if (CAUSAL) ok = ok && key <= tile_pos(base, q, p.Nq);
+                        const float pr = ex2_ftz(fmaf(__uint_as_float(sv[i + u]), sl2, L[i + u]));
+                        pp[u] = ok ? pr : 0.0f;
+                        dd[u] = ok ? pr * (__uint_as_float(dp[i + u]) + Dl[i + u]) : 0.0f;
+                    }
+                    pw[i >> 1] = pack2<BF16>(pp[0], pp[1]);
+                    dw[i >> 1] = pack2<BF16>(dd[0], dd[1]);
+                }
             }
+            // The packed P^T / dS^T of this chunk go to the first 16 of its own
+            // 32 columns, which are already read into registers.
+            tmem_st16(tS, pw);
+            tmem_st16(tDP, dw);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&p_full[hq]);
             ++n;
         }
-        // epilogue: dV and scale * dK of this key row
+        // epilogue: dV and scale * dK of this key row, D/4 columns per warp
+        constexpr int CW = D / 4;   // 32 (D = 128) or 16 (D = 64)
+        const int col0 = (hq + 2 * cc) * CW;
         const bool ok = *abort_flag == 0;
         const int64_t grow = static_cast<int64_t>(group) * p.Nk + key;
-        uint16_t* dvp = static_cast<uint16_t*>(p.dv) + grow * D;
-        uint16_t* dkp = static_cast<uint16_t*>(p.dk) + grow * D;
+        uint16_t* dvp = static_cast<uint16_t*>(p.dv) + grow * D + col0;
+        uint16_t* dkp = static_cast<uint16_t*>(p.dk) + grow * D + col0;
         if (n > 0) warp_wait(acc_full, 0, abort_flag, p.status);
         tc_fence_after();
+        // dV first, then dK, so only one accumulator chunk is live at a time.
 #pragma unroll 1
-        for (int c = hq * (D / 64); c < (hq + 1) * (D / 64); ++c) {   // this half's columns
-            uint32_t a[32], b[32];
+        for (int which = 0; which < 2; ++which) {
+            uint32_t a[CW];
             if (n > 0) {
-                tmem_ld32(tmem + lb + 256 + c * 32, a);
-                tmem_ld32(tmem + lb + 256 + D + c * 32, b);
+                const uint32_t src = tmem + lb + 256 + which * D + col0;
+                if constexpr (CW == 32) tmem_ld32(src, a);
+                else tmem_ld16(src, a);
                 tmem_wait_ld();
                 reg_fence(a);
-                reg_fence(b);
             } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) a[i] = b[i] = 0u;
+                for (int i = 0; i < CW; ++i) a[i] = 0u;
             }
             if (ok && key < p.Nk) {
-                uint32_t wv[16], wk[16];
+                const float sc = which ? p.scale : 1.0f;
+                uint32_t w[CW / 2];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    wv[i] = pack2<BF16>(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
-                    wk[i] = pack2<BF16>(__uint_as_float(b[2 * i]) * p.scale,
-                                        __uint_as_float(b[2 * i + 1]) * p.scale);
-                }
+                for (int i = 0; i < CW / 2; ++i)
+                    w[i] = pack2<BF16>(__uint_as_float(a[2 * i]) * sc, __uint_as_float(a[2 * i + 1]) * sc);
+                uint4* dst = reinterpret_cast<uint4*>(which ? dkp : dvp);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    reinterpret_cast<uint4*>(dvp + c * 32)[i] =
-                        make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
-                    reinterpret_cast<uint4*>(dkp + c * 32)[i] =
-                        make_uint4(wk[4 * i], wk[4 * i + 1], wk[4 * i + 2], wk[4 * i + 3]);
-                }
+                for (int i = 0; i < CW / 8; ++i)
+                    dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
             }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == kKvMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -660,7 +666,7 @@ cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         const long long ctas = static_cast<long long>(p.n_groups) * p.n_ktiles;
-        e = launch_kernel(kern, dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, stream,
+        e = launch_kernel(kern, dim3(static_cast<unsigned>(ctas)), dim3(kKvThreads), smem, stream,
                           tmQ, tmDO, tmK, tmV, p);
         if (e != cudaSuccess) return e;
     }

@@ -289,6 +289,26 @@ __device__ __forceinline__ void mma_ts_k64(uint32_t d, uint32_t a, uint64_t b, u
         : "memory");
 }
 
+// As mma_ts_k64, but the 64 K values of A come from two TMEM column ranges:
+// steps 0-1 from a_lo, a_lo+8, steps 2-3 from a_hi, a_hi+8.
+__device__ __forceinline__ void mma_ts_k64_split(uint32_t d, uint32_t a_lo, uint32_t a_hi,
+                                                 uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .b32 lid, a1, a3;\n\t.reg .pred e, p, t;\n\t"
+        ".reg .b64 b1, b2, b3;\n\t"
+        "elect.sync lid|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "setp.eq.b32 t, 0, 0;\n\t"
+        "add.s32 a1, %1, 8;\n\tadd.s32 a3, %2, 8;\n\t"
+        "add.s64 b1, %3, 128;\n\tadd.s64 b2, %3, 256;\n\tadd.s64 b3, %3, 384;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %3, %4, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %4, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], b2, %4, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %4, t;\n\t}" ::"r"(d),
+        "r"(a_lo), "r"(a_hi), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
 // As mma_ts_k128, but the 128 K values of A come from two TMEM column ranges:
 // steps 0-3 from a_lo (+8 per step), steps 4-7 from a_hi (+8 per step).
 __device__ __forceinline__ void mma_ts_k128_split(uint32_t d, uint32_t a_lo, uint32_t a_hi,
@@ -361,6 +381,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
           "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
 
