@@ -101,6 +101,21 @@ __device__ __forceinline__ int tile_max_pos(int64_t row0, const BwdParams& p) {
     return (row0 / p.Nq == last / p.Nq) ? static_cast<int>(last % p.Nq) : p.Nq - 1;
 }
 
+// The same from the position `pos` of the tile's first row, without any
+// division (the dK/dV kernel walks all query tiles of a group in order).
+__device__ __forceinline__ int tile_max_pos_at(int qi, int pos, const BwdParams& p) {
+    const int64_t left = p.rows_per_group - static_cast<int64_t>(qi) * kRows;  // rows from row0 on
+    const int span = left < kRows ? static_cast<int>(left) - 1 : kRows - 1;    // last - row0
+    return pos + span < p.Nq ? pos + span : p.Nq - 1;
+}
+
+// Position of the first row of the next 128-row tile.
+__device__ __forceinline__ int next_tile_pos(int pos, int Nq) {
+    pos += kRows;
+    if (pos >= Nq) pos = Nq >= kRows ? pos - Nq : pos % Nq;  // at most one wrap when Nq >= 128
+    return pos;
+}
+
 constexpr int kDqKStages = 3;  // dQ kernel: K ring (live from S_j to dQ_j)
 constexpr int kDqVStages = 2;  // dQ kernel: V ring (live until dP_j)
 
@@ -156,9 +171,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     const int group = static_cast<int>(blockIdx.x / p.n_ktiles);
     const int kt = static_cast<int>(blockIdx.x % p.n_ktiles);
     const int key0 = kt * kRows;
-    auto visit = [&](int qi) {
-        return !CAUSAL || tile_max_pos(static_cast<int64_t>(qi) * kRows, p) >= key0;
-    };
+    // Query tile qi (first-row position pos) meets this key tile.
+    auto visit = [&](int qi, int pos) { return !CAUSAL || tile_max_pos_at(qi, pos, p) >= key0; };
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
@@ -188,8 +202,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 tma_load_3d(&tmV, kv_full, sV + kb * (kRows * 128), kb * 64, key0, group);
             }
             int n = 0;
-            for (int qi = 0; qi < p.n_qtiles; ++qi) {
-                if (!visit(qi)) continue;
+            for (int qi = 0, pos = 0; qi < p.n_qtiles; ++qi, pos = next_tile_pos(pos, p.Nq)) {
+                if (!visit(qi, pos)) continue;
                 const int slot = n % QS;
                 if (!mbar_wait(&q_empty[slot], ((n / QS) & 1) ^ 1, abort_flag, p.status)) break;
                 mbar_arrive_expect_tx(&q_full[slot], 2 * TB + 2 * kRows * 4);
@@ -237,7 +251,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             mma_commit_elect(&s_full[u]);
         };
         int n_vis = 0;   // query tiles this key tile meets (the producer loads them in order)
-        for (int qi = 0; qi < p.n_qtiles; ++qi) n_vis += visit(qi) ? 1 : 0;
+        for (int qi = 0, pos = 0; qi < p.n_qtiles; ++qi, pos = next_tile_pos(pos, p.Nq))
+            n_vis += visit(qi, pos) ? 1 : 0;
         warp_wait(kv_full, 0, abort_flag, p.status);
         if (n_vis > 0) {
             warp_wait(&q_full[0], 0, abort_flag, p.status);
@@ -283,8 +298,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         const uint32_t tS = tmem + lb + 128 * hq + 32 * cc, tDP = tS + 64;
         const float sl2 = p.scale_log2;
         int n = 0;
-        for (int qi = 0; qi < p.n_qtiles; ++qi) {
-            if (!visit(qi)) continue;
+        for (int qi = 0, pos = 0; qi < p.n_qtiles; ++qi, pos = next_tile_pos(pos, p.Nq)) {
+            if (!visit(qi, pos)) continue;
             const int slot = n % QS;
             warp_wait(&q_full[slot], (n / QS) & 1, abort_flag, p.status);
             warp_wait(&s_full[hq], n & 1, abort_flag, p.status);
@@ -293,7 +308,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             tmem_ld32(tS, sv);
             tmem_ld32(tDP, dp);
             const int64_t row0 = static_cast<int64_t>(qi) * kRows;
-            const int base = static_cast<int>(row0 % p.Nq);
+            const int base = pos;
             const float* L = sL + slot * kRows + c * 32;
             const float* Dl = sDl + slot * kRows + c * 32;
             // No mask anywhere in this warp's 32 x 32 block: every column is a
