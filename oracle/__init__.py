@@ -57,6 +57,11 @@ def _load():
                                                  ctypes.c_double, ctypes.c_int, _i64p, i64,
                                                  _dp, _dp, ctypes.c_int]
             lib.oracle_attn_fwd_rows.restype = ctypes.c_int
+            lib.oracle_attn_fwd_rows_bias.argtypes = [_dp, _dp, _dp, i64, i64, i64, i64, i64, i64,
+                                                      ctypes.c_double, ctypes.c_int,
+                                                      _dp, i64, i64, i64, _i64p, i64,
+                                                      _dp, _dp, ctypes.c_int]
+            lib.oracle_attn_fwd_rows_bias.restype = ctypes.c_int
             lib.oracle_attn_bwd.argtypes = [_dp, _dp, _dp, _dp, i64, i64, i64, i64, i64, i64,
                                             ctypes.c_double, ctypes.c_int, _dp, _dp, _dp,
                                             ctypes.c_int]
@@ -101,17 +106,44 @@ def _shapes(q, k, v):
     return B, Hq, Hkv, Nq, Nk, D
 
 
+def _bias_f64(mask, B, Hq, Nq, Nk):
+    """An SDPA-style attn_mask as an fp64 additive bias and its element
+    strides over (batch, query head, query): bool -> 0 where True, -inf where
+    False; any other dtype is taken as an additive bias.  The mask must
+    broadcast to [B, Hq, Nq, Nk]; size-1 dimensions get stride 0."""
+    if hasattr(mask, "detach"):          # a torch tensor
+        t = mask.detach().cpu()
+        m = t.numpy() if str(t.dtype) == "torch.bool" else t.double().numpy()
+    else:
+        m = np.asarray(mask)
+    if m.dtype == np.bool_:
+        m = np.where(m, 0.0, -np.inf)
+    m = np.asarray(m, dtype=np.float64)
+    while m.ndim < 4:
+        m = m[None]
+    if m.ndim != 4 or m.shape[-1] != Nk:
+        raise ValueError(f"mask must broadcast to {(B, Hq, Nq, Nk)}, got {m.shape}")
+    for dim, full in zip(m.shape[:3], (B, Hq, Nq)):
+        if dim not in (1, full):
+            raise ValueError(f"mask shape {m.shape} does not broadcast to {(B, Hq, Nq, Nk)}")
+    m = np.ascontiguousarray(m)
+    strides = tuple(0 if m.shape[i] == 1 else m.strides[i] // 8 for i in range(3))
+    return m, strides
+
+
 def attention_fwd(q, k, v, causal=False, scale: float | None = None,
-                  rows=None, threads: int | None = None):
+                  rows=None, threads: int | None = None, mask=None):
     """Forward definition in fp64.
 
     q: [B,Hq,Nq,D]; k, v: [B,Hkv,Nk,D].  Returns (o, lse) as fp64 arrays.  With
     ``rows`` (flattened ids ``(b*Hq + h)*Nq + i``) only those rows are
     computed and o is [len(rows), D], lse [len(rows)]; otherwise o is
-    [B,Hq,Nq,D] and lse [B,Hq,Nq].
+    [B,Hq,Nq,D] and lse [B,Hq,Nq].  ``mask``: optional attn_mask broadcastable
+    to [B,Hq,Nq,Nk], boolean (True keeps a key) or additive.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Hq, Hkv, Nq, Nk, D = _shapes(q, k, v)
+    bias, bstr = (None, (0, 0, 0)) if mask is None else _bias_f64(mask, B, Hq, Nq, Nk)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if rows is None:
@@ -126,11 +158,13 @@ def attention_fwd(q, k, v, causal=False, scale: float | None = None,
         rows_p = rows_a.ctypes.data_as(_i64p)
         if n == 0:
             return o, lse
-    rc = _load().oracle_attn_fwd_rows(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nk, D,
-                                      float(scale), causal_code(causal), rows_p, n,
-                                      _ptr(o), _ptr(lse), int(threads or default_threads()))
+    rc = _load().oracle_attn_fwd_rows_bias(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nk, D,
+                                           float(scale), causal_code(causal),
+                                           None if bias is None else _ptr(bias), *bstr,
+                                           rows_p, n, _ptr(o), _ptr(lse),
+                                           int(threads or default_threads()))
     if rc != 0:
-        raise RuntimeError(f"oracle_attn_fwd_rows failed with {rc}")
+        raise RuntimeError(f"oracle_attn_fwd_rows_bias failed with {rc}")
     return o, lse
 
 

@@ -24,7 +24,13 @@
  *   post patches).  The forward also takes causal = 2, bottom-right
  *   alignment: the Nq queries are the LAST Nq positions of a sequence whose
  *   first Nk positions are the keys, so query i sees keys j <= i + (Nk - Nq)
- *   (the KV-cache decode of the post's LLM-inference table; Nq <= Nk).  The default scale 1/sqrt(D) is the one the ai-manual.ru
+ *   (the KV-cache decode of the post's LLM-inference table; Nq <= Nk).
+ *
+ *   Optional attention bias (the attn_mask argument of the SDPA call the
+ *   post patches): b[b,h,i,j] is added to s_j before the softmax (natural-log
+ *   units; -inf removes key j; a boolean mask is b = 0 / -inf).  A row whose
+ *   every key is removed has no softmax: the reading used here is O = 0 and
+ *   lse = -inf (the same as a row with no allowed key).  The default scale 1/sqrt(D) is the one the ai-manual.ru
  *   page's chunked snippet divides by (section "3 Samopisnyi memory-efficient
  *   attention"); the caller passes it explicitly.  No flush-to-zero and no
  *   epsilon: this is the exact result the tiled method approximates.
@@ -58,9 +64,10 @@ static int64_t allowed_keys(int64_t i, int64_t Nk, int causal)
     return (i + 1 < Nk) ? (i + 1) : Nk;
 }
 
-/* One query row of the forward definition.  s: scratch of Nk doubles. */
+/* One query row of the forward definition.  s: scratch of Nk doubles.
+ * bias_row: the row's additive bias over the keys, or NULL. */
 static void fwd_one_row(const double *q_row, const double *k_head, const double *v_head,
-                        int64_t nkeys, int64_t D, double scale,
+                        const double *bias_row, int64_t nkeys, int64_t D, double scale,
                         double *s, double *o_row, double *lse_out)
 {
     double m = -INFINITY;
@@ -69,7 +76,13 @@ static void fwd_one_row(const double *q_row, const double *k_head, const double 
         double dot = 0.0;
         for (int64_t d = 0; d < D; ++d) dot += q_row[d] * k_row[d];
         s[j] = scale * dot;
+        if (bias_row) s[j] += bias_row[j];
         if (s[j] > m) m = s[j];
+    }
+    if (m == -INFINITY) {   /* every key removed: O = 0, lse = -inf */
+        for (int64_t d = 0; d < D; ++d) o_row[d] = 0.0;
+        *lse_out = -INFINITY;
+        return;
     }
     double l = 0.0;
     for (int64_t j = 0; j < nkeys; ++j) {
@@ -91,6 +104,8 @@ typedef struct {
     int64_t Hq, Hkv, Nq, Nk, D;
     double scale;
     int causal;
+    const double *bias;    /* additive bias, or NULL */
+    int64_t bsb, bsh, bsq; /* its element strides over batch, query head, query (0: broadcast) */
     const int64_t *rows;   /* flattened row ids (b*Hq + h)*Nq + i, or NULL for all */
     int64_t row_begin, row_end; /* this thread's slice of the row list */
     int status;
@@ -113,8 +128,9 @@ static void *fwd_worker(void *arg)
         const double *v_head = jb->v + (b * jb->Hkv + g) * jb->Nk * jb->D;
         /* bottom-right: query i sits at sequence position i + (Nk - Nq) */
         const int64_t seq_pos = (jb->causal == 2) ? i + (jb->Nk - jb->Nq) : i;
-        fwd_one_row(q_row, k_head, v_head, allowed_keys(seq_pos, jb->Nk, jb->causal), jb->D,
-                    jb->scale, s, jb->o + t * jb->D, jb->lse + t);
+        const double *bias_row = jb->bias ? jb->bias + b * jb->bsb + h * jb->bsh + i * jb->bsq : NULL;
+        fwd_one_row(q_row, k_head, v_head, bias_row, allowed_keys(seq_pos, jb->Nk, jb->causal),
+                    jb->D, jb->scale, s, jb->o + t * jb->D, jb->lse + t);
     }
     free(s);
     jb->status = 0;
@@ -133,12 +149,14 @@ static int check_shape(int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t N
  * written compactly: o[t*D + d], lse[t].  rows == NULL means every row in
  * order, so o and lse then have the full [B,Hq,Nq,(D)] layout.
  */
-int oracle_attn_fwd_rows(const double *q, const double *k, const double *v,
-                         int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t D,
-                         double scale, int causal,
-                         const int64_t *rows, int64_t n_rows,
-                         double *o, double *lse, int nthreads)
+int oracle_attn_fwd_rows_bias(const double *q, const double *k, const double *v,
+                              int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t D,
+                              double scale, int causal,
+                              const double *bias, int64_t bsb, int64_t bsh, int64_t bsq,
+                              const int64_t *rows, int64_t n_rows,
+                              double *o, double *lse, int nthreads)
 {
+    if (bias && (bsb < 0 || bsh < 0 || bsq < 0)) return -1;
     if (check_shape(B, Hq, Hkv, Nq, Nk, D)) return -1;
     if (!q || !k || !v || !o || !lse) return -1;
     if (causal < 0 || causal > 2 || (causal == 2 && Nq > Nk)) return -1;
@@ -158,6 +176,7 @@ int oracle_attn_fwd_rows(const double *q, const double *k, const double *v,
         jb->q = q; jb->k = k; jb->v = v; jb->o = o; jb->lse = lse;
         jb->Hq = Hq; jb->Hkv = Hkv; jb->Nq = Nq; jb->Nk = Nk; jb->D = D;
         jb->scale = scale; jb->causal = causal; jb->rows = rows;
+        jb->bias = bias; jb->bsb = bsb; jb->bsh = bsh; jb->bsq = bsq;
         jb->row_begin = total * t / nthreads;
         jb->row_end = total * (t + 1) / nthreads;
         jb->status = -2;
@@ -173,6 +192,17 @@ int oracle_attn_fwd_rows(const double *q, const double *k, const double *v,
     }
     free(jobs); free(tids);
     return rc;
+}
+
+/* Forward over a list of rows without a bias. */
+int oracle_attn_fwd_rows(const double *q, const double *k, const double *v,
+                         int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t D,
+                         double scale, int causal,
+                         const int64_t *rows, int64_t n_rows,
+                         double *o, double *lse, int nthreads)
+{
+    return oracle_attn_fwd_rows_bias(q, k, v, B, Hq, Hkv, Nq, Nk, D, scale, causal, NULL, 0, 0, 0,
+                                     rows, n_rows, o, lse, nthreads);
 }
 
 /* Full forward: every row, outputs in the [B,Hq,Nq,D] / [B,Hq,Nq] layout. */

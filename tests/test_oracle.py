@@ -251,6 +251,66 @@ def test_bottom_right_argument_checks():
         oracle.attention_bwd(q[:, :, :5], k, k, q[:, :, :5], causal="bottom_right")
 
 
+@pytest.mark.parametrize("shape,kind,causal", [
+    ((2, 1, 1, 23), "bool", False),       # key padding, broadcast over heads and queries
+    ((2, 1, 13, 23), "bool", True),       # per-query mask with the causal mask on top
+    ((1, 4, 13, 23), "additive", False),  # per-head bias (ALiBi-like)
+    ((2, 4, 13, 23), "additive", True),
+    ((13, 23), "additive", False),        # 2-D mask, broadcast over batch and heads
+])
+def test_mask_matches_torch_sdpa_f64(shape, kind, causal):
+    """attn_mask against torch's fp64 SDPA (an independent library routine)
+    and torch.logsumexp of the biased scores."""
+    B, Hq, Hkv, Nq, Nk, D = 2, 4, 2, 13, 23, 8
+    q, k, v = rnd((B, Hq, Nq, D), 101), rnd((B, Hkv, Nk, D), 102), rnd((B, Hkv, Nk, D), 103)
+    g = torch.Generator().manual_seed(104)
+    if kind == "bool":
+        mask = torch.rand(shape, generator=g) > 0.4
+        mask[..., 0] = True   # every row keeps key 0 (so no row is empty)
+    else:
+        mask = torch.randn(shape, generator=g, dtype=torch.float64) * 2.0
+    o, lse = oracle.attention_fwd(q, k, v, causal=causal, mask=mask)
+    qt, kt, vt = (torch.as_tensor(x) for x in (q, k, v))
+    kt, vt = kt.repeat_interleave(Hq // Hkv, dim=1), vt.repeat_interleave(Hq // Hkv, dim=1)
+    bias = mask if kind == "additive" else torch.zeros(shape, dtype=torch.float64).masked_fill(
+        ~mask, -math.inf)
+    if causal:
+        bias = bias + torch.zeros(Nq, Nk, dtype=torch.float64).masked_fill(
+            ~torch.ones(Nq, Nk, dtype=torch.bool).tril(), -math.inf)
+    ref = F.scaled_dot_product_attention(qt, kt, vt, attn_mask=bias)
+    np.testing.assert_allclose(o, ref.numpy(), rtol=0, atol=1e-12)
+    s = qt @ kt.transpose(-1, -2) / math.sqrt(D) + bias
+    np.testing.assert_allclose(lse, torch.logsumexp(s, dim=-1).numpy(), rtol=0, atol=1e-12)
+
+
+def test_mask_closed_forms():
+    """A constant bias c leaves O alone and adds c to the LSE; with Q = 0 a
+    bias ln w_j gives the w-weighted mean of V and LSE = ln sum w; a mask that
+    keeps one key returns that key's value row; a row with every key masked
+    is O = 0, LSE = -inf."""
+    Nq, Nk, D = 5, 11, 4
+    q, k, v = rnd((1, 1, Nq, D), 105), rnd((1, 1, Nk, D), 106), rnd((1, 1, Nk, D), 107)
+    o0, l0 = oracle.attention_fwd(q, k, v)
+    o1, l1 = oracle.attention_fwd(q, k, v, mask=np.full((Nq, Nk), 0.75))
+    np.testing.assert_allclose(o1, o0, atol=1e-14)
+    np.testing.assert_allclose(l1, l0 + 0.75, atol=1e-14)
+    w = np.exp(rnd((Nk,), 108))
+    oz, lz = oracle.attention_fwd(np.zeros_like(q), k, v, mask=np.log(w)[None, :])
+    np.testing.assert_allclose(oz[0, 0], np.broadcast_to(w @ v[0, 0] / w.sum(), (Nq, D)),
+                               atol=1e-14)
+    np.testing.assert_allclose(lz, math.log(w.sum()), atol=1e-14)
+    keep = np.zeros((Nq, Nk), dtype=bool)
+    keep[np.arange(Nq), np.arange(Nq) * 2] = True
+    keep[4] = False                     # row 4: every key masked
+    om, lm = oracle.attention_fwd(q, k, v, mask=torch.as_tensor(keep))
+    for i in range(4):
+        np.testing.assert_allclose(om[0, 0, i], v[0, 0, 2 * i], atol=1e-15)
+        np.testing.assert_allclose(lm[0, 0, i], q[0, 0, i] @ k[0, 0, 2 * i] / math.sqrt(D),
+                                   atol=1e-14)
+    np.testing.assert_array_equal(om[0, 0, 4], 0.0)
+    assert lm[0, 0, 4] == -math.inf
+
+
 def test_causal_row_zero_is_first_value():
     q, k, v = rnd((2, 2, 9, 8), 28), rnd((2, 2, 9, 8), 29), rnd((2, 2, 9, 8), 30)
     o, _ = oracle.attention_fwd(q, k, v, causal=True)

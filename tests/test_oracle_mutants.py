@@ -2,7 +2,7 @@
 
 A mutant is the oracle's own source with one plausible slip written into it
 (a dropped scale, a flipped exponent, a wrong GQA head, an off-by-one causal
-mask (top-left or bottom-right), a missing normalisation, V swapped for K, a log2 for a log, a missing
+mask (top-left or bottom-right), a bias subtracted or read from the wrong query, a missing normalisation, V swapped for K, a log2 for a log, a missing
 Delta or scale in the backward).  Each is compiled with gcc into a temporary
 library, swapped in for the real one, and run through a battery of the pins
 in test_oracle.py; the test passes only if the battery rejects it.  All on the
@@ -36,6 +36,8 @@ MUTANTS = {
                           "dv_head[j * D + d] += p[j] * q_row[d];"),
     "bottom_right_off_by_one": ("? i + (jb->Nk - jb->Nq) : i;", "? i + (jb->Nk - jb->Nq) - 1 : i;"),
     "bottom_right_as_top_left": ("? i + (jb->Nk - jb->Nq) : i;", "? i : i;"),
+    "mask_subtracted": ("if (bias_row) s[j] += bias_row[j];", "if (bias_row) s[j] -= bias_row[j];"),
+    "mask_query_stride_ignored": ("+ i * jb->bsq", "+ 0 * jb->bsq"),
 }
 
 
@@ -52,6 +54,8 @@ def battery():
         ("bottom_right", pins.test_bottom_right_matches_torch_causal_lower_right,
          (2, 4, 2, 1, 23, 16)),
         ("bottom_right_prefix", pins.test_zero_query_bottom_right_gives_prefix_means, ()),
+        ("mask_closed_forms", pins.test_mask_closed_forms, ()),
+        ("mask_sdpa", pins.test_mask_matches_torch_sdpa_f64, ((2, 4, 13, 23), "additive", True)),
     ]
     failed = []
     for name, fn, args in checks:
@@ -76,7 +80,7 @@ def swap_lib(tmp_path, monkeypatch):
         import ctypes
         lib = ctypes.CDLL(str(so))
         real = oracle._load()
-        for fname in ("oracle_attn_fwd_rows", "oracle_attn_bwd"):
+        for fname in ("oracle_attn_fwd_rows", "oracle_attn_fwd_rows_bias", "oracle_attn_bwd"):
             getattr(lib, fname).argtypes = getattr(real, fname).argtypes
             getattr(lib, fname).restype = getattr(real, fname).restype
         monkeypatch.setattr(oracle, "_lib", lib)
