@@ -54,6 +54,8 @@ typedef enum {
     ATTN_CAUSAL_BOTTOM_RIGHT = 2
 } attn_causal_t;
 
+typedef enum { ATTN_MASK_BOOL = 1, ATTN_MASK_ADDITIVE = 2 } attn_mask_kind_t;
+
 typedef enum {
     ATTN_OK = 0,
     ATTN_ERR_INVALID = 1,     /* null pointer, non-positive size, Hq % Hkv, bad scale/dtype */
@@ -72,6 +74,26 @@ typedef enum {
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
              int Hkv, int Nq, int Nk, int D, float scale, int causal, int dtype, void* stream);
+
+/*
+ * Forward with an attention bias: the attn_mask argument of the SDPA call
+ * that the forum post patches ("Other areas where this could be useful":
+ * every SDPA call, e.g. from HuggingFace Transformers, which pass padding and
+ * causal masks this way).  Element (b, h, i, j) of the mask is at
+ *     mask + b*mask_stride_b + h*mask_stride_h + i*mask_stride_q + j
+ * elements (h = query head; a stride of 0 broadcasts that dimension; keys are
+ * contiguous).  ATTN_MASK_BOOL: one byte per element, nonzero keeps key j.
+ * ATTN_MASK_ADDITIVE: 16-bit values in `dtype`, added to scale * q.k (natural
+ * log units; -inf removes the key).  The causal mask, if any, applies on top.
+ * A row whose every key is removed gets out = 0 and lse = -inf.
+ * Requirements beyond attn_fwd's: mask 16-byte aligned and every stride times
+ * the element size a multiple of 16 bytes (ATTN_ERR_ALIGN otherwise); the
+ * mask is read, never written, and must stay valid until the work completes.
+ */
+int attn_fwd_masked(const void* q, const void* k, const void* v, void* out, float* lse,
+                    const void* mask, int mask_kind, long long mask_stride_b,
+                    long long mask_stride_h, long long mask_stride_q, int B, int Hq, int Hkv,
+                    int Nq, int Nk, int D, float scale, int causal, int dtype, void* stream);
 
 /*
  * Split-key forward for short query blocks against long key sequences (LLM

@@ -1,0 +1,106 @@
+"""Forward with an attention mask (attn_fwd_masked, the SDPA attn_mask) on the
+GPU, through the C ABI, against the fp64 oracle on the same seeded inputs and
+the same (dtype-rounded) mask.  Every row is checked; rows whose every key is
+masked must come back as O = 0 and LSE = -inf, the oracle's reading."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import helpers
+from tiled_memory_efficient_gb300 import _lib, inputs, sdpa
+
+pytestmark = pytest.mark.gpu
+
+F16, BF16 = torch.float16, torch.bfloat16
+
+
+def make_mask(shape, kind, dtype, seed, Nk, empty_rows=False):
+    g = torch.Generator().manual_seed(seed)
+    if kind == "padding":                 # [B,1,1,Nk]: per-sequence key lengths
+        B = shape[0]
+        lens = torch.randint(Nk // 3, Nk + 1, (B,), generator=g)
+        lens[0] = Nk
+        return (torch.arange(Nk)[None, :] < lens[:, None]).reshape(B, 1, 1, Nk)
+    if kind == "bool":
+        m = torch.rand(shape, generator=g) > 0.35
+        if empty_rows:
+            m[..., 3, :] = False          # query row 3: no key at all
+        return m
+    m = torch.randn(shape, generator=g) * 2.0
+    m = m.masked_fill(torch.rand(shape, generator=g) < 0.1, -math.inf)
+    return m.to(dtype)                    # the kernel reads the bias in the input dtype
+
+
+def check(x, out, lse, causal, mask, what):
+    o_ref, lse_ref = oracle.attention_fwd(x["q"], x["k"], x["v"], causal=causal, mask=mask)
+    o_gpu = out.double().cpu().numpy()
+    lse_gpu = lse.double().cpu().numpy()
+    empty = np.isneginf(lse_ref)
+    assert np.array_equal(np.isneginf(lse_gpu), empty), f"{what}: empty rows differ"
+    assert np.all(o_gpu[empty] == 0.0), f"{what}: an empty row is not zero"
+    keep = ~empty
+    eo, el = helpers.assert_fwd_close(o_gpu[keep], lse_gpu[keep], o_ref[keep], lse_ref[keep],
+                                      x["q"].dtype, what)
+    return eo, el, int(empty.sum())
+
+
+CASES = [
+    # B, Hq, Hkv, Nq, Nk, D, dtype, causal, mask shape (None: padding), kind
+    (2, 4, 4, 300, 300, 64, F16, False, None, "padding"),
+    (1, 14, 2, 250, 517, 64, F16, True, (1, 1, 250, 517), "bool"),
+    (1, 4, 2, 200, 333, 128, BF16, False, (1, 4, 200, 333), "additive"),
+    (2, 3, 3, 128, 256, 128, BF16, True, (2, 3, 128, 256), "additive"),
+    (1, 2, 2, 64, 1000, 64, F16, False, (1000,), "bool"),           # 1-D: over keys only
+    (1, 6, 2, 77, 77, 128, F16, False, (77, 77), "additive"),       # rows not 16-byte aligned
+    (2, 2, 1, 130, 140, 64, BF16, "bottom_right", (2, 1, 130, 140), "bool"),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,D,dtype,causal,shape,kind", CASES)
+def test_masked_forward_matches_oracle(cuda_lib, B, Hq, Hkv, Nq, Nk, D, dtype, causal, shape, kind):
+    x = inputs.make_custom(B, Hq, Hkv, Nq, Nk, D, dtype, seed=Nq + 3 * Nk)
+    mask = make_mask(shape or (B, 1, 1, Nk), kind, dtype, seed=Nk, Nk=Nk)
+    q, k, v = (x[n].cuda() for n in "qkv")
+    out, lse = _lib.attn_fwd(q, k, v, causal=causal, mask=mask.cuda())
+    assert _lib.sync_status() == _lib.ATTN_OK
+    eo, el, n_empty = check(x, out, lse, causal, mask, f"mask {kind} {shape} {causal}")
+    print(f"{kind} {shape}: max|dO|={eo:.2e} max|dLSE|={el:.2e} empty rows={n_empty}")
+
+
+def test_rows_with_every_key_masked(cuda_lib):
+    x = inputs.make_custom(1, 2, 2, 40, 300, 64, F16, seed=11)
+    mask = make_mask((1, 2, 40, 300), "bool", F16, seed=12, Nk=300, empty_rows=True)
+    q, k, v = (x[n].cuda() for n in "qkv")
+    out, lse = _lib.attn_fwd(q, k, v, mask=mask.cuda())
+    assert _lib.sync_status() == _lib.ATTN_OK
+    _, _, n_empty = check(x, out, lse, False, mask, "empty rows")
+    assert n_empty == 2
+
+
+def test_all_true_mask_is_the_unmasked_forward(cuda_lib):
+    """A mask that keeps every key gives the unmasked result (to rounding:
+    the masked kernel scales the scores before the max)."""
+    x = inputs.make_custom(1, 4, 4, 256, 384, 128, BF16, seed=13)
+    q, k, v = (x[n].cuda() for n in "qkv")
+    a = _lib.attn_fwd(q, k, v)
+    b = _lib.attn_fwd(q, k, v, mask=torch.ones(384, dtype=torch.bool, device="cuda"))
+    torch.cuda.synchronize()
+    assert (a[0].float() - b[0].float()).abs().max().item() <= 1e-2
+    assert (a[1] - b[1]).abs().max().item() <= 1e-4
+
+
+def test_sdpa_with_attn_mask(cuda_lib):
+    x = inputs.make_custom(2, 4, 2, 200, 200, 64, F16, seed=14)
+    mask = make_mask((2, 1, 1, 200), "padding", F16, seed=15, Nk=200)
+    q, k, v = (x[n].cuda() for n in "qkv")
+    out = sdpa.scaled_dot_product_attention(q, k, v, attn_mask=mask.cuda(), enable_gqa=True)
+    o_ref, _ = oracle.attention_fwd(x["q"], x["k"], x["v"], mask=mask)
+    helpers.assert_close_elementwise(out.double().cpu().numpy(), o_ref, helpers.TOL_O[F16], F16,
+                                     "sdpa mask", "O")
+    qg = q.clone().requires_grad_(True)
+    y = sdpa.scaled_dot_product_attention(qg, k, v, attn_mask=mask.cuda(), enable_gqa=True)
+    with pytest.raises(NotImplementedError):
+        y.sum().backward()

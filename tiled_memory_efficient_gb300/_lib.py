@@ -29,6 +29,8 @@ ATTN_BF16 = 1
 ATTN_CAUSAL_NONE = 0
 ATTN_CAUSAL_TOP_LEFT = 1
 ATTN_CAUSAL_BOTTOM_RIGHT = 2
+ATTN_MASK_BOOL = 1
+ATTN_MASK_ADDITIVE = 2
 _CAUSAL_NAMES = {"none": ATTN_CAUSAL_NONE, "top_left": ATTN_CAUSAL_TOP_LEFT,
                  "bottom_right": ATTN_CAUSAL_BOTTOM_RIGHT}
 
@@ -40,6 +42,9 @@ _i = ctypes.c_int
 _SIGNATURES = {
     "attn_fwd": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i, _vp],
                  _i),
+    "attn_fwd_masked": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, ctypes.c_longlong, ctypes.c_longlong,
+                         ctypes.c_longlong, _i, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i, _vp],
+                        _i),
     "attn_fwd_splitkv": ([_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _i, _i, _i, _i, _i, _i,
                           ctypes.c_float, _i, _i, _i, _vp], _i),
     "attn_fwd_splitkv_workspace_size": ([_i, _i, _i, _i, _i, _i, _i], ctypes.c_size_t),
@@ -133,12 +138,51 @@ def _check(q, k, v):
         raise ValueError(f"shapes q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
 
 
-def attn_fwd(q, k, v, causal=False, scale: float | None = None, out=None, lse=None):
+def prepare_mask(mask, q, Nk: int):
+    """An SDPA attn_mask as the C ABI's (tensor, kind, strides): bool stays a
+    byte mask (True keeps the key); a floating mask becomes an additive bias
+    in q's dtype.  It must broadcast to [B, Hq, Nq, Nk].  If its rows are not
+    16-byte aligned it is copied into a padded buffer (same values),
+    allocated on the current stream, the one the kernel runs on."""
+    import torch
+    B, Hq, Nq, _ = q.shape
+    if not isinstance(mask, torch.Tensor) or mask.device != q.device:
+        raise ValueError("attn_mask must be a tensor on q's device")
+    if mask.dtype == torch.bool:
+        kind, m = ATTN_MASK_BOOL, mask
+    elif mask.is_floating_point():
+        kind, m = ATTN_MASK_ADDITIVE, mask.to(q.dtype)
+    else:
+        raise TypeError(f"attn_mask dtype {mask.dtype} is neither bool nor floating point")
+    while m.dim() < 4:
+        m = m.unsqueeze(0)
+    if m.dim() != 4 or m.shape[-1] != Nk or any(
+            d not in (1, full) for d, full in zip(m.shape[:3], (B, Hq, Nq))):
+        raise ValueError(f"attn_mask shape {tuple(mask.shape)} does not broadcast to "
+                         f"{(B, Hq, Nq, Nk)}")
+    if m.stride(-1) != 1:
+        m = m.contiguous()
+    esz = m.element_size()
+
+    def strides(t):
+        return [0 if t.shape[i] == 1 else t.stride(i) for i in range(3)]
+    st = strides(m)
+    if m.data_ptr() % 16 or any((x * esz) % 16 for x in st):
+        per = 16 // esz
+        buf = torch.zeros((*m.shape[:3], (Nk + per - 1) // per * per), dtype=m.dtype,
+                          device=m.device)
+        buf[..., :Nk] = m
+        m = buf
+        st = strides(m)
+    return m, kind, st
+
+
+def attn_fwd(q, k, v, causal=False, scale: float | None = None, out=None, lse=None, mask=None):
     """O, LSE = attention(q, k, v).  q [B,Hq,Nq,D]; k, v [B,Hkv,Nk,D] (CUDA).
 
     Returns (out [B,Hq,Nq,D] in q's dtype, lse [B,Hq,Nq] fp32 natural log).
-    causal: see causal_code.  Enqueued on torch's current stream; no
-    synchronisation.
+    causal: see causal_code.  mask: optional SDPA-style attn_mask (see
+    prepare_mask).  Enqueued on torch's current stream; no synchronisation.
     """
     import torch
     _check(q, k, v)
@@ -150,6 +194,18 @@ def attn_fwd(q, k, v, causal=False, scale: float | None = None, out=None, lse=No
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, Hq, Nq), device=q.device, dtype=torch.float32)
+    if mask is not None:
+        m, kind, (sb, sh, sq) = prepare_mask(mask, q, Nk)
+        rc = load().attn_fwd_masked(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                    lse.data_ptr(), m.data_ptr(), kind, sb, sh, sq, B, Hq, Hkv, Nq,
+                                    Nk, D, float(scale), causal_code(causal), _dtype_code(q),
+                                    _stream_handle(q.device))
+        if rc != ATTN_OK:
+            raise AttnError("attn_fwd_masked", rc)
+        # (a converted / padded copy was allocated on this stream, after which
+        # the kernel is queued: the allocator reuses it only for later work
+        # on the same stream, so it may be released now)
+        return out, lse
     rc = load().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                          lse.data_ptr(), B, Hq, Hkv, Nq, Nk, D, float(scale), causal_code(causal),
                          _dtype_code(q), _stream_handle(q.device))

@@ -186,6 +186,9 @@ int fwd_prepare(const void* q, const void* k, const void* v, void* out, float* l
     p->n_splits = 1;
     p->tiles_per_split = static_cast<int>(key_tiles(Nk));
     p->scale_log2 = scale * 1.4426950408889634f;
+    p->mask = nullptr;
+    p->Hkv = Hkv;
+    p->G = Hq / Hkv;
     return ATTN_OK;
 }
 
@@ -200,6 +203,34 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, 
     const int rc = fwd_prepare(q, k, v, out, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype,
                                &tmQ, &tmK, &tmV, &p);
     if (rc != ATTN_OK) return rc;
+    const cudaError_t e = launch_fwd(D, dtype == ATTN_BF16, causal != ATTN_CAUSAL_NONE, tmQ, tmK,
+                                     tmV, p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+extern "C" int attn_fwd_masked(const void* q, const void* k, const void* v, void* out, float* lse,
+                               const void* mask, int mask_kind, long long mask_stride_b,
+                               long long mask_stride_h, long long mask_stride_q, int B, int Hq,
+                               int Hkv, int Nq, int Nk, int D, float scale, int causal, int dtype,
+                               void* stream) {
+    if (!mask) return ATTN_ERR_INVALID;
+    if (mask_kind != ATTN_MASK_BOOL && mask_kind != ATTN_MASK_ADDITIVE) return ATTN_ERR_INVALID;
+    if (mask_stride_b < 0 || mask_stride_h < 0 || mask_stride_q < 0) return ATTN_ERR_INVALID;
+    const long long esz = mask_kind == ATTN_MASK_ADDITIVE ? 2 : 1;
+    // 16-byte vector loads of 32 keys: the start of every bias row is aligned
+    if (!aligned16(mask) || (mask_stride_b * esz) % 16 || (mask_stride_h * esz) % 16 ||
+        (mask_stride_q * esz) % 16)
+        return ATTN_ERR_ALIGN;
+    CUtensorMap tmQ, tmK, tmV;
+    FwdParams p;
+    const int rc = fwd_prepare(q, k, v, out, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype,
+                               &tmQ, &tmK, &tmV, &p);
+    if (rc != ATTN_OK) return rc;
+    p.mask = mask;
+    p.mask_kind = mask_kind;
+    p.msb = mask_stride_b;
+    p.msh = mask_stride_h;
+    p.msq = mask_stride_q;
     const cudaError_t e = launch_fwd(D, dtype == ATTN_BF16, causal != ATTN_CAUSAL_NONE, tmQ, tmK,
                                      tmV, p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;

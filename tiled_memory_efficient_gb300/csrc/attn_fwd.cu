@@ -23,6 +23,7 @@
 // TMEM (512 columns): S_0 [0,128) S_1 [128,256) O_0 [256,256+D) O_1 [256+D,256+2D);
 // P_t overwrites the first 64 columns of S_t (two 16-bit values per column).
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -39,7 +40,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 // the true max exceeds it by more than this many powers of two.
 constexpr float kRescaleThreshold = 8.0f;
 
-template <int D>
+template <int D, bool MASK = false>
 struct FwdCfg {
     static constexpr int kTileBytes = kRows * D * 2;         // one 128 x D tile, 16-bit
     static constexpr int kKStages = (D == 128) ? 2 : 3;
@@ -63,7 +64,9 @@ struct FwdCfg {
     //  D=64:  the softmax is the bottleneck, so every row is split over two
     //         warps of 64 keys each: warps 0-15 softmax (Q tile (w/4)%2, key
     //         half w/8), warp 16 producer, warps 17/18 MMA issuers.
-    static constexpr bool kSplit = (D == 64);
+    // (The masked variant keeps one thread per 128-key row at D = 64 too: its
+    // bias loads need the registers the split layout does not have.)
+    static constexpr bool kSplit = (D == 64 && !MASK);
     static constexpr int kSoftmaxWarps = kSplit ? 16 : 8;
     static constexpr int kProducerWarp = kSplit ? 16 : 11;
     static constexpr int kMmaWarp0 = kSplit ? 17 : 9;
@@ -176,12 +179,89 @@ __device__ __forceinline__ float row_max64(const uint32_t (&s)[2][32]) {
     return fmaxf(fmax3(u[0], u[1], u[2]), fmax3(u[3], u[4], fmax3(u[5], u[6], u[7])));
 }
 
-template <int D, bool BF16, bool CAUSAL>
-__global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
+// Attention bias (SDPA attn_mask) of one 32-key chunk of a row, applied in
+// the log2 domain: t = s * sl2 + b * log2(e) for an additive bias (16-bit,
+// the input dtype), t = s * sl2 or -inf for a boolean keep-mask (bytes).
+struct BiasChunk {
+    uint4 w[4];
+};
+
+__device__ __forceinline__ void bias_load(BiasChunk& b, const uint8_t* row, int kind, int key,
+                                          bool full) {
+    if (!full) return;
+    if (kind == 2) {
+        const uint4* src = reinterpret_cast<const uint4*>(row + 2 * static_cast<int64_t>(key));
+        b.w[0] = src[0];
+        b.w[1] = src[1];
+        b.w[2] = src[2];
+        b.w[3] = src[3];
+    } else {
+        const uint4* src = reinterpret_cast<const uint4*>(row + key);
+        b.w[0] = src[0];
+        b.w[1] = src[1];
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ float half_to_float(uint32_t h) {
+    if constexpr (BF16) return __uint_as_float(h << 16);
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+}
+
+// `full`: the 32 keys are in range and the row is real, and b holds them.
+// Otherwise keys are read one by one (keys >= Nk and unreal rows: no bias).
+template <bool BF16>
+__device__ __forceinline__ void bias_apply(uint32_t (&s)[32], const BiasChunk& b,
+                                           const uint8_t* row, int kind, int key, int Nk,
+                                           float sl2, bool full, bool row_ok) {
+    constexpr float kLog2e = 1.4426950408889634f;
+    if (full) {
+        if (kind == 2) {
+            const uint64_t sl22 = f2(sl2, sl2), l2e2 = f2(kLog2e, kLog2e);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint4 q4 = b.w[i >> 2];
+                const uint32_t w = (i & 3) == 0 ? q4.x : (i & 3) == 1 ? q4.y : (i & 3) == 2 ? q4.z : q4.w;
+                const uint64_t bb = fmul2(f2(half_to_float<BF16>(w & 0xffffu), half_to_float<BF16>(w >> 16)),
+                                          l2e2);
+                const uint64_t t = ffma2(f2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
+                                         sl22, bb);
+                s[2 * i] = __float_as_uint(f2lo(t));
+                s[2 * i + 1] = __float_as_uint(f2hi(t));
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const uint4 q4 = b.w[i >> 4];
+                const int wi = (i >> 2) & 3;
+                const uint32_t w = wi == 0 ? q4.x : wi == 1 ? q4.y : wi == 2 ? q4.z : q4.w;
+                const bool keep = ((w >> (8 * (i & 3))) & 0xffu) != 0u;
+                s[i] = __float_as_uint(keep ? __uint_as_float(s[i]) * sl2 : -INFINITY);
+            }
+        }
+        return;
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        float t = __uint_as_float(s[i]) * sl2;
+        if (row_ok && key + i < Nk) {
+            if (kind == 2) {
+                const uint16_t h = reinterpret_cast<const uint16_t*>(row)[key + i];
+                t += half_to_float<BF16>(h) * kLog2e;
+            } else if (row[key + i] == 0) {
+                t = -INFINITY;
+            }
+        }
+        s[i] = __float_as_uint(t);
+    }
+}
+
+template <int D, bool BF16, bool CAUSAL, bool MASK>
+__global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-    using C = FwdCfg<D>;
+    using C = FwdCfg<D, MASK>;
     constexpr int KS = C::kKStages, VS = C::kVStages;
     constexpr int kProducerWarp = C::kProducerWarp;
     constexpr int kMmaWarp0 = C::kMmaWarp0;
@@ -536,6 +616,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         const int64_t row = row0 + quad * 32 + lane;
         const bool row_valid = row < p.rows_per_group;
         const int pos = static_cast<int>(row % p.Nq);
+        // This row's bias: query head hkv*G + row/Nq of batch group/Hkv.
+        const uint8_t* mrow = nullptr;
+        if constexpr (MASK) {
+            const int64_t h = static_cast<int64_t>(group % p.Hkv) * p.G + row / p.Nq;
+            const int64_t b = group / p.Hkv;
+            const int esz = p.mask_kind == 2 ? 2 : 1;
+            mrow = static_cast<const uint8_t*>(p.mask) + (b * p.msb + h * p.msh + pos * p.msq) * esz;
+        }
         // Smallest query position among this warp's rows: masking is needed on
         // key tiles that reach past it (or past Nk).
         const int64_t wr0 = row0 + quad * 32;
@@ -555,6 +643,26 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         for (int j = 0; j < n_t; ++j) {
             if (!warp_wait(&s_full[t], j & 1, abort_flag, p.status)) { ok = false; break; }
             tc_fence_after();
+            const int key0 = (kt0 + j) * kRows;
+            if constexpr (MASK) {
+                // Scores -> log2-domain logits with the bias, in place in TMEM
+                // one 32-key chunk at a time (few live registers); the rest of
+                // the tile then runs with scale 1 (sc below).
+                const bool full = row_valid && key0 + kRows <= p.Nk;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    BiasChunk b;
+                    bias_load(b, mrow, p.mask_kind, key0 + 32 * c, full);
+                    uint32_t x[32];
+                    tmem_ld32(tS + c * 32, x);
+                    tmem_wait_ld();
+                    reg_fence(x);
+                    bias_apply<BF16>(x, b, mrow, p.mask_kind, key0 + 32 * c, p.Nk, sl2, full,
+                                     row_valid);
+                    tmem_st32(tS + c * 32, x);
+                }
+                tmem_wait_st();
+            }
             uint32_t sr[4][32];
 #pragma unroll
             for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
@@ -567,7 +675,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
                 mbar_arrive(&s_free[t]);
             }
 
-            const int key0 = (kt0 + j) * kRows;
+            const float sc = MASK ? 1.0f : sl2;   // scale still to apply to sr
             const bool need_mask =
                 (key0 + kRows > p.Nk) || (CAUSAL && key0 + kRows - 1 > warp_min_pos + p.causal_off);
             if (need_mask) {
@@ -580,7 +688,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
                         if (key0 + c * 32 + i >= lim) sr[c][i] = __float_as_uint(-INFINITY);
             }
             const float mx = row_max128(sr);
-            const float m_new = fmaxf(m, mx * sl2);
+            const float m_new = fmaxf(m, mx * sc);
             const bool need = m_new > m + kRescaleThreshold;
             // Branch-free: alpha is only used when need (m = -inf gives 0).
             const float alpha = need ? ex2_ftz(m - m_new) : 1.0f;
@@ -597,7 +705,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             // partial row sums of p, as packed pairs; bf16: of the rounded p
             uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
             float accr[4] = {0.f, 0.f, 0.f, 0.f};
-            const uint64_t sl22 = f2(sl2, sl2), nm2 = f2(-m_sub, -m_sub);
+            const uint64_t sl22 = f2(sc, sc), nm2 = f2(-m_sub, -m_sub);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 // P of keys 32c..32c+31 goes to TMEM columns 16c..16c+15 as soon
@@ -675,12 +783,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     }
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool MASK>
 cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                        const FwdParams& p, cudaStream_t stream) {
-    auto kern = attn_fwd_kernel<D, BF16, CAUSAL>;
-    constexpr int smem = FwdCfg<D>::kSmemBytes;
-    constexpr int kThreads = FwdCfg<D>::kThreads;
+    auto kern = attn_fwd_kernel<D, BF16, CAUSAL, MASK>;
+    constexpr int smem = FwdCfg<D, MASK>::kSmemBytes;
+    constexpr int kThreads = FwdCfg<D, MASK>::kThreads;
     // Re-applied on every call: a cheap attribute write that is correct on
     // whichever device is current.
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -695,16 +803,22 @@ cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
 cudaError_t launch_fwd(int D, bool bf16, bool causal, const CUtensorMap& tmQ,
                        const CUtensorMap& tmK, const CUtensorMap& tmV, const FwdParams& p,
                        cudaStream_t stream) {
-#define TME_CASE(d, b, c) \
-    if (D == d && bf16 == b && causal == c) return launch_one<d, b, c>(tmQ, tmK, tmV, p, stream);
-    TME_CASE(64, false, false)
-    TME_CASE(64, false, true)
-    TME_CASE(64, true, false)
-    TME_CASE(64, true, true)
-    TME_CASE(128, false, false)
-    TME_CASE(128, false, true)
-    TME_CASE(128, true, false)
-    TME_CASE(128, true, true)
+    const bool mask = p.mask != nullptr;
+#define TME_CASE(d, b, c, m)                                  \
+    if (D == d && bf16 == b && causal == c && mask == m)      \
+        return launch_one<d, b, c, m>(tmQ, tmK, tmV, p, stream);
+#define TME_CASES(m)              \
+    TME_CASE(64, false, false, m)  \
+    TME_CASE(64, false, true, m)   \
+    TME_CASE(64, true, false, m)   \
+    TME_CASE(64, true, true, m)    \
+    TME_CASE(128, false, false, m) \
+    TME_CASE(128, false, true, m)  \
+    TME_CASE(128, true, false, m)  \
+    TME_CASE(128, true, true, m)
+    TME_CASES(false)
+    TME_CASES(true)
+#undef TME_CASES
 #undef TME_CASE
     return cudaErrorInvalidValue;
 }

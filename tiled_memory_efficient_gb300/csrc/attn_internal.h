@@ -41,9 +41,17 @@ struct FwdParams {
     int n_splits;            // key ranges (1: no split)
     int tiles_per_split;     // 128-key tiles per range
     float scale_log2;        // scale * log2(e)
+    // Optional attention bias (masked kernels only): element (b, h, i, j) at
+    // mask + b*msb + h*msh + i*msq + j elements; kind 1: bytes, nonzero keeps
+    // the key; kind 2: additive, 16-bit in the input dtype.
+    const void* mask;
+    int mask_kind;
+    int64_t msb, msh, msq;
+    int Hkv, G;              // KV heads, query heads per KV head
 };
 
 // Launches the forward kernel for one (D, dtype, causal) instantiation.
+// p.mask != nullptr selects the masked instantiation.
 cudaError_t launch_fwd(int D, bool bf16, bool causal, const CUtensorMap& tmQ,
                        const CUtensorMap& tmK, const CUtensorMap& tmV, const FwdParams& p,
                        cudaStream_t stream);

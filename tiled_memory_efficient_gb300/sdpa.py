@@ -14,8 +14,9 @@ for training.  This module provides that surface on GB300:
   ``torch.nn.functional.scaled_dot_product_attention``.
 
 There is no backend probing and no fallback to another implementation: an
-argument the kernels do not support (an attention mask, dropout, another head
-dim or dtype, a CPU tensor) raises ``NotImplementedError`` or ``ValueError``.
+argument the kernels do not support (dropout, another head dim or dtype, a CPU
+tensor, the gradient of a masked call) raises ``NotImplementedError`` or
+``ValueError``.
 """
 from __future__ import annotations
 
@@ -29,6 +30,19 @@ __all__ = ["attention", "scaled_dot_product_attention", "patch", "unpatch", "is_
 
 _SUPPORTED_D = (64, 128)
 _original_sdpa = None
+
+
+class _TiledAttentionMasked(torch.autograd.Function):
+    """Forward with an attn_mask; the backward of a masked call is not built."""
+    @staticmethod
+    def forward(ctx, q, k, v, mask, is_causal, scale):
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        out, _ = _lib.attn_fwd(q, k, v, causal=is_causal, scale=scale, mask=mask)
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        raise NotImplementedError("the backward of attention with attn_mask is not implemented")
 
 
 class _TiledAttention(torch.autograd.Function):
@@ -74,13 +88,16 @@ def _validate(q, k, v):
         raise ValueError("query heads must be a multiple of key/value heads")
 
 
-def attention(q, k, v, is_causal: bool = False, scale: float | None = None):
+def attention(q, k, v, is_causal: bool = False, scale: float | None = None, attn_mask=None):
     """Differentiable tiled attention.  q [B,Hq,Nq,D]; k, v [B,Hkv,Nk,D] with
     Hq a multiple of Hkv (query head h uses KV head h // (Hq//Hkv)); causal is
-    top-left aligned; scale defaults to 1/sqrt(D)."""
+    top-left aligned; scale defaults to 1/sqrt(D).  attn_mask: bool (True
+    keeps a key) or additive, broadcastable to [B,Hq,Nq,Nk]; forward only."""
     _validate(q, k, v)
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[-1])
+    if attn_mask is not None:
+        return _TiledAttentionMasked.apply(q, k, v, attn_mask, bool(is_causal), float(scale))
     return _TiledAttention.apply(q, k, v, bool(is_causal), float(scale))
 
 
@@ -88,17 +105,17 @@ def scaled_dot_product_attention(query, key, value, attn_mask=None, dropout_p=0.
                                  is_causal=False, scale=None, enable_gqa=False):
     """The SDPA call, served by the tiled kernels.
 
-    Supported: no attn_mask, dropout_p == 0, fp16/bf16 CUDA tensors
-    [B, H, N, D] with D in (64, 128).  With Hq != Hkv, enable_gqa must be set
-    (as for torch's own SDPA).  Anything else raises.
+    Supported: dropout_p == 0, fp16/bf16 CUDA tensors [B, H, N, D] with D in
+    (64, 128), an optional attn_mask (bool or floating, broadcastable to
+    [B, Hq, Nq, Nk]; its backward is not implemented and raises).  With
+    Hq != Hkv, enable_gqa must be set (as for torch's own SDPA).  Anything
+    else raises.
     """
-    if attn_mask is not None:
-        raise NotImplementedError("attn_mask is not supported by the tiled kernels")
     if dropout_p != 0.0:
         raise NotImplementedError("dropout is not supported by the tiled kernels")
     if query.dim() == 4 and key.dim() == 4 and query.shape[1] != key.shape[1] and not enable_gqa:
         raise ValueError("query and key head counts differ: pass enable_gqa=True")
-    return attention(query, key, value, is_causal=is_causal, scale=scale)
+    return attention(query, key, value, is_causal=is_causal, scale=scale, attn_mask=attn_mask)
 
 
 def patch():
