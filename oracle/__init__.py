@@ -66,6 +66,10 @@ def _load():
                                             ctypes.c_double, ctypes.c_int, _dp, _dp, _dp,
                                             ctypes.c_int]
             lib.oracle_attn_bwd.restype = ctypes.c_int
+            lib.oracle_attn_bwd_bias.argtypes = [_dp, _dp, _dp, _dp, i64, i64, i64, i64, i64, i64,
+                                                 ctypes.c_double, ctypes.c_int, _dp, i64, i64, i64,
+                                                 _dp, _dp, _dp, ctypes.c_int]
+            lib.oracle_attn_bwd_bias.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -169,10 +173,12 @@ def attention_fwd(q, k, v, causal=False, scale: float | None = None,
 
 
 def attention_bwd(q, k, v, dout, causal: bool = False, scale: float | None = None,
-                  threads: int | None = None):
-    """Gradients of the forward definition, in fp64: returns (dq, dk, dv)."""
+                  threads: int | None = None, mask=None):
+    """Gradients of the forward definition, in fp64: returns (dq, dk, dv).
+    ``mask`` as for attention_fwd (rows with every key masked get zero)."""
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     B, Hq, Hkv, Nq, Nk, D = _shapes(q, k, v)
+    bias, bstr = (None, (0, 0, 0)) if mask is None else _bias_f64(mask, B, Hq, Nq, Nk)
     if dout.shape != q.shape:
         raise ValueError("dout must have q's shape")
     if scale is None:
@@ -180,11 +186,13 @@ def attention_bwd(q, k, v, dout, causal: bool = False, scale: float | None = Non
     dq = np.empty_like(q)
     dk = np.empty_like(k)
     dv = np.empty_like(v)
-    rc = _load().oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B, Hq, Hkv, Nq, Nk, D,
-                                 float(scale), causal_code(causal), _ptr(dq), _ptr(dk), _ptr(dv),
-                                 int(threads or default_threads()))
+    rc = _load().oracle_attn_bwd_bias(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B, Hq, Hkv, Nq, Nk,
+                                      D, float(scale), causal_code(causal),
+                                      None if bias is None else _ptr(bias), *bstr,
+                                      _ptr(dq), _ptr(dk), _ptr(dv),
+                                      int(threads or default_threads()))
     if rc != 0:
-        raise RuntimeError(f"oracle_attn_bwd failed with {rc}")
+        raise RuntimeError(f"oracle_attn_bwd_bias failed with {rc}")
     return dq, dk, dv
 
 

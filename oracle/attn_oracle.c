@@ -222,6 +222,8 @@ typedef struct {
     int64_t Hq, Hkv, Nq, Nk, D;
     double scale;
     int causal;
+    const double *bias;            /* additive bias as in the forward, or NULL */
+    int64_t bsb, bsh, bsq;
     int64_t row_begin, row_end;    /* slice of the unit's G*Nq rows (head-major) */
     int status;
 } bwd_job_t;
@@ -250,13 +252,19 @@ static void *bwd_worker(void *arg)
         const double *do_row = jb->dout + r * D;
         double *dq_row = jb->dq + r * D;
         const int64_t nkeys = allowed_keys(i, Nk, jb->causal);
+        const double *bias_row = jb->bias ? jb->bias + b * jb->bsb + h * jb->bsh + i * jb->bsq : NULL;
         /* scores and their log-sum-exp, as in the forward definition */
         double m = -INFINITY;
         for (int64_t j = 0; j < nkeys; ++j) {
             double dot = 0.0;
             for (int64_t d = 0; d < D; ++d) dot += q_row[d] * k_head[j * D + d];
             p[j] = jb->scale * dot;
+            if (bias_row) p[j] += bias_row[j];
             if (p[j] > m) m = p[j];
+        }
+        if (m == -INFINITY) {   /* every key removed: O = 0 does not depend on q, k, v */
+            for (int64_t d = 0; d < D; ++d) dq_row[d] = 0.0;
+            continue;
         }
         double l = 0.0;
         for (int64_t j = 0; j < nkeys; ++j) l += exp(p[j] - m);
@@ -291,12 +299,14 @@ static void *bwd_worker(void *arg)
  * rows' contributions to dk/dv in a private buffer, and the buffers are added
  * up after the join, so no two threads ever write the same element.
  */
-int oracle_attn_bwd(const double *q, const double *k, const double *v, const double *dout,
-                    int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t D,
-                    double scale, int causal,
-                    double *dq, double *dk, double *dv, int nthreads)
+int oracle_attn_bwd_bias(const double *q, const double *k, const double *v, const double *dout,
+                         int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t D,
+                         double scale, int causal,
+                         const double *bias, int64_t bsb, int64_t bsh, int64_t bsq,
+                         double *dq, double *dk, double *dv, int nthreads)
 {
     if (check_shape(B, Hq, Hkv, Nq, Nk, D)) return -1;
+    if (bias && (bsb < 0 || bsh < 0 || bsq < 0)) return -1;
     if (!q || !k || !v || !dout || !dq || !dk || !dv) return -1;
     if (causal < 0 || causal > 1) return -1;   /* the backward covers none / top-left */
     const int64_t G = Hq / Hkv;
@@ -318,6 +328,7 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v, const dou
                 jb->b = b; jb->g = g;
                 jb->Hq = Hq; jb->Hkv = Hkv; jb->Nq = Nq; jb->Nk = Nk; jb->D = D;
                 jb->scale = scale; jb->causal = causal;
+                jb->bias = bias; jb->bsb = bsb; jb->bsh = bsh; jb->bsq = bsq;
                 jb->row_begin = unit_rows * t / nthreads;
                 jb->row_end = unit_rows * (t + 1) / nthreads;
                 jb->status = -2;
@@ -345,4 +356,14 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v, const dou
     }
     free(jobs); free(tids); free(parts);
     return rc;
+}
+
+/* Backward without a bias. */
+int oracle_attn_bwd(const double *q, const double *k, const double *v, const double *dout,
+                    int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t D,
+                    double scale, int causal,
+                    double *dq, double *dk, double *dv, int nthreads)
+{
+    return oracle_attn_bwd_bias(q, k, v, dout, B, Hq, Hkv, Nq, Nk, D, scale, causal, NULL, 0, 0, 0,
+                                dq, dk, dv, nthreads);
 }

@@ -311,6 +311,37 @@ def test_mask_closed_forms():
     assert lm[0, 0, 4] == -math.inf
 
 
+@pytest.mark.parametrize("kind", ["bool", "additive"])
+def test_masked_backward_matches_torch_autograd(kind):
+    """Gradients with an attn_mask against torch.autograd through fp64 SDPA
+    (GQA by repeat_interleave, so dk/dv are summed over the group); a query
+    row with every key masked contributes nothing."""
+    B, Hq, Hkv, Nq, Nk, D = 2, 4, 2, 11, 17, 8
+    q, k, v = rnd((B, Hq, Nq, D), 111), rnd((B, Hkv, Nk, D), 112), rnd((B, Hkv, Nk, D), 113)
+    do = rnd((B, Hq, Nq, D), 114)
+    g = torch.Generator().manual_seed(115)
+    if kind == "bool":
+        mask = torch.rand(B, 1, Nq, Nk, generator=g) > 0.4
+        mask[..., 0] = True
+        mask[1, 0, 5] = False             # an empty row
+        bias = torch.zeros(B, 1, Nq, Nk, dtype=torch.float64).masked_fill(~mask, -math.inf)
+    else:
+        mask = torch.randn(1, Hq, Nq, Nk, generator=g, dtype=torch.float64)
+        bias = mask
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, mask=mask)
+    qt, kt, vt = (torch.as_tensor(x).requires_grad_(True) for x in (q, k, v))
+    G = Hq // Hkv
+    keep = torch.isfinite(bias).any(-1, keepdim=True)         # torch gives NaN on empty rows
+    safe = torch.where(keep, bias, torch.zeros_like(bias))
+    out = F.scaled_dot_product_attention(qt, kt.repeat_interleave(G, 1), vt.repeat_interleave(G, 1),
+                                         attn_mask=safe) * keep
+    out.backward(torch.as_tensor(do))
+    for name, got, ref in (("dq", dq, qt.grad), ("dk", dk, kt.grad), ("dv", dv, vt.grad)):
+        np.testing.assert_allclose(got, ref.numpy(), rtol=0, atol=1e-11, err_msg=name)
+    if kind == "bool":
+        np.testing.assert_array_equal(dq[1, 0, 5], 0.0)
+
+
 def test_causal_row_zero_is_first_value():
     q, k, v = rnd((2, 2, 9, 8), 28), rnd((2, 2, 9, 8), 29), rnd((2, 2, 9, 8), 30)
     o, _ = oracle.attention_fwd(q, k, v, causal=True)

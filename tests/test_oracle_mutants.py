@@ -37,7 +37,8 @@ MUTANTS = {
     "bottom_right_off_by_one": ("? i + (jb->Nk - jb->Nq) : i;", "? i + (jb->Nk - jb->Nq) - 1 : i;"),
     "bottom_right_as_top_left": ("? i + (jb->Nk - jb->Nq) : i;", "? i : i;"),
     "mask_subtracted": ("if (bias_row) s[j] += bias_row[j];", "if (bias_row) s[j] -= bias_row[j];"),
-    "mask_query_stride_ignored": ("+ i * jb->bsq", "+ 0 * jb->bsq"),
+    "mask_query_stride_ignored": ("+ i * jb->bsq : NULL;\n        fwd_one_row", "+ 0 * jb->bsq : NULL;\n        fwd_one_row"),
+    "bwd_mask_ignored": ("if (bias_row) p[j] += bias_row[j];", "if (bias_row) p[j] += 0.0;"),
 }
 
 
@@ -56,6 +57,7 @@ def battery():
         ("bottom_right_prefix", pins.test_zero_query_bottom_right_gives_prefix_means, ()),
         ("mask_closed_forms", pins.test_mask_closed_forms, ()),
         ("mask_sdpa", pins.test_mask_matches_torch_sdpa_f64, ((2, 4, 13, 23), "additive", True)),
+        ("mask_autograd", pins.test_masked_backward_matches_torch_autograd, ("bool",)),
     ]
     failed = []
     for name, fn, args in checks:
@@ -80,7 +82,8 @@ def swap_lib(tmp_path, monkeypatch):
         import ctypes
         lib = ctypes.CDLL(str(so))
         real = oracle._load()
-        for fname in ("oracle_attn_fwd_rows", "oracle_attn_fwd_rows_bias", "oracle_attn_bwd"):
+        for fname in ("oracle_attn_fwd_rows", "oracle_attn_fwd_rows_bias", "oracle_attn_bwd",
+                      "oracle_attn_bwd_bias"):
             getattr(lib, fname).argtypes = getattr(real, fname).argtypes
             getattr(lib, fname).restype = getattr(real, fname).restype
         monkeypatch.setattr(oracle, "_lib", lib)
