@@ -160,6 +160,19 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
              int causal, int dtype, void* stream);
 
 /*
+ * Backward of attn_fwd_masked: the same bias (same mask, kind and strides)
+ * enters the recomputed scores; rows whose every key was masked (forward LSE
+ * -inf) contribute nothing.  Other arguments, layouts and errors are those of
+ * attn_bwd and attn_fwd_masked.
+ */
+int attn_bwd_masked(const void* q, const void* k, const void* v, const void* out,
+                    const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                    void* workspace, size_t workspace_bytes, const void* mask, int mask_kind,
+                    long long mask_stride_b, long long mask_stride_h, long long mask_stride_q,
+                    int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal,
+                    int dtype, void* stream);
+
+/*
  * attn_bwd without a workspace argument, for callers that cannot allocate
  * device memory (for example an operator handed its buffers by a framework
  * that owns every device allocation, or code that must not call cudaMalloc /

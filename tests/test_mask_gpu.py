@@ -100,7 +100,40 @@ def test_sdpa_with_attn_mask(cuda_lib):
     o_ref, _ = oracle.attention_fwd(x["q"], x["k"], x["v"], mask=mask)
     helpers.assert_close_elementwise(out.double().cpu().numpy(), o_ref, helpers.TOL_O[F16], F16,
                                      "sdpa mask", "O")
-    qg = q.clone().requires_grad_(True)
-    y = sdpa.scaled_dot_product_attention(qg, k, v, attn_mask=mask.cuda(), enable_gqa=True)
-    with pytest.raises(NotImplementedError):
-        y.sum().backward()
+
+
+BWD_CASES = [
+    # B, Hq, Hkv, N, D, dtype, causal, mask shape (None: padding), kind
+    (2, 4, 2, 300, 64, F16, False, None, "padding"),
+    (1, 4, 4, 257, 128, BF16, True, (1, 4, 257, 257), "additive"),
+    (2, 6, 2, 200, 128, BF16, False, (2, 1, 200, 200), "bool"),
+    (1, 14, 2, 90, 64, F16, True, (90, 90), "bool"),     # heads of 90 rows: tiles span heads
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,D,dtype,causal,shape,kind", BWD_CASES)
+def test_masked_backward_matches_oracle(cuda_lib, B, Hq, Hkv, N, D, dtype, causal, shape, kind):
+    x = inputs.make_custom(B, Hq, Hkv, N, N, D, dtype, seed=7 * N + D, with_grad=True)
+    mask = make_mask(shape or (B, 1, 1, N), kind, dtype, seed=N + 1, Nk=N)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    mc = mask.cuda()
+    out, lse = _lib.attn_fwd(q, k, v, causal=causal, mask=mc)
+    dq, dk, dv = _lib.attn_bwd(q, k, v, out, do, lse, causal=causal, mask=mc)
+    assert _lib.sync_status() == _lib.ATTN_OK
+    ref = oracle.attention_bwd(x["q"], x["k"], x["v"], x["do"], causal=causal, mask=mask)
+    for name, t, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        e = helpers.assert_close_elementwise(t.double().cpu().numpy(), r, helpers.TOL_BWD[dtype],
+                                             dtype, f"masked bwd {kind} {shape}", name)
+        print(f"{kind} {shape} {name}: max err {e:.2e}")
+
+
+def test_sdpa_masked_autograd(cuda_lib):
+    x = inputs.make_custom(1, 4, 4, 256, 256, 128, BF16, seed=16, with_grad=True)
+    mask = make_mask((1, 1, 256, 256), "bool", BF16, seed=17, Nk=256, empty_rows=True)
+    q, k, v = (x[n].cuda().requires_grad_(True) for n in "qkv")
+    out = sdpa.scaled_dot_product_attention(q, k, v, attn_mask=mask.cuda())
+    out.backward(x["do"].cuda())
+    ref = oracle.attention_bwd(x["q"], x["k"], x["v"], x["do"], mask=mask)
+    for name, t, r in zip(("dq", "dk", "dv"), (q, k, v), ref):
+        helpers.assert_close_elementwise(t.grad.double().cpu().numpy(), r, helpers.TOL_BWD[BF16],
+                                         BF16, "sdpa masked bwd", name)

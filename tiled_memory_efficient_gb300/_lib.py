@@ -52,6 +52,9 @@ _SIGNATURES = {
     "attn_bwd_workspace_size": ([_i, _i, _i, _i, _i, _i, _i], ctypes.c_size_t),
     "attn_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
                   _i, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i, _vp], _i),
+    "attn_bwd_masked": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp,
+                         _i, ctypes.c_longlong, ctypes.c_longlong, ctypes.c_longlong,
+                         _i, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i, _vp], _i),
     "attn_bwd_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                           _i, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i, _vp], _i),
     "attn_sync_status": ([_vp], _i),
@@ -258,8 +261,9 @@ def attn_fwd_splitkv(q, k, v, causal=False, scale: float | None = None, splits: 
 
 
 def attn_bwd(q, k, v, out, dout, lse, causal: bool = False, scale: float | None = None,
-             dq=None, dk=None, dv=None, workspace=None):
-    """dq, dk, dv of attn_fwd (dk, dv summed over each GQA group)."""
+             dq=None, dk=None, dv=None, workspace=None, mask=None):
+    """dq, dk, dv of attn_fwd (dk, dv summed over each GQA group); with the
+    forward's mask, of attn_fwd(mask=...)."""
     import torch
     _check(q, k, v)
     B, Hq, Nq, D = q.shape
@@ -274,6 +278,17 @@ def attn_bwd(q, k, v, out, dout, lse, causal: bool = False, scale: float | None 
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    if mask is not None:
+        m, kind, (sb, sh, sq) = prepare_mask(mask, q, Nk)
+        rc = lib.attn_bwd_masked(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                 dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                 dv.data_ptr(), workspace.data_ptr(),
+                                 workspace.numel() * workspace.element_size(), m.data_ptr(), kind,
+                                 sb, sh, sq, B, Hq, Hkv, Nq, Nk, D, float(scale),
+                                 causal_code(causal), dt, _stream_handle(q.device))
+        if rc != ATTN_OK:
+            raise AttnError("attn_bwd_masked", rc)
+        return dq, dk, dv
     rc = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), dout.data_ptr(),
                       lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                       workspace.data_ptr(), workspace.numel() * workspace.element_size(),

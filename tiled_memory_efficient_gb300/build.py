@@ -19,7 +19,7 @@ LIB = os.path.join(BUILD, "libattn.so")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 
 SOURCES = ["abi.cu", "attn_fwd.cu", "attn_bwd.cu", "bwd_noalloc.cu", "splitkv.cu"]
-HEADERS = ["ptx.cuh", "attn_internal.h"]
+HEADERS = ["ptx.cuh", "attn_internal.h", "bias.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

@@ -147,6 +147,18 @@ int effective_splits(int Nk, int requested) {
     return static_cast<int>((tiles + per - 1) / per);
 }
 
+// Checks shared by the mask entry points: kind, strides, alignment of the
+// 16-byte vector loads of bias rows.
+int check_mask(const void* mask, int kind, long long sb, long long sh, long long sq) {
+    if (!mask) return ATTN_ERR_INVALID;
+    if (kind != ATTN_MASK_BOOL && kind != ATTN_MASK_ADDITIVE) return ATTN_ERR_INVALID;
+    if (sb < 0 || sh < 0 || sq < 0) return ATTN_ERR_INVALID;
+    const long long esz = kind == ATTN_MASK_ADDITIVE ? 2 : 1;
+    if (!aligned16(mask) || (sb * esz) % 16 || (sh * esz) % 16 || (sq * esz) % 16)
+        return ATTN_ERR_ALIGN;
+    return ATTN_OK;
+}
+
 // Checks shared by the forward entry points; fills everything in FwdParams
 // but the split fields.
 int fwd_prepare(const void* q, const void* k, const void* v, void* out, float* lse, int B,
@@ -213,17 +225,11 @@ extern "C" int attn_fwd_masked(const void* q, const void* k, const void* v, void
                                long long mask_stride_h, long long mask_stride_q, int B, int Hq,
                                int Hkv, int Nq, int Nk, int D, float scale, int causal, int dtype,
                                void* stream) {
-    if (!mask) return ATTN_ERR_INVALID;
-    if (mask_kind != ATTN_MASK_BOOL && mask_kind != ATTN_MASK_ADDITIVE) return ATTN_ERR_INVALID;
-    if (mask_stride_b < 0 || mask_stride_h < 0 || mask_stride_q < 0) return ATTN_ERR_INVALID;
-    const long long esz = mask_kind == ATTN_MASK_ADDITIVE ? 2 : 1;
-    // 16-byte vector loads of 32 keys: the start of every bias row is aligned
-    if (!aligned16(mask) || (mask_stride_b * esz) % 16 || (mask_stride_h * esz) % 16 ||
-        (mask_stride_q * esz) % 16)
-        return ATTN_ERR_ALIGN;
+    int rc = check_mask(mask, mask_kind, mask_stride_b, mask_stride_h, mask_stride_q);
+    if (rc != ATTN_OK) return rc;
     CUtensorMap tmQ, tmK, tmV;
     FwdParams p;
-    const int rc = fwd_prepare(q, k, v, out, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype,
+    rc = fwd_prepare(q, k, v, out, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype,
                                &tmQ, &tmK, &tmV, &p);
     if (rc != ATTN_OK) return rc;
     p.mask = mask;
@@ -318,10 +324,14 @@ extern "C" size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk
     return (2 * groups * rows_pad * sizeof(float) + 255) & ~static_cast<size_t>(255);
 }
 
-extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* out,
-                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
-                        void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int Nq,
-                        int Nk, int D, float scale, int causal, int dtype, void* stream) {
+namespace tme {
+namespace {
+
+int bwd_run(const void* q, const void* k, const void* v, const void* out, const void* dout,
+            const float* lse, void* dq, void* dk, void* dv, void* workspace,
+            size_t workspace_bytes, int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale,
+            int causal, int dtype, const void* mask, int mask_kind, long long msb, long long msh,
+            long long msq, void* stream) {
     if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv || !workspace)
         return ATTN_ERR_INVALID;
     int rc = check_shape(B, Hq, Hkv, Nq, Nk, D, scale, dtype);
@@ -368,11 +378,42 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
     p.n_ktiles = (Nk + 127) / 128;
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.mask = mask;
+    p.mask_kind = mask_kind;
+    p.msb = msb;
+    p.msh = msh;
+    p.msq = msq;
+    p.Hkv = Hkv;
+    p.G = static_cast<int>(G);
     if (groups * p.n_ktiles > 0x7fffffffll || groups * n_qtiles > 0x7fffffffll)
         return ATTN_ERR_UNSUPPORTED;
     const cudaError_t e = launch_bwd(D, bf16, causal != 0, tmQ, tmK, tmV, tmDO, p,
                                      static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace tme
+
+extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                        void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int Nq,
+                        int Nk, int D, float scale, int causal, int dtype, void* stream) {
+    return bwd_run(q, k, v, out, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, Nq,
+                   Nk, D, scale, causal, dtype, nullptr, 0, 0, 0, 0, stream);
+}
+
+extern "C" int attn_bwd_masked(const void* q, const void* k, const void* v, const void* out,
+                               const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                               void* workspace, size_t workspace_bytes, const void* mask,
+                               int mask_kind, long long mask_stride_b, long long mask_stride_h,
+                               long long mask_stride_q, int B, int Hq, int Hkv, int Nq, int Nk,
+                               int D, float scale, int causal, int dtype, void* stream) {
+    const int rc = check_mask(mask, mask_kind, mask_stride_b, mask_stride_h, mask_stride_q);
+    if (rc != ATTN_OK) return rc;
+    return bwd_run(q, k, v, out, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, Nq,
+                   Nk, D, scale, causal, dtype, mask, mask_kind, mask_stride_b, mask_stride_h,
+                   mask_stride_q, stream);
 }
 
 extern "C" int attn_sync_status(void* stream) {

@@ -25,6 +25,7 @@
 #include <cstdint>
 
 #include "attn_internal.h"
+#include "bias.cuh"
 #include "ptx.cuh"
 
 namespace tme {
@@ -83,7 +84,9 @@ __global__ void __launch_bounds__(256) bwd_stats_kernel(const BwdParams p) {
     if (row < p.total_rows && sub == 0) {
         const int64_t g = row / p.rows_per_group, r = row % p.rows_per_group;
         p.ndelta[g * p.rows_pad + r] = -acc;
-        p.nlse2[g * p.rows_pad + r] = -p.lse[row] * kLog2e;
+        // A row whose every key was masked (LSE = -inf) gets P = 0 everywhere.
+        const float lse = p.lse[row];
+        p.nlse2[g * p.rows_pad + r] = lse == -INFINITY ? -INFINITY : -lse * kLog2e;
     }
 }
 
@@ -116,6 +119,52 @@ __device__ __forceinline__ int next_tile_pos(int pos, int Nq) {
     return pos;
 }
 
+// The same, also tracking the head (within the group) of that row.
+__device__ __forceinline__ void next_tile(int& pos, int& head, int Nq) {
+    pos += kRows;
+    if (pos >= Nq) {
+        if (Nq >= kRows) {
+            pos -= Nq;
+            ++head;
+        } else {
+            head += pos / Nq;
+            pos %= Nq;
+        }
+    }
+}
+
+// dK/dV layout: a thread owns one key; the bias of its 32 query rows
+// (first row at head `head`, position `pos`, all of them real if row_ok_all,
+// else only rows below `rows_left`) runs down a column of the mask.  The
+// scores in x become log2-domain logits, in place.
+template <bool BF16>
+__device__ __forceinline__ void bias_apply_column(uint32_t (&x)[32], const BwdParams& p,
+                                                  int64_t b_off, int head, int pos, int key,
+                                                  int rows_left, float sl2) {
+    constexpr float kL2e = 1.4426950408889634f;
+    const uint8_t* base = static_cast<const uint8_t*>(p.mask);
+    const int esz = p.mask_kind == 2 ? 2 : 1;
+    int64_t off = b_off + static_cast<int64_t>(head) * p.msh + static_cast<int64_t>(pos) * p.msq;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        float t = __uint_as_float(x[i]) * sl2;
+        if (i < rows_left && key < p.Nk) {
+            const uint8_t* e = base + (off + key) * esz;
+            if (p.mask_kind == 2)
+                t += half_to_float<BF16>(*reinterpret_cast<const uint16_t*>(e)) * kL2e;
+            else if (*e == 0)
+                t = -INFINITY;
+        }
+        x[i] = __float_as_uint(t);
+        if (++pos == p.Nq) {   // the next row starts the next head
+            pos = 0;
+            off += p.msh - static_cast<int64_t>(p.Nq - 1) * p.msq;
+        } else {
+            off += p.msq;
+        }
+    }
+}
+
 constexpr int kDqKStages = 3;  // dQ kernel: K ring (live from S_j to dQ_j)
 constexpr int kDqVStages = 2;  // dQ kernel: V ring (live until dP_j)
 
@@ -138,7 +187,7 @@ struct BwdCfg {
 // its P^T / dS^T are in TMEM, then S^T / dP^T of half u of tile n+1 into the
 // same columns (the tensor pipe runs in order, so the products of tile n have
 // read them first).
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool MASK>
 __global__ void __launch_bounds__(kKvThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmDO,
@@ -297,13 +346,34 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         const uint32_t lb = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t tS = tmem + lb + 128 * hq + 32 * cc, tDP = tS + 64;
         const float sl2 = p.scale_log2;
+        const float sc = MASK ? 1.0f : sl2;   // scale still to apply to the scores read below
+        const int64_t b_off = MASK ? static_cast<int64_t>(group / p.Hkv) * p.msb : 0;
+        const int head0 = MASK ? (group % p.Hkv) * p.G : 0;
         int n = 0;
-        for (int qi = 0, pos = 0; qi < p.n_qtiles; ++qi, pos = next_tile_pos(pos, p.Nq)) {
+        int head = 0;   // head within the group of the current tile's first row
+        for (int qi = 0, pos = 0; qi < p.n_qtiles; ++qi, next_tile(pos, head, p.Nq)) {
             if (!visit(qi, pos)) continue;
             const int slot = n % QS;
             warp_wait(&q_full[slot], (n / QS) & 1, abort_flag, p.status);
             warp_wait(&s_full[hq], n & 1, abort_flag, p.status);
             tc_fence_after();
+            if constexpr (MASK) {
+                // this chunk's scores -> logits with the bias, in place in TMEM
+                uint32_t x[32];
+                tmem_ld32(tS, x);
+                int cpos = pos + 32 * c, chead = head;   // first query row of the chunk
+                while (cpos >= p.Nq) {
+                    cpos -= p.Nq;
+                    ++chead;
+                }
+                const int64_t left = p.rows_per_group - static_cast<int64_t>(qi) * kRows - 32 * c;
+                tmem_wait_ld();
+                reg_fence(x);
+                bias_apply_column<BF16>(x, p, b_off, head0 + chead, cpos, key,
+                                        left < 32 ? static_cast<int>(left) : 32, sl2);
+                tmem_st32(tS, x);
+                tmem_wait_st();
+            }
             uint32_t sv[32], dp[32];
             tmem_ld32(tS, sv);
             tmem_ld32(tDP, dp);
@@ -319,7 +389,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             bool fast = (row0 + q_first + 32 <= p.rows_per_group) && (wkey_last < p.Nk);
             if (CAUSAL)
                 fast = fast && (base + q_first + 32 <= p.Nq) && (wkey_last <= base + q_first);
-            const uint64_t sl22 = f2(sl2, sl2);
+            const uint64_t sl22 = f2(sc, sc);
             tmem_wait_ld();
             reg_fence(sv);
             reg_fence(dp);
@@ -352,7 +422,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                         const int q = q_first + i + u;
                         bool ok = (row0 + q < p.rows_per_group) && (key < p.Nk);
                         if (CAUSAL) ok = ok && key <= tile_pos(base, q, p.Nq);
-                        const float pr = ex2_ftz(fmaf(__uint_as_float(sv[i + u]), sl2, L[i + u]));
+                        const float pr = ex2_ftz(fmaf(__uint_as_float(sv[i + u]), sc, L[i + u]));
                         pp[u] = ok ? pr : 0.0f;
                         dd[u] = ok ? pr * (__uint_as_float(dp[i + u]) + Dl[i + u]) : 0.0f;
                     }
@@ -418,7 +488,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 // Warpgroup h owns key columns [64h, 64h+64).  dS has its own columns, so once
 // both warpgroups have read S_j and dP_j into registers (s_free) the tensor
 // core computes S_{j+1} and dP_{j+1} while the elementwise work on j runs.
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool MASK>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmDO,
@@ -576,12 +646,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t wr0 = row0 + quad * 32;
         const int64_t wr1 = min(wr0 + 31, p.rows_per_group - 1);
         const int warp_min_pos = (wr0 / p.Nq == wr1 / p.Nq) ? static_cast<int>(wr0 % p.Nq) : 0;
-        const uint64_t sl22 = f2(sl2, sl2), nl2 = f2(nl, nl), nd2 = f2(nd, nd);
+        const float sc = MASK ? 1.0f : sl2;   // scale still to apply to the scores read below
+        const uint64_t sl22 = f2(sc, sc), nl2 = f2(nl, nl), nd2 = f2(nd, nd);
         const uint32_t tDS = tmem + lb + 384;
+        // This row's bias: query head hkv*G + row/Nq of batch group/Hkv.
+        const uint8_t* mrow = nullptr;
+        if constexpr (MASK) {
+            const int64_t h = static_cast<int64_t>(group % p.Hkv) * p.G + row / p.Nq;
+            const int64_t b = group / p.Hkv;
+            mrow = static_cast<const uint8_t*>(p.mask) +
+                   (b * p.msb + h * p.msh + pos * p.msq) * (p.mask_kind == 2 ? 2 : 1);
+        }
         for (int j = 0; j < nkv; ++j) {
             warp_wait(s_full, j & 1, abort_flag, p.status);
             tc_fence_after();
             const int k0 = j * kRows;
+            if constexpr (MASK) {
+                // this half's scores -> logits with the bias, in place in TMEM
+#pragma unroll 1
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int key = k0 + (2 * hq + cc) * 32;
+                    const bool full = row_ok && key + 32 <= p.Nk;
+                    BiasChunk b;
+                    bias_load(b, mrow, p.mask_kind, key, full);
+                    uint32_t x[32];
+                    tmem_ld32(tS + (2 * hq + cc) * 32, x);
+                    tmem_wait_ld();
+                    reg_fence(x);
+                    bias_apply<BF16>(x, b, mrow, p.mask_kind, key, p.Nk, sl2, full, row_ok);
+                    tmem_st32(tS + (2 * hq + cc) * 32, x);
+                }
+                tmem_wait_st();
+            }
             const bool need_mask = (k0 + kRows > p.Nk) || (CAUSAL && k0 + kRows - 1 > warp_min_pos);
             uint32_t sv[2][32], dp[2][32];
 #pragma unroll
@@ -666,7 +762,7 @@ constexpr int dq_smem() {
     return (2 + kDqKStages + kDqVStages) * BwdCfg<D>::kTileBytes + 2 * kRows * 4 + 256 + 1024;
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool MASK>
 cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                        const CUtensorMap& tmDO, const BwdParams& p, cudaStream_t stream) {
     {
@@ -676,7 +772,7 @@ cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
         if (e != cudaSuccess) return e;
     }
     {
-        auto kern = bwd_dkdv_kernel<D, BF16, CAUSAL>;
+        auto kern = bwd_dkdv_kernel<D, BF16, CAUSAL, MASK>;
         constexpr int smem = dkdv_smem<D>();
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
@@ -686,7 +782,7 @@ cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
         if (e != cudaSuccess) return e;
     }
     {
-        auto kern = bwd_dq_kernel<D, BF16, CAUSAL>;
+        auto kern = bwd_dq_kernel<D, BF16, CAUSAL, MASK>;
         constexpr int smem = dq_smem<D>();
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
@@ -703,17 +799,22 @@ cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
 cudaError_t launch_bwd(int D, bool bf16, bool causal, const CUtensorMap& tmQ,
                        const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmDO,
                        const BwdParams& p, cudaStream_t stream) {
-#define TME_CASE(d, b, c)                   \
-    if (D == d && bf16 == b && causal == c) \
-        return launch_one<d, b, c>(tmQ, tmK, tmV, tmDO, p, stream);
-    TME_CASE(64, false, false)
-    TME_CASE(64, false, true)
-    TME_CASE(64, true, false)
-    TME_CASE(64, true, true)
-    TME_CASE(128, false, false)
-    TME_CASE(128, false, true)
-    TME_CASE(128, true, false)
-    TME_CASE(128, true, true)
+    const bool mask = p.mask != nullptr;
+#define TME_CASE(d, b, c, m)                              \
+    if (D == d && bf16 == b && causal == c && mask == m)  \
+        return launch_one<d, b, c, m>(tmQ, tmK, tmV, tmDO, p, stream);
+#define TME_CASES(m)              \
+    TME_CASE(64, false, false, m)  \
+    TME_CASE(64, false, true, m)   \
+    TME_CASE(64, true, false, m)   \
+    TME_CASE(64, true, true, m)    \
+    TME_CASE(128, false, false, m) \
+    TME_CASE(128, false, true, m)  \
+    TME_CASE(128, true, false, m)  \
+    TME_CASE(128, true, true, m)
+    TME_CASES(false)
+    TME_CASES(true)
+#undef TME_CASES
 #undef TME_CASE
     return cudaErrorInvalidValue;
 }

@@ -83,9 +83,15 @@ struct BwdParams {
     int n_ktiles;            // ceil(Nk / 128)
     float scale;
     float scale_log2;
+    // Optional attention bias, as in FwdParams (masked kernels only).
+    const void* mask;
+    int mask_kind;
+    int64_t msb, msh, msq;
+    int Hkv, G;
 };
 
-// Launches the three backward kernels (statistics, dK/dV, dQ) in order.
+// Launches the three backward kernels (statistics, dK/dV, dQ) in order;
+// p.mask != nullptr selects the masked instantiations.
 cudaError_t launch_bwd(int D, bool bf16, bool causal, const CUtensorMap& tmQ,
                        const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmDO,
                        const BwdParams& p, cudaStream_t stream);

@@ -1,0 +1,90 @@
+// bias.cuh -- the attention bias (the SDPA call's attn_mask) applied to a
+// row of scores, shared by the forward and backward kernels.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace tme {
+
+// Attention bias (SDPA attn_mask) of one 32-key chunk of a row, applied in
+// the log2 domain: t = s * sl2 + b * log2(e) for an additive bias (16-bit,
+// the input dtype), t = s * sl2 or -inf for a boolean keep-mask (bytes).
+struct BiasChunk {
+    uint4 w[4];
+};
+
+__device__ __forceinline__ void bias_load(BiasChunk& b, const uint8_t* row, int kind, int key,
+                                          bool full) {
+    if (!full) return;
+    if (kind == 2) {
+        const uint4* src = reinterpret_cast<const uint4*>(row + 2 * static_cast<int64_t>(key));
+        b.w[0] = src[0];
+        b.w[1] = src[1];
+        b.w[2] = src[2];
+        b.w[3] = src[3];
+    } else {
+        const uint4* src = reinterpret_cast<const uint4*>(row + key);
+        b.w[0] = src[0];
+        b.w[1] = src[1];
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ float half_to_float(uint32_t h) {
+    if constexpr (BF16) return __uint_as_float(h << 16);
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+}
+
+// `full`: the 32 keys are in range and the row is real, and b holds them.
+// Otherwise keys are read one by one (keys >= Nk and unreal rows: no bias).
+template <bool BF16>
+__device__ __forceinline__ void bias_apply(uint32_t (&s)[32], const BiasChunk& b,
+                                           const uint8_t* row, int kind, int key, int Nk,
+                                           float sl2, bool full, bool row_ok) {
+    constexpr float kLog2e = 1.4426950408889634f;
+    if (full) {
+        if (kind == 2) {
+            const uint64_t sl22 = f2(sl2, sl2), l2e2 = f2(kLog2e, kLog2e);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint4 q4 = b.w[i >> 2];
+                const uint32_t w = (i & 3) == 0 ? q4.x : (i & 3) == 1 ? q4.y : (i & 3) == 2 ? q4.z : q4.w;
+                const uint64_t bb = fmul2(f2(half_to_float<BF16>(w & 0xffffu), half_to_float<BF16>(w >> 16)),
+                                          l2e2);
+                const uint64_t t = ffma2(f2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
+                                         sl22, bb);
+                s[2 * i] = __float_as_uint(f2lo(t));
+                s[2 * i + 1] = __float_as_uint(f2hi(t));
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const uint4 q4 = b.w[i >> 4];
+                const int wi = (i >> 2) & 3;
+                const uint32_t w = wi == 0 ? q4.x : wi == 1 ? q4.y : wi == 2 ? q4.z : q4.w;
+                const bool keep = ((w >> (8 * (i & 3))) & 0xffu) != 0u;
+                s[i] = __float_as_uint(keep ? __uint_as_float(s[i]) * sl2 : -INFINITY);
+            }
+        }
+        return;
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        float t = __uint_as_float(s[i]) * sl2;
+        if (row_ok && key + i < Nk) {
+            if (kind == 2) {
+                const uint16_t h = reinterpret_cast<const uint16_t*>(row)[key + i];
+                t += half_to_float<BF16>(h) * kLog2e;
+            } else if (row[key + i] == 0) {
+                t = -INFINITY;
+            }
+        }
+        s[i] = __float_as_uint(t);
+    }
+}
+
+}  // namespace tme

@@ -15,8 +15,7 @@ for training.  This module provides that surface on GB300:
 
 There is no backend probing and no fallback to another implementation: an
 argument the kernels do not support (dropout, another head dim or dtype, a CPU
-tensor, the gradient of a masked call) raises ``NotImplementedError`` or
-``ValueError``.
+tensor) raises ``NotImplementedError`` or ``ValueError``.
 """
 from __future__ import annotations
 
@@ -33,16 +32,22 @@ _original_sdpa = None
 
 
 class _TiledAttentionMasked(torch.autograd.Function):
-    """Forward with an attn_mask; the backward of a masked call is not built."""
+    """Attention with an attn_mask (the mask itself gets no gradient)."""
     @staticmethod
     def forward(ctx, q, k, v, mask, is_causal, scale):
         q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
-        out, _ = _lib.attn_fwd(q, k, v, causal=is_causal, scale=scale, mask=mask)
+        out, lse = _lib.attn_fwd(q, k, v, causal=is_causal, scale=scale, mask=mask)
+        ctx.save_for_backward(q, k, v, out, lse, mask)
+        ctx.is_causal = is_causal
+        ctx.scale = scale
         return out
 
     @staticmethod
     def backward(ctx, dout):
-        raise NotImplementedError("the backward of attention with attn_mask is not implemented")
+        q, k, v, out, lse, mask = ctx.saved_tensors
+        dq, dk, dv = _lib.attn_bwd(q, k, v, out, dout.contiguous(), lse, causal=ctx.is_causal,
+                                   scale=ctx.scale, mask=mask)
+        return dq, dk, dv, None, None, None
 
 
 class _TiledAttention(torch.autograd.Function):
@@ -92,7 +97,7 @@ def attention(q, k, v, is_causal: bool = False, scale: float | None = None, attn
     """Differentiable tiled attention.  q [B,Hq,Nq,D]; k, v [B,Hkv,Nk,D] with
     Hq a multiple of Hkv (query head h uses KV head h // (Hq//Hkv)); causal is
     top-left aligned; scale defaults to 1/sqrt(D).  attn_mask: bool (True
-    keeps a key) or additive, broadcastable to [B,Hq,Nq,Nk]; forward only."""
+    keeps a key) or additive, broadcastable to [B,Hq,Nq,Nk]."""
     _validate(q, k, v)
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[-1])
@@ -107,7 +112,7 @@ def scaled_dot_product_attention(query, key, value, attn_mask=None, dropout_p=0.
 
     Supported: dropout_p == 0, fp16/bf16 CUDA tensors [B, H, N, D] with D in
     (64, 128), an optional attn_mask (bool or floating, broadcastable to
-    [B, Hq, Nq, Nk]; its backward is not implemented and raises).  With
+    [B, Hq, Nq, Nk]; it gets no gradient).  With
     Hq != Hkv, enable_gqa must be set (as for torch's own SDPA).  Anything
     else raises.
     """
