@@ -207,6 +207,8 @@ def run_ours(args):
     if decode and bwd:
         raise SystemExit("the decode workload has no backward pass")
     splits = {n: _lib.num_splits(w.B, w.Hq, w.Hkv, w.queries(n), n, w.D) for n in seq}
+    if args.mask != "none" and decode:
+        raise SystemExit("--mask is for the prefill / training workloads")
     # inputs resident in HBM before the timed region
     bufs = []
     for n in seq:
@@ -218,8 +220,9 @@ def run_ours(args):
         out = torch.empty_like(q)
         lse = torch.empty(q.shape[:3], device=dev, dtype=torch.float32)
         extra = None
+        x["mask"] = make_bench_mask(args.mask, w, n, dev)
         if bwd:
-            _lib.attn_fwd(q, k, v, causal=w.causal, out=out, lse=lse)
+            _lib.attn_fwd(q, k, v, causal=w.causal, out=out, lse=lse, mask=x["mask"])
             do = x["do"].to(dev)
             ws = torch.empty(max(16, _lib.load().attn_bwd_workspace_size(
                 w.B, w.Hq, w.Hkv, n, n, w.D, 1 if w.dtype == torch.bfloat16 else 0)),
@@ -232,16 +235,16 @@ def run_ours(args):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
     def launch(b):
-        n, q, k, v, out, lse, _, extra = b
+        n, q, k, v, out, lse, x, extra = b
         if bwd:
             do, dq, dk, dv, ws = extra
             _lib.attn_bwd(q, k, v, out, do, lse, causal=w.causal, dq=dq, dk=dk, dv=dv,
-                          workspace=ws)
+                          workspace=ws, mask=x["mask"])
         elif decode:
             _lib.attn_fwd_splitkv(q, k, v, causal=w.causal, splits=splits[n], out=out, lse=lse,
                                   workspace=extra)
         else:
-            _lib.attn_fwd(q, k, v, causal=w.causal, out=out, lse=lse)
+            _lib.attn_fwd(q, k, v, causal=w.causal, out=out, lse=lse, mask=x["mask"])
 
     for _ in range(args.warmup):
         for b in bufs:
@@ -343,7 +346,7 @@ def run_ours(args):
             dist.destroy_process_group()
         return
 
-    cpu = None if (args.no_cpu_baseline or world > 1 or bwd) else \
+    cpu = None if (args.no_cpu_baseline or world > 1 or bwd or args.mask != "none") else \
         cpu_baseline(w, seq, budget_s=args.cpu_budget)
     if decode:
         sweep = [{"Nk": n, "ms": round(ms, 4), "splits": splits[n],
@@ -366,6 +369,7 @@ def run_ours(args):
         "data": "synthetic",
         "config": {"workload": w.note, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
                    "causal": w.causal, "seq_lens": seq, "Nq": w.nq if decode else "= N",
+                   "mask": MASK_NOTES[args.mask],
                    "inputs": "seeded N(0,1) rounded to dtype" +
                              ("; 1% of key rows x8" if w.outlier_keys else ""),
                    "l2": "flushed before every launch (256 MiB write, outside the timed events)",
@@ -377,6 +381,30 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+MASK_NOTES = {
+    "none": None,
+    "padding": "bool key-padding mask [B,1,1,N] keeping the first 7N/8 keys; FLOPs counted "
+               "unmasked (every key tile is still visited)",
+    "additive": "additive N(0,1) bias [1,1,N,N] in the input dtype",
+}
+
+
+def make_bench_mask(kind, w, n, dev):
+    """The attn_mask of a masked measurement (None for unmasked runs)."""
+    import torch
+    if kind == "none":
+        return None
+    if kind == "padding":
+        return (torch.arange(n, device=dev) < n - n // 8).reshape(1, 1, 1, n).expand(
+            w.B, 1, 1, n).contiguous()
+    g = torch.Generator().manual_seed(inputs_seed_for_mask(n))
+    return torch.randn((1, 1, n, n), generator=g).to(w.dtype).to(dev)
+
+
+def inputs_seed_for_mask(n: int) -> int:
+    return 77_000 + n
 
 
 def cpu_baseline(w, seq, budget_s: float = 15.0, n_override=None):
@@ -510,6 +538,8 @@ def main():
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
                     help="time the forward (default) or the backward")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--mask", choices=["none", "padding", "additive"], default="none",
+                    help="time the masked kernels with this attn_mask")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     args = ap.parse_args()
