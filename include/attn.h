@@ -63,7 +63,8 @@ typedef enum {
     ATTN_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
     ATTN_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
     ATTN_ERR_TIMEOUT = 5,     /* a device wait gave up (reported by attn_sync_status) */
-    ATTN_ERR_WORKSPACE = 6    /* workspace too small */
+    ATTN_ERR_WORKSPACE = 6,   /* workspace too small */
+    ATTN_ERR_MISMATCH = 7     /* a run-time check found two results that must agree differ (ffn.h) */
 } attn_status_t;
 
 /*

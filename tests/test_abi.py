@@ -20,7 +20,9 @@ def test_header_declares_the_boundary():
     names = _lib.declared_functions()
     for required in ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_sync_status",
                      "attn_strerror", "attn_selftest_timeout", "attn_version", "attn_fwd_splitkv",
-                     "attn_fwd_splitkv_workspace_size", "attn_fwd_num_splits"):
+                     "attn_fwd_splitkv_workspace_size", "attn_fwd_num_splits", "attn_fwd_masked",
+                     "attn_bwd_masked", "ffn_forward", "ffn_check_chunking",
+                     "ffn_workspace_size"):
         assert required in names
 
 
@@ -118,3 +120,18 @@ def test_splitkv_workspace_and_validation(lib):
     assert lib.attn_fwd_splitkv(P, P, P, P, P, 0, ws, *args, 8, None) == 1
     assert lib.attn_fwd_splitkv(P, P, P, P, P, P + 8, ws, *args, 8, None) == 3
     assert lib.attn_fwd_splitkv(P, P, P, P, P, P, ws - 16, *args, 8, None) == 6
+
+
+def test_ffn_host_checks(lib):
+    assert lib.ffn_workspace_size(1000, 4864, 256) == 256 * 4864 * 2
+    assert lib.ffn_workspace_size(100, 4864, 256) == (100 * 4864 * 2 + 255) // 256 * 256
+    assert lib.ffn_workspace_size(0, 4864, 256) == 0
+    ws = lib.ffn_workspace_size(1000, 4864, 256)
+    args = (1000, 896, 4864, 4, 256, P, ws, 1, None)
+    # null x, unknown activation, d_model not a multiple of 8, misaligned, short workspace
+    assert lib.ffn_forward(0, P, 0, P, 0, P, *args) == 1
+    assert lib.ffn_forward(P, P, 0, P, 0, P, 1000, 896, 4864, 9, 256, P, ws, 1, None) == 1
+    assert lib.ffn_forward(P, P, 0, P, 0, P, 1000, 900, 4864, 4, 256, P, ws, 1, None) == 2
+    assert lib.ffn_forward(P + 8, P, 0, P, 0, P, *args) == 3
+    assert lib.ffn_forward(P, P, 0, P, 0, P, 1000, 896, 4864, 4, 256, P, ws - 256, 1, None) == 6
+    assert lib.attn_strerror(7) == b"results that must agree differ"

@@ -15,7 +15,8 @@ import threading
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "_build", "libattn.so")
-HEADER = os.path.join(os.path.dirname(PKG), "include", "attn.h")
+INCLUDE = os.path.join(os.path.dirname(PKG), "include")
+HEADERS = [os.path.join(INCLUDE, "attn.h"), os.path.join(INCLUDE, "ffn.h")]
 
 ATTN_OK = 0
 ATTN_ERR_INVALID = 1
@@ -24,6 +25,8 @@ ATTN_ERR_ALIGN = 3
 ATTN_ERR_CUDA = 4
 ATTN_ERR_TIMEOUT = 5
 ATTN_ERR_WORKSPACE = 6
+ATTN_ERR_MISMATCH = 7
+FFN_ACTS = {"none": 0, "relu": 1, "gelu_tanh": 2, "silu": 3, "swiglu": 4}
 ATTN_F16 = 0
 ATTN_BF16 = 1
 ATTN_CAUSAL_NONE = 0
@@ -58,6 +61,11 @@ _SIGNATURES = {
     "attn_bwd_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                           _i, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i, _vp], _i),
     "attn_sync_status": ([_vp], _i),
+    "ffn_workspace_size": ([_i, _i, _i], ctypes.c_size_t),
+    "ffn_forward": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, ctypes.c_size_t, _i,
+                     _vp], _i),
+    "ffn_check_chunking": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp,
+                            ctypes.c_size_t, _i, _vp], _i),
     "attn_selftest_timeout": ([ctypes.c_ulonglong, _vp], _i),
     "attn_strerror": ([_i], ctypes.c_char_p),
     "attn_version": ([], _i),
@@ -71,10 +79,12 @@ class AttnError(RuntimeError):
 
 
 def declared_functions() -> list:
-    """Names of the functions include/attn.h declares."""
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
+    """Names of the functions include/attn.h and include/ffn.h declare."""
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names.update(re.findall(r"\b((?:attn|ffn)_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def load(path: str | None = None):
@@ -304,3 +314,51 @@ def sync_status(device=None) -> int:
     import torch
     dev = device if device is not None else torch.cuda.current_device()
     return load().attn_sync_status(_stream_handle(dev))
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def ffn_forward(x, w1, b1, w2, b2, act: str = "gelu_tanh", chunk: int = 4096, out=None,
+                workspace=None):
+    """y = act(x W1^T + b1) W2^T + b2 over x [T, d_model], `chunk` tokens at a
+    time (include/ffn.h).  swiglu: W1 = [Wg; Wu] of 2*d_ff rows."""
+    import torch
+    T, d_model = x.shape
+    d_ff = w2.shape[1]
+    for name, t in (("x", x), ("w1", w1), ("w2", w2)):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != x.dtype:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor of x's dtype")
+    lib = load()
+    if workspace is None:
+        workspace = torch.empty(max(16, lib.ffn_workspace_size(T, d_ff, chunk)),
+                                dtype=torch.uint8, device=x.device)
+    y = torch.empty((T, d_model), dtype=x.dtype, device=x.device) if out is None else out
+    rc = lib.ffn_forward(x.data_ptr(), w1.data_ptr(), _ptr(b1), w2.data_ptr(), _ptr(b2),
+                         y.data_ptr(), T, d_model, d_ff, FFN_ACTS[act], int(chunk),
+                         workspace.data_ptr(), workspace.numel(), _dtype_code(x),
+                         _stream_handle(x.device))
+    if rc != ATTN_OK:
+        raise AttnError("ffn_forward", rc)
+    return y
+
+
+def ffn_check_chunking(x, w1, b1, w2, b2, act: str = "gelu_tanh", chunk: int = 4096):
+    """Runs the FFN chunked and unchunked and compares bit for bit on the
+    device; returns (y, ok)."""
+    import torch
+    T, d_model = x.shape
+    d_ff = w2.shape[1]
+    lib = load()
+    ws = torch.empty(max(16, lib.ffn_workspace_size(T, d_ff, T)), dtype=torch.uint8,
+                     device=x.device)
+    y = torch.empty((T, d_model), dtype=x.dtype, device=x.device)
+    y_ref = torch.empty_like(y)
+    rc = lib.ffn_check_chunking(x.data_ptr(), w1.data_ptr(), _ptr(b1), w2.data_ptr(), _ptr(b2),
+                                y.data_ptr(), y_ref.data_ptr(), T, d_model, d_ff, FFN_ACTS[act],
+                                int(chunk), ws.data_ptr(), ws.numel(), _dtype_code(x),
+                                _stream_handle(x.device))
+    if rc not in (ATTN_OK, ATTN_ERR_MISMATCH):
+        raise AttnError("ffn_check_chunking", rc)
+    return y, rc == ATTN_OK

@@ -128,6 +128,14 @@ __global__ void selftest_timeout_kernel(unsigned long long wait_ns, unsigned int
 }
 
 }  // namespace
+
+// For the other translation units of the library (ffn.cu).
+int device_setup_public(unsigned int** status) { return device_setup(status); }
+int make_map_public(CUtensorMap* map, const void* base, bool bf16, int cols, int64_t rows,
+                    int64_t groups) {
+    return make_map(map, base, bf16, cols, rows, groups);
+}
+
 }  // namespace tme
 
 using namespace tme;
@@ -454,6 +462,7 @@ extern "C" const char* attn_strerror(int status) {
         case ATTN_ERR_CUDA: return "CUDA runtime or driver error";
         case ATTN_ERR_TIMEOUT: return "a device-side wait timed out";
         case ATTN_ERR_WORKSPACE: return "workspace too small";
+        case ATTN_ERR_MISMATCH: return "results that must agree differ";
         default: return "unknown status";
     }
 }

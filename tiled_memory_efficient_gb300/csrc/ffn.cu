@@ -1,0 +1,355 @@
+// ffn.cu -- the token-chunked feed-forward block.
+//
+// The noflash-attention forum post (ai-navigate-news, section "The DIY
+// approach", list "What worked") lists FFN chunking, with a runtime safety
+// check, next to the tiled attention: the feed-forward block acts on every
+// token on its own, so running it a slice of tokens at a time never holds the
+// [tokens x d_ff] intermediate of the whole sequence.  Per token row x:
+//     h = act(x W1^T + b1),   y = h W2^T + b2
+// (swiglu: W1 = [Wg; Wu], h = silu(x Wg^T + bg) * (x Wu^T + bu)).
+//
+// Both products run in one tcgen05 kernel with a fused epilogue: a CTA
+// computes a 128-row x 256-column fp32 tile in TMEM (TMA ring of 4 stages of
+// 64-wide K slices, one elected lane issuing M=128 N=256 MMAs), then four
+// warps add the bias, apply the activation, round to the 16-bit dtype and
+// store.  For swiglu the 256 columns are 128 gate columns and the same 128
+// up columns, so the epilogue combines them in registers.  The host loop runs
+// chunk after chunk through a caller-sized intermediate buffer.  Every output
+// element is one fixed-order K reduction of its own row, so a chunked run is
+// bit-identical to an unchunked one; ffn_check_chunking verifies that at run
+// time.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/ffn.h"
+#include "attn_internal.h"
+#include "ptx.cuh"
+
+namespace tme {
+
+// Defined in abi.cu: device set-up (context, architecture, status word,
+// tensor-map encoder) and the 3-D TMA map over a [groups][rows][cols] tensor.
+int device_setup_public(unsigned int** status);
+int make_map_public(CUtensorMap* map, const void* base, bool bf16, int cols, int64_t rows,
+                    int64_t groups);
+
+namespace {
+
+constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
+constexpr int kGemmThreads = 192;  // warps 0-3 epilogue, 4 TMA producer, 5 MMA issuer
+constexpr int kProducerWarp = 4, kMmaWarp = 5;   // warps 0-3: epilogue
+constexpr int kTileA = kBM * kBK * 2;              // 16 KiB
+constexpr int kTileB = kBN * kBK * 2;              // 32 KiB
+constexpr int kStageBytes = kTileA + kTileB;
+constexpr int kBarOff = kStages * kStageBytes;
+constexpr int kGemmSmem = kBarOff + 256 + 1024;    // barriers + alignment slack
+
+struct GemmParams {
+    void* c;              // output rows of this launch, [M][ldc] 16-bit
+    const void* bias;     // 16-bit, or nullptr (swiglu: gate biases, then up biases)
+    unsigned int* status;
+    int M, N, K;          // rows, output columns, reduction length
+    int a_row0;           // first row of A (TMA coordinate)
+    int ldc;              // output row stride in elements
+    int glu_off;          // swiglu: first B row of the up projection (= d_ff)
+};
+
+__device__ __forceinline__ float tanh_approx(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// The activations from their definitions (gelu: the tanh form of Hendrycks
+// and Gimpel; silu: a / (1 + e^-a), with e^-a = 2^(-a log2 e)).
+template <int ACT>
+__device__ __forceinline__ float act_fn(float a) {
+    if constexpr (ACT == FFN_ACT_RELU) return fmaxf(a, 0.0f);
+    if constexpr (ACT == FFN_ACT_GELU_TANH) {
+        const float u = 0.7978845608028654f * fmaf(0.044715f * a, a * a, a);
+        return 0.5f * a * (1.0f + tanh_approx(u));
+    }
+    if constexpr (ACT == FFN_ACT_SILU || ACT == FFN_ACT_SWIGLU)
+        return __fdividef(a, 1.0f + ex2_ftz(-1.4426950408889634f * a));
+    return a;
+}
+
+template <bool BF16>
+__device__ __forceinline__ float load16(const void* base, int i) {
+    const uint16_t h = static_cast<const uint16_t*>(base)[i];
+    if constexpr (BF16) return __uint_as_float(static_cast<uint32_t>(h) << 16);
+    return __half2float(__ushort_as_half(h));
+}
+
+template <int ACT, bool BF16>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    ffn_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+    constexpr bool GLU = ACT == FFN_ACT_SWIGLU;
+    constexpr int kOutN = GLU ? 128 : 256;   // output columns of a tile
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);   // [kStages]
+    uint64_t* empty = full + kStages;                               // [kStages]
+    uint64_t* acc_full = empty + kStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_mt = (p.M + kBM - 1) / kBM;
+    const int mt = static_cast<int>(blockIdx.x % n_mt);   // CTAs of one column tile are adjacent
+    const int nt = static_cast<int>(blockIdx.x / n_mt);
+    const int m0 = mt * kBM, n0 = nt * kOutN;
+    const int n_kb = (p.K + kBK - 1) / kBK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) tmem_alloc(tmem_slot, 256);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+            const int b1 = GLU ? p.glu_off + n0 : n0 + 128;   // second 128-row box of B
+            int issued = 0;
+            for (int kb = 0; kb < n_kb; ++kb) {
+                const int s = kb % kStages;
+                if (kb >= kStages &&
+                    !mbar_wait(&empty[s], ((kb / kStages) - 1) & 1, abort_flag, p.status))
+                    break;
+                uint8_t* sA = smem + s * kStageBytes;
+                mbar_arrive_expect_tx(&full[s], kStageBytes);
+                tma_load_3d(&tmA, &full[s], sA, kb * kBK, p.a_row0 + m0, 0);
+                tma_load_3d(&tmB, &full[s], sA + kTileA, kb * kBK, n0, 0);
+                tma_load_3d(&tmB, &full[s], sA + kTileA + kTileB / 2, kb * kBK, b1, 0);
+                ++issued;
+            }
+            // never leave a copy in flight into shared memory about to be released
+            for (int n = (issued > kStages ? issued - kStages : 0); n < issued; ++n)
+                mbar_wait_bounded(&full[n % kStages], (n / kStages) & 1, p.status);
+        }
+    } else if (warp == kMmaWarp) {
+        constexpr uint32_t idesc = idesc_f16(kBM, kBN, BF16, false);
+        for (int kb = 0; kb < n_kb; ++kb) {
+            const int s = kb % kStages;
+            warp_wait(&full[s], (kb / kStages) & 1, abort_flag, p.status);
+            tc_fence_after();
+            const uint32_t a = smem_u32(smem + s * kStageBytes);
+            mma_ss_k64(tmem, smem_desc_sw128(a, 16, 1024), smem_desc_sw128(a + kTileA, 16, 1024),
+                       idesc, kb > 0 ? 1u : 0u);
+            mma_commit_elect(&empty[s]);
+        }
+        mma_commit_elect(acc_full);
+    } else {
+        // epilogue: thread = output row (TMEM lane)
+        const int row = m0 + warp * 32 + lane;
+        const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+        const bool ok = n_kb > 0 && warp_wait(acc_full, 0, abort_flag, p.status) && *abort_flag == 0;
+        tc_fence_after();
+        uint16_t* crow = static_cast<uint16_t*>(p.c) + static_cast<int64_t>(row) * p.ldc;
+#pragma unroll 1
+        for (int c = 0; c < kOutN / 32; ++c) {
+            const int col0 = n0 + 32 * c;
+            uint32_t a[32];
+            tmem_ld32(tmem + lb + 32 * c, a);
+            float h[32];
+            if constexpr (GLU) {
+                uint32_t u[32];
+                tmem_ld32(tmem + lb + 128 + 32 * c, u);
+                tmem_wait_ld();
+                reg_fence(a);
+                reg_fence(u);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float g = __uint_as_float(a[i]), v = __uint_as_float(u[i]);
+                    if (p.bias && col0 + i < p.N) {
+                        g += load16<BF16>(p.bias, col0 + i);
+                        v += load16<BF16>(p.bias, p.glu_off + col0 + i);
+                    }
+                    h[i] = act_fn<ACT>(g) * v;
+                }
+            } else {
+                tmem_wait_ld();
+                reg_fence(a);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float v = __uint_as_float(a[i]);
+                    if (p.bias && col0 + i < p.N) v += load16<BF16>(p.bias, col0 + i);
+                    h[i] = act_fn<ACT>(v);
+                }
+            }
+            if (ok && row < p.M) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {   // 8 columns per 16-byte store; N % 8 == 0
+                    if (col0 + 8 * g + 8 > p.N) break;
+                    const uint4 w = make_uint4(pack2<BF16>(h[8 * g], h[8 * g + 1]),
+                                               pack2<BF16>(h[8 * g + 2], h[8 * g + 3]),
+                                               pack2<BF16>(h[8 * g + 4], h[8 * g + 5]),
+                                               pack2<BF16>(h[8 * g + 6], h[8 * g + 7]));
+                    *reinterpret_cast<uint4*>(crow + col0 + 8 * g) = w;
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+template <int ACT, bool BF16>
+cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
+                        cudaStream_t stream) {
+    auto kern = ffn_gemm_kernel<ACT, BF16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kGemmSmem);
+    if (e != cudaSuccess) return e;
+    constexpr int kOutN = ACT == FFN_ACT_SWIGLU ? 128 : 256;
+    const long long ctas = static_cast<long long>((p.M + kBM - 1) / kBM) * ((p.N + kOutN - 1) / kOutN);
+    return launch_kernel(kern, dim3(static_cast<unsigned>(ctas)), dim3(kGemmThreads), kGemmSmem,
+                         stream, tmA, tmB, p);
+}
+
+cudaError_t gemm(int act, bool bf16, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                 const GemmParams& p, cudaStream_t stream) {
+#define TME_GEMM(a)                                                                 \
+    if (act == a) return bf16 ? launch_gemm<a, true>(tmA, tmB, p, stream)          \
+                              : launch_gemm<a, false>(tmA, tmB, p, stream);
+    TME_GEMM(FFN_ACT_NONE)
+    TME_GEMM(FFN_ACT_RELU)
+    TME_GEMM(FFN_ACT_GELU_TANH)
+    TME_GEMM(FFN_ACT_SILU)
+    TME_GEMM(FFN_ACT_SWIGLU)
+#undef TME_GEMM
+    return cudaErrorInvalidValue;
+}
+
+// Sets *flag when two 16-bit buffers differ anywhere.
+__global__ void compare_kernel(const uint16_t* a, const uint16_t* b, int64_t n,
+                               unsigned int* flag) {
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        if (a[i] != b[i]) {
+            atomicOr(flag, 1u);
+            return;
+        }
+}
+
+__device__ unsigned int g_mismatch;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_args(const void* x, const void* w1, const void* b1, const void* w2, const void* b2,
+               const void* y, int T, int d_model, int d_ff, int act, int chunk, int dtype) {
+    if (!x || !w1 || !w2 || !y) return ATTN_ERR_INVALID;
+    if (T <= 0 || d_model <= 0 || d_ff <= 0 || chunk <= 0) return ATTN_ERR_INVALID;
+    if (act < FFN_ACT_NONE || act > FFN_ACT_SWIGLU) return ATTN_ERR_INVALID;
+    if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID;
+    if (d_model % 8 || d_ff % 8) return ATTN_ERR_UNSUPPORTED;   // 16-byte rows for TMA and stores
+    if (d_ff > (1 << 28) || d_model > (1 << 28)) return ATTN_ERR_UNSUPPORTED;
+    const void* ptrs[] = {x, w1, w2, y};
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return ATTN_ERR_ALIGN;
+    return ATTN_OK;
+}
+
+int run(const void* x, const void* w1, const void* b1, const void* w2, const void* b2, void* y,
+        int T, int d_model, int d_ff, int act, int chunk, void* workspace, size_t workspace_bytes,
+        int dtype, cudaStream_t stream) {
+    int rc = check_args(x, w1, b1, w2, b2, y, T, d_model, d_ff, act, chunk, dtype);
+    if (rc != ATTN_OK) return rc;
+    if (chunk > T) chunk = T;
+    if (!workspace) return ATTN_ERR_INVALID;
+    if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
+    if (workspace_bytes < static_cast<size_t>(chunk) * d_ff * 2) return ATTN_ERR_WORKSPACE;
+    unsigned int* status = nullptr;
+    rc = device_setup_public(&status);
+    if (rc != ATTN_OK) return rc;
+    const bool bf16 = dtype == ATTN_BF16;
+    const bool glu = act == FFN_ACT_SWIGLU;
+    CUtensorMap tmX, tmW1, tmH, tmW2;
+    if (make_map_public(&tmX, x, bf16, d_model, T, 1) != ATTN_OK ||
+        make_map_public(&tmW1, w1, bf16, d_model, glu ? 2 * static_cast<int64_t>(d_ff) : d_ff, 1) !=
+            ATTN_OK ||
+        make_map_public(&tmH, workspace, bf16, d_ff, chunk, 1) != ATTN_OK ||
+        make_map_public(&tmW2, w2, bf16, d_ff, d_model, 1) != ATTN_OK)
+        return ATTN_ERR_CUDA;
+    for (int t0 = 0; t0 < T; t0 += chunk) {
+        const int m = T - t0 < chunk ? T - t0 : chunk;
+        GemmParams g1{workspace, b1, status, m, d_ff, d_model, t0, d_ff, glu ? d_ff : 0};
+        cudaError_t e = gemm(act, bf16, tmX, tmW1, g1, stream);
+        if (e != cudaSuccess) return ATTN_ERR_CUDA;
+        GemmParams g2{static_cast<uint16_t*>(y) + static_cast<int64_t>(t0) * d_model, b2, status, m,
+                      d_model, d_ff, 0, d_model, 0};
+        e = gemm(FFN_ACT_NONE, bf16, tmH, tmW2, g2, stream);
+        if (e != cudaSuccess) return ATTN_ERR_CUDA;
+    }
+    return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace tme
+
+using namespace tme;
+
+extern "C" size_t ffn_workspace_size(int T, int d_ff, int chunk) {
+    if (T <= 0 || d_ff <= 0 || chunk <= 0) return 0;
+    const int c = chunk < T ? chunk : T;
+    return (static_cast<size_t>(c) * d_ff * 2 + 255) & ~static_cast<size_t>(255);
+}
+
+extern "C" int ffn_forward(const void* x, const void* w1, const void* b1, const void* w2,
+                           const void* b2, void* y, int T, int d_model, int d_ff, int act,
+                           int chunk, void* workspace, size_t workspace_bytes, int dtype,
+                           void* stream) {
+    return run(x, w1, b1, w2, b2, y, T, d_model, d_ff, act, chunk, workspace, workspace_bytes,
+               dtype, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int ffn_check_chunking(const void* x, const void* w1, const void* b1, const void* w2,
+                                  const void* b2, void* y, void* y_ref, int T, int d_model,
+                                  int d_ff, int act, int chunk, void* workspace,
+                                  size_t workspace_bytes, int dtype, void* stream) {
+    if (!y_ref) return ATTN_ERR_INVALID;
+    if (!aligned16(y_ref)) return ATTN_ERR_ALIGN;
+    if (workspace_bytes < ffn_workspace_size(T, d_ff, T)) return ATTN_ERR_WORKSPACE;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int rc = run(x, w1, b1, w2, b2, y, T, d_model, d_ff, act, chunk, workspace, workspace_bytes,
+                 dtype, st);
+    if (rc != ATTN_OK) return rc;
+    rc = run(x, w1, b1, w2, b2, y_ref, T, d_model, d_ff, act, T, workspace, workspace_bytes, dtype,
+             st);
+    if (rc != ATTN_OK) return rc;
+    void* flag = nullptr;
+    if (cudaGetSymbolAddress(&flag, g_mismatch) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (cudaMemsetAsync(flag, 0, sizeof(unsigned int), st) != cudaSuccess) return ATTN_ERR_CUDA;
+    const int64_t n = static_cast<int64_t>(T) * d_model;
+    if (launch_kernel(compare_kernel, dim3(1024), dim3(256), 0, st,
+                      static_cast<const uint16_t*>(y), static_cast<const uint16_t*>(y_ref), n,
+                      static_cast<unsigned int*>(flag)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    unsigned int host = 0;
+    if (cudaMemcpyAsync(&host, flag, sizeof(host), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return host ? ATTN_ERR_MISMATCH : ATTN_OK;
+}
