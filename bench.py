@@ -527,6 +527,75 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+FFN_CONFIG = {"workload": "token-chunked SwiGLU FFN of the Qwen 2.5 0.5B shape (d_model 896, "
+                          "d_ff 4864, no biases), bf16, 16384 tokens in chunks of 4096",
+              "T": 16384, "d_model": 896, "d_ff": 4864, "act": "swiglu", "chunk": 4096}
+METRIC_FFN = "token-chunked FFN TFLOP/s on 1 GB300 (both products, 3 d_model x d_ff GEMMs per token)"
+
+
+def run_ffn(args):
+    """--config ffn: the chunked FFN (include/ffn.h), one step = one forward
+    over T tokens; FLOPs = 2 T d_model (2 d_ff) + 2 T d_ff d_model."""
+    import torch
+
+    from tiled_memory_efficient_gb300 import _lib
+    dist, rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    c = FFN_CONFIG
+    T, d, f = c["T"], c["d_model"], c["d_ff"]
+    g = torch.Generator().manual_seed(9000)
+    x = torch.randn(T, d, generator=g).to(torch.bfloat16).to(dev)
+    w1 = (torch.randn(2 * f, d, generator=g) / d ** 0.5).to(torch.bfloat16).to(dev)
+    w2 = (torch.randn(d, f, generator=g) / f ** 0.5).to(torch.bfloat16).to(dev)
+    y = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    lib = _lib.load()
+    ws = torch.empty(lib.ffn_workspace_size(T, f, c["chunk"]), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flops = 2.0 * T * d * 2 * f + 2.0 * T * f * d
+
+    def step():
+        _lib.ffn_forward(x, w1, None, w2, None, act=c["act"], chunk=c["chunk"], out=y, workspace=ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with ClockSampler(dev.index or 0) as clk:
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            step()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+    rc = _lib.sync_status(dev)
+    if rc != _lib.ATTN_OK:
+        raise RuntimeError(f"device status after timing: {_lib.strerror(rc)}")
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+    ms = max_over_ranks(ms, dist, dev)
+    pk = peaks()
+    tf = flops / (ms * 1e-3) / 1e12
+    n_chunks = (T + c["chunk"] - 1) // c["chunk"]
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC_FFN, "value": round(world * tf, 2), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": dict(c, l2="flushed before every step (256 MiB write, outside the events)"),
+            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": pk["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": round(tf / pk["bf16_tflops"], 4),
+                         "traffic": None, "kernel": "ffn_gemm_kernel (both products, all chunks)",
+                         "peak_source": f"{pk['source']} bf16 dense (burst)"},
+            "cpu_baseline": None, "e2e": None, "gpu_launches": args.steps * 2 * n_chunks,
+            "clocks": clk.summary()}), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -545,7 +614,13 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.config == "ffn":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the "
+                              "attention oracle; the FFN has no CPU reference leg here"}))
+            return
+        run_ffn(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
