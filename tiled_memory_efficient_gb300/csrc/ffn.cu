@@ -8,10 +8,11 @@
 //     h = act(x W1^T + b1),   y = h W2^T + b2
 // (swiglu: W1 = [Wg; Wu], h = silu(x Wg^T + bg) * (x Wu^T + bu)).
 //
-// Both products run in one tcgen05 kernel with a fused epilogue: a CTA
-// computes a 128-row x 256-column fp32 tile in TMEM (TMA ring of 4 stages of
-// 64-wide K slices, one elected lane issuing M=128 N=256 MMAs), then four
-// warps add the bias, apply the activation, round to the 16-bit dtype and
+// Both products run in one persistent tcgen05 kernel with a fused epilogue:
+// each CTA walks its tiles of 128 rows x 256 columns, accumulating in fp32 in
+// one of two TMEM buffers (TMA ring of 4 stages of 64-wide K slices, one
+// elected lane issuing M=128 N=256 MMAs) while four warps empty the other
+// buffer: add the bias, apply the activation, round to the 16-bit dtype and
 // store.  For swiglu the 256 columns are 128 gate columns and the same 128
 // up columns, so the epilogue combines them in registers.  The host loop runs
 // chunk after chunk through a caller-sized intermediate buffer.  Every output
@@ -42,6 +43,7 @@ namespace {
 constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
 constexpr int kGemmThreads = 192;  // warps 0-3 epilogue, 4 TMA producer, 5 MMA issuer
 constexpr int kProducerWarp = 4, kMmaWarp = 5;   // warps 0-3: epilogue
+constexpr int kEpiThreads = 128;
 constexpr int kTileA = kBM * kBK * 2;              // 16 KiB
 constexpr int kTileB = kBN * kBK * 2;              // 32 KiB
 constexpr int kStageBytes = kTileA + kTileB;
@@ -96,27 +98,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);   // [kStages]
     uint64_t* empty = full + kStages;                               // [kStages]
-    uint64_t* acc_full = empty + kStages;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+    uint64_t* acc_full = empty + kStages;                           // [2] accumulator b written
+    uint64_t* acc_empty = acc_full + 2;                             // [2] accumulator b read
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_mt = (p.M + kBM - 1) / kBM;
-    const int mt = static_cast<int>(blockIdx.x % n_mt);   // CTAs of one column tile are adjacent
-    const int nt = static_cast<int>(blockIdx.x / n_mt);
-    const int m0 = mt * kBM, n0 = nt * kOutN;
+    const int n_tiles = n_mt * ((p.N + kOutN - 1) / kOutN);
     const int n_kb = (p.K + kBK - 1) / kBK;
+    // Persistent CTAs: tiles blockIdx.x, blockIdx.x + gridDim.x, ...; the
+    // row tiles of one column tile are adjacent (B stays in L2).
+    auto tile_m0 = [&](int t) { return (t % n_mt) * kBM; };
+    auto tile_n0 = [&](int t) { return (t / n_mt) * kOutN; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(acc_full, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], kEpiThreads);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == kMmaWarp) tmem_alloc(tmem_slot, 256);
+    if (warp == kMmaWarp) tmem_alloc(tmem_slot, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -126,83 +134,111 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0) {
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
-            const int b1 = GLU ? p.glu_off + n0 : n0 + 128;   // second 128-row box of B
-            int issued = 0;
-            for (int kb = 0; kb < n_kb; ++kb) {
-                const int s = kb % kStages;
-                if (kb >= kStages &&
-                    !mbar_wait(&empty[s], ((kb / kStages) - 1) & 1, abort_flag, p.status))
-                    break;
-                uint8_t* sA = smem + s * kStageBytes;
-                mbar_arrive_expect_tx(&full[s], kStageBytes);
-                tma_load_3d(&tmA, &full[s], sA, kb * kBK, p.a_row0 + m0, 0);
-                tma_load_3d(&tmB, &full[s], sA + kTileA, kb * kBK, n0, 0);
-                tma_load_3d(&tmB, &full[s], sA + kTileA + kTileB / 2, kb * kBK, b1, 0);
-                ++issued;
+            int g = 0;   // K slices issued by this CTA (ring position)
+            bool okp = true;
+            for (int t = blockIdx.x; okp && t < n_tiles; t += gridDim.x) {
+                const int m0 = tile_m0(t), n0 = tile_n0(t);
+                const int b1 = GLU ? p.glu_off + n0 : n0 + 128;   // second 128-row box of B
+                for (int kb = 0; kb < n_kb; ++kb, ++g) {
+                    const int s = g % kStages;
+                    if (g >= kStages &&
+                        !mbar_wait(&empty[s], ((g / kStages) - 1) & 1, abort_flag, p.status)) {
+                        okp = false;
+                        break;
+                    }
+                    uint8_t* sA = smem + s * kStageBytes;
+                    mbar_arrive_expect_tx(&full[s], kStageBytes);
+                    tma_load_3d(&tmA, &full[s], sA, kb * kBK, p.a_row0 + m0, 0);
+                    tma_load_3d(&tmB, &full[s], sA + kTileA, kb * kBK, n0, 0);
+                    tma_load_3d(&tmB, &full[s], sA + kTileA + kTileB / 2, kb * kBK, b1, 0);
+                }
             }
             // never leave a copy in flight into shared memory about to be released
-            for (int n = (issued > kStages ? issued - kStages : 0); n < issued; ++n)
+            for (int n = (g > kStages ? g - kStages : 0); n < g; ++n)
                 mbar_wait_bounded(&full[n % kStages], (n / kStages) & 1, p.status);
         }
     } else if (warp == kMmaWarp) {
         constexpr uint32_t idesc = idesc_f16(kBM, kBN, BF16, false);
-        for (int kb = 0; kb < n_kb; ++kb) {
-            const int s = kb % kStages;
-            warp_wait(&full[s], (kb / kStages) & 1, abort_flag, p.status);
-            tc_fence_after();
-            const uint32_t a = smem_u32(smem + s * kStageBytes);
-            mma_ss_k64(tmem, smem_desc_sw128(a, 16, 1024), smem_desc_sw128(a + kTileA, 16, 1024),
-                       idesc, kb > 0 ? 1u : 0u);
-            mma_commit_elect(&empty[s]);
+        int g = 0, i = 0;
+        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
+            const int b = i & 1;
+            if (i >= 2) {   // the epilogue has read this accumulator's previous tile
+                warp_wait(&acc_empty[b], ((i >> 1) - 1) & 1, abort_flag, p.status);
+                tc_fence_after();
+            }
+            for (int kb = 0; kb < n_kb; ++kb, ++g) {
+                const int s = g % kStages;
+                warp_wait(&full[s], (g / kStages) & 1, abort_flag, p.status);
+                tc_fence_after();
+                const uint32_t a = smem_u32(smem + s * kStageBytes);
+                mma_ss_k64(tmem + 256 * b, smem_desc_sw128(a, 16, 1024),
+                           smem_desc_sw128(a + kTileA, 16, 1024), idesc, kb > 0 ? 1u : 0u);
+                mma_commit_elect(&empty[s]);
+            }
+            mma_commit_elect(&acc_full[b]);
         }
-        mma_commit_elect(acc_full);
     } else {
         // epilogue: thread = output row (TMEM lane)
-        const int row = m0 + warp * 32 + lane;
         const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
-        const bool ok = n_kb > 0 && warp_wait(acc_full, 0, abort_flag, p.status) && *abort_flag == 0;
-        tc_fence_after();
-        uint16_t* crow = static_cast<uint16_t*>(p.c) + static_cast<int64_t>(row) * p.ldc;
+        int i = 0;
+        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
+            const int b = i & 1;
+            const int m0 = tile_m0(t), n0 = tile_n0(t);
+            const int row = m0 + warp * 32 + lane;
+            const bool ok = warp_wait(&acc_full[b], (i >> 1) & 1, abort_flag, p.status) &&
+                            *abort_flag == 0;
+            tc_fence_after();
+            const uint32_t tacc = tmem + lb + 256 * b;
+            uint16_t* crow = static_cast<uint16_t*>(p.c) + static_cast<int64_t>(row) * p.ldc;
 #pragma unroll 1
-        for (int c = 0; c < kOutN / 32; ++c) {
-            const int col0 = n0 + 32 * c;
-            uint32_t a[32];
-            tmem_ld32(tmem + lb + 32 * c, a);
-            float h[32];
-            if constexpr (GLU) {
-                uint32_t u[32];
-                tmem_ld32(tmem + lb + 128 + 32 * c, u);
-                tmem_wait_ld();
-                reg_fence(a);
-                reg_fence(u);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    float g = __uint_as_float(a[i]), v = __uint_as_float(u[i]);
-                    if (p.bias && col0 + i < p.N) {
-                        g += load16<BF16>(p.bias, col0 + i);
-                        v += load16<BF16>(p.bias, p.glu_off + col0 + i);
+            for (int c = 0; c < kOutN / 32; ++c) {
+                const int col0 = n0 + 32 * c;
+                uint32_t a[32];
+                tmem_ld32(tacc + 32 * c, a);
+                float h[32];
+                if constexpr (GLU) {
+                    uint32_t u[32];
+                    tmem_ld32(tacc + 128 + 32 * c, u);
+                    tmem_wait_ld();
+                    reg_fence(a);
+                    reg_fence(u);
+                    if (c == kOutN / 32 - 1) {   // the accumulator is read: release it
+                        tc_fence_before();
+                        mbar_arrive(&acc_empty[b]);
                     }
-                    h[i] = act_fn<ACT>(g) * v;
-                }
-            } else {
-                tmem_wait_ld();
-                reg_fence(a);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    float v = __uint_as_float(a[i]);
-                    if (p.bias && col0 + i < p.N) v += load16<BF16>(p.bias, col0 + i);
-                    h[i] = act_fn<ACT>(v);
-                }
-            }
-            if (ok && row < p.M) {
+                    for (int e = 0; e < 32; ++e) {
+                        float gt = __uint_as_float(a[e]), v = __uint_as_float(u[e]);
+                        if (p.bias && col0 + e < p.N) {
+                            gt += load16<BF16>(p.bias, col0 + e);
+                            v += load16<BF16>(p.bias, p.glu_off + col0 + e);
+                        }
+                        h[e] = act_fn<ACT>(gt) * v;
+                    }
+                } else {
+                    tmem_wait_ld();
+                    reg_fence(a);
+                    if (c == kOutN / 32 - 1) {
+                        tc_fence_before();
+                        mbar_arrive(&acc_empty[b]);
+                    }
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {   // 8 columns per 16-byte store; N % 8 == 0
-                    if (col0 + 8 * g + 8 > p.N) break;
-                    const uint4 w = make_uint4(pack2<BF16>(h[8 * g], h[8 * g + 1]),
-                                               pack2<BF16>(h[8 * g + 2], h[8 * g + 3]),
-                                               pack2<BF16>(h[8 * g + 4], h[8 * g + 5]),
-                                               pack2<BF16>(h[8 * g + 6], h[8 * g + 7]));
-                    *reinterpret_cast<uint4*>(crow + col0 + 8 * g) = w;
+                    for (int e = 0; e < 32; ++e) {
+                        float v = __uint_as_float(a[e]);
+                        if (p.bias && col0 + e < p.N) v += load16<BF16>(p.bias, col0 + e);
+                        h[e] = act_fn<ACT>(v);
+                    }
+                }
+                if (ok && row < p.M) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {   // 8 columns per 16-byte store; N % 8 == 0
+                        if (col0 + 8 * q + 8 > p.N) break;
+                        const uint4 w = make_uint4(pack2<BF16>(h[8 * q], h[8 * q + 1]),
+                                                   pack2<BF16>(h[8 * q + 2], h[8 * q + 3]),
+                                                   pack2<BF16>(h[8 * q + 4], h[8 * q + 5]),
+                                                   pack2<BF16>(h[8 * q + 6], h[8 * q + 7]));
+                        *reinterpret_cast<uint4*>(crow + col0 + 8 * q) = w;
+                    }
                 }
             }
         }
@@ -212,7 +248,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     if (warp == kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, 512);
     }
 }
 
@@ -224,7 +260,13 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const Ge
                                          kGemmSmem);
     if (e != cudaSuccess) return e;
     constexpr int kOutN = ACT == FFN_ACT_SWIGLU ? 128 : 256;
-    const long long ctas = static_cast<long long>((p.M + kBM - 1) / kBM) * ((p.N + kOutN - 1) / kOutN);
+    const long long tiles = static_cast<long long>((p.M + kBM - 1) / kBM) * ((p.N + kOutN - 1) / kOutN);
+    // persistent: one CTA per SM at most (its shared memory and 512 TMEM columns)
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaErrorUnknown;
+    const long long ctas = tiles < sms ? tiles : sms;
     return launch_kernel(kern, dim3(static_cast<unsigned>(ctas)), dim3(kGemmThreads), kGemmSmem,
                          stream, tmA, tmB, p);
 }
