@@ -29,45 +29,68 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
     constexpr int V = D / 32;  // columns per lane
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
+    // Launched as a programmatic dependent of the split kernel: wait here
+    // until that grid has finished and its partials are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (row >= p.total_rows) return;
 
-    float M = -INFINITY;
-    for (int s = lane; s < p.n_splits; s += 32)
-        M = fmaxf(M, p.lse_part[static_cast<int64_t>(s) * p.total_rows + row]);
+    // Every lane holds the LSE of ranges lane, lane + 32, ...: the maximum and
+    // the weights need no further loads, so all partial-output loads below
+    // are independent of each other.
+    float ls[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int s = lane + 32 * u;
+        ls[u] = s < p.n_splits ? p.lse_part[static_cast<int64_t>(s) * p.total_rows + row]
+                               : -INFINITY;
+    }
+    float M = ls[0];
+#pragma unroll
+    for (int u = 1; u < 8; ++u) M = fmaxf(M, ls[u]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float w[8];
+    float wsum = 0.0f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        w[u] = (M == -INFINITY || ls[u] == -INFINITY) ? 0.0f : expf(ls[u] - M);
+        wsum += w[u];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
 
     float acc[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) acc[i] = 0.0f;
-    float wsum = 0.0f;
-    if (M != -INFINITY) {
-        for (int s = 0; s < p.n_splits; ++s) {
-            const int64_t idx = static_cast<int64_t>(s) * p.total_rows + row;
-            const float ls = p.lse_part[idx];
-            if (ls == -INFINITY) continue;  // an empty range (same for the whole warp)
-            const float w = expf(ls - M);
-            const float* src = p.o_part + idx * D + lane * V;
+    const float* src = p.o_part + row * D + lane * V;
+    const int64_t step = p.total_rows * D;   // one range further (kMaxSplits = 256 = 8 x 32)
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {   // ranges 32u .. 32u + 31, weight from lane s - 32u
+        if (32 * u >= p.n_splits) break;
+        const int cnt = p.n_splits - 32 * u < 32 ? p.n_splits - 32 * u : 32;
+#pragma unroll 4
+        for (int l = 0; l < cnt; ++l) {
+            const float ws = __shfl_sync(0xffffffffu, w[u], l);
+            const float* r = src + (32 * u + l) * step;
             if constexpr (V == 4) {
-                const float4 o = *reinterpret_cast<const float4*>(src);
-                acc[0] += w * o.x;
-                acc[1] += w * o.y;
-                acc[2] += w * o.z;
-                acc[3] += w * o.w;
+                const float4 o = *reinterpret_cast<const float4*>(r);
+                acc[0] += ws * o.x;
+                acc[1] += ws * o.y;
+                acc[2] += ws * o.z;
+                acc[3] += ws * o.w;
             } else {
-                const float2 o = *reinterpret_cast<const float2*>(src);
-                acc[0] += w * o.x;
-                acc[1] += w * o.y;
+                const float2 o = *reinterpret_cast<const float2*>(r);
+                acc[0] += ws * o.x;
+                acc[1] += ws * o.y;
             }
-            wsum += w;
         }
     }
     const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
     uint16_t* out = static_cast<uint16_t*>(p.out) + row * D + lane * V;
     if constexpr (V == 4) {
-        const uint2 w = make_uint2(pack2<BF16>(acc[0] * inv, acc[1] * inv),
+        const uint2 o = make_uint2(pack2<BF16>(acc[0] * inv, acc[1] * inv),
                                    pack2<BF16>(acc[2] * inv, acc[3] * inv));
-        *reinterpret_cast<uint2*>(out) = w;
+        *reinterpret_cast<uint2*>(out) = o;
     } else {
         *reinterpret_cast<uint32_t*>(out) = pack2<BF16>(acc[0] * inv, acc[1] * inv);
     }
@@ -78,9 +101,20 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 
 cudaError_t launch_splitkv_merge(int D, bool bf16, const FwdParams& p, cudaStream_t stream) {
     const long long blocks = (p.total_rows + kMergeWarps - 1) / kMergeWarps;
-    const dim3 grid(static_cast<unsigned>(blocks)), block(kMergeWarps * 32);
+    // Programmatic dependent launch: the merge grid is set up while the split
+    // kernel drains, and waits for it on the device (griddepcontrol.wait).
+    cudaLaunchAttribute attr{};
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kMergeWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
 #define TME_MERGE(d, b) \
-    if (D == d && bf16 == b) return launch_kernel(splitkv_merge_kernel<d, b>, grid, block, 0, stream, p);
+    if (D == d && bf16 == b) return cudaLaunchKernelEx(&cfg, splitkv_merge_kernel<d, b>, p);
     TME_MERGE(64, false)
     TME_MERGE(64, true)
     TME_MERGE(128, false)
