@@ -658,23 +658,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                    (b * p.msb + h * p.msh + pos * p.msq) * (p.mask_kind == 2 ? 2 : 1);
         }
         for (int j = 0; j < nkv; ++j) {
+            const int k0 = j * kRows;
+            // this half's bias, loaded before the wait for S (hides the latency)
+            BiasChunk b0, b1;
+            if constexpr (MASK) {
+                const int key = k0 + 2 * hq * 32;
+                bias_load(b0, mrow, p.mask_kind, key, row_ok && key + 32 <= p.Nk);
+                bias_load(b1, mrow, p.mask_kind, key + 32, row_ok && key + 64 <= p.Nk);
+            }
             warp_wait(s_full, j & 1, abort_flag, p.status);
             tc_fence_after();
-            const int k0 = j * kRows;
             if constexpr (MASK) {
                 // this half's scores -> logits with the bias, in place in TMEM
 #pragma unroll 1
                 for (int cc = 0; cc < 2; ++cc) {
                     const int key = k0 + (2 * hq + cc) * 32;
                     const bool full = row_ok && key + 32 <= p.Nk;
-                    BiasChunk b;
-                    bias_load(b, mrow, p.mask_kind, key, full);
                     uint32_t x[32];
                     tmem_ld32(tS + (2 * hq + cc) * 32, x);
                     tmem_wait_ld();
                     reg_fence(x);
-                    bias_apply<BF16>(x, b, mrow, p.mask_kind, key, p.Nk, sl2, full, row_ok);
+                    bias_apply<BF16>(x, b0, mrow, p.mask_kind, key, p.Nk, sl2, full, row_ok);
                     tmem_st32(tS + (2 * hq + cc) * 32, x);
+                    b0 = b1;
                 }
                 tmem_wait_st();
             }
