@@ -321,19 +321,51 @@ def run_ours(args):
             h2d += sum(t.numel() * t.element_size() for t in ((hq,) if decode else (hq, hk, hv)))
             d2h += ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
         e2e_steps = max(1, min(args.steps, 10))
+        # Copies overlap the kernels (decode excepted): inputs go up on one stream, outputs come
+        # back on another, the kernels run on the compute stream; events order
+        # every reuse of a buffer (its upload waits for the previous step's
+        # kernel on it, the kernel for the previous download of its outputs).
+        up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        nb = len(bufs)
+        h2d_done = [torch.cuda.Event() for _ in range(nb)]
+        k_done = [torch.cuda.Event() for _ in range(nb)]
+        d2h_done = [torch.cuda.Event() for _ in range(nb)]
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(e2e_steps):
-            for b, (hq, hk, hv, ho, hl) in zip(bufs, host):
+        up.wait_event(e0)
+        down.wait_event(e0)
+        for step in range(e2e_steps):
+            for i, (b, (hq, hk, hv, ho, hl)) in enumerate(zip(bufs, host)):
                 n, q, k, v, out, lse = b[:6]
-                q.copy_(hq, non_blocking=True)
-                if not decode:
-                    k.copy_(hk, non_blocking=True)
-                    v.copy_(hv, non_blocking=True)
+                if decode:
+                    # a few KB each way: cross-stream events would cost more
+                    # than they hide, so everything stays on one stream
+                    q.copy_(hq, non_blocking=True)
+                    launch(b)
+                    ho.copy_(out, non_blocking=True)
+                    hl.copy_(lse, non_blocking=True)
+                    continue
+                with torch.cuda.stream(up):
+                    if step > 0:
+                        up.wait_event(k_done[i])
+                    q.copy_(hq, non_blocking=True)
+                    if not decode:
+                        k.copy_(hk, non_blocking=True)
+                        v.copy_(hv, non_blocking=True)
+                    h2d_done[i].record(up)
+                stream.wait_event(h2d_done[i])
+                if step > 0:
+                    stream.wait_event(d2h_done[i])
                 launch(b)
-                ho.copy_(out, non_blocking=True)
-                hl.copy_(lse, non_blocking=True)
+                k_done[i].record(stream)
+                with torch.cuda.stream(down):
+                    down.wait_event(k_done[i])
+                    ho.copy_(out, non_blocking=True)
+                    hl.copy_(lse, non_blocking=True)
+                    d2h_done[i].record(down)
+        stream.wait_stream(down)
+        stream.wait_stream(up)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
