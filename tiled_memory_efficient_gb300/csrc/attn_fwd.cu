@@ -44,8 +44,8 @@ constexpr float kRescaleThreshold = 8.0f;
 template <int D, bool MASK = false>
 struct FwdCfg {
     static constexpr int kTileBytes = kRows * D * 2;         // one 128 x D tile, 16-bit
-    static constexpr int kKStages = (D == 128) ? 2 : 3;
-    static constexpr int kVStages = (D == 128) ? 2 : 3;
+    static constexpr int kKStages = (D == 128) ? 2 : 4;   // D = 128: shared memory is full
+    static constexpr int kVStages = (D == 128) ? 2 : 4;
     static constexpr int kQOff = 0;
     static constexpr int kKOff = kQOff + 2 * kTileBytes;
     static constexpr int kVOff = kKOff + kKStages * kTileBytes;
