@@ -55,6 +55,9 @@ CASES = [
     (130, 96, 136, "silu", F16, 1000),         # one chunk
     (64, 64, 128, "relu", F16, 64),
     (200, 136, 72, "none", BF16, 50),
+    (1, 8, 8, "gelu_tanh", BF16, 1),           # one token, the narrowest rows (16 bytes)
+    (3, 16, 24, "swiglu", F16, 2),             # tiles far larger than the problem
+    (129, 64, 8, "silu", BF16, 128),           # a one-row second chunk
 ]
 
 
