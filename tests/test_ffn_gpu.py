@@ -95,3 +95,20 @@ def test_qwen_sized_swiglu_sampled(cuda_lib):
     rows[0], rows[-1] = 0, 4095
     e = check(y, x, w1, b1, w2, b2, "swiglu", BF16, rows=rows, what="qwen mlp")
     print(f"qwen-sized swiglu: max err {e:.2e}")
+
+
+def test_ffn_benchmark_config_sampled(cuda_lib):
+    """The FFN exactly as the benchmark times it (16384 tokens in chunks of
+    4096, d_model 896, d_ff 4864, swiglu, bf16, no biases, the benchmark's
+    seed and scaling): 64 sampled rows, including both ends of every chunk."""
+    g = torch.Generator().manual_seed(9000)
+    T, d, f = 16384, 896, 4864
+    x = torch.randn(T, d, generator=g).to(BF16)
+    w1 = (torch.randn(2 * f, d, generator=g) / d ** 0.5).to(BF16)
+    w2 = (torch.randn(d, f, generator=g) / f ** 0.5).to(BF16)
+    y = _lib.ffn_forward(x.cuda(), w1.cuda(), None, w2.cuda(), None, act="swiglu", chunk=4096)
+    assert _lib.sync_status() == _lib.ATTN_OK
+    edges = [c + e for c in range(0, T, 4096) for e in (0, 4095)]
+    rows = np.unique(np.concatenate([edges, np.random.default_rng(6).choice(T, 56, replace=False)]))
+    e = check(y, x, w1, None, w2, None, "swiglu", BF16, rows=rows, what="ffn bench config")
+    print(f"ffn benchmark config: max err {e:.2e}")

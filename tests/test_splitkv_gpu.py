@@ -116,3 +116,16 @@ def test_splitkv_rejects_short_workspace(cuda_lib):
     with pytest.raises(_lib.AttnError) as e:
         _lib.attn_fwd_splitkv(q, k, v, splits=8, workspace=ws)
     assert e.value.code == _lib.ATTN_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("nk", inputs.WORKLOADS["gqa_decode"].seq_lens)
+def test_gqa_decode_workload_every_row(cuda_lib, nk):
+    """The decode workload exactly as the benchmark times it (8 sequences,
+    14 query heads on 2 KV heads, one new token, bottom-right causal, the
+    library's range count): every output row against the oracle."""
+    w = inputs.WORKLOADS["gqa_decode"]
+    x = inputs.make_inputs(w, nk)
+    q, k, v = (x[n].cuda() for n in "qkv")
+    out, lse = _lib.attn_fwd_splitkv(q, k, v, causal=w.causal)
+    assert _lib.sync_status() == _lib.ATTN_OK
+    check_all_rows(x, out, lse, w.causal, f"gqa_decode Nk={nk}")
