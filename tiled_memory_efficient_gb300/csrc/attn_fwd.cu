@@ -420,7 +420,19 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
         float m = -INFINITY;  // running max (log2 domain, scaled), same in both halves
         float l = 0.0f;       // this half's running sum of p
         float lr = 0.0f;      // bf16: this half's running sum of the rounded p
+        // A warp whose 32 rows all lie past the group (a short group, e.g. a
+        // decode step) has nothing to compute; it only keeps the barrier
+        // counts, and waits for each p_full phase to complete before it can
+        // arrive on the next one.  Both warps of a pair are alike.
+        const bool warp_live = wr0 < p.rows_per_group;
         for (int j = 0; j < n_t; ++j) {
+            if (!warp_live) {
+                warp_wait(&s_full[t], j & 1, abort_flag, p.status);
+                mbar_arrive(&s_free[t]);
+                mbar_arrive(&p_full[t]);
+                warp_wait(&p_full[t], j & 1, abort_flag, p.status);
+                continue;
+            }
             warp_wait(&s_full[t], j & 1, abort_flag, p.status);
             tc_fence_after();
             uint32_t sr[2][32];
@@ -498,7 +510,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
             mbar_arrive(&p_full[t]);
         }
 
-        if (n_t > 0) {
+        if (n_t > 0 && warp_live) {
             warp_wait(&o_full[t], 0, abort_flag, p.status);
             tc_fence_after();
             st_shared_f32(xl_slot, l);
@@ -564,7 +576,18 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
         float l = 0.0f;       // running sum of p (gives the LSE)
         float lr = 0.0f;      // bf16: running sum of the rounded p (normalises O)
         bool ok = true;
+        // A warp with no real row only keeps the barrier counts (as in the
+        // split layout above).  (Not in the masked variant, whose registers
+        // are already at the limit.)
+        const bool warp_live = MASK || wr0 < p.rows_per_group;
         for (int j = 0; j < n_t; ++j) {
+            if (!warp_live) {
+                warp_wait(&s_full[t], j & 1, abort_flag, p.status);
+                if constexpr (C::kSepP) mbar_arrive(&s_free[t]);
+                mbar_arrive(&p_full[t]);
+                warp_wait(&p_full[t], j & 1, abort_flag, p.status);
+                continue;
+            }
             if (!warp_wait(&s_full[t], j & 1, abort_flag, p.status)) { ok = false; break; }
             tc_fence_after();
             const int key0 = (kt0 + j) * kRows;
@@ -671,7 +694,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
             mbar_arrive(&p_full[t]);
         }
 
-        if (ok && n_t > 0 && warp_wait(&o_full[t], 0, abort_flag, p.status)) {
+        if (ok && warp_live && n_t > 0 && warp_wait(&o_full[t], 0, abort_flag, p.status)) {
             tc_fence_after();
             const float l_out = BF16 ? lr : l;
             const float inv_l = l_out > 0.0f ? 1.0f / l_out : 0.0f;
