@@ -58,6 +58,8 @@ CASES = [
     (1, 8, 8, "gelu_tanh", BF16, 1),           # one token, the narrowest rows (16 bytes)
     (3, 16, 24, "swiglu", F16, 2),             # tiles far larger than the problem
     (129, 64, 8, "silu", BF16, 128),           # a one-row second chunk
+    (150, 256, 512, "relu", F16, 64),          # 256-column tiles in both products
+    (100, 480, 160, "gelu_tanh", F16, 64),     # 160-column tiles: three across d_model
 ]
 
 

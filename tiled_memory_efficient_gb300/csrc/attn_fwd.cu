@@ -8,20 +8,23 @@
 // to zero, and optionally apply a causal mask.
 //
 // GB300 design (one CTA = 256 flattened query rows of one KV group, two
-// 128-row Q tiles ping-ponging on the tensor core):
-//   warp 8      TMA producer: Q tiles once, then K_j / V_j tiles through two
-//               mbarrier-guarded shared-memory rings (128-byte swizzle).
-//   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T with tcgen05.mma
-//               (both operands in shared memory, fp32 accumulator in TMEM),
-//               then O_t += P_t V_j with P_t read from TMEM.
-//   warps 0-7   softmax, one warpgroup per Q tile, one thread per query row:
-//               tcgen05.ld of the S row, masked row max, lazy rescale of the
-//               running state, exp2 with a flush-to-zero threshold, P packed
-//               to fp16/bf16 and written back over S in TMEM; at the end the
-//               epilogue divides O by the row sum and stores O and the
-//               natural-log LSE.
-// TMEM (512 columns): S_0 [0,128) S_1 [128,256) O_0 [256,256+D) O_1 [256+D,256+2D);
-// P_t overwrites the first 64 columns of S_t (two 16-bit values per column).
+// 128-row Q tiles ping-ponging on the tensor core; warp numbers in FwdCfg):
+//   producer    one thread: Q tiles once, then K_j / V_j tiles through two
+//               mbarrier-guarded shared-memory rings (TMA, 128-byte swizzle).
+//   MMA issuer  one elected lane: S_t = Q_t K_j^T with tcgen05.mma (both
+//               operands in shared memory, fp32 accumulator in TMEM), then
+//               O_t += P_t V_j with P_t read from TMEM.
+//   softmax     one thread per query row at D = 128 and with a mask, one
+//               per (row, 64-key half) otherwise: tcgen05.ld of the S row, masked
+//               row max, lazy rescale of the running state, exp2 with a
+//               flush-to-zero threshold, P packed to fp16/bf16 into TMEM; at
+//               the end the epilogue divides O by the row sum and stores O
+//               and the natural-log LSE.
+// TMEM (512 columns): S_0 [0,128) S_1 [128,256) O_0 [256,256+D)
+// O_1 [256+D,256+2D).  D = 128: P_t overwrites the first 64 columns of S_t
+// (two 16-bit values per column).  D = 64: P_t has its own 64 columns at
+// [384+64t, 448+64t), so S of the next key tile can be computed while the
+// softmax still works on this one.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>

@@ -9,9 +9,10 @@
 // (swiglu: W1 = [Wg; Wu], h = silu(x Wg^T + bg) * (x Wu^T + bu)).
 //
 // Both products run in one persistent tcgen05 kernel with a fused epilogue:
-// each CTA walks its tiles of 128 rows x 256 columns, accumulating in fp32 in
-// one of two TMEM buffers (TMA ring of 4 stages of 64-wide K slices, one
-// elected lane issuing M=128 N=256 MMAs) while four warps empty the other
+// each CTA walks its tiles of 128 rows x 128..256 columns (the width that pads
+// the product's columns least), accumulating in fp32 in one of two TMEM
+// buffers (TMA ring of 4 stages of 64-wide K slices, one elected lane issuing
+// M=128 MMAs as wide as the tile) while four warps empty the other
 // buffer: add the bias, apply the activation, round to the 16-bit dtype and
 // store.  For swiglu the 256 columns are 128 gate columns and the same 128
 // up columns, so the epilogue combines them in registers.  The host loop runs
@@ -58,6 +59,7 @@ struct GemmParams {
     int a_row0;           // first row of A (TMA coordinate)
     int ldc;              // output row stride in elements
     int glu_off;          // swiglu: first B row of the up projection (= d_ff)
+    int bn;               // output columns of a tile: 128 for swiglu, else 128..256
 };
 
 __device__ __forceinline__ float tanh_approx(float x) {
@@ -92,7 +94,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     ffn_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
     constexpr bool GLU = ACT == FFN_ACT_SWIGLU;
-    constexpr int kOutN = GLU ? 128 : 256;   // output columns of a tile
+    const int out_n = p.bn;   // output columns of a tile (the MMA's N unless swiglu)
+    // The second 128-row box of B is needed for swiglu (the up rows) and for
+    // tiles wider than 128 columns.
+    const bool two_b = GLU || out_n > 128;
+    const uint32_t stage_tx = two_b ? kStageBytes : kTileA + kTileB / 2;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -105,12 +111,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_mt = (p.M + kBM - 1) / kBM;
-    const int n_tiles = n_mt * ((p.N + kOutN - 1) / kOutN);
+    const int n_tiles = n_mt * ((p.N + out_n - 1) / out_n);
     const int n_kb = (p.K + kBK - 1) / kBK;
     // Persistent CTAs: tiles blockIdx.x, blockIdx.x + gridDim.x, ...; the
     // row tiles of one column tile are adjacent (B stays in L2).
     auto tile_m0 = [&](int t) { return (t % n_mt) * kBM; };
-    auto tile_n0 = [&](int t) { return (t / n_mt) * kOutN; };
+    auto tile_n0 = [&](int t) { return (t / n_mt) * out_n; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -147,10 +153,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     uint8_t* sA = smem + s * kStageBytes;
-                    mbar_arrive_expect_tx(&full[s], kStageBytes);
+                    mbar_arrive_expect_tx(&full[s], stage_tx);
                     tma_load_3d(&tmA, &full[s], sA, kb * kBK, p.a_row0 + m0, 0);
                     tma_load_3d(&tmB, &full[s], sA + kTileA, kb * kBK, n0, 0);
-                    tma_load_3d(&tmB, &full[s], sA + kTileA + kTileB / 2, kb * kBK, b1, 0);
+                    if (two_b)
+                        tma_load_3d(&tmB, &full[s], sA + kTileA + kTileB / 2, kb * kBK, b1, 0);
                 }
             }
             // never leave a copy in flight into shared memory about to be released
@@ -158,7 +165,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 mbar_wait_bounded(&full[n % kStages], (n / kStages) & 1, p.status);
         }
     } else if (warp == kMmaWarp) {
-        constexpr uint32_t idesc = idesc_f16(kBM, kBN, BF16, false);
+        // swiglu: N = 256 (128 gate + 128 up columns); else N = the tile width
+        const uint32_t idesc = idesc_f16(kBM, GLU ? kBN : out_n, BF16, false);
         int g = 0, i = 0;
         for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
             const int b = i & 1;
@@ -191,7 +199,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint32_t tacc = tmem + lb + 256 * b;
             uint16_t* crow = static_cast<uint16_t*>(p.c) + static_cast<int64_t>(row) * p.ldc;
 #pragma unroll 1
-            for (int c = 0; c < kOutN / 32; ++c) {
+            for (int c = 0; c < out_n / 32; ++c) {   // out_n is a multiple of 32
                 const int col0 = n0 + 32 * c;
                 uint32_t a[32];
                 tmem_ld32(tacc + 32 * c, a);
@@ -202,7 +210,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tmem_wait_ld();
                     reg_fence(a);
                     reg_fence(u);
-                    if (c == kOutN / 32 - 1) {   // the accumulator is read: release it
+                    if (c == out_n / 32 - 1) {   // the accumulator is read: release it
                         tc_fence_before();
                         mbar_arrive(&acc_empty[b]);
                     }
@@ -218,7 +226,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 } else {
                     tmem_wait_ld();
                     reg_fence(a);
-                    if (c == kOutN / 32 - 1) {
+                    if (c == out_n / 32 - 1) {
                         tc_fence_before();
                         mbar_arrive(&acc_empty[b]);
                     }
@@ -259,8 +267,7 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const Ge
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kGemmSmem);
     if (e != cudaSuccess) return e;
-    constexpr int kOutN = ACT == FFN_ACT_SWIGLU ? 128 : 256;
-    const long long tiles = static_cast<long long>((p.M + kBM - 1) / kBM) * ((p.N + kOutN - 1) / kOutN);
+    const long long tiles = static_cast<long long>((p.M + kBM - 1) / kBM) * ((p.N + p.bn - 1) / p.bn);
     // persistent: one CTA per SM at most (its shared memory and 512 TMEM columns)
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -314,6 +321,19 @@ int check_args(const void* x, const void* w1, const void* b1, const void* w2, co
     return ATTN_OK;
 }
 
+// Tile width of a product with n output columns: the multiple of 32 in
+// [128, 256] that pads n least, the widest on a tie (d_model = 896 runs as
+// four 224-column tiles rather than four 256-column ones, 1/8 of them idle).
+int tile_width(int n) {
+    int best = 256;
+    long long best_pad = (static_cast<long long>(n) + 255) / 256 * 256;
+    for (int w = 224; w >= 128; w -= 32) {
+        const long long pad = (static_cast<long long>(n) + w - 1) / w * w;
+        if (pad < best_pad) best = w, best_pad = pad;
+    }
+    return best;
+}
+
 int run(const void* x, const void* w1, const void* b1, const void* w2, const void* b2, void* y,
         int T, int d_model, int d_ff, int act, int chunk, void* workspace, size_t workspace_bytes,
         int dtype, cudaStream_t stream) {
@@ -337,11 +357,12 @@ int run(const void* x, const void* w1, const void* b1, const void* w2, const voi
         return ATTN_ERR_CUDA;
     for (int t0 = 0; t0 < T; t0 += chunk) {
         const int m = T - t0 < chunk ? T - t0 : chunk;
-        GemmParams g1{workspace, b1, status, m, d_ff, d_model, t0, d_ff, glu ? d_ff : 0};
+        GemmParams g1{workspace, b1, status, m, d_ff, d_model, t0, d_ff, glu ? d_ff : 0,
+                      glu ? 128 : tile_width(d_ff)};
         cudaError_t e = gemm(act, bf16, tmX, tmW1, g1, stream);
         if (e != cudaSuccess) return ATTN_ERR_CUDA;
         GemmParams g2{static_cast<uint16_t*>(y) + static_cast<int64_t>(t0) * d_model, b2, status, m,
-                      d_model, d_ff, 0, d_model, 0};
+                      d_model, d_ff, 0, d_model, 0, tile_width(d_model)};
         e = gemm(FFN_ACT_NONE, bf16, tmH, tmW2, g2, stream);
         if (e != cudaSuccess) return ATTN_ERR_CUDA;
     }
