@@ -86,6 +86,22 @@ SAMPLED = [("sweep", n) for n in inputs.WORKLOADS["sweep"].seq_lens] + \
           [("training", 8192)]
 
 
+FULL = [("sweep", n) for n in inputs.WORKLOADS["sweep"].seq_lens] + \
+       [("gqa_prefill", n) for n in inputs.WORKLOADS["gqa_prefill"].seq_lens] + \
+       [("video_dit", 17600), ("training", 8192)]
+
+
+@pytest.mark.parametrize("name,n", FULL)
+def test_workloads_every_row(cuda_lib, name, n):
+    """The benchmark workloads exactly as the benchmark runs them (all but
+    video-DiT at N = 75600, which is row-sampled below): every output row of
+    every head against the oracle."""
+    w = inputs.WORKLOADS[name]
+    x = inputs.make_inputs(w, n)
+    eo, el = check_full(x, w.causal, what=f"{name} N={n} every row")
+    print(f"{name} N={n} every row: max|dO|={eo:.2e} max|dLSE|={el:.2e}")
+
+
 @pytest.mark.parametrize("name,n", SAMPLED)
 def test_workloads_sampled_rows(cuda_lib, name, n):
     w = inputs.WORKLOADS[name]
