@@ -218,15 +218,28 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Work unit: consecutive CTAs share a KV group (its K/V stay hot in L2),
-    // and within a group the heaviest pair goes first (under the causal mask
-    // the last rows of a head attend to the most keys).
-    // With split keys, the CTAs of one (group, pair) are adjacent and each
-    // takes the key tiles [kt0, kt0 + tiles_per_split).
+    // Work unit (group, pair of Q tiles).  The heaviest units go first so the
+    // last wave holds light ones: under the causal mask a pair's work grows
+    // with the position of its rows in its head.  When every head is a whole
+    // number m of pairs (Nq % 256 == 0) the order runs over the pair
+    // position k = m-1 .. 0 and, within one position, over every (group,
+    // head), which is heaviest-first across the whole grid.  Otherwise
+    // consecutive CTAs share a KV group (its K/V stay hot in L2), heaviest
+    // pair first within the group.  With split keys, the CTAs of one unit
+    // are adjacent and each takes the key tiles [kt0, kt0 + tiles_per_split).
     const int split = static_cast<int>(blockIdx.x % p.n_splits);
     const int unit = static_cast<int>(blockIdx.x / p.n_splits);
-    const int group = unit / p.n_pairs;
-    const int pair = p.n_pairs - 1 - unit % p.n_pairs;
+    int group, pair;
+    if (CAUSAL && p.Nq % (2 * kRows) == 0) {
+        const int m = p.Nq / (2 * kRows);        // pairs per head (n_pairs = G * m)
+        const int heads = p.n_groups * p.G;      // (group, head) combinations
+        const int r = unit % heads;
+        group = r / p.G;
+        pair = (r % p.G) * m + (m - 1 - unit / heads);
+    } else {
+        group = unit / p.n_pairs;
+        pair = p.n_pairs - 1 - unit % p.n_pairs;
+    }
     const int64_t row_base = static_cast<int64_t>(pair) * (2 * kRows);
     const int kt0 = split * p.tiles_per_split;
     const int n0 = tiles_in_range(kv_tiles_for(row_base, p, CAUSAL), kt0, p);
