@@ -56,6 +56,12 @@ CASES = [
     (1, 2, 2, 64, 1000, 64, F16, False, (1000,), "bool"),           # 1-D: over keys only
     (1, 6, 2, 77, 77, 128, F16, False, (77, 77), "additive"),       # rows not 16-byte aligned
     (2, 2, 1, 130, 140, 64, BF16, "bottom_right", (2, 1, 130, 140), "bool"),
+    # key-only boolean masks at D=64 run in the split layout:
+    (2, 14, 2, 200, 700, 64, BF16, True, None, "padding"),          # GQA, causal, Nq < Nk
+    (2, 4, 4, 150, 260, 64, F16, "bottom_right", (2, 4, 1, 260), "bool"),  # per head, G = 1
+    (1, 3, 3, 300, 4100, 64, BF16, False, (1, 1, 1, 4100), "bool"), # many key tiles, ragged
+    # a per-head key mask with G > 1 takes the general masked layout:
+    (1, 6, 2, 100, 300, 64, F16, False, (1, 6, 1, 300), "bool"),
 ]
 
 
@@ -68,6 +74,19 @@ def test_masked_forward_matches_oracle(cuda_lib, B, Hq, Hkv, Nq, Nk, D, dtype, c
     assert _lib.sync_status() == _lib.ATTN_OK
     eo, el, n_empty = check(x, out, lse, causal, mask, f"mask {kind} {shape} {causal}")
     print(f"{kind} {shape}: max|dO|={eo:.2e} max|dLSE|={el:.2e} empty rows={n_empty}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_padding_mask_with_an_empty_sequence(cuda_lib, causal):
+    """A key-padding mask whose second sequence keeps no key: every row of
+    that sequence is O = 0, LSE = -inf; the first keeps 200 of 333 keys."""
+    x = inputs.make_custom(2, 4, 2, 160, 333, 64, F16, seed=13)
+    mask = (torch.arange(333)[None, :] < torch.tensor([200, 0])[:, None]).reshape(2, 1, 1, 333)
+    q, k, v = (x[n].cuda() for n in "qkv")
+    out, lse = _lib.attn_fwd(q, k, v, causal=causal, mask=mask.cuda())
+    assert _lib.sync_status() == _lib.ATTN_OK
+    _, _, n_empty = check(x, out, lse, causal, mask, f"padding with an empty sequence {causal}")
+    assert n_empty >= 4 * 160
 
 
 def test_rows_with_every_key_masked(cuda_lib):
@@ -90,6 +109,20 @@ def test_all_true_mask_is_the_unmasked_forward(cuda_lib):
     torch.cuda.synchronize()
     assert (a[0].float() - b[0].float()).abs().max().item() <= 1e-2
     assert (a[1] - b[1]).abs().max().item() <= 1e-4
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_all_true_padding_mask_is_the_unmasked_forward_bitwise(cuda_lib, causal):
+    """At D=64 a key-only keep-mask runs in the unmasked kernel's layout and
+    only drops keys: keeping every key must give the unmasked result bit for
+    bit."""
+    x = inputs.make_custom(2, 14, 2, 300, 700, 64, F16, seed=16)
+    q, k, v = (x[n].cuda() for n in "qkv")
+    a = _lib.attn_fwd(q, k, v, causal=causal)
+    b = _lib.attn_fwd(q, k, v, causal=causal,
+                      mask=torch.ones((2, 1, 1, 700), dtype=torch.bool, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
 def test_sdpa_with_attn_mask(cuda_lib):

@@ -44,7 +44,10 @@ constexpr float kLn2 = 0.6931471805599453f;
 // the true max exceeds it by more than this many powers of two.
 constexpr float kRescaleThreshold = 8.0f;
 
-template <int D, bool MASK = false>
+// MK: 0 no mask; 1 a general attention bias (boolean or additive, any
+// broadcast); 2 a boolean keep-mask that depends on the key alone (a padding
+// mask, [B,1,1,Nk] or per head when G = 1), applied in the split layout.
+template <int D, int MK = 0>
 struct FwdCfg {
     static constexpr int kTileBytes = kRows * D * 2;         // one 128 x D tile, 16-bit
     static constexpr int kKStages = (D == 128) ? 2 : 4;   // D = 128: shared memory is full
@@ -70,7 +73,7 @@ struct FwdCfg {
     //         half w/8), warp 16 producer, warps 17/18 MMA issuers.
     // (The masked variant keeps one thread per 128-key row at D = 64 too: its
     // bias loads need the registers the split layout does not have.)
-    static constexpr bool kSplit = (D == 64 && !MASK);
+    static constexpr bool kSplit = (D == 64 && MK != 1);
     static constexpr int kSoftmaxWarps = kSplit ? 16 : 8;
     static constexpr int kProducerWarp = kSplit ? 16 : 11;
     static constexpr int kMmaWarp0 = kSplit ? 17 : 9;
@@ -183,12 +186,14 @@ __device__ __forceinline__ float row_max64(const uint32_t (&s)[2][32]) {
     return fmaxf(fmax3(u[0], u[1], u[2]), fmax3(u[3], u[4], fmax3(u[5], u[6], u[7])));
 }
 
-template <int D, bool BF16, bool CAUSAL, bool MASK>
-__global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
+template <int D, bool BF16, bool CAUSAL, int MK>
+__global__ void __launch_bounds__(FwdCfg<D, MK>::kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-    using C = FwdCfg<D, MASK>;
+    using C = FwdCfg<D, MK>;
+    constexpr bool MASK = MK == 1;      // general bias: the one-thread-per-row layout
+    constexpr bool KEYMASK = MK == 2;   // key-only keep-mask: the split layout
     constexpr int KS = C::kKStages, VS = C::kVStages;
     constexpr int kProducerWarp = C::kProducerWarp;
     constexpr int kMmaWarp0 = C::kMmaWarp0;
@@ -441,6 +446,25 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
         // counts, and waits for each p_full phase to complete before it can
         // arrive on the next one.  Both warps of a pair are alike.
         const bool warp_live = wr0 < p.rows_per_group;
+        // Key-padding mask: one row of keep bytes for the whole CTA (batch
+        // group / Hkv; head group % Hkv when a KV group is one query head).
+        // Lane l holds 16 of this half's 64 keep bytes (chunk l & 3), loaded
+        // one key tile ahead so the load never waits; the four chunks meet
+        // by shuffles.  A tile with no dropped key costs one minimum.
+        const uint8_t* krow = nullptr;
+        if constexpr (KEYMASK)
+            krow = static_cast<const uint8_t*>(p.mask) + (group / p.Hkv) * p.msb +
+                   (group % p.Hkv) * p.msh;
+        // Keep bytes of key tile jj (zeros for a tile past the end or with
+        // keys past Nk: those go key by key below).
+        auto kload = [&](int jj) -> uint4 {
+            const int k0 = (kt0 + jj) * kRows + 64 * h;
+            if (jj < n_t && k0 + 64 <= p.Nk) return reinterpret_cast<const uint4*>(krow + k0)[lane & 3];
+            return make_uint4(0u, 0u, 0u, 0u);
+        };
+        uint4 knext = make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (KEYMASK)
+            if (warp_live) knext = kload(0);
         for (int j = 0; j < n_t; ++j) {
             if (!warp_live) {
                 warp_wait(&s_full[t], j & 1, abort_flag, p.status);
@@ -449,6 +473,9 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
                 warp_wait(&p_full[t], j & 1, abort_flag, p.status);
                 continue;
             }
+            const int key0 = (kt0 + j) * kRows + 64 * h;
+            uint4 kcur = knext;
+            if constexpr (KEYMASK) knext = kload(j + 1);
             warp_wait(&s_full[t], j & 1, abort_flag, p.status);
             tc_fence_after();
             uint32_t sr[2][32];
@@ -461,7 +488,33 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
             tc_fence_before();
             mbar_arrive(&s_free[t]);
 
-            const int key0 = (kt0 + j) * kRows + 64 * h;
+            if constexpr (KEYMASK) {
+                uint32_t mn = __vminu4(__vminu4(kcur.x, kcur.y), __vminu4(kcur.z, kcur.w));
+                mn = __vminu4(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
+                mn = __vminu4(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
+                if (__vcmpeq4(mn, 0u) != 0u) {   // the same in every lane
+                    if (key0 + 64 <= p.Nk) {
+#pragma unroll
+                        for (int w = 0; w < 16; ++w) {
+                            const uint32_t mine = (w & 3) == 0 ? kcur.x : (w & 3) == 1 ? kcur.y
+                                                 : (w & 3) == 2 ? kcur.z : kcur.w;
+                            const uint32_t word = __shfl_sync(0xffffffffu, mine, w >> 2);
+#pragma unroll
+                            for (int b = 0; b < 4; ++b)
+                                if (((word >> (8 * b)) & 0xffu) == 0u)
+                                    sr[w >> 3][(4 * w + b) & 31] = __float_as_uint(-INFINITY);
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                const int key = key0 + 32 * c + i;
+                                if (key < p.Nk && krow[key] == 0) sr[c][i] = __float_as_uint(-INFINITY);
+                            }
+                    }
+                }
+            }
             const bool need_mask =
                 (key0 + 64 > p.Nk) || (CAUSAL && key0 + 63 > warp_min_pos + p.causal_off);
             if (need_mask) {
@@ -746,12 +799,12 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
     }
 }
 
-template <int D, bool BF16, bool CAUSAL, bool MASK>
+template <int D, bool BF16, bool CAUSAL, int MK>
 cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                        const FwdParams& p, cudaStream_t stream) {
-    auto kern = attn_fwd_kernel<D, BF16, CAUSAL, MASK>;
-    constexpr int smem = FwdCfg<D, MASK>::kSmemBytes;
-    constexpr int kThreads = FwdCfg<D, MASK>::kThreads;
+    auto kern = attn_fwd_kernel<D, BF16, CAUSAL, MK>;
+    constexpr int smem = FwdCfg<D, MK>::kSmemBytes;
+    constexpr int kThreads = FwdCfg<D, MK>::kThreads;
     // Re-applied on every call: a cheap attribute write that is correct on
     // whichever device is current.
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -766,9 +819,16 @@ cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
 cudaError_t launch_fwd(int D, bool bf16, bool causal, const CUtensorMap& tmQ,
                        const CUtensorMap& tmK, const CUtensorMap& tmV, const FwdParams& p,
                        cudaStream_t stream) {
-    const bool mask = p.mask != nullptr;
+    // A boolean mask that depends on the key alone (no query stride, and no
+    // head stride unless every KV group is one query head) runs in the D=64
+    // split layout; every other mask takes the general masked layout.
+    int mk = 0;
+    if (p.mask != nullptr) {
+        const bool key_only = p.mask_kind == 1 && p.msq == 0 && (p.msh == 0 || p.G == 1);
+        mk = (D == 64 && key_only) ? 2 : 1;
+    }
 #define TME_CASE(d, b, c, m)                                  \
-    if (D == d && bf16 == b && causal == c && mask == m)      \
+    if (D == d && bf16 == b && causal == c && mk == m)        \
         return launch_one<d, b, c, m>(tmQ, tmK, tmV, p, stream);
 #define TME_CASES(m)              \
     TME_CASE(64, false, false, m)  \
@@ -779,8 +839,12 @@ cudaError_t launch_fwd(int D, bool bf16, bool causal, const CUtensorMap& tmQ,
     TME_CASE(128, false, true, m)  \
     TME_CASE(128, true, false, m)  \
     TME_CASE(128, true, true, m)
-    TME_CASES(false)
-    TME_CASES(true)
+    TME_CASES(0)
+    TME_CASES(1)
+    TME_CASE(64, false, false, 2)
+    TME_CASE(64, false, true, 2)
+    TME_CASE(64, true, false, 2)
+    TME_CASE(64, true, true, 2)
 #undef TME_CASES
 #undef TME_CASE
     return cudaErrorInvalidValue;
