@@ -241,6 +241,12 @@ __global__ void __launch_bounds__(FwdCfg<D, MK>::kThreads, 1)
         const int r = unit % heads;
         group = r / p.G;
         pair = (r % p.G) * m + (m - 1 - unit / heads);
+    } else if (MASK && !CAUSAL) {
+        // A general mask is often one bias for every head (and batch): with
+        // the pairs walked position-major over the groups, the CTAs that read
+        // one block of bias rows run together and share it through L2.
+        group = unit % p.n_groups;
+        pair = unit / p.n_groups;
     } else {
         group = unit / p.n_pairs;
         pair = p.n_pairs - 1 - unit % p.n_pairs;
