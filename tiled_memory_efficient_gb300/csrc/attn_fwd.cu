@@ -228,10 +228,12 @@ __global__ void __launch_bounds__(FwdCfg<D, MK>::kThreads, 1)
     // with the position of its rows in its head.  When every head is a whole
     // number m of pairs (Nq % 256 == 0) the order runs over the pair
     // position k = m-1 .. 0 and, within one position, over every (group,
-    // head), which is heaviest-first across the whole grid.  Otherwise
-    // consecutive CTAs share a KV group (its K/V stay hot in L2), heaviest
-    // pair first within the group.  With split keys, the CTAs of one unit
-    // are adjacent and each takes the key tiles [kt0, kt0 + tiles_per_split).
+    // head), which is heaviest-first across the whole grid.  A general mask
+    // without the causal mask walks the pairs position-major (below).
+    // Otherwise consecutive CTAs share a KV group (its K/V stay hot in L2),
+    // heaviest pair first within the group.  With split keys, the CTAs of one
+    // unit are adjacent and each takes the key tiles [kt0, kt0 +
+    // tiles_per_split).
     const int split = static_cast<int>(blockIdx.x % p.n_splits);
     const int unit = static_cast<int>(blockIdx.x / p.n_splits);
     int group, pair;
