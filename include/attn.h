@@ -90,6 +90,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
  * Requirements beyond attn_fwd's: mask 16-byte aligned and every stride times
  * the element size a multiple of 16 bytes (ATTN_ERR_ALIGN otherwise); the
  * mask is read, never written, and must stay valid until the work completes.
+ * Speed: at D = 64 a boolean mask that depends on the key alone (stride_q 0,
+ * and stride_h 0 unless Hq == Hkv: a padding mask) runs about as fast as the
+ * unmasked forward; any other mask takes a slower general path.
  */
 int attn_fwd_masked(const void* q, const void* k, const void* v, void* out, float* lse,
                     const void* mask, int mask_kind, long long mask_stride_b,
