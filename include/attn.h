@@ -91,8 +91,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
  * the element size a multiple of 16 bytes (ATTN_ERR_ALIGN otherwise); the
  * mask is read, never written, and must stay valid until the work completes.
  * Speed: at D = 64 a boolean mask that depends on the key alone (stride_q 0,
- * and stride_h 0 unless Hq == Hkv: a padding mask) runs about as fast as the
- * unmasked forward; any other mask takes a slower general path.
+ * and stride_h 0 unless Hq == Hkv: a padding mask) runs in the unmasked
+ * forward's layout, at most of its speed; any other mask takes a slower
+ * general path (one thread per query row, the bias folded into the scores).
  */
 int attn_fwd_masked(const void* q, const void* k, const void* v, void* out, float* lse,
                     const void* mask, int mask_kind, long long mask_stride_b,
