@@ -368,9 +368,8 @@ def run_ours(args):
                     if step > 0:
                         up.wait_event(k_done[i])
                     q.copy_(hq, non_blocking=True)
-                    if not decode:
-                        k.copy_(hk, non_blocking=True)
-                        v.copy_(hv, non_blocking=True)
+                    k.copy_(hk, non_blocking=True)
+                    v.copy_(hv, non_blocking=True)
                     h2d_done[i].record(up)
                 stream.wait_event(h2d_done[i])
                 if step > 0:
