@@ -71,8 +71,9 @@ struct FwdCfg {
     //  D=64:  the softmax is the bottleneck, so every row is split over two
     //         warps of 64 keys each: warps 0-15 softmax (Q tile (w/4)%2, key
     //         half w/8), warp 16 producer, warps 17/18 MMA issuers.
-    // (The masked variant keeps one thread per 128-key row at D = 64 too: its
-    // bias loads need the registers the split layout does not have.)
+    // (A general mask, MK = 1, keeps one thread per 128-key row at D = 64
+    // too: its bias loads need the registers the split layout does not have.
+    // A key-only mask, MK = 2, needs 16 bytes per lane and runs split.)
     static constexpr bool kSplit = (D == 64 && MK != 1);
     static constexpr int kSoftmaxWarps = kSplit ? 16 : 8;
     static constexpr int kProducerWarp = kSplit ? 16 : 11;
