@@ -530,8 +530,8 @@ def run_reference(args):
         x = inputs.make_inputs(w, n)
         data[n] = (x["q"][:1, :1], x["k"][:1, :1], x["v"][:1, :1])
     nqs = {n: w.queries(n) for n in seq}
-    # rows per N per step, sized so the whole run takes about 60-120 s
-    budget_step = max(0.5, 90.0 / (args.steps + args.warmup))
+    # rows per N per step, sized so the whole run takes about --ref-seconds
+    budget_step = max(0.05, args.ref_seconds / (args.steps + args.warmup))
     cost = {n: 4.0 * w.D * n for n in seq}          # flops per full row
     tot = sum(cost.values())
     rng = np.random.default_rng(0)
@@ -589,6 +589,66 @@ FFN_CONFIG = {"workload": "token-chunked SwiGLU FFN of the Qwen 2.5 0.5B shape (
 METRIC_FFN = "token-chunked FFN TFLOP/s on 1 GB300 (both products, 3 d_model x d_ff GEMMs per token)"
 
 
+def ffn_host_inputs():
+    """The FFN workload's seeded host tensors (bf16): x, W1 = [Wg; Wu], W2."""
+    import torch
+    c = FFN_CONFIG
+    T, d, f = c["T"], c["d_model"], c["d_ff"]
+    g = torch.Generator().manual_seed(9000)
+    x = torch.randn(T, d, generator=g).to(torch.bfloat16)
+    w1 = (torch.randn(2 * f, d, generator=g) / d ** 0.5).to(torch.bfloat16)
+    w2 = (torch.randn(d, f, generator=g) / f ** 0.5).to(torch.bfloat16)
+    return x, w1, w2
+
+
+def ffn_oracle_sample(x, w1, w2, budget_s: float, seed: int = 0):
+    """Times the fp64 FFN oracle on seeded row samples of x for about
+    budget_s seconds.  Returns (TFLOP/s, rows per call, calls, cores, seconds)."""
+    import numpy as np
+    import torch
+
+    from oracle import ffn as ffn_oracle
+    c = FFN_CONFIG
+    d, f = c["d_model"], c["d_ff"]
+    rng = np.random.default_rng(seed)
+    rows = 64
+    w1d, w2d = w1.double().numpy(), w2.double().numpy()
+    calls, flops, t_all = 0, 0.0, 0.0
+    while t_all < budget_s:
+        idx = rng.choice(x.shape[0], size=rows, replace=False)
+        xs = x[idx].double().numpy()
+        t0 = time.perf_counter()
+        ffn_oracle.ffn_fwd(xs, w1d, None, w2d, None, c["act"], h_dtype=torch.bfloat16)
+        t_all += time.perf_counter() - t0
+        flops += 2.0 * rows * d * 2 * f + 2.0 * rows * f * d
+        calls += 1
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return flops / t_all / 1e12, rows, calls, cores, t_all
+
+
+def run_reference_ffn(args):
+    """Reference arm of --config ffn: the fp64 FFN oracle (numpy matrix
+    products and the activations) on the host cores, a bounded row sample of
+    the same workload per step."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    x, w1, w2 = ffn_host_inputs()
+    per_step = max(0.2, args.ref_seconds / (args.steps + args.warmup))
+    ffn_oracle_sample(x, w1, w2, per_step * args.warmup, seed=1)
+    tf, rows, calls, cores, secs = ffn_oracle_sample(x, w1, w2, per_step * args.steps, seed=2)
+    sample = f"{calls} calls of {rows} seeded token rows each, fp64 (numpy BLAS)"
+    print(json.dumps({
+        "metric": METRIC_FFN, "value": round(tf, 6), "unit": "TFLOP/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "impl": "reference", "config": FFN_CONFIG,
+        "cpu_baseline": {"value": round(tf, 6), "unit": "TFLOP/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(tf, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}), flush=True)
+
+
 def run_ffn(args):
     """--config ffn: the chunked FFN (include/ffn.h), one step = one forward
     over T tokens; FLOPs = 2 T d_model (2 d_ff) + 2 T d_ff d_model."""
@@ -600,10 +660,8 @@ def run_ffn(args):
     torch.cuda.set_device(dev)
     c = FFN_CONFIG
     T, d, f = c["T"], c["d_model"], c["d_ff"]
-    g = torch.Generator().manual_seed(9000)
-    x = torch.randn(T, d, generator=g).to(torch.bfloat16).to(dev)
-    w1 = (torch.randn(2 * f, d, generator=g) / d ** 0.5).to(torch.bfloat16).to(dev)
-    w2 = (torch.randn(d, f, generator=g) / f ** 0.5).to(torch.bfloat16).to(dev)
+    hx, hw1, hw2 = ffn_host_inputs()
+    x, w1, w2 = hx.to(dev), hw1.to(dev), hw2.to(dev)
     y = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
     lib = _lib.load()
     ws = torch.empty(lib.ffn_workspace_size(T, f, c["chunk"]), dtype=torch.uint8, device=dev)
@@ -635,6 +693,11 @@ def run_ffn(args):
     pk = peaks()
     tf = flops / (ms * 1e-3) / 1e12
     n_chunks = (T + c["chunk"] - 1) // c["chunk"]
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        ctf, rows, calls, cores, _ = ffn_oracle_sample(hx, hw1, hw2, args.cpu_budget)
+        cpu = {"value": round(ctf, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"{calls} calls of {rows} seeded token rows each, fp64 (numpy BLAS)"}
     if rank == 0:
         print(json.dumps({
             "metric": METRIC_FFN, "value": round(world * tf, 2), "unit": "TFLOP/s",
@@ -646,7 +709,7 @@ def run_ffn(args):
                          "unit": "TFLOP/s", "frac": round(tf / pk["bf16_tflops"], 4),
                          "traffic": None, "kernel": "ffn_gemm_kernel (both products, all chunks)",
                          "peak_source": f"{pk['source']} bf16 dense (burst)"},
-            "cpu_baseline": None, "e2e": None, "gpu_launches": args.steps * 2 * n_chunks,
+            "cpu_baseline": cpu, "e2e": None, "gpu_launches": args.steps * 2 * n_chunks,
             "clocks": clk.summary()}), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -666,14 +729,16 @@ def main():
     ap.add_argument("--mask", choices=["none", "padding", "additive"], default="none",
                     help="time the masked kernels with this attn_mask")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle time for the cpu_baseline of a GPU run")
+    ap.add_argument("--ref-seconds", type=float, default=90.0,
+                    help="seconds of oracle time for a whole --impl reference run")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     if args.config == "ffn":
         if args.impl == "reference":
-            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the "
-                              "attention oracle; the FFN has no CPU reference leg here"}))
+            run_reference_ffn(args)
             return
         run_ffn(args)
     elif args.impl == "reference":
