@@ -41,3 +41,22 @@ def test_reference_arm_prints_one_contract_line(extra, unit):
 def test_warmup_below_three_is_refused():
     out = run("--impl", "reference", "--warmup", "2")
     assert out.returncode != 0 and "warmup" in (out.stderr + out.stdout)
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """Launched as the multi-GPU bench is (one process per rank), only rank 0
+    runs the reference arm and prints; the other rank exits 0 without work."""
+    import socket
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2", "--config",
+           "tiny", "--steps", "3", "--warmup", "3", "--ref-seconds", "2"]
+    out = subprocess.run(cmd, capture_output=True, text=True, timeout=240, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip().startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
