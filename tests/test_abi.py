@@ -103,6 +103,10 @@ def test_num_splits_heuristic(lib):
     # one unit, long keys: 152 ranges of 7 tiles cover 1024 tiles in 147
     assert lib.attn_fwd_num_splits(1, 1, 1, 1, 131072, 128, 152) == 147
     assert lib.attn_fwd_num_splits(1, 3, 2, 1, 4096, 64, 152) == 1   # invalid sizes
+    # the decode benchmark's cache lengths: the counts a GB300 sweep of 1-32 ranges found
+    # fastest (1K: 4 or 8 tied; 4K: 8 or 9 tied; 16K and 64K: 9)
+    for nk, best in ((1024, (4, 8)), (4096, (8, 9)), (16384, (9,)), (65536, (9,))):
+        assert lib.attn_fwd_num_splits(8, 14, 2, 1, nk, 64, 152) in best, nk
 
 
 def test_splitkv_workspace_and_validation(lib):
