@@ -54,6 +54,13 @@ __device__ __forceinline__ float2 unpack2(uint32_t w) {
     }
 }
 
+// Low-order bf16 parts of two fp32 values whose bf16 roundings are packed in
+// hi (first value in the low half): bf16(x - x_hi), so that x_hi + x_lo holds x
+// to about 16 significant bits (the subtraction is exact in fp32).
+__device__ __forceinline__ uint32_t bf16x2_residual(float x0, float x1, uint32_t hi) {
+    return pack2<true>(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xffff0000u));
+}
+
 // ---------------------------------------------------------------- statistics
 // One query row per D/8 lanes (16-byte loads): ndelta = -sum_d dO * O in fp32,
 // nlse2 = -LSE * log2(e).  Output rows go to the per-group padded layout.
@@ -183,6 +190,10 @@ struct BwdCfg {
 // into the first 16 of its own 32 columns ([128u+32c, +16) and
 // [128u+64+32c, +16)), which it has already read, so the products read A
 // from two column ranges.  dV at [256, 256+D), dK at [256+D, 256+2D).
+// bf16: P^T has 8 significant bits, too few for dV = sum_i P_i dO_i over many
+// queries; the chunk's warp also packs the low-order part of P^T (bf16(p -
+// P^T)) into the other 16 of its 32 S^T columns, and a second product adds
+// it, so dV sees P to about 16 bits.
 // MMA order per tile n: for u = 0, 1: dV/dK += (half u of tile n) as soon as
 // its P^T / dS^T are in TMEM, then S^T / dP^T of half u of tile n+1 into the
 // same columns (the tensor pipe runs in order, so the products of tile n have
@@ -322,6 +333,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 const uint32_t pu = tmem + 128 * u;
                 mma_ts_k64_split(tmem + 256, pu, pu + 32, dDOm + slot * kStep + u * kHalf, idesc_g,
                                  acc);
+                if constexpr (BF16)   // dV += (low-order part of P^T_u) dO_u
+                    mma_ts_k64_split(tmem + 256, pu + 16, pu + 48, dDOm + slot * kStep + u * kHalf,
+                                     idesc_g, 1u);
                 mma_ts_k64_split(tmem + 256 + D, pu + 64, pu + 96, dQm + slot * kStep + u * kHalf,
                                  idesc_g, acc);
                 if (u == 1) mma_commit_elect(&q_empty[slot]);
@@ -394,6 +408,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             reg_fence(sv);
             reg_fence(dp);
             uint32_t pw[16], dw[16];
+            uint32_t plw[BF16 ? 16 : 1];   // bf16: low-order parts of P^T
             if (fast) {
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
@@ -411,6 +426,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                                   h ? f2(d4.z, d4.w) : f2(d4.x, d4.y)));
                         pw[e >> 1] = pack2<BF16>(p0, p1);
                         dw[e >> 1] = pack2<BF16>(f2lo(dd), f2hi(dd));
+                        if constexpr (BF16) plw[e >> 1] = bf16x2_residual(p0, p1, pw[e >> 1]);
                     }
                 }
             } else {
@@ -428,12 +444,14 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                     }
                     pw[i >> 1] = pack2<BF16>(pp[0], pp[1]);
                     dw[i >> 1] = pack2<BF16>(dd[0], dd[1]);
+                    if constexpr (BF16) plw[i >> 1] = bf16x2_residual(pp[0], pp[1], pw[i >> 1]);
                 }
             }
             // The packed P^T / dS^T of this chunk go to the first 16 of its own
             // 32 columns, which are already read into registers.
             tmem_st16(tS, pw);
             tmem_st16(tDP, dw);
+            if constexpr (BF16) tmem_st16(tS + 16, plw);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&p_full[hq]);

@@ -47,11 +47,12 @@ constexpr float kRescaleThreshold = 8.0f;
 // MK: 0 no mask; 1 a general attention bias (boolean or additive, any
 // broadcast); 2 a boolean keep-mask that depends on the key alone (a padding
 // mask, [B,1,1,Nk] or per head when G = 1), applied in the split layout.
-template <int D, int MK = 0>
+// BF16: bf16 inputs (their value tiles are converted to fp16 in shared memory).
+template <int D, int MK = 0, bool BF16 = false>
 struct FwdCfg {
     static constexpr int kTileBytes = kRows * D * 2;         // one 128 x D tile, 16-bit
     static constexpr int kKStages = (D == 128) ? 2 : 4;   // D = 128: shared memory is full
-    static constexpr int kVStages = (D == 128) ? 2 : 4;
+    static constexpr int kVStages = (D == 128) ? 3 : 4;   // D = 128: 225.5 KB in all
     static constexpr int kQOff = 0;
     static constexpr int kKOff = kQOff + 2 * kTileBytes;
     static constexpr int kVOff = kKOff + kKStages * kTileBytes;
@@ -73,13 +74,20 @@ struct FwdCfg {
     //         half w/8), warp 16 producer, warps 17/18 MMA issuers.
     // (A general mask, MK = 1, keeps one thread per 128-key row at D = 64
     // too: its bias loads need the registers the split layout does not have.
-    // A key-only mask, MK = 2, needs 16 bytes per lane and runs split.)
-    static constexpr bool kSplit = (D == 64 && MK != 1);
+    // A key-only mask, MK = 2, needs 16 bytes per lane and runs split.  bf16
+    // inputs keep one thread per row as well: their value-tile converters
+    // take the warps that layout leaves idle.)
+    static constexpr bool kSplit = (D == 64 && MK != 1 && !BF16);
     static constexpr int kSoftmaxWarps = kSplit ? 16 : 8;
     static constexpr int kProducerWarp = kSplit ? 16 : 11;
     static constexpr int kMmaWarp0 = kSplit ? 17 : 9;
     static constexpr int kThreads = kSplit ? 19 * 32 : 12 * 32;
     static constexpr int kTileThreads = kSplit ? 256 : 128;  // softmax threads per Q tile
+    // bf16 inputs: warps that rewrite each value tile as fp16 in shared memory
+    // so that P can be packed as fp16 (11 significant bits instead of 8):
+    // warp 8 and, at D = 128 (one MMA issuer), warp 10.
+    static constexpr int kConvWarps = (BF16 && !kSplit) ? (kSepP ? 1 : 2) : 0;
+    static constexpr int kConvWarp0 = 8, kConvWarp1 = 10;
     // Split rows exchange partial maxima (double-buffered by key-tile parity)
     // and, at the end, partial sums: xm[2][2 tiles][128 rows][2 halves],
     // xl[2 tiles][128][2], xr[2 tiles][128][2] (floats).
@@ -187,12 +195,29 @@ __device__ __forceinline__ float row_max64(const uint32_t (&s)[2][32]) {
     return fmaxf(fmax3(u[0], u[1], u[2]), fmax3(u[3], u[4], fmax3(u[5], u[6], u[7])));
 }
 
+// The 128 softmax terms of one row (one thread per row): p = 2^(s * scale - m)
+// pairwise, summed into acc2 (fp32 pairs), rounded to 16 bits (bf16 when
+// OUT_BF16, else fp16) and stored to the row's P columns in TMEM, 32 keys
+// (16 columns) at a time.
+template <bool OUT_BF16>
+__device__ __forceinline__ void pack_p128(const uint32_t (&sr)[4][32], uint32_t tP, uint64_t sl22,
+                                          uint64_t nm2, uint64_t (&acc2)[4]) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2)
+            pk[i >> 1] = softmax_pair<OUT_BF16>(sr[c][i], sr[c][i + 1], sl22, nm2, acc2[(i >> 1) & 3]);
+        tmem_st16(tP + c * 16, pk);
+    }
+}
+
 template <int D, bool BF16, bool CAUSAL, int MK>
-__global__ void __launch_bounds__(FwdCfg<D, MK>::kThreads, 1)
+__global__ void __launch_bounds__(FwdCfg<D, MK, BF16>::kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-    using C = FwdCfg<D, MK>;
+    using C = FwdCfg<D, MK, BF16>;
     constexpr bool MASK = MK == 1;      // general bias: the one-thread-per-row layout
     constexpr bool KEYMASK = MK == 2;   // key-only keep-mask: the split layout
     constexpr int KS = C::kKStages, VS = C::kVStages;
@@ -218,8 +243,12 @@ __global__ void __launch_bounds__(FwdCfg<D, MK>::kThreads, 1)
     uint64_t* s_free = o_full + 2;     // [2] softmax has read S_t (kSepP)
     uint64_t* pv_done = s_free + 2;    // [2] PV of tile t done (kSepP)
     uint64_t* mma_done = pv_done + 2;  // [2] every MMA of tile t done
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 2);
+    uint64_t* v_cvt = mma_done + 2;    // [VS] bf16: the slot's value tile is converted (or kept)
+    uint64_t* cv_sync = v_cvt + VS;    // [2] the two converter warps have both read a tile
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cv_sync + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* v_keep16 = abort_flag + 1;  // [VS] 1: the slot's value tile stayed bf16
+    volatile int* cv_wide = v_keep16 + VS;    // [2 buffers][2 converter warps] range flags
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -280,6 +309,11 @@ __global__ void __launch_bounds__(FwdCfg<D, MK>::kThreads, 1)
             mbar_init(&pv_done[t], 1);
             mbar_init(&mma_done[t], 1);
         }
+        if constexpr (C::kConvWarps > 0) {
+            for (int i = 0; i < VS; ++i) mbar_init(&v_cvt[i], C::kConvWarps);
+            mbar_init(&cv_sync[0], 2);
+            mbar_init(&cv_sync[1], 2);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -334,13 +368,15 @@ __global__ void __launch_bounds__(FwdCfg<D, MK>::kThreads, 1)
             for (int n = (nv > VS ? nv - VS : 0); n < nv; ++n)
                 mbar_wait_bounded(&v_full[n % VS], (n / VS) & 1, p.status);
         }
-    } else if (warp == kMmaWarp0 || warp == kMmaWarp0 + 1) {
+    } else if (warp == kMmaWarp0 || (C::kSepP && warp == kMmaWarp0 + 1)) {
         // ------------------------------------------------------------ MMA issue
         // Converged warps; one elected lane issues each MMA group.  An issuing
         // thread waits while its previous group drains, so everything else it
         // does leaves the tensor pipe idle unless another issuer fills it.
         constexpr uint32_t idesc_s = idesc_f16(kRows, kRows, BF16, false);
         constexpr uint32_t idesc_o = idesc_f16(kRows, D, BF16, true);
+        // bf16 inputs: P and the converted value tile are fp16
+        constexpr uint32_t idesc_o16 = idesc_f16(kRows, D, false, true);
         // Descriptor start addresses are in 16-byte units: one tile is
         // kTileBytes/16, a 64-column block 1024.
         constexpr uint64_t kTileStep = C::kTileBytes >> 4;
@@ -366,12 +402,18 @@ __global__ void __launch_bounds__(FwdCfg<D, MK>::kThreads, 1)
         // O_t += P_t V_j with P_t from TMEM, then release V_j for tile t.
         auto issue_pv = [&](int t, int j) {
             const int vslot = j % VS;
-            warp_wait(&v_full[vslot], (j / VS) & 1, abort_flag, p.status);
+            uint32_t idesc_pv = idesc_o;
+            if constexpr (C::kConvWarps > 0) {
+                warp_wait(&v_cvt[vslot], (j / VS) & 1, abort_flag, p.status);
+                if (v_keep16[vslot] == 0) idesc_pv = idesc_o16;
+            } else {
+                warp_wait(&v_full[vslot], (j / VS) & 1, abort_flag, p.status);
+            }
             warp_wait(&p_full[t], j & 1, abort_flag, p.status);
             tc_fence_after();
             mma_ts_k128(tmem + C::kOCol + t * D,
                         tmem + (C::kSepP ? C::kPCol + t * 64 : t * kRows),
-                        dv0 + vslot * kTileStep, idesc_o, j > 0 ? 1u : 0u);
+                        dv0 + vslot * kTileStep, idesc_pv, j > 0 ? 1u : 0u);
             if constexpr (C::kSepP) mma_commit_elect(&pv_done[t]);
             mma_commit_elect(&v_empty[2 * vslot + t]);
             if (j == nt(t) - 1) mma_commit_elect(&o_full[t]);
@@ -413,6 +455,72 @@ __global__ void __launch_bounds__(FwdCfg<D, MK>::kThreads, 1)
             mma_commit_elect(&mma_done[0]);
             mbar_wait_bounded(&mma_done[0], 0, p.status);
         }
+    } else if (C::kConvWarps > 0 &&
+               (warp == C::kConvWarp0 || (C::kConvWarps == 2 && warp == C::kConvWarp1))) {
+        // ------------------------------------------------------------ value-tile converter (bf16)
+        // Rewrites each bf16 value tile in place as fp16, so that the PV
+        // product runs with fp16 P (its rounding error is 2^-11 relative
+        // instead of bf16's 2^-8).  A tile is converted when its largest
+        // magnitude lies in [2^-8, 2^16): fp16 holds every such bf16 value
+        // exactly down to 2^-14, and the smaller ones (fp16 subnormals) are
+        // off by at most 2^-25, under 2^-17 of the tile's largest value.  Any
+        // other tile (a value of 2^16 or more, an inf or NaN, or only values
+        // below 2^-8) is left as bf16 and flagged, and that key tile's P is
+        // packed as bf16.  Two converter warps split a tile and agree on the
+        // flag through shared memory before either writes.
+        const int cw = warp == C::kConvWarp0 ? 0 : 1;
+        constexpr int kChunks = C::kTileBytes / 16 / (C::kConvWarps > 0 ? C::kConvWarps : 1);
+        for (int j = 0; j < nmax; ++j) {
+            const int vs = j % VS;
+            const bool okw = warp_wait(&v_full[vs], (j / VS) & 1, abort_flag, p.status);
+            uint4* base = reinterpret_cast<uint4*>(sV + vs * C::kTileBytes) + cw * kChunks;
+            // largest bf16 exponent field of the tile (both halves of each word)
+            uint32_t ex = 0u;
+            if (okw) {
+#pragma unroll 4
+                for (int i = lane; i < kChunks; i += 32) {
+                    const uint4 w = base[i];
+                    ex = __vmaxu2(ex, __vmaxu2(__vmaxu2(w.x & 0x7f807f80u, w.y & 0x7f807f80u),
+                                               __vmaxu2(w.z & 0x7f807f80u, w.w & 0x7f807f80u)));
+                }
+            }
+            uint32_t emax = __reduce_max_sync(0xffffffffu, max(ex & 0xffffu, ex >> 16) >> 7);
+            if constexpr (C::kConvWarps == 2) {
+                // Both warps publish their half's exponent and wait (bounded)
+                // until both have, before either rewrites the tile.  Tiles j
+                // and j+2 share a flag buffer and a barrier, whose phase for
+                // tile j is j/2: a warp reaches tile j+2 only after the other
+                // has arrived for tile j+1, i.e. after it read tile j's flags.
+                volatile int* flags = cv_wide + 2 * (j & 1);
+                if (lane == 0) {
+                    flags[cw] = static_cast<int>(emax);
+                    mbar_arrive(&cv_sync[j & 1]);
+                }
+                __syncwarp();
+                warp_wait(&cv_sync[j & 1], (j >> 1) & 1, abort_flag, p.status);
+                emax = max(static_cast<uint32_t>(flags[0]), static_cast<uint32_t>(flags[1]));
+            }
+            // exponent field 119..142: largest magnitude in [2^-8, 2^16)
+            const int wide = (emax >= 143u || emax <= 118u) ? 1 : 0;
+            if (okw && !wide) {
+#pragma unroll 4
+                for (int i = lane; i < kChunks; i += 32) {
+                    uint4 w = base[i];
+                    w.x = bf16x2_to_f16x2(w.x);
+                    w.y = bf16x2_to_f16x2(w.y);
+                    w.z = bf16x2_to_f16x2(w.z);
+                    w.w = bf16x2_to_f16x2(w.w);
+                    base[i] = w;
+                }
+            }
+            // the tensor core reads these bytes after the arrival below
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                if (cw == 0) v_keep16[vs] = wide;
+                mbar_arrive(&v_cvt[vs]);
+            }
+        }
     } else if (C::kSplit && warp < C::kSoftmaxWarps) {
         // ------------------------------------------------------------ split softmax (D=64)
         // Thread = (row, half of the key tile).  The two warps of a row pair
@@ -449,7 +557,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MK>::kThreads, 1)
 
         float m = -INFINITY;  // running max (log2 domain, scaled), same in both halves
         float l = 0.0f;       // this half's running sum of p
-        float lr = 0.0f;      // bf16: this half's running sum of the rounded p
+        float lres = 0.0f;    // running sum of the rounding residuals of the half-tile maxima
         // A warp whose 32 rows all lie past the group (a short group, e.g. a
         // decode step) has nothing to compute; it only keeps the barrier
         // counts, and waits for each p_full phase to complete before it can
@@ -548,15 +656,18 @@ __global__ void __launch_bounds__(FwdCfg<D, MK>::kThreads, 1)
             const float m_sub = (m == -INFINITY) ? 0.0f : m;
 
             uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
-            float accr[4] = {0.f, 0.f, 0.f, 0.f};
             const uint64_t sl22 = f2(sl2, sl2), nm2 = f2(-m_sub, -m_sub);
+            // The largest term of this half-tile (the one that dominates a
+            // one-hot row) is rounded like every term; its rounding residual
+            // joins the normaliser, so such a row gets exactly its value row.
+            const float rtop = round16_residual<BF16>(pm, sl2, -m_sub);
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 2)
                     pk[i >> 1] = softmax_pair<BF16>(sr[c][i], sr[c][i + 1], sl22, nm2,
-                                                    acc2[(i >> 1) & 3], accr[(i >> 1) & 3]);
+                                                    acc2[(i >> 1) & 3]);
                 if (c == 0 && j > 0) {
                     // P_t and O_t are still in use by the PV product of tile j-1.
                     warp_wait(&pv_done[t], (j - 1) & 1, abort_flag, p.status);
@@ -566,7 +677,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MK>::kThreads, 1)
             }
             const uint64_t a2 = fadd2(fadd2(acc2[0], acc2[1]), fadd2(acc2[2], acc2[3]));
             const float rs = f2lo(a2) + f2hi(a2);
-            if constexpr (BF16) lr = lr * alpha + ((accr[0] + accr[1]) + (accr[2] + accr[3]));
+            lres = lres * alpha + rtop;
             // Each half rescales its half of O's columns (the decision is the
             // same in both halves).
             if (j > 0 && __any_sync(0xffffffffu, need)) {
@@ -592,12 +703,14 @@ __global__ void __launch_bounds__(FwdCfg<D, MK>::kThreads, 1)
             warp_wait(&o_full[t], 0, abort_flag, p.status);
             tc_fence_after();
             st_shared_f32(xl_slot, l);
-            st_shared_f32(xr_slot, lr);
+            st_shared_f32(xr_slot, lres);
             named_bar_sync(pair_bar, 64);
             const float lt = l + ld_shared_f32(xl_slot ^ 4u);
-            const float lrt = lr + ld_shared_f32(xr_slot ^ 4u);
+            const float lrest = lres + ld_shared_f32(xr_slot ^ 4u);
             const bool ok = *abort_flag == 0;
-            const float l_out = BF16 ? lrt : lt;
+            // O is normalised by the sum of p plus the residuals of the tile
+            // maxima; the LSE uses the sum of p alone.
+            const float l_out = lt + lrest;
             const float inv_l = l_out > 0.0f ? 1.0f / l_out : 0.0f;
             const int64_t grow = static_cast<int64_t>(group) * p.rows_per_group + row;
 #pragma unroll
@@ -652,7 +765,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MK>::kThreads, 1)
 
         float m = -INFINITY;  // running max (log2 domain, scaled) used for exponentiation
         float l = 0.0f;       // running sum of p (gives the LSE)
-        float lr = 0.0f;      // bf16: running sum of the rounded p (normalises O)
+        float lres = 0.0f;    // running sum of the rounding residuals of the tile maxima
         bool ok = true;
         // A warp with no real row only keeps the barrier counts (as in the
         // split layout above).  (Not in the masked variant, whose registers
@@ -727,28 +840,31 @@ __global__ void __launch_bounds__(FwdCfg<D, MK>::kThreads, 1)
                     tc_fence_after();
                 }
             }
-            // partial row sums of p, as packed pairs; bf16: of the rounded p
+            // bf16 inputs: P is fp16 unless this key tile's values had to stay bf16
+            bool p_bf16 = BF16;
+            if constexpr (C::kConvWarps > 0) {
+                const int vs = j % VS;
+                if (!warp_wait(&v_cvt[vs], (j / VS) & 1, abort_flag, p.status)) { ok = false; break; }
+                p_bf16 = v_keep16[vs] != 0;
+            }
+            // partial row sums of p, as packed pairs; P of keys 32c..32c+31 goes
+            // to TMEM columns 16c..16c+15 as soon as it is packed (with P over S
+            // those scores are already read).  The largest term (the one that
+            // dominates a one-hot row) is rounded like every term; its rounding
+            // residual joins the normaliser, so such a row gets exactly its value row.
             uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
-            float accr[4] = {0.f, 0.f, 0.f, 0.f};
             const uint64_t sl22 = f2(sc, sc), nm2 = f2(-m_sub, -m_sub);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                // P of keys 32c..32c+31 goes to TMEM columns 16c..16c+15 as soon
-                // as it is packed (with P over S those scores are already read).
-                uint32_t pk[16];
-#pragma unroll
-                // bf16 also sums the weights the PV product actually uses (bf16 P
-                // has a 2^-8 unit roundoff) and normalises O by that sum: O is
-                // then an exact weighted mean of the value rows, and a row
-                // dominated by one key returns that key's value row.
-                for (int i = 0; i < 32; i += 2)
-                    pk[i >> 1] = softmax_pair<BF16>(sr[c][i], sr[c][i + 1], sl22, nm2,
-                                                    acc2[(i >> 1) & 3], accr[(i >> 1) & 3]);
-                tmem_st16(tP + c * 16, pk);
+            float rtop;
+            if (p_bf16) {
+                rtop = round16_residual<true>(mx, sc, -m_sub);
+                pack_p128<true>(sr, tP, sl22, nm2, acc2);
+            } else {
+                rtop = round16_residual<false>(mx, sc, -m_sub);
+                pack_p128<false>(sr, tP, sl22, nm2, acc2);
             }
             const uint64_t a2 = fadd2(fadd2(acc2[0], acc2[1]), fadd2(acc2[2], acc2[3]));
             const float rs = f2lo(a2) + f2hi(a2);
-            if constexpr (BF16) lr = lr * alpha + ((accr[0] + accr[1]) + (accr[2] + accr[3]));
+            lres = lres * alpha + rtop;
 
             // O_t must be rescaled before the next PV accumulates into it.  PV
             // of key tile j-1 is complete: with P over S, S_t of tile j was
@@ -774,7 +890,9 @@ __global__ void __launch_bounds__(FwdCfg<D, MK>::kThreads, 1)
 
         if (ok && warp_live && n_t > 0 && warp_wait(&o_full[t], 0, abort_flag, p.status)) {
             tc_fence_after();
-            const float l_out = BF16 ? lr : l;
+            // O is normalised by the sum of p plus the residuals of the tile
+            // maxima; the LSE uses the sum of p alone.
+            const float l_out = l + lres;
             const float inv_l = l_out > 0.0f ? 1.0f / l_out : 0.0f;
             const int64_t grow = static_cast<int64_t>(group) * p.rows_per_group + row;
 #pragma unroll
@@ -812,8 +930,8 @@ template <int D, bool BF16, bool CAUSAL, int MK>
 cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                        const FwdParams& p, cudaStream_t stream) {
     auto kern = attn_fwd_kernel<D, BF16, CAUSAL, MK>;
-    constexpr int smem = FwdCfg<D, MK>::kSmemBytes;
-    constexpr int kThreads = FwdCfg<D, MK>::kThreads;
+    constexpr int smem = FwdCfg<D, MK, BF16>::kSmemBytes;
+    constexpr int kThreads = FwdCfg<D, MK, BF16>::kThreads;
     // Re-applied on every call: a cheap attribute write that is correct on
     // whichever device is current.
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -830,11 +948,12 @@ cudaError_t launch_fwd(int D, bool bf16, bool causal, const CUtensorMap& tmQ,
                        cudaStream_t stream) {
     // A boolean mask that depends on the key alone (no query stride, and no
     // head stride unless every KV group is one query head) runs in the D=64
-    // split layout; every other mask takes the general masked layout.
+    // split layout (fp16 inputs; bf16 inputs never use that layout); every
+    // other mask takes the general masked layout.
     int mk = 0;
     if (p.mask != nullptr) {
         const bool key_only = p.mask_kind == 1 && p.msq == 0 && (p.msh == 0 || p.G == 1);
-        mk = (D == 64 && key_only) ? 2 : 1;
+        mk = (D == 64 && key_only && !bf16) ? 2 : 1;
     }
 #define TME_CASE(d, b, c, m)                                  \
     if (D == d && bf16 == b && causal == c && mk == m)        \
@@ -852,8 +971,6 @@ cudaError_t launch_fwd(int D, bool bf16, bool causal, const CUtensorMap& tmQ,
     TME_CASES(1)
     TME_CASE(64, false, false, 2)
     TME_CASE(64, false, true, 2)
-    TME_CASE(64, true, false, 2)
-    TME_CASE(64, true, true, 2)
 #undef TME_CASES
 #undef TME_CASE
     return cudaErrorInvalidValue;

@@ -512,26 +512,23 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
 
 // Two softmax terms in one step: x = s * scale2 + negm2 (packed pair),
 // p = 2^x per lane (flush-to-zero), acc += p (packed pair), and p rounded to a
-// 16-bit pair (low half = first term).  BF16 also adds the two ROUNDED terms
-// to accr.  Written as one asm block so the 64-bit pairs stay register pairs.
-template <bool BF16>
+// 16-bit pair (low half = first term): bf16 when OUT_BF16, else fp16.  Written
+// as one asm block so the 64-bit pairs stay register pairs.
+template <bool OUT_BF16>
 __device__ __forceinline__ uint32_t softmax_pair(uint32_t s0, uint32_t s1, uint64_t scale2,
-                                                 uint64_t negm2, uint64_t& acc, float& accr) {
+                                                 uint64_t negm2, uint64_t& acc) {
     uint32_t w;
-    if constexpr (BF16) {
-        asm("{\n\t.reg .b64 x, p;\n\t.reg .f32 a, b;\n\t.reg .b16 lo, hi;\n\t"
-            "mov.b64 x, {%3, %4};\n\t"
-            "fma.rn.f32x2 x, x, %5, %6;\n\t"
+    if constexpr (OUT_BF16) {
+        asm("{\n\t.reg .b64 x, p;\n\t.reg .f32 a, b;\n\t"
+            "mov.b64 x, {%2, %3};\n\t"
+            "fma.rn.f32x2 x, x, %4, %5;\n\t"
             "mov.b64 {a, b}, x;\n\t"
             "ex2.approx.ftz.f32 a, a;\n\t"
             "ex2.approx.ftz.f32 b, b;\n\t"
             "mov.b64 p, {a, b};\n\t"
             "add.rn.f32x2 %1, %1, p;\n\t"
-            "cvt.rn.bf16x2.f32 %0, b, a;\n\t"
-            "mov.b32 {lo, hi}, %0;\n\t"
-            "add.rn.f32.bf16 %2, lo, %2;\n\t"
-            "add.rn.f32.bf16 %2, hi, %2;\n\t}"
-            : "=r"(w), "+l"(acc), "+f"(accr)
+            "cvt.rn.bf16x2.f32 %0, b, a;\n\t}"
+            : "=r"(w), "+l"(acc)
             : "r"(s0), "r"(s1), "l"(scale2), "l"(negm2));
     } else {
         asm("{\n\t.reg .b64 x, p;\n\t.reg .f32 a, b;\n\t"
@@ -549,16 +546,50 @@ __device__ __forceinline__ uint32_t softmax_pair(uint32_t s0, uint32_t s1, uint6
     return w;
 }
 
-// acc + lo + hi, where lo/hi are the two bf16 halves of w (mixed-precision
-// adds: the bf16 operand is widened exactly, the sum is rounded in fp32).
-__device__ __forceinline__ float add_bf16x2_f32(float acc, uint32_t w) {
-    asm("{\n\t.reg .b16 lo, hi;\n\t"
-        "mov.b32 {lo, hi}, %1;\n\t"
-        "add.rn.f32.bf16 %0, lo, %0;\n\t"
-        "add.rn.f32.bf16 %0, hi, %0;\n\t}"
-        : "+f"(acc)
-        : "r"(w));
-    return acc;
+// The softmax term of a score s: p = 2^(s * scale - m) computed exactly as
+// softmax_pair computes it (the same fused multiply-add and ex2), and the
+// rounding error of the 16-bit value the PV product uses for it: returns
+// round16(p) - p (exact in fp32: the two are within one 16-bit ulp).
+template <bool OUT_BF16>
+__device__ __forceinline__ float round16_residual(float s, float scale, float neg_m) {
+    float p, r;
+    asm("{\n\t.reg .f32 x;\n\t"
+        "fma.rn.f32 x, %1, %2, %3;\n\t"
+        "ex2.approx.ftz.f32 %0, x;\n\t}"
+        : "=f"(p)
+        : "f"(s), "f"(scale), "f"(neg_m));
+    if constexpr (OUT_BF16) {
+        asm("{\n\t.reg .b16 h;\n\t"
+            "cvt.rn.bf16.f32 h, %1;\n\t"
+            "cvt.f32.bf16 %0, h;\n\t}"
+            : "=f"(r)
+            : "f"(p));
+    } else {
+        asm("{\n\t.reg .b16 h;\n\t"
+            "cvt.rn.f16.f32 h, %1;\n\t"
+            "cvt.f32.f16 %0, h;\n\t}"
+            : "=f"(r)
+            : "f"(p));
+    }
+    return r - p;
+}
+
+// Two bf16 values (one 32-bit word) as two fp16 values, rounded to nearest
+// (exact for magnitudes in [2^-14, 2^16); smaller ones become fp16
+// subnormals, off by at most 2^-25).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;"
+        : "=r"(r)
+        : "f"(__uint_as_float(w & 0xffff0000u)), "f"(__uint_as_float(w << 16)));
+    return r;
+}
+
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy reads (tcgen05.mma operands) that another thread's barrier
+// arrival releases.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 template <bool BF16>
