@@ -35,7 +35,7 @@ def nvcc() -> str:
 
 def _deps_mtime() -> float:
     files = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
-    files.append(os.path.join(INCLUDE, "attn.h"))
+    files += [os.path.join(INCLUDE, h) for h in ("attn.h", "ffn.h")]
     return max(os.path.getmtime(f) for f in files)
 
 
