@@ -77,6 +77,41 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
              int Hkv, int Nq, int Nk, int D, float scale, int causal, int dtype, void* stream);
 
 /*
+ * Forward with a caller workspace.  The same operation, arguments, layouts and
+ * errors as attn_fwd, plus workspace / workspace_bytes.
+ *
+ * Why: the PV product takes P as 16-bit values, and the tensor core takes P
+ * in the format of V.  fp16 P carries 11 significant bits, bf16 P only 8, and
+ * where a few keys share a row's weight the bf16 rounding of P moves O by up
+ * to about 0.4% of the spread of their value rows (the forum post's
+ * "What worked": online softmax, "same math" -- the result should be the
+ * softmax attention itself).  So for bf16 inputs the value tiles are used as
+ * fp16.  attn_fwd does that conversion inside every CTA that reads a tile;
+ * this call does it once, in a first kernel, into the workspace: an fp16 copy
+ * of v (same layout) plus one flag byte per (KV head, 128-key tile).  A tile
+ * is copied when fp16 represents it well (largest magnitude in [2^-8, 2^16),
+ * or only zeros); a CTA whose key tiles are all copied reads the copy, any
+ * other reads v and packs P as bf16.  The results agree with attn_fwd's to
+ * rounding; this call runs about 20% faster at D = 128.
+ *
+ * workspace: a 16-byte-aligned device buffer of at least
+ * attn_fwd_workspace_size() bytes (ATTN_ERR_WORKSPACE if smaller, checked
+ * before anything is launched); its contents on entry do not matter, and the
+ * call writes it.  For fp16 inputs no workspace is needed (size 0; it may be
+ * NULL) and the call is attn_fwd.
+ */
+int attn_fwd_ws(const void* q, const void* k, const void* v, void* out, float* lse,
+                void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int Nq, int Nk,
+                int D, float scale, int causal, int dtype, void* stream);
+
+/*
+ * Workspace bytes attn_fwd_ws needs: for bf16, B*Hkv*Nk*D*2 (the fp16 copy of
+ * v) plus B*Hkv*ceil(Nk/128) flag bytes, each part padded to 256 bytes; 0 for
+ * fp16 and for invalid sizes.  Host-only.
+ */
+size_t attn_fwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int D, int dtype);
+
+/*
  * Forward with an attention bias: the attn_mask argument of the SDPA call
  * that the forum post patches ("Other areas where this could be useful":
  * every SDPA call, e.g. from HuggingFace Transformers, which pass padding and

@@ -22,7 +22,7 @@ def test_header_declares_the_boundary():
                      "attn_strerror", "attn_selftest_timeout", "attn_version", "attn_fwd_splitkv",
                      "attn_fwd_splitkv_workspace_size", "attn_fwd_num_splits", "attn_fwd_masked",
                      "attn_bwd_masked", "ffn_forward", "ffn_check_chunking",
-                     "ffn_workspace_size"):
+                     "ffn_workspace_size", "attn_fwd_ws", "attn_fwd_workspace_size"):
         assert required in names
 
 
@@ -82,6 +82,25 @@ def test_bwd_validation_and_workspace(lib):
     bad = [P] * 9
     bad[4] = P + 8
     assert lib.attn_bwd(*bad, P, ws, 2, 16, 16, 8192, 8192, 128, 0.08, 1, 1, None) == 3
+
+
+def test_fwd_ws_workspace_size_and_validation(lib):
+    """bf16: the fp16 copy of v and one flag byte per (KV head, 128-key tile),
+    each padded to 256 bytes; fp16 needs none.  Workspace errors come before
+    any device call."""
+    # 2*16 KV heads x 8192 keys x 128 dims x 2 bytes, then 32 x 64 flag bytes
+    assert lib.attn_fwd_workspace_size(2, 16, 16, 8192, 8192, 128, 1) == \
+        2 * 16 * 8192 * 128 * 2 + 2048
+    # ragged: 1 x 2 heads x 300 keys x 64 x 2 = 76800 -> 76800; 2 x 3 flags -> 256
+    assert lib.attn_fwd_workspace_size(1, 14, 2, 300, 300, 64, 1) == 76800 + 256
+    assert lib.attn_fwd_workspace_size(1, 2, 2, 300, 300, 64, 0) == 0
+    assert lib.attn_fwd_workspace_size(1, 3, 2, 300, 300, 64, 1) == 0   # invalid sizes
+    ws = lib.attn_fwd_workspace_size(1, 2, 2, 128, 128, 64, 1)
+    args = (1, 2, 2, 128, 128, 64, 0.125, 0, 1, None)
+    assert lib.attn_fwd_ws(*([P] * 5), 0, ws, *args) == 1          # null workspace
+    assert lib.attn_fwd_ws(*([P] * 5), P + 8, ws, *args) == 3      # misaligned workspace
+    assert lib.attn_fwd_ws(*([P] * 5), P, ws - 1, *args) == 6      # too small
+    assert lib.attn_fwd_ws(*([P] * 5), P, ws, 1, 2, 2, 128, 128, 96, 0.125, 0, 1, None) == 2
 
 
 def test_bwd_rejects_bottom_right(lib):

@@ -197,3 +197,109 @@ def test_bounded_wait_reports_timeout(cuda_lib):
     # the context is still usable afterwards
     x = inputs.make_custom(1, 2, 2, 128, 128, 64, F16, seed=14)
     check_full(x, False, what="after timeout")
+
+
+# ---------------------------------------------------------------- attn_fwd_ws
+# bf16 inputs: the value tiles are converted to fp16 once into a workspace
+# instead of inside every CTA; fp16 inputs take attn_fwd itself.
+
+WS_SHAPES = [
+    # B, Hq, Hkv, Nq, Nk, D, causal
+    (1, 2, 2, 300, 300, 128, False),
+    (1, 2, 2, 300, 300, 128, True),
+    (1, 4, 4, 200, 333, 128, False),     # Nq != Nk, both ragged
+    (1, 14, 2, 250, 250, 64, True),      # GQA G=7, D=64
+    (2, 4, 2, 1024, 1024, 128, True),    # several key tiles, causal skipping
+    (1, 3, 3, 1, 517, 64, False),        # one query row
+]
+
+
+def run_fwd_ws(x, causal, scale=None):
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    out, lse = _lib.attn_fwd_ws(q, k, v, causal=causal, scale=scale)
+    assert _lib.sync_status() == _lib.ATTN_OK
+    return out, lse
+
+
+def check_ws(x, causal, what):
+    out, lse = run_fwd_ws(x, causal)
+    o_ref, lse_ref = helpers.oracle_rows(x["q"], x["k"], x["v"],
+                                         np.arange(x["q"].shape[0] * x["q"].shape[1] *
+                                                   x["q"].shape[2]), causal)
+    return helpers.assert_fwd_close(out.reshape(-1, out.shape[-1]).double().cpu().numpy(),
+                                    lse.reshape(-1).double().cpu().numpy(), o_ref, lse_ref,
+                                    x["q"].dtype, what)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,D,causal", WS_SHAPES)
+def test_ws_small_shapes_every_row(cuda_lib, B, Hq, Hkv, Nq, Nk, D, causal):
+    x = inputs.make_custom(B, Hq, Hkv, Nq, Nk, D, BF16, seed=Nq * 5 + Nk + D)
+    check_ws(x, causal, f"ws {(B, Hq, Hkv, Nq, Nk, D, causal)}")
+
+
+def test_ws_stress_one_hot_rows(cuda_lib):
+    x = inputs.make_custom(1, 3, 3, 300, 520, 128, BF16, seed=6, std=4.0, v_std=1.0)
+    check_ws(x, False, "ws std4 D=128")
+    check_ws(x, True, "ws std4 D=128 causal")
+
+
+@pytest.mark.parametrize("name,n", [("video_dit", 17600), ("training", 8192)])
+def test_ws_matches_attn_fwd_bitwise(cuda_lib, name, n):
+    """Every value tile of these workloads converts, so both paths run the
+    same fp16 PV products: the outputs agree bit for bit (attn_fwd itself is
+    checked against the oracle on every row of both workloads)."""
+    w = inputs.WORKLOADS[name]
+    x = inputs.make_inputs(w, n)
+    a = run_fwd(x, w.causal)
+    b = run_fwd_ws(x, w.causal)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("path", ["attn_fwd", "attn_fwd_ws"])
+def test_value_tile_below_fp16_precision_stays_bf16(cuda_lib, path):
+    """A value tile whose largest magnitude is below 2^-8 stays bf16 (its
+    small values would lose bits as fp16 subnormals); the other tiles still
+    convert.  Both paths against the oracle at the usual bound."""
+    x = inputs.make_custom(1, 2, 2, 384, 700, 128, BF16, seed=41)
+    v = x["v"].clone()
+    v[0, 1, 256:384] *= 1.0e-4           # key tile 2 of head 1
+    x["v"] = v.to(BF16)
+    if path == "attn_fwd":
+        check_full(x, False, what="tiny value tile attn_fwd")
+    else:
+        check_ws(x, False, "tiny value tile attn_fwd_ws")
+
+
+@pytest.mark.parametrize("path", ["attn_fwd", "attn_fwd_ws"])
+def test_value_tile_beyond_fp16_range_stays_bf16(cuda_lib, path):
+    """A value of magnitude 2^16 or more (here 1e5) does not fit fp16: its
+    tile (attn_fwd) or the CTAs that read it (attn_fwd_ws) keep bf16 values
+    and pack P as bf16.  bf16 P is rounded to 2^-8 relative, which moves O by
+    up to 2^-8 of the weighted mean of |v| -- about half an ulp of the large
+    outputs this value makes -- so the bound here adds 2^-7 * sum_j p_j |v_j|
+    (exact softmax weights p) to the usual one."""
+    x = inputs.make_custom(1, 2, 2, 384, 700, 128, BF16, seed=41)
+    v = x["v"].clone()
+    v[0, 0, 200, 5] = 1.0e5              # key tile 1 of head 0
+    x["v"] = v.to(BF16)
+    out, lse = run_fwd(x, False) if path == "attn_fwd" else run_fwd_ws(x, False)
+    q, k, vv = (x[n][0].double().numpy() for n in ("q", "k", "v"))
+    o_ref, lse_ref = helpers.oracle_rows(x["q"], x["k"], x["v"], np.arange(2 * 384), False)
+    slack = np.concatenate([
+        (lambda s: (np.exp(s - s.max(1, keepdims=True)) /
+                    np.exp(s - s.max(1, keepdims=True)).sum(1, keepdims=True)) @ np.abs(vv[h]))(
+            q[h] @ k[h].T / np.sqrt(128))
+        for h in range(2)])
+    got = out.reshape(-1, 128).double().cpu().numpy()
+    err = np.abs(got - o_ref)
+    bound = helpers.bound_for(o_ref, helpers.TOL_O[BF16], BF16) + 2.0 ** -7 * slack
+    assert np.all(np.isfinite(got)) and np.all(err <= bound), float((err - bound).max())
+    assert helpers.max_err(lse.reshape(-1).double().cpu().numpy(), lse_ref) <= helpers.TOL_LSE
+
+
+def test_ws_fp16_is_attn_fwd(cuda_lib):
+    x = inputs.make_custom(1, 2, 2, 300, 300, 64, F16, seed=43)
+    assert _lib.fwd_workspace_size(1, 2, 2, 300, 300, 64, F16) == 0
+    a = run_fwd(x, True)
+    b = run_fwd_ws(x, True)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])

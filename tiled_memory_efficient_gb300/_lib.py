@@ -51,6 +51,9 @@ _SIGNATURES = {
     "attn_fwd_splitkv": ([_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _i, _i, _i, _i, _i, _i,
                           ctypes.c_float, _i, _i, _i, _vp], _i),
     "attn_fwd_splitkv_workspace_size": ([_i, _i, _i, _i, _i, _i, _i], ctypes.c_size_t),
+    "attn_fwd_ws": ([_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _i, _i, _i, _i, _i, _i,
+                     ctypes.c_float, _i, _i, _vp], _i),
+    "attn_fwd_workspace_size": ([_i, _i, _i, _i, _i, _i, _i], ctypes.c_size_t),
     "attn_fwd_num_splits": ([_i, _i, _i, _i, _i, _i, _i], _i),
     "attn_bwd_workspace_size": ([_i, _i, _i, _i, _i, _i, _i], ctypes.c_size_t),
     "attn_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
@@ -224,6 +227,42 @@ def attn_fwd(q, k, v, causal=False, scale: float | None = None, out=None, lse=No
                          _dtype_code(q), _stream_handle(q.device))
     if rc != ATTN_OK:
         raise AttnError("attn_fwd", rc)
+    return out, lse
+
+
+def fwd_workspace_size(B, Hq, Hkv, Nq, Nk, D, dtype) -> int:
+    """Bytes of workspace attn_fwd_ws needs (0 for fp16)."""
+    code = dtype if isinstance(dtype, int) else (ATTN_BF16 if str(dtype).endswith("bfloat16")
+                                                 else ATTN_F16)
+    return load().attn_fwd_workspace_size(B, Hq, Hkv, Nq, Nk, D, code)
+
+
+def attn_fwd_ws(q, k, v, causal=False, scale: float | None = None, out=None, lse=None,
+                workspace=None):
+    """attn_fwd through attn_fwd_ws: for bf16 inputs the value tiles are
+    converted to fp16 once, into a workspace (allocated here on q's device
+    when not given), instead of inside every CTA."""
+    import torch
+    _check(q, k, v)
+    B, Hq, Nq, D = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), device=q.device, dtype=torch.float32)
+    lib = load()
+    ws_bytes = lib.attn_fwd_workspace_size(B, Hq, Hkv, Nq, Nk, D, _dtype_code(q))
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes, device=q.device, dtype=torch.uint8)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib.attn_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                         ws_ptr, ws_len, B, Hq, Hkv, Nq, Nk, D, float(scale), causal_code(causal),
+                         _dtype_code(q), _stream_handle(q.device))
+    if rc != ATTN_OK:
+        raise AttnError("attn_fwd_ws", rc)
     return out, lse
 
 

@@ -18,7 +18,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libattn.so")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 
-SOURCES = ["abi.cu", "attn_fwd.cu", "attn_bwd.cu", "bwd_noalloc.cu", "splitkv.cu", "ffn.cu"]
+SOURCES = ["abi.cu", "attn_fwd.cu", "attn_bwd.cu", "bwd_noalloc.cu", "splitkv.cu", "ffn.cu",
+           "vconv.cu"]
 HEADERS = ["ptx.cuh", "attn_internal.h", "bias.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -228,6 +228,47 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, 
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+extern "C" size_t attn_fwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int D,
+                                          int dtype) {
+    if (check_shape(B, Hq, Hkv, Nq, Nk, D, 1.0f, dtype) != ATTN_OK) return 0;
+    if (dtype != ATTN_BF16) return 0;
+    const size_t groups = static_cast<size_t>(B) * Hkv;
+    const size_t v_bytes = (groups * Nk * D * 2 + 255) & ~size_t(255);
+    const size_t f_bytes = (groups * static_cast<size_t>(key_tiles(Nk)) + 255) & ~size_t(255);
+    return v_bytes + f_bytes;
+}
+
+extern "C" int attn_fwd_ws(const void* q, const void* k, const void* v, void* out, float* lse,
+                           void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+                           int Nq, int Nk, int D, float scale, int causal, int dtype,
+                           void* stream) {
+    if (dtype != ATTN_BF16)
+        return attn_fwd(q, k, v, out, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype, stream);
+    int rc = check_shape(B, Hq, Hkv, Nq, Nk, D, scale, dtype);
+    if (rc != ATTN_OK) return rc;
+    // Workspace checks come before any device call.
+    if (!workspace) return ATTN_ERR_INVALID;
+    if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
+    if (workspace_bytes < attn_fwd_workspace_size(B, Hq, Hkv, Nq, Nk, D, dtype))
+        return ATTN_ERR_WORKSPACE;
+    CUtensorMap tmQ, tmK, tmV, tmV16;
+    FwdParams p;
+    rc = fwd_prepare(q, k, v, out, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype, &tmQ, &tmK,
+                     &tmV, &p);
+    if (rc != ATTN_OK) return rc;
+    const int64_t groups = static_cast<int64_t>(B) * Hkv;
+    const size_t v_bytes = (static_cast<size_t>(groups) * Nk * D * 2 + 255) & ~size_t(255);
+    uint8_t* flags = static_cast<uint8_t*>(workspace) + v_bytes;
+    if (make_map(&tmV16, workspace, false, D, Nk, groups) != ATTN_OK) return ATTN_ERR_CUDA;
+    p.vflags = flags;
+    p.n_ktiles = static_cast<int>(key_tiles(Nk));
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_v_to_f16(D, v, workspace, flags, groups, Nk, st);
+    if (e == cudaSuccess)
+        e = launch_fwd(D, true, causal != ATTN_CAUSAL_NONE, tmQ, tmK, tmV, p, st, &tmV16);
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 extern "C" int attn_fwd_masked(const void* q, const void* k, const void* v, void* out, float* lse,
                                const void* mask, int mask_kind, long long mask_stride_b,
                                long long mask_stride_h, long long mask_stride_q, int B, int Hq,

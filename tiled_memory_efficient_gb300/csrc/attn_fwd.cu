@@ -47,8 +47,10 @@ constexpr float kRescaleThreshold = 8.0f;
 // MK: 0 no mask; 1 a general attention bias (boolean or additive, any
 // broadcast); 2 a boolean keep-mask that depends on the key alone (a padding
 // mask, [B,1,1,Nk] or per head when G = 1), applied in the split layout.
-// BF16: bf16 inputs (their value tiles are converted to fp16 in shared memory).
-template <int D, int MK = 0, bool BF16 = false>
+// BF16: bf16 inputs, whose value tiles the PV product takes as fp16: converted
+// in shared memory by converter warps, or (VPRE) read from an fp16 copy that
+// the caller's workspace holds.
+template <int D, int MK = 0, bool BF16 = false, bool VPRE = false>
 struct FwdCfg {
     static constexpr int kTileBytes = kRows * D * 2;         // one 128 x D tile, 16-bit
     static constexpr int kKStages = (D == 128) ? 2 : 4;   // D = 128: shared memory is full
@@ -86,7 +88,7 @@ struct FwdCfg {
     // bf16 inputs: warps that rewrite each value tile as fp16 in shared memory
     // so that P can be packed as fp16 (11 significant bits instead of 8):
     // warp 8 and, at D = 128 (one MMA issuer), warp 10.
-    static constexpr int kConvWarps = (BF16 && !kSplit) ? (kSepP ? 1 : 2) : 0;
+    static constexpr int kConvWarps = (BF16 && !kSplit && !VPRE) ? (kSepP ? 1 : 2) : 0;
     static constexpr int kConvWarp0 = 8, kConvWarp1 = 10;
     // Split rows exchange partial maxima (double-buffered by key-tile parity)
     // and, at the end, partial sums: xm[2][2 tiles][128 rows][2 halves],
@@ -212,12 +214,13 @@ __device__ __forceinline__ void pack_p128(const uint32_t (&sr)[4][32], uint32_t 
     }
 }
 
-template <int D, bool BF16, bool CAUSAL, int MK>
-__global__ void __launch_bounds__(FwdCfg<D, MK, BF16>::kThreads, 1)
+template <int D, bool BF16, bool CAUSAL, int MK, bool VPRE>
+__global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-    using C = FwdCfg<D, MK, BF16>;
+                    const __grid_constant__ CUtensorMap tmV,
+                    const __grid_constant__ CUtensorMap tmV16, const FwdParams p) {
+    using C = FwdCfg<D, MK, BF16, VPRE>;
     constexpr bool MASK = MK == 1;      // general bias: the one-thread-per-row layout
     constexpr bool KEYMASK = MK == 2;   // key-only keep-mask: the split layout
     constexpr int KS = C::kKStages, VS = C::kVStages;
@@ -249,6 +252,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16>::kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* v_keep16 = abort_flag + 1;  // [VS] 1: the slot's value tile stayed bf16
     volatile int* cv_wide = v_keep16 + VS;    // [2 buffers][2 converter warps] range flags
+    volatile int* cta_v16 = cv_wide + 4;      // VPRE: 1 when every value tile of the CTA is fp16
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -317,6 +321,17 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16>::kThreads, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
+    if constexpr (VPRE) {
+        // The CTA reads the fp16 copy of V only if the copy holds every one of
+        // its key tiles (flag 0); otherwise all of them come from the bf16 V.
+        if (warp == 0) {
+            const uint8_t* fl = p.vflags + static_cast<int64_t>(group) * p.n_ktiles + kt0;
+            bool wide = false;
+            for (int i = lane; i < nmax; i += 32) wide |= fl[i] != 0;
+            wide = __any_sync(0xffffffffu, wide);
+            if (lane == 0) *cta_v16 = wide ? 0 : 1;
+        }
+    }
     if (warp == kMmaWarp0) tmem_alloc(tmem_slot, 512);
     tc_fence_before();
     __syncthreads();
@@ -329,6 +344,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16>::kThreads, 1)
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
+            if constexpr (VPRE) tma_prefetch_desc(&tmV16);
             mbar_arrive_expect_tx(q_full, 2 * C::kTileBytes);
             for (int t = 0; t < 2; ++t)
                 for (int kb = 0; kb < KB; ++kb)
@@ -356,8 +372,9 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16>::kThreads, 1)
                         okp = mbar_wait(&v_empty[2 * vs + t], ((j - VS) / VS) & 1, abort_flag, p.status);
                 if (!okp) break;
                 mbar_arrive_expect_tx(&v_full[vs], C::kTileBytes);
+                const CUtensorMap* mv = (VPRE && *cta_v16) ? &tmV16 : &tmV;
                 for (int kb = 0; kb < KB; ++kb)
-                    tma_load_3d(&tmV, &v_full[vs], sV + vs * C::kTileBytes + kb * (kRows * 128),
+                    tma_load_3d(mv, &v_full[vs], sV + vs * C::kTileBytes + kb * (kRows * 128),
                                 kb * 64, (kt0 + j) * kRows, group);
                 ++nv;
             }
@@ -402,7 +419,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16>::kThreads, 1)
         // O_t += P_t V_j with P_t from TMEM, then release V_j for tile t.
         auto issue_pv = [&](int t, int j) {
             const int vslot = j % VS;
-            uint32_t idesc_pv = idesc_o;
+            uint32_t idesc_pv = (VPRE && *cta_v16) ? idesc_o16 : idesc_o;
             if constexpr (C::kConvWarps > 0) {
                 warp_wait(&v_cvt[vslot], (j / VS) & 1, abort_flag, p.status);
                 if (v_keep16[vslot] == 0) idesc_pv = idesc_o16;
@@ -841,7 +858,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16>::kThreads, 1)
                 }
             }
             // bf16 inputs: P is fp16 unless this key tile's values had to stay bf16
-            bool p_bf16 = BF16;
+            bool p_bf16 = BF16 && !(VPRE && *cta_v16);
             if constexpr (C::kConvWarps > 0) {
                 const int vs = j % VS;
                 if (!warp_wait(&v_cvt[vs], (j / VS) & 1, abort_flag, p.status)) { ok = false; break; }
@@ -926,26 +943,26 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16>::kThreads, 1)
     }
 }
 
-template <int D, bool BF16, bool CAUSAL, int MK>
+template <int D, bool BF16, bool CAUSAL, int MK, bool VPRE>
 cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                       const FwdParams& p, cudaStream_t stream) {
-    auto kern = attn_fwd_kernel<D, BF16, CAUSAL, MK>;
-    constexpr int smem = FwdCfg<D, MK, BF16>::kSmemBytes;
-    constexpr int kThreads = FwdCfg<D, MK, BF16>::kThreads;
+                       const CUtensorMap& tmV16, const FwdParams& p, cudaStream_t stream) {
+    auto kern = attn_fwd_kernel<D, BF16, CAUSAL, MK, VPRE>;
+    constexpr int smem = FwdCfg<D, MK, BF16, VPRE>::kSmemBytes;
+    constexpr int kThreads = FwdCfg<D, MK, BF16, VPRE>::kThreads;
     // Re-applied on every call: a cheap attribute write that is correct on
     // whichever device is current.
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const long long ctas = static_cast<long long>(p.n_groups) * p.n_pairs * p.n_splits;
     return launch_kernel(kern, dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, stream,
-                         tmQ, tmK, tmV, p);
+                         tmQ, tmK, tmV, tmV16, p);
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(int D, bool bf16, bool causal, const CUtensorMap& tmQ,
                        const CUtensorMap& tmK, const CUtensorMap& tmV, const FwdParams& p,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, const CUtensorMap* tmV16) {
     // A boolean mask that depends on the key alone (no query stride, and no
     // head stride unless every KV group is one query head) runs in the D=64
     // split layout (fp16 inputs; bf16 inputs never use that layout); every
@@ -955,9 +972,19 @@ cudaError_t launch_fwd(int D, bool bf16, bool causal, const CUtensorMap& tmQ,
         const bool key_only = p.mask_kind == 1 && p.msq == 0 && (p.msh == 0 || p.G == 1);
         mk = (D == 64 && key_only && !bf16) ? 2 : 1;
     }
+    // bf16 without a mask, given the fp16 copy of V (p.vflags and tmV16):
+    // the instantiation without converter warps.
+    if (tmV16 != nullptr) {
+        if (!bf16 || mk != 0 || p.vflags == nullptr) return cudaErrorInvalidValue;
+        if (D == 64 && !causal) return launch_one<64, true, false, 0, true>(tmQ, tmK, tmV, *tmV16, p, stream);
+        if (D == 64 && causal) return launch_one<64, true, true, 0, true>(tmQ, tmK, tmV, *tmV16, p, stream);
+        if (D == 128 && !causal) return launch_one<128, true, false, 0, true>(tmQ, tmK, tmV, *tmV16, p, stream);
+        if (D == 128 && causal) return launch_one<128, true, true, 0, true>(tmQ, tmK, tmV, *tmV16, p, stream);
+        return cudaErrorInvalidValue;
+    }
 #define TME_CASE(d, b, c, m)                                  \
     if (D == d && bf16 == b && causal == c && mk == m)        \
-        return launch_one<d, b, c, m>(tmQ, tmK, tmV, p, stream);
+        return launch_one<d, b, c, m, false>(tmQ, tmK, tmV, tmV, p, stream);
 #define TME_CASES(m)              \
     TME_CASE(64, false, false, m)  \
     TME_CASE(64, false, true, m)   \

@@ -48,13 +48,23 @@ struct FwdParams {
     int mask_kind;
     int64_t msb, msh, msq;
     int Hkv, G;              // KV heads, query heads per KV head
+    // bf16 with an fp16 copy of V (attn_fwd_ws): one flag byte per (KV group,
+    // 128-key tile), 0 when the copy holds that tile.
+    const uint8_t* vflags;
+    int n_ktiles;            // ceil(Nk / 128)
 };
 
 // Launches the forward kernel for one (D, dtype, causal) instantiation.
-// p.mask != nullptr selects the masked instantiation.
+// p.mask != nullptr selects the masked instantiation; tmV16 (with p.vflags)
+// the bf16 instantiation that reads the fp16 copy of V where it exists.
 cudaError_t launch_fwd(int D, bool bf16, bool causal, const CUtensorMap& tmQ,
                        const CUtensorMap& tmK, const CUtensorMap& tmV, const FwdParams& p,
-                       cudaStream_t stream);
+                       cudaStream_t stream, const CUtensorMap* tmV16 = nullptr);
+
+// Writes the fp16 copy of a bf16 value tensor [groups][Nk][D] and one flag
+// byte per (group, 128-key tile) (vconv.cu).
+cudaError_t launch_v_to_f16(int D, const void* v, void* v16, uint8_t* flags, int64_t groups,
+                            int Nk, cudaStream_t stream);
 
 // Combines the n_splits partial results of a split forward into out / lse.
 cudaError_t launch_splitkv_merge(int D, bool bf16, const FwdParams& p, cudaStream_t stream);

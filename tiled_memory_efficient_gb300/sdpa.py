@@ -63,7 +63,9 @@ class _TiledAttention(torch.autograd.Function):
             out, lse = _lib.attn_fwd_splitkv(q, k, v, causal=is_causal, scale=scale,
                                              splits=splits)
         else:
-            out, lse = _lib.attn_fwd(q, k, v, causal=is_causal, scale=scale)
+            # bf16: the value tiles are converted to fp16 once, in a workspace
+            # torch allocates (fp16: the plain forward)
+            out, lse = _lib.attn_fwd_ws(q, k, v, causal=is_causal, scale=scale)
         ctx.save_for_backward(q, k, v, out, lse)
         ctx.is_causal = is_causal
         ctx.scale = scale
