@@ -599,6 +599,19 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
         uint4 knext = make_uint4(0u, 0u, 0u, 0u);
         if constexpr (KEYMASK)
             if (warp_live) knext = kload(0);
+        // First key tile j whose half-tile (keys key0(j) .. key0(j) + 63,
+        // key0(j) = (kt0 + j) * 128 + 64 h) needs a per-key mask: it reaches
+        // past Nk, or (causal) past what this warp's first row may see.  Both
+        // conditions only grow with j.
+        auto first_tile_past = [&](int64_t lim) -> int {   // first j with key0(j) + 63 >= lim
+            const int64_t t = lim - 63 - 64 * h;            // need (kt0 + j) * 128 >= t
+            if (t <= 0) return 0;
+            const int64_t jj = (t + kRows - 1) / kRows - kt0;
+            return jj < 0 ? 0 : static_cast<int>(jj);
+        };
+        int j_mask = first_tile_past(p.Nk);
+        if (CAUSAL) j_mask = min(j_mask, first_tile_past(static_cast<int64_t>(warp_min_pos) +
+                                                         p.causal_off + 1));
         for (int j = 0; j < n_t; ++j) {
             if (!warp_live) {
                 warp_wait(&s_full[t], j & 1, abort_flag, p.status);
@@ -613,8 +626,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
             warp_wait(&s_full[t], j & 1, abort_flag, p.status);
             tc_fence_after();
             uint32_t sr[2][32];
-            tmem_ld32(tS, sr[0]);
-            tmem_ld32(tS + 32, sr[1]);
+            tmem_ld64(tS, sr[0], sr[1]);
             tmem_wait_ld();
             reg_fence(sr[0]);
             reg_fence(sr[1]);
@@ -649,9 +661,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
                     }
                 }
             }
-            const bool need_mask =
-                (key0 + 64 > p.Nk) || (CAUSAL && key0 + 63 > warp_min_pos + p.causal_off);
-            if (need_mask) {
+            if (j >= j_mask) {
                 // keys [0, lim) allowed
                 const int lim = CAUSAL ? min(p.Nk, pos + p.causal_off + 1) : p.Nk;
 #pragma unroll
@@ -672,26 +682,29 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
             m = need ? m_new : m;
             const float m_sub = (m == -INFINITY) ? 0.0f : m;
 
-            uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+            uint64_t acc2[4];
             const uint64_t sl22 = f2(sl2, sl2), nm2 = f2(-m_sub, -m_sub);
             // The largest term of this half-tile (the one that dominates a
             // one-hot row) is rounded like every term; its rounding residual
             // joins the normaliser, so such a row gets exactly its value row.
             const float rtop = round16_residual<BF16>(pm, sl2, -m_sub);
+            // keys 64h + i -> P column 32h + i/2; four running sums of pairs,
+            // each started by its first pair
+            uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t pk[16];
+            for (int i = 0; i < 8; i += 2)
+                pk[i >> 1] = softmax_pair<BF16, false>(sr[0][i], sr[0][i + 1], sl22, nm2,
+                                                       acc2[i >> 1]);
 #pragma unroll
-                for (int i = 0; i < 32; i += 2)
-                    pk[i >> 1] = softmax_pair<BF16>(sr[c][i], sr[c][i + 1], sl22, nm2,
-                                                    acc2[(i >> 1) & 3]);
-                if (c == 0 && j > 0) {
-                    // P_t and O_t are still in use by the PV product of tile j-1.
-                    warp_wait(&pv_done[t], (j - 1) & 1, abort_flag, p.status);
-                    tc_fence_after();
-                }
-                tmem_st16(tP + c * 16, pk);   // keys 64h + 32c.. -> P columns 32h + 16c..
+            for (int i = 8; i < 64; i += 2)
+                pk[i >> 1] = softmax_pair<BF16>(sr[i >> 5][i & 31], sr[i >> 5][(i & 31) + 1], sl22,
+                                                nm2, acc2[(i >> 1) & 3]);
+            if (j > 0) {
+                // P_t and O_t are still in use by the PV product of tile j-1.
+                warp_wait(&pv_done[t], (j - 1) & 1, abort_flag, p.status);
+                tc_fence_after();
             }
+            tmem_st32(tP, pk);
             const uint64_t a2 = fadd2(fadd2(acc2[0], acc2[1]), fadd2(acc2[2], acc2[3]));
             const float rs = f2lo(a2) + f2hi(a2);
             lres = lres * alpha + rtop;

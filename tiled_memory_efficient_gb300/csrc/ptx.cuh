@@ -384,6 +384,29 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "r"(taddr));
 }
 
+// 64 consecutive columns in one instruction: lane i reads columns 0-31 of
+// TMEM lane (lane base) + i into r0 and columns 32-63 into r1.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r0)[32], uint32_t (&r1)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+        "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+        : "=r"(r0[0]), "=r"(r0[1]), "=r"(r0[2]), "=r"(r0[3]), "=r"(r0[4]), "=r"(r0[5]),
+          "=r"(r0[6]), "=r"(r0[7]), "=r"(r0[8]), "=r"(r0[9]), "=r"(r0[10]), "=r"(r0[11]),
+          "=r"(r0[12]), "=r"(r0[13]), "=r"(r0[14]), "=r"(r0[15]), "=r"(r0[16]), "=r"(r0[17]),
+          "=r"(r0[18]), "=r"(r0[19]), "=r"(r0[20]), "=r"(r0[21]), "=r"(r0[22]), "=r"(r0[23]),
+          "=r"(r0[24]), "=r"(r0[25]), "=r"(r0[26]), "=r"(r0[27]), "=r"(r0[28]), "=r"(r0[29]),
+          "=r"(r0[30]), "=r"(r0[31]), "=r"(r1[0]), "=r"(r1[1]), "=r"(r1[2]), "=r"(r1[3]),
+          "=r"(r1[4]), "=r"(r1[5]), "=r"(r1[6]), "=r"(r1[7]), "=r"(r1[8]), "=r"(r1[9]),
+          "=r"(r1[10]), "=r"(r1[11]), "=r"(r1[12]), "=r"(r1[13]), "=r"(r1[14]), "=r"(r1[15]),
+          "=r"(r1[16]), "=r"(r1[17]), "=r"(r1[18]), "=r"(r1[19]), "=r"(r1[20]), "=r"(r1[21]),
+          "=r"(r1[22]), "=r"(r1[23]), "=r"(r1[24]), "=r"(r1[25]), "=r"(r1[26]), "=r"(r1[27]),
+          "=r"(r1[28]), "=r"(r1[29]), "=r"(r1[30]), "=r"(r1[31])
+        : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
@@ -510,15 +533,39 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    uint32_t r;
+    if constexpr (BF16) {
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    } else {
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    }
+    return r;
+}
+
 // Two softmax terms in one step: x = s * scale2 + negm2 (packed pair),
 // p = 2^x per lane (flush-to-zero), acc += p (packed pair), and p rounded to a
 // 16-bit pair (low half = first term): bf16 when OUT_BF16, else fp16.  Written
 // as one asm block so the 64-bit pairs stay register pairs.
-template <bool OUT_BF16>
+template <bool OUT_BF16, bool ADD = true>
 __device__ __forceinline__ uint32_t softmax_pair(uint32_t s0, uint32_t s1, uint64_t scale2,
                                                  uint64_t negm2, uint64_t& acc) {
     uint32_t w;
-    if constexpr (OUT_BF16) {
+    if constexpr (!ADD) {
+        // the accumulator's first pair: acc = p
+        float a, b;
+        asm("{\n\t.reg .b64 x;\n\t"
+            "mov.b64 x, {%2, %3};\n\t"
+            "fma.rn.f32x2 x, x, %4, %5;\n\t"
+            "mov.b64 {%0, %1}, x;\n\t"
+            "ex2.approx.ftz.f32 %0, %0;\n\t"
+            "ex2.approx.ftz.f32 %1, %1;\n\t}"
+            : "=f"(a), "=f"(b)
+            : "r"(s0), "r"(s1), "l"(scale2), "l"(negm2));
+        acc = f2(a, b);
+        return pack2<OUT_BF16>(a, b);
+    } else if constexpr (OUT_BF16) {
         asm("{\n\t.reg .b64 x, p;\n\t.reg .f32 a, b;\n\t"
             "mov.b64 x, {%2, %3};\n\t"
             "fma.rn.f32x2 x, x, %4, %5;\n\t"
@@ -592,15 +639,5 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-template <bool BF16>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-    uint32_t r;
-    if constexpr (BF16) {
-        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    } else {
-        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    }
-    return r;
-}
 
 }  // namespace tme
