@@ -303,3 +303,21 @@ def test_ws_fp16_is_attn_fwd(cuda_lib):
     a = run_fwd(x, True)
     b = run_fwd_ws(x, True)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("D,dtype", [(64, F16), (128, BF16)])
+def test_out_only_16_byte_aligned(cuda_lib, D, dtype):
+    """The epilogue writes 32-byte sectors when out is 32-byte aligned and
+    16-byte chunks when it is only 16-byte aligned: both give the same bits."""
+    x = inputs.make_custom(1, 2, 2, 300, 300, D, dtype, seed=44)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    ref, ref_lse = _lib.attn_fwd(q, k, v, causal=True)
+    n = q.numel()
+    buf = torch.zeros(n + 64, device="cuda", dtype=dtype)
+    assert buf.data_ptr() % 32 == 0
+    out = buf[8:8 + n].view_as(q)          # 16 bytes past a 32-byte boundary
+    assert out.data_ptr() % 32 == 16
+    _, lse = _lib.attn_fwd(q, k, v, causal=True, out=out)
+    assert _lib.sync_status() == _lib.ATTN_OK
+    assert torch.equal(out, ref) and torch.equal(lse, ref_lse)
+    assert torch.all(buf[:8] == 0) and torch.all(buf[8 + n:] == 0)

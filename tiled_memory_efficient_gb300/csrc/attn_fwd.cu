@@ -148,7 +148,10 @@ __device__ __forceinline__ int tiles_in_range(int n_full, int kt0, const FwdPara
 }
 
 // Epilogue stores.  Normal mode: 32 output columns of row `grow` rounded to
-// the 16-bit dtype (4 x 16-byte stores) and the row's LSE.  Split mode: the
+// the 16-bit dtype, as two 32-byte stores: each lane writes whole 32-byte
+// sectors of its row (rows are D * 2 bytes apart and the 32 columns start at
+// a multiple of 64 bytes, so they are 32-byte aligned whenever out is; an out
+// that is only 16-byte aligned takes four 16-byte stores).  Split mode: the
 // same values in fp32 to this key range's partial arrays.
 template <int D, bool BF16>
 __device__ __forceinline__ void store_o32(const FwdParams& p, int split, int64_t grow, int c,
@@ -162,14 +165,22 @@ __device__ __forceinline__ void store_o32(const FwdParams& p, int split, int64_t
                                  __uint_as_float(o[4 * i + 2]) * inv_l,
                                  __uint_as_float(o[4 * i + 3]) * inv_l);
     } else {
-        uint32_t w[16];
+        uint32_t w[2][8];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-            w[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + grow * D + c * 32);
+            w[i >> 3][i & 7] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l,
+                                           __uint_as_float(o[2 * i + 1]) * inv_l);
+        uint16_t* dst = static_cast<uint16_t*>(p.out) + grow * D + c * 32;
+        if ((reinterpret_cast<uintptr_t>(p.out) & 31u) == 0) {
+            st_global_v8(dst, w[0]);
+            st_global_v8(dst + 16, w[1]);
+        } else {   // out only 16-byte aligned: half sectors
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            for (int i = 0; i < 4; ++i)
+                d4[i] = make_uint4(w[i >> 1][4 * (i & 1)], w[i >> 1][4 * (i & 1) + 1],
+                                   w[i >> 1][4 * (i & 1) + 2], w[i >> 1][4 * (i & 1) + 3]);
+        }
     }
 }
 
