@@ -265,6 +265,7 @@ def run_ours(args):
     # N = 17600 and 75600, the training forward at N = 8192), timed in the
     # same region as the sweep with their own events; reported under "d128".
     d128 = []
+    bwdp = []
     if (args.config == "sweep" and not bwd and args.mask == "none" and args.n is None
             and not args.no_d128):
         for name, n in D128_POINTS:
@@ -276,6 +277,22 @@ def run_ours(args):
                              device=dev, dtype=torch.uint8)
             d128.append((wd, n, q, k, v, torch.empty_like(q),
                          torch.empty(q.shape[:3], device=dev, dtype=torch.float32), ws))
+            del x
+        # the backward of the training workload and of GQA prefill (attn_bwd,
+        # with the workspace attn_bwd_workspace_size recommends)
+        for name, n in BWD_POINTS:
+            wd = inputs.WORKLOADS[name]
+            x = inputs.make_inputs(wd, n)
+            if "do" not in x:
+                g = torch.Generator().manual_seed(inputs.seed_for(wd, n) + 1)
+                x["do"] = torch.randn(x["q"].shape, generator=g).to(wd.dtype)
+            q, k, v, do = (x[m].to(dev) for m in ("q", "k", "v", "do"))
+            out, lse = _lib.attn_fwd(q, k, v, causal=wd.causal)
+            ws = torch.empty(max(16, _lib.load().attn_bwd_workspace_size(
+                wd.B, wd.Hq, wd.Hkv, n, n, wd.D, 1 if wd.dtype == torch.bfloat16 else 0)),
+                device=dev, dtype=torch.uint8)
+            bwdp.append((wd, n, q, k, v, out, lse, do, torch.empty_like(q), torch.empty_like(k),
+                         torch.empty_like(v), ws))
             del x
     flush = L2Flush(dev)
 
@@ -298,10 +315,17 @@ def run_ours(args):
         else:       # attn_fwd_ws: converted once per call into the workspace (timed with it)
             _lib.attn_fwd_ws(q, k, v, causal=wd.causal, out=out, lse=lse, workspace=ws)
 
+    def launch_bwdp(b):
+        wd, n, q, k, v, out, lse, do, dq, dk, dv, ws = b
+        _lib.attn_bwd(q, k, v, out, do, lse, causal=wd.causal, dq=dq, dk=dk, dv=dv, workspace=ws)
+
     for _ in range(args.warmup):
         for b in bufs:
             flush()
             launch(b)
+        for b in bwdp:
+            flush()
+            launch_bwdp(b)
         for b in d128:
             flush()
             launch_d128(b)
@@ -317,6 +341,8 @@ def run_ours(args):
              for _ in d128] for _ in range(args.steps)]
     ev_p = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
              for _ in d128] for _ in range(args.steps)]
+    ev_b = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in bwdp] for _ in range(args.steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -328,6 +354,11 @@ def run_ours(args):
                 ev[s][i][0].record(stream)
                 launch(b)
                 ev[s][i][1].record(stream)
+            for i, b in enumerate(bwdp):
+                flush()
+                ev_b[s][i][0].record(stream)
+                launch_bwdp(b)
+                ev_b[s][i][1].record(stream)
             for i, b in enumerate(d128):
                 flush()
                 ev_d[s][i][0].record(stream)
@@ -460,7 +491,22 @@ def run_ours(args):
                   "frac_of_peak": round(f / (ms * 1e-3) / 1e12 / peak, 4)}
                  for n, ms, f in zip(seq, ms_each, flops)]
     launches_per_step = sum((2 if splits[n] > 1 else 1) if decode else (3 if bwd else 1)
-                            for n in seq) + 3 * len(d128)
+                            for n in seq) + 3 * len(d128) + 4 * len(bwdp)
+    bwd_rep = None
+    if bwdp:
+        pts = []
+        for i, (wd, n, *_rest) in enumerate(bwdp):
+            ms = statistics.median(ev_b[s_][i][0].elapsed_time(ev_b[s_][i][1])
+                                   for s_ in range(args.steps))
+            tf = 2.5 * wd.flops_fwd(n) / (ms * 1e-3) / 1e12
+            pts.append({"workload": wd.note, "N": n, "ms": round(ms, 4), "tflops": round(tf, 1),
+                        "frac_of_peak": round(tf / pk["bf16_tflops"], 4)})
+        bwd_rep = {"entry": "attn_bwd (statistics, dK/dV, dQ kernels; dK/dV partial sums and "
+                            "their reduction when the dK/dV grid is below one wave)",
+                   "flops": "5 products of the forward's size (2.5 x the forward's "
+                            "4*B*Hq*Nq*Nk*D, halved under the causal mask)",
+                   "timing": "median call time over the timed steps, CUDA events, L2 flushed "
+                             "before every call", "points": pts}
     d128_rep = None
     if d128:
         pts = []
@@ -497,7 +543,7 @@ def run_ours(args):
         "config": bench_config(w, seq, args.mask, world),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": args.steps * launches_per_step,
-        "clocks": clocks, "sweep": sweep, "d128": d128_rep,
+        "clocks": clocks, "sweep": sweep, "d128": d128_rep, "bwd": bwd_rep,
         "wall_s_timed_region": round(t_wall, 3),
     }
     print(json.dumps(line), flush=True)
@@ -506,6 +552,7 @@ def run_ours(args):
 
 
 D128_POINTS = (("video_dit", 17600), ("video_dit", 75600), ("training", 8192))
+BWD_POINTS = (("training", 8192), ("gqa_prefill", 4096))
 
 
 def bench_config(w, seq, mask, world):

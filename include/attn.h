@@ -179,8 +179,13 @@ size_t attn_fwd_splitkv_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, i
 int attn_fwd_num_splits(int B, int Hq, int Hkv, int Nq, int Nk, int D, int num_sms);
 
 /*
- * Bytes of device workspace attn_bwd needs for these sizes (fp32 per-row
- * statistics).  Returns 0 for invalid sizes.
+ * Bytes of device workspace for attn_bwd at these sizes: the fp32 per-row
+ * statistics, 2 * B*Hkv * ceil(G*Nq/128)*128 * 4 bytes (G = Hq/Hkv; padded to
+ * 256), plus -- when B*Hkv*ceil(Nk/128) dK/dV CTAs would leave SMs of the
+ * current device idle (small batches, GQA) -- fp32 partial sums of dK and dV
+ * for the S query ranges the dK/dV work is cut into, 2 * S * B*Hkv*Nk*D * 4
+ * bytes.  Returns 0 for invalid sizes.  Needs the current device only for its
+ * SM count (without one: the statistics alone).
  */
 size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int D, int dtype);
 
@@ -189,8 +194,13 @@ size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int D, in
  * the autograd tier for training).  Inputs: q, k, v, the forward's out and
  * lse, and the upstream gradient dout.  Outputs dq [B,Hq,Nq,D], and dk, dv
  * [B,Hkv,Nk,D] summed over the query heads of each group (overwritten, not
- * accumulated).  workspace: caller-owned device memory of at least
- * attn_bwd_workspace_size() bytes; its contents on entry do not matter.
+ * accumulated).  workspace: caller-owned device memory of at least the
+ * statistics part of attn_bwd_workspace_size() (ATTN_ERR_WORKSPACE otherwise);
+ * the dK/dV work is cut into as many query ranges as the rest of the given
+ * bytes hold partial sums for (at most the count that size was computed
+ * with), summed in a fixed order by a last kernel, so the result is
+ * deterministic for a given workspace size.  Its contents on entry do not
+ * matter.
  * causal: ATTN_CAUSAL_NONE or ATTN_CAUSAL_TOP_LEFT (bottom-right returns
  * ATTN_ERR_UNSUPPORTED).
  */
@@ -221,9 +231,10 @@ int attn_bwd_masked(const void* q, const void* k, const void* v, const void* out
  *
  * The scratch comes from one fixed 4 MiB array inside the library's device
  * image (present on every GPU that loads the library until the process
- * exits); nothing is allocated per call.  Problems whose
- * attn_bwd_workspace_size() exceeds 4 MiB return ATTN_ERR_WORKSPACE without
- * launching; invalid or unsupported sizes return ATTN_ERR_INVALID.  All calls
+ * exits); nothing is allocated per call.  Problems whose per-row statistics
+ * (the first part of attn_bwd_workspace_size()) exceed 4 MiB return
+ * ATTN_ERR_WORKSPACE without launching; invalid or unsupported sizes return
+ * ATTN_ERR_INVALID.  The result equals attn_bwd's with a 4 MiB workspace.  All calls
  * on a device share the array, so calls that may run on the GPU at the same
  * time (e.g. unordered streams) race and must be ordered by the caller.  The
  * array keeps the last call's contents; nothing in it needs to start at zero.

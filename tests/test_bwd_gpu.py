@@ -101,3 +101,40 @@ def test_backward_workspace_contents_do_not_matter(cuda_lib):
     assert _lib.sync_status() == _lib.ATTN_OK
     for a, b in zip(*res):
         assert torch.equal(a, b)
+
+
+def test_gqa_backward_split_every_head(cuda_lib):
+    """GQA 14:2 at N = 2048 (causal, fp16): 2 KV heads x 16 key tiles are far
+    fewer dK/dV CTAs than SMs, so the query tiles of each key tile are cut
+    into ranges whose fp32 partial sums a last kernel adds.  Every head of
+    every gradient against the oracle."""
+    x = inputs.make_custom(1, 14, 2, 2048, 2048, 64, F16, seed=61, with_grad=True)
+    got = gpu_grads(x, True)
+    ref = oracle.attention_bwd(x["q"], x["k"], x["v"], x["do"], causal=True)
+    errs = check(got, ref, F16, "gqa 14:2 N=2048 split backward")
+    print(f"gqa 14:2 N=2048 backward: max err dq/dk/dv = {errs}")
+
+
+def test_backward_split_matches_unsplit(cuda_lib):
+    """The same backward with the statistics-only workspace (no split of the
+    dK/dV work) and with the recommended one agree within the tolerance, and
+    each is deterministic."""
+    x = inputs.make_custom(1, 8, 2, 1024, 1024, 128, BF16, seed=62, with_grad=True)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    out, lse = _lib.attn_fwd(q, k, v, causal=False)
+    lib = _lib.load()
+    rec = lib.attn_bwd_workspace_size(1, 8, 2, 1024, 1024, 128, 1)
+    stats = 2 * 2 * (4 * 1024) * 4        # 2 arrays x 2 KV heads x G*Nq rows x 4 bytes
+    assert rec > stats                    # 16 dK/dV CTAs: the work is split
+    res = []
+    for nbytes in (stats, rec, stats, rec):
+        ws = torch.empty(nbytes, device="cuda", dtype=torch.uint8)
+        res.append(_lib.attn_bwd(q, k, v, out, do, lse, causal=False, workspace=ws))
+    assert _lib.sync_status() == _lib.ATTN_OK
+    for a, b in zip(res[0], res[2]):
+        assert torch.equal(a, b)
+    for a, b in zip(res[1], res[3]):
+        assert torch.equal(a, b)
+    for name, a, b in zip(("dq", "dk", "dv"), res[0], res[1]):
+        helpers.assert_close_elementwise(a.double().cpu().numpy(), b.double().cpu().numpy(),
+                                         helpers.TOL_BWD[BF16], BF16, "split vs unsplit", name)

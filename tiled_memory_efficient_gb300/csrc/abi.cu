@@ -362,15 +362,63 @@ extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, voi
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-extern "C" size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int D,
-                                          int dtype) {
-    if (check_shape(B, Hq, Hkv, Nq, Nk, D, 1.0f, dtype) != ATTN_OK) return 0;
-    // Two fp32 arrays (LSE * log2(e) and rowsum(dO * O)), each laid out per
-    // KV group with the group's rows padded to a multiple of 128.
+namespace tme {
+
+// Two fp32 arrays (LSE * log2(e) and rowsum(dO * O)), each laid out per KV
+// group with the group's rows padded to a multiple of 128.
+size_t bwd_stats_bytes(int B, int Hq, int Hkv, int Nq) {
     const size_t groups = static_cast<size_t>(B) * Hkv;
     const size_t rows = static_cast<size_t>(Hq / Hkv) * Nq;
     const size_t rows_pad = (rows + 127) / 128 * 128;
     return (2 * groups * rows_pad * sizeof(float) + 255) & ~static_cast<size_t>(255);
+}
+
+// Partial dV and dK of `splits` query ranges: two fp32 arrays
+// [splits][B * Hkv * Nk][D], each padded to 256 bytes.
+size_t bwd_split_bytes(int B, int Hkv, int Nk, int D, int splits) {
+    if (splits <= 1) return 0;
+    const size_t one = static_cast<size_t>(splits) * B * Hkv * Nk * D * sizeof(float);
+    return 2 * ((one + 255) & ~static_cast<size_t>(255));
+}
+
+namespace {
+
+// Query ranges for the dK/dV kernel: enough CTAs (B * Hkv * key tiles *
+// ranges) to give every SM of the current device one, keeping at least four
+// query tiles per range and at most 32 ranges; 1 when the unsplit grid
+// already fills the device or the SM count is unknown.  Every range is
+// non-empty (the count is recomputed from the tiles per range).
+int bwd_splits(int B, int Hq, int Hkv, int Nq, int Nk, int* tiles_per_split) {
+    const int64_t groups = static_cast<int64_t>(B) * Hkv;
+    const int64_t n_qtiles = (static_cast<int64_t>(Hq / Hkv) * Nq + 127) / 128;
+    *tiles_per_split = static_cast<int>(n_qtiles);
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0) {
+        cudaGetLastError();   // leave no error behind on a machine without a device
+        return 1;
+    }
+    const int64_t units = groups * key_tiles(Nk);
+    if (units >= sms) return 1;
+    int64_t want = (sms + units - 1) / units;
+    if (want > n_qtiles / 4) want = n_qtiles / 4;
+    if (want > 32) want = 32;
+    if (want <= 1) return 1;
+    const int64_t per = (n_qtiles + want - 1) / want;
+    *tiles_per_split = static_cast<int>(per);
+    return static_cast<int>((n_qtiles + per - 1) / per);
+}
+
+}  // namespace
+}  // namespace tme
+
+extern "C" size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int D,
+                                          int dtype) {
+    if (check_shape(B, Hq, Hkv, Nq, Nk, D, 1.0f, dtype) != ATTN_OK) return 0;
+    int per = 0;
+    const int splits = bwd_splits(B, Hq, Hkv, Nq, Nk, &per);
+    return bwd_stats_bytes(B, Hq, Hkv, Nq) + bwd_split_bytes(B, Hkv, Nk, D, splits);
 }
 
 namespace tme {
@@ -390,11 +438,31 @@ int bwd_run(const void* q, const void* k, const void* v, const void* out, const 
     const void* ptrs[] = {q, k, v, out, dout, lse, dq, dk, dv, workspace};
     for (const void* ptr : ptrs)
         if (!aligned16(ptr)) return ATTN_ERR_ALIGN;
-    if (workspace_bytes < attn_bwd_workspace_size(B, Hq, Hkv, Nq, Nk, D, dtype))
-        return ATTN_ERR_WORKSPACE;
+    const size_t stats_bytes = bwd_stats_bytes(B, Hq, Hkv, Nq);
+    if (workspace_bytes < stats_bytes) return ATTN_ERR_WORKSPACE;
     unsigned int* status = nullptr;
     rc = device_setup(&status);
     if (rc != ATTN_OK) return rc;
+    // Query ranges of the dK/dV kernel: as many as the device wants and the
+    // workspace holds the partial sums of.
+    int per = 0;
+    int splits = bwd_splits(B, Hq, Hkv, Nq, Nk, &per);
+    if (splits > 1) {
+        const size_t per_split = bwd_split_bytes(B, Hkv, Nk, D, 2) / 2;   // both arrays, one range
+        const size_t room = workspace_bytes - stats_bytes;
+        int fit = static_cast<int>(room / (per_split + 512));
+        if (fit < splits) {
+            const int64_t nqt = (static_cast<int64_t>(Hq / Hkv) * Nq + 127) / 128;
+            splits = fit;
+            if (splits > 1) {
+                per = static_cast<int>((nqt + splits - 1) / splits);
+                splits = static_cast<int>((nqt + per - 1) / per);
+            } else {
+                per = static_cast<int>(nqt);
+                splits = 1;
+            }
+        }
+    }
 
     const bool bf16 = dtype == ATTN_BF16;
     const int64_t G = Hq / Hkv;
@@ -434,7 +502,14 @@ int bwd_run(const void* q, const void* k, const void* v, const void* out, const 
     p.msq = msq;
     p.Hkv = Hkv;
     p.G = static_cast<int>(G);
-    if (groups * p.n_ktiles > 0x7fffffffll || groups * n_qtiles > 0x7fffffffll)
+    p.kv_splits = splits;
+    p.qtiles_per_split = per;
+    if (splits > 1) {
+        const size_t one = bwd_split_bytes(B, Hkv, Nk, D, splits) / 2;
+        p.dv_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + stats_bytes);
+        p.dk_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + stats_bytes + one);
+    }
+    if (groups * p.n_ktiles * splits > 0x7fffffffll || groups * n_qtiles > 0x7fffffffll)
         return ATTN_ERR_UNSUPPORTED;
     const cudaError_t e = launch_bwd(D, bf16, causal != 0, tmQ, tmK, tmV, tmDO, p,
                                      static_cast<cudaStream_t>(stream));

@@ -228,9 +228,19 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Heaviest first: under the causal mask low key tiles meet the most queries.
-    const int group = static_cast<int>(blockIdx.x / p.n_ktiles);
-    const int kt = static_cast<int>(blockIdx.x % p.n_ktiles);
+    // CTA (group, key tile kt, query range sp): consecutive CTAs share a key
+    // tile; range sp takes query tiles [qi0, qi1).
+    const int unit = static_cast<int>(blockIdx.x / p.kv_splits);
+    const int sp = static_cast<int>(blockIdx.x % p.kv_splits);
+    const int group = unit / p.n_ktiles;
+    const int kt = unit % p.n_ktiles;
     const int key0 = kt * kRows;
+    const int qi0 = sp * p.qtiles_per_split;
+    const int qi1 = min(p.n_qtiles, qi0 + p.qtiles_per_split);
+    // head (within the group) and position of the first row of query tile qi0
+    const int64_t r0 = static_cast<int64_t>(qi0) * kRows;
+    const int head_0 = static_cast<int>(r0 / p.Nq);
+    const int pos_0 = static_cast<int>(r0 % p.Nq);
     // Query tile qi (first-row position pos) meets this key tile.
     auto visit = [&](int qi, int pos) { return !CAUSAL || tile_max_pos_at(qi, pos, p) >= key0; };
 
@@ -262,7 +272,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 tma_load_3d(&tmV, kv_full, sV + kb * (kRows * 128), kb * 64, key0, group);
             }
             int n = 0;
-            for (int qi = 0, pos = 0; qi < p.n_qtiles; ++qi, pos = next_tile_pos(pos, p.Nq)) {
+            for (int qi = qi0, pos = pos_0; qi < qi1; ++qi, pos = next_tile_pos(pos, p.Nq)) {
                 if (!visit(qi, pos)) continue;
                 const int slot = n % QS;
                 if (!mbar_wait(&q_empty[slot], ((n / QS) & 1) ^ 1, abort_flag, p.status)) break;
@@ -311,7 +321,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             mma_commit_elect(&s_full[u]);
         };
         int n_vis = 0;   // query tiles this key tile meets (the producer loads them in order)
-        for (int qi = 0, pos = 0; qi < p.n_qtiles; ++qi, pos = next_tile_pos(pos, p.Nq))
+        for (int qi = qi0, pos = pos_0; qi < qi1; ++qi, pos = next_tile_pos(pos, p.Nq))
             n_vis += visit(qi, pos) ? 1 : 0;
         warp_wait(kv_full, 0, abort_flag, p.status);
         if (n_vis > 0) {
@@ -364,8 +374,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         const int64_t b_off = MASK ? static_cast<int64_t>(group / p.Hkv) * p.msb : 0;
         const int head0 = MASK ? (group % p.Hkv) * p.G : 0;
         int n = 0;
-        int head = 0;   // head within the group of the current tile's first row
-        for (int qi = 0, pos = 0; qi < p.n_qtiles; ++qi, next_tile(pos, head, p.Nq)) {
+        int head = head_0;   // head within the group of the current tile's first row
+        for (int qi = qi0, pos = pos_0; qi < qi1; ++qi, next_tile(pos, head, p.Nq)) {
             if (!visit(qi, pos)) continue;
             const int slot = n % QS;
             warp_wait(&q_full[slot], (n / QS) & 1, abort_flag, p.status);
@@ -480,7 +490,16 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 #pragma unroll
                 for (int i = 0; i < CW; ++i) a[i] = 0u;
             }
-            if (ok && key < p.Nk) {
+            if (ok && key < p.Nk && p.kv_splits > 1) {
+                // this query range's fp32 partial sum (dK unscaled)
+                float* dst = (which ? p.dk_part : p.dv_part) +
+                             (static_cast<int64_t>(sp) * p.n_groups * p.Nk + grow) * D + col0;
+#pragma unroll
+                for (int i = 0; i < CW / 4; ++i)
+                    reinterpret_cast<float4*>(dst)[i] =
+                        make_float4(__uint_as_float(a[4 * i]), __uint_as_float(a[4 * i + 1]),
+                                    __uint_as_float(a[4 * i + 2]), __uint_as_float(a[4 * i + 3]));
+            } else if (ok && key < p.Nk) {
                 const float sc = which ? p.scale : 1.0f;
                 uint32_t w[CW / 2];
 #pragma unroll
@@ -786,6 +805,31 @@ constexpr int dq_smem() {
     return (2 + kDqKStages + kDqVStages) * BwdCfg<D>::kTileBytes + 2 * kRows * 4 + 256 + 1024;
 }
 
+// Sum of the kv_splits partial dV / dK (fp32, in range order) into dv / dk
+// in the input dtype (dK scaled): 8 consecutive elements per thread.
+template <bool BF16>
+__global__ void __launch_bounds__(256) bwd_dkdv_reduce_kernel(const BwdParams p, int64_t n8) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= n8) return;
+    const int64_t stride = n8 * 8;   // elements per range
+#pragma unroll 1
+    for (int which = 0; which < 2; ++which) {
+        const float* src = (which ? p.dk_part : p.dv_part) + i * 8;
+        float4 a = reinterpret_cast<const float4*>(src)[0];
+        float4 b = reinterpret_cast<const float4*>(src)[1];
+        for (int s = 1; s < p.kv_splits; ++s) {
+            const float4 c = reinterpret_cast<const float4*>(src + s * stride)[0];
+            const float4 d = reinterpret_cast<const float4*>(src + s * stride)[1];
+            a = make_float4(a.x + c.x, a.y + c.y, a.z + c.z, a.w + c.w);
+            b = make_float4(b.x + d.x, b.y + d.y, b.z + d.z, b.w + d.w);
+        }
+        const float sc = which ? p.scale : 1.0f;
+        reinterpret_cast<uint4*>(which ? p.dk : p.dv)[i] =
+            make_uint4(pack2<BF16>(a.x * sc, a.y * sc), pack2<BF16>(a.z * sc, a.w * sc),
+                       pack2<BF16>(b.x * sc, b.y * sc), pack2<BF16>(b.z * sc, b.w * sc));
+    }
+}
+
 template <int D, bool BF16, bool CAUSAL, bool MASK>
 cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                        const CUtensorMap& tmDO, const BwdParams& p, cudaStream_t stream) {
@@ -800,10 +844,17 @@ cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
         constexpr int smem = dkdv_smem<D>();
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        const long long ctas = static_cast<long long>(p.n_groups) * p.n_ktiles;
+        const long long ctas = static_cast<long long>(p.n_groups) * p.n_ktiles * p.kv_splits;
         e = launch_kernel(kern, dim3(static_cast<unsigned>(ctas)), dim3(kKvThreads), smem, stream,
                           tmQ, tmDO, tmK, tmV, p);
         if (e != cudaSuccess) return e;
+        if (p.kv_splits > 1) {
+            const int64_t n8 = static_cast<int64_t>(p.n_groups) * p.Nk * D / 8;
+            e = launch_kernel(bwd_dkdv_reduce_kernel<BF16>,
+                              dim3(static_cast<unsigned>((n8 + 255) / 256)), dim3(256), 0, stream,
+                              p, n8);
+            if (e != cudaSuccess) return e;
+        }
     }
     {
         auto kern = bwd_dq_kernel<D, BF16, CAUSAL, MASK>;

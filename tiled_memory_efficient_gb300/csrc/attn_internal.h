@@ -98,7 +98,21 @@ struct BwdParams {
     int mask_kind;
     int64_t msb, msh, msq;
     int Hkv, G;
+    // dK/dV with the query tiles of a key tile cut into kv_splits ranges of
+    // qtiles_per_split tiles (kv_splits > 1: when B * Hkv * n_ktiles CTAs
+    // would leave SMs idle): each range's CTA writes fp32 partial sums to
+    // dv_part / dk_part ([kv_splits][n_groups * Nk][D]; dK not yet scaled)
+    // and a last kernel adds them in range order.
+    int kv_splits;
+    int qtiles_per_split;
+    float* dv_part;
+    float* dk_part;
 };
+
+// Workspace bytes of the backward without the split of dK/dV (the per-row
+// statistics only), and the bytes the partial sums of `splits` ranges add.
+size_t bwd_stats_bytes(int B, int Hq, int Hkv, int Nq);
+size_t bwd_split_bytes(int B, int Hkv, int Nk, int D, int splits);
 
 // Launches the three backward kernels (statistics, dK/dV, dQ) in order;
 // p.mask != nullptr selects the masked instantiations.

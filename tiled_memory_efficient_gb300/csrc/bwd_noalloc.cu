@@ -14,8 +14,10 @@
 // Costs and rules of that array:
 //   * It is kScratchBytes (4 MiB) on every GPU that loads the library, held
 //     until the process exits.
-//   * Problems whose scratch need (attn_bwd_workspace_size) exceeds that are
-//     rejected with ATTN_ERR_WORKSPACE before anything is launched.
+//   * Problems whose per-row statistics (the first part of
+//     attn_bwd_workspace_size) exceed that are rejected with
+//     ATTN_ERR_WORKSPACE before anything is launched; the rest of the array
+//     holds as many of attn_bwd's partial dK/dV sums as fit.
 //   * All calls on a device share the one array.  Calls that can run on the
 //     GPU at the same time (for example on two streams without ordering
 //     between them) race on it and produce wrong gradients; order them.
@@ -31,6 +33,7 @@
 #include <mutex>
 
 #include "../../include/attn.h"
+#include "attn_internal.h"
 
 namespace {
 
@@ -66,9 +69,11 @@ extern "C" int attn_bwd_noalloc(const void* q, const void* k, const void* v, con
                                 const void* dout, const float* lse, void* dq, void* dk, void* dv,
                                 int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale,
                                 int causal, int dtype, void* stream) {
-    const size_t need = attn_bwd_workspace_size(B, Hq, Hkv, Nq, Nk, D, dtype);
-    if (need == 0) return ATTN_ERR_INVALID;   // sizes attn_bwd would reject
-    if (need > kScratchBytes) return ATTN_ERR_WORKSPACE;
+    if (attn_bwd_workspace_size(B, Hq, Hkv, Nq, Nk, D, dtype) == 0)
+        return ATTN_ERR_INVALID;   // sizes attn_bwd would reject
+    // The per-row statistics must fit; attn_bwd splits the dK/dV work over
+    // more CTAs only as far as the rest of the array holds its partial sums.
+    if (tme::bwd_stats_bytes(B, Hq, Hkv, Nq) > kScratchBytes) return ATTN_ERR_WORKSPACE;
     void* scratch = nullptr;
     const int rc = scratch_address(&scratch);
     if (rc != ATTN_OK) return rc;
