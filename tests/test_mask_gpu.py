@@ -170,3 +170,27 @@ def test_sdpa_masked_autograd(cuda_lib):
     for name, t, r in zip(("dq", "dk", "dv"), (q, k, v), ref):
         helpers.assert_close_elementwise(t.grad.double().cpu().numpy(), r, helpers.TOL_BWD[BF16],
                                          BF16, "sdpa masked bwd", name)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,D,dtype,causal,lens", [
+    (2, 14, 2, 1000, 64, F16, False, (1000, 300)),    # sequence 1: key tiles 3-7 all masked
+    (2, 4, 4, 700, 128, BF16, True, (130, 700)),      # sequence 0: key tiles 2-5 all masked
+])
+def test_padding_mask_whole_key_tiles_masked(cuda_lib, B, Hq, Hkv, N, D, dtype, causal, lens):
+    """A key-padding mask ([B,1,1,N]) whose sequences end in whole masked key
+    tiles: the forward stops at each sequence's last kept key, the dQ kernel
+    does the same, and dK/dV CTAs of masked key tiles visit no query.  Forward
+    and backward against the oracle."""
+    x = inputs.make_custom(B, Hq, Hkv, N, N, D, dtype, seed=N + D, with_grad=True)
+    mask = (torch.arange(N)[None, :] < torch.tensor(lens)[:, None]).reshape(B, 1, 1, N)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    mc = mask.cuda()
+    out, lse = _lib.attn_fwd(q, k, v, causal=causal, mask=mc)
+    assert _lib.sync_status() == _lib.ATTN_OK
+    check(x, out, lse, causal, mask, f"padding {lens}")
+    dq, dk, dv = _lib.attn_bwd(q, k, v, out, do, lse, causal=causal, mask=mc)
+    assert _lib.sync_status() == _lib.ATTN_OK
+    ref = oracle.attention_bwd(x["q"], x["k"], x["v"], x["do"], causal=causal, mask=mask)
+    for name, t, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        helpers.assert_close_elementwise(t.double().cpu().numpy(), r, helpers.TOL_BWD[dtype],
+                                         dtype, f"padding {lens} bwd", name)

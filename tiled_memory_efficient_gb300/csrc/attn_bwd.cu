@@ -242,7 +242,21 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     const int head_0 = static_cast<int>(r0 / p.Nq);
     const int pos_0 = static_cast<int>(r0 % p.Nq);
     // Query tile qi (first-row position pos) meets this key tile.
-    auto visit = [&](int qi, int pos) { return !CAUSAL || tile_max_pos_at(qi, pos, p) >= key0; };
+    // A boolean mask that depends on the key alone (one row of keep bytes per
+    // KV group, as a padding mask is) may remove every key of this tile: then
+    // no query tile is visited and dK, dV of the tile are zero.
+    const bool key_only = MASK && p.mask_kind == 1 && p.msq == 0 && (p.msh == 0 || p.G == 1);
+    volatile int* tile_kept = reinterpret_cast<volatile int*>(abort_flag + 1);
+    if (key_only && warp == 0) {
+        const uint8_t* krow = static_cast<const uint8_t*>(p.mask) + (group / p.Hkv) * p.msb +
+                              (group % p.Hkv) * p.msh;
+        const int last = last_kept_key(krow, key0, min(p.Nk, key0 + kRows), lane);
+        if (lane == 0) *tile_kept = last >= 0 ? 1 : 0;
+    }
+    bool any_kept = true;   // set after the set-up barrier
+    auto visit = [&](int qi, int pos) {
+        return any_kept && (!CAUSAL || tile_max_pos_at(qi, pos, p) >= key0);
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
@@ -261,6 +275,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if (key_only) any_kept = *tile_kept != 0;
 
     if (warp == kKvProducerWarp) {
         if (lane == 0) {
@@ -567,6 +582,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int keys = min(tile_max_pos(row0, p) + 1, p.Nk);
         nkv = (keys + kRows - 1) / kRows;
     }
+    // A boolean mask that depends on the key alone: the key tiles past its last
+    // kept key contribute nothing to dQ (at least one tile is kept, so rows with
+    // no kept key still end with dQ = 0).
+    const bool key_only = MASK && p.mask_kind == 1 && p.msq == 0 && (p.msh == 0 || p.G == 1);
+    volatile int* key_lim = reinterpret_cast<volatile int*>(abort_flag + 1);
+    if (key_only && warp == 0 && nkv > 0) {
+        const uint8_t* krow = static_cast<const uint8_t*>(p.mask) + (group / p.Hkv) * p.msb +
+                              (group % p.Hkv) * p.msh;
+        const int last = last_kept_key(krow, 0, min(p.Nk, nkv * kRows), lane);
+        if (lane == 0) *key_lim = last < 0 ? 1 : last / kRows + 1;
+    }
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -586,6 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if (key_only && nkv > 0) nkv = min(nkv, *key_lim);
 
     if (warp == kProducerWarp) {
         if (lane == 0) {

@@ -264,6 +264,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
     volatile int* v_keep16 = abort_flag + 1;  // [VS] 1: the slot's value tile stayed bf16
     volatile int* cv_wide = v_keep16 + VS;    // [2 buffers][2 converter warps] range flags
     volatile int* cta_v16 = cv_wide + 4;      // VPRE: 1 when every value tile of the CTA is fp16
+    volatile int* key_lim = cta_v16 + 1;      // key-only masks: key tiles the CTA needs
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -300,9 +301,14 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
     }
     const int64_t row_base = static_cast<int64_t>(pair) * (2 * kRows);
     const int kt0 = split * p.tiles_per_split;
-    const int n0 = tiles_in_range(kv_tiles_for(row_base, p, CAUSAL), kt0, p);
-    const int n1 = tiles_in_range(kv_tiles_for(row_base + kRows, p, CAUSAL), kt0, p);
-    const int nmax = n0 > n1 ? n0 : n1;
+    int n0 = tiles_in_range(kv_tiles_for(row_base, p, CAUSAL), kt0, p);
+    int n1 = tiles_in_range(kv_tiles_for(row_base + kRows, p, CAUSAL), kt0, p);
+    int nmax = n0 > n1 ? n0 : n1;
+    // A boolean mask that depends on the key alone (one row of keep bytes for
+    // the whole CTA, as a padding mask is) removes every key tile past its
+    // last kept key: the CTA stops there (keeping at least one tile, so rows
+    // with no kept key still end with O = 0 and LSE = -inf).
+    const bool key_only = MK != 0 && p.mask_kind == 1 && p.msq == 0 && (p.msh == 0 || p.G == 1);
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -343,11 +349,23 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
             if (lane == 0) *cta_v16 = wide ? 0 : 1;
         }
     }
+    if (key_only && warp == 0 && nmax > 0) {
+        const uint8_t* krow_all = static_cast<const uint8_t*>(p.mask) +
+                                  (group / p.Hkv) * p.msb + (group % p.Hkv) * p.msh;
+        const int last = last_kept_key(krow_all, kt0 * kRows, min(p.Nk, (kt0 + nmax) * kRows), lane);
+        if (lane == 0) *key_lim = last < 0 ? 1 : last / kRows + 1 - kt0;
+    }
     if (warp == kMmaWarp0) tmem_alloc(tmem_slot, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if (key_only && nmax > 0) {
+        const int lim = *key_lim;
+        n0 = min(n0, lim);
+        n1 = min(n1, lim);
+        nmax = max(n0, n1);
+    }
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer

@@ -10,6 +10,34 @@
 
 namespace tme {
 
+// Last kept key in [lo, hi) of a row of boolean keep bytes (row 16-byte
+// aligned, lo a multiple of 16), or -1 if none: warp-collective, scanning from
+// the top down -- the ragged tail byte by byte, then 16-byte chunks, 2 KB per
+// warp per round -- so trailing padding costs one round per 2 KB of it.
+__device__ __forceinline__ int last_kept_key(const uint8_t* row, int lo, int hi, int lane) {
+    const int hi16 = hi & ~15;
+    int found = -1;
+    for (int k = hi16 + lane; k < hi; k += 32)
+        if (row[k] != 0) found = k;
+    int last = __reduce_max_sync(0xffffffffu, found);
+    for (int top = hi16; last < 0 && top > lo; top -= 2048) {
+        found = -1;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int c0 = top - 16 * (1 + lane + 32 * u);
+            if (c0 >= lo) {
+                const uint4 w = *reinterpret_cast<const uint4*>(row + c0);
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int q = 3; q >= 0; --q)
+                    if (ws[q] != 0u && found < 0) found = c0 + 4 * q + 3 - (__clz(ws[q]) >> 3);
+            }
+        }
+        last = __reduce_max_sync(0xffffffffu, found);
+    }
+    return last;
+}
+
 // Attention bias (SDPA attn_mask) of one 32-key chunk of a row, applied in
 // the log2 domain: t = s * sl2 + b * log2(e) for an additive bias (16-bit,
 // the input dtype), t = s * sl2 or -inf for a boolean keep-mask (bytes).
