@@ -94,7 +94,7 @@ def kernel_source_hash() -> str:
     change of code voids it."""
     import re
     h = hashlib.sha256()
-    for f in ("attn_fwd.cu", "ptx.cuh"):
+    for f in ("attn_fwd.cu", "ptx.cuh", "bias.cuh", "splitkv.cu", "vconv.cu"):
         with open(os.path.join(ROOT, "tiled_memory_efficient_gb300", "csrc", f)) as fh:
             src = fh.read()
         src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
@@ -260,6 +260,10 @@ def run_ours(args):
         elif decode:
             extra = torch.empty(max(16, _lib.splitkv_workspace_size(
                 w.B, w.Hq, w.Hkv, w.queries(n), n, w.D, splits[n])), device=dev, dtype=torch.uint8)
+        elif args.ws:
+            extra = torch.empty(max(16, _lib.fwd_workspace_size(w.B, w.Hq, w.Hkv, n, n, w.D,
+                                                               w.dtype)),
+                                device=dev, dtype=torch.uint8)
         bufs.append((n, q, k, v, out, lse, x, extra))
     # The head-dim-128 points of the >= 60%-of-peak target (video-DiT at
     # N = 17600 and 75600, the training forward at N = 8192), timed in the
@@ -305,6 +309,8 @@ def run_ours(args):
         elif decode:
             _lib.attn_fwd_splitkv(q, k, v, causal=w.causal, splits=splits[n], out=out, lse=lse,
                                   workspace=extra)
+        elif args.ws:
+            _lib.attn_fwd_ws(q, k, v, causal=w.causal, out=out, lse=lse, workspace=extra)
         else:
             _lib.attn_fwd(q, k, v, causal=w.causal, out=out, lse=lse, mask=x["mask"])
 
@@ -393,7 +399,7 @@ def run_ours(args):
     dom = max(range(len(seq)), key=lambda i: ms_each[i])
     achieved = work[dom] / (ms_each[dom] * 1e-3) / scale
     peak = pk["hbm_gbs"] if decode else pk["bf16_tflops"]
-    traffic = traffic_for(args.config, seq[dom])
+    traffic = traffic_for(args.config + ("_ws" if args.ws else ""), seq[dom])
     if bwd:
         traffic = None
     if decode:
@@ -401,7 +407,8 @@ def run_ours(args):
                   if splits[seq[dom]] > 1 else "attn_fwd_kernel")
         peak_source = f"{pk['source']} HBM copy bandwidth"
     else:
-        kernel = "attn_bwd (stats + dK/dV + dQ kernels)" if bwd else "attn_fwd_kernel"
+        kernel = ("attn_bwd (stats + dK/dV + dQ kernels)" if bwd else
+                  "attn_fwd_ws (v_to_f16_kernel + attn_fwd_kernel)" if args.ws else "attn_fwd_kernel")
         peak_source = f"{pk['source']} bf16 dense (burst; fp16 runs at the same tensor rate)"
     roofline = {"bound": "hbm" if decode else "tensor", "achieved": round(achieved, 1),
                 "peak": peak, "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -852,6 +859,9 @@ def main():
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
                     help="time the forward (default) or the backward")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ws", action="store_true",
+                    help="time attn_fwd_ws (bf16: the value tensor converted to fp16 once per "
+                         "call, into a workspace) instead of attn_fwd")
     ap.add_argument("--no-d128", action="store_true",
                     help="leave the head-dim-128 target points out of the default sweep run")
     ap.add_argument("--mask", choices=["none", "padding", "additive"], default="none",
