@@ -62,6 +62,13 @@ CASES = [
     (1, 3, 3, 300, 4100, 64, BF16, False, (1, 1, 1, 4100), "bool"), # many key tiles, ragged
     # a per-head key mask with G > 1 takes the general masked layout:
     (1, 6, 2, 100, 300, 64, F16, False, (1, 6, 1, 300), "bool"),
+    # D=64 general masks (bias staged in shared memory a key tile ahead):
+    # GQA with partly real warps and a ragged last key tile; many whole key
+    # tiles; heads of 90 rows, so Q tiles and warps span heads
+    (1, 4, 2, 300, 600, 64, F16, False, (1, 4, 300, 600), "additive"),
+    (1, 2, 2, 256, 2048, 64, F16, False, (1, 1, 256, 2048), "additive"),
+    (1, 6, 2, 90, 390, 64, BF16, True, (1, 6, 90, 390), "additive"),
+    (2, 2, 2, 200, 1024, 64, F16, "bottom_right", (2, 2, 200, 1024), "bool"),
 ]
 
 

@@ -141,34 +141,48 @@ __device__ __forceinline__ void next_tile(int& pos, int& head, int Nq) {
 }
 
 // dK/dV layout: a thread owns one key; the bias of its 32 query rows
-// (first row at head `head`, position `pos`, all of them real if row_ok_all,
-// else only rows below `rows_left`) runs down a column of the mask.  The
-// scores in x become log2-domain logits, in place.
-template <bool BF16>
-__device__ __forceinline__ void bias_apply_column(uint32_t (&x)[32], const BwdParams& p,
-                                                  int64_t b_off, int head, int pos, int key,
-                                                  int rows_left, float sl2) {
-    constexpr float kL2e = 1.4426950408889634f;
+// (first row at head `head`, position `pos`, all of them real if rows_left
+// >= 32, else only rows below `rows_left`) runs down a column of the mask.
+// bias_load_column reads that column (raw 16-bit values or bytes; rows and
+// keys outside the problem get the neutral 0 / keep), bias_fold_column turns
+// the scores in x into log2-domain logits with it, in place.
+__device__ __forceinline__ void bias_load_column(uint32_t (&r)[32], const BwdParams& p,
+                                                 int64_t b_off, int head, int pos, int key,
+                                                 int rows_left) {
     const uint8_t* base = static_cast<const uint8_t*>(p.mask);
-    const int esz = p.mask_kind == 2 ? 2 : 1;
+    const bool add = p.mask_kind == 2;
     int64_t off = b_off + static_cast<int64_t>(head) * p.msh + static_cast<int64_t>(pos) * p.msq;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-        float t = __uint_as_float(x[i]) * sl2;
+        uint32_t v = add ? 0u : 1u;
         if (i < rows_left && key < p.Nk) {
-            const uint8_t* e = base + (off + key) * esz;
-            if (p.mask_kind == 2)
-                t += half_to_float<BF16>(*reinterpret_cast<const uint16_t*>(e)) * kL2e;
-            else if (*e == 0)
-                t = -INFINITY;
+            if (add)
+                v = *reinterpret_cast<const uint16_t*>(base + (off + key) * 2);
+            else
+                v = base[off + key];
         }
-        x[i] = __float_as_uint(t);
+        r[i] = v;
         if (++pos == p.Nq) {   // the next row starts the next head
             pos = 0;
             off += p.msh - static_cast<int64_t>(p.Nq - 1) * p.msq;
         } else {
             off += p.msq;
         }
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void bias_fold_column(uint32_t (&x)[32], const uint32_t (&r)[32],
+                                                 int kind, float sl2) {
+    constexpr float kL2e = 1.4426950408889634f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        float t = __uint_as_float(x[i]) * sl2;
+        if (kind == 2)
+            t += half_to_float<BF16>(r[i]) * kL2e;
+        else if (r[i] == 0u)
+            t = -INFINITY;
+        x[i] = __float_as_uint(t);
     }
 }
 
@@ -393,6 +407,19 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         for (int qi = qi0, pos = pos_0; qi < qi1; ++qi, next_tile(pos, head, p.Nq)) {
             if (!visit(qi, pos)) continue;
             const int slot = n % QS;
+            // This chunk's bias column, requested before the waits for the
+            // tile's Q and S (their latency hides the loads').
+            uint32_t bcol[MASK ? 32 : 1];
+            if constexpr (MASK) {
+                int cpos = pos + 32 * c, chead = head;   // first query row of the chunk
+                while (cpos >= p.Nq) {
+                    cpos -= p.Nq;
+                    ++chead;
+                }
+                const int64_t left = p.rows_per_group - static_cast<int64_t>(qi) * kRows - 32 * c;
+                bias_load_column(bcol, p, b_off, head0 + chead, cpos, key,
+                                 left <= 0 ? 0 : left < 32 ? static_cast<int>(left) : 32);
+            }
             warp_wait(&q_full[slot], (n / QS) & 1, abort_flag, p.status);
             warp_wait(&s_full[hq], n & 1, abort_flag, p.status);
             tc_fence_after();
@@ -400,16 +427,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 // this chunk's scores -> logits with the bias, in place in TMEM
                 uint32_t x[32];
                 tmem_ld32(tS, x);
-                int cpos = pos + 32 * c, chead = head;   // first query row of the chunk
-                while (cpos >= p.Nq) {
-                    cpos -= p.Nq;
-                    ++chead;
-                }
-                const int64_t left = p.rows_per_group - static_cast<int64_t>(qi) * kRows - 32 * c;
                 tmem_wait_ld();
                 reg_fence(x);
-                bias_apply_column<BF16>(x, p, b_off, head0 + chead, cpos, key,
-                                        left < 32 ? static_cast<int>(left) : 32, sl2);
+                bias_fold_column<BF16>(x, bcol, p.mask_kind, sl2);
                 tmem_st32(tS, x);
                 tmem_wait_st();
             }

@@ -95,7 +95,14 @@ struct FwdCfg {
     // xl[2 tiles][128][2], xr[2 tiles][128][2] (floats).
     static constexpr int kXOff = kBarOff + 512;
     static constexpr int kXBytes = kSplit ? (4096 + 2048 + 2048) : 0;
-    static constexpr int kSmemBytes = kBarOff + 512 + kXBytes + 1024;
+    // A general mask at D = 64 stages the bias of the next key tile in shared
+    // memory while the softmax works on this one: 8 warps x 32 rows x 256
+    // bytes (a 16-bit additive bias; a boolean one uses half).  At D = 128
+    // shared memory has no room for it and each row reads its bias directly.
+    static constexpr bool kBiasSmem = (MK == 1 && D == 64);
+    static constexpr int kBOff = kXOff + kXBytes;
+    static constexpr int kBiasBytes = kBiasSmem ? 8 * 32 * 256 : 0;
+    static constexpr int kSmemBytes = kBarOff + 512 + kXBytes + kBiasBytes + 1024;
 };
 
 // Flush-to-zero threshold in the log2 domain: a softmax term p = 2^x with
@@ -816,6 +823,15 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
         const int64_t wr1 = min(wr0 + 31, p.rows_per_group - 1);
         const int warp_min_pos =
             (wr0 / p.Nq == wr1 / p.Nq) ? static_cast<int>(wr0 % p.Nq) : 0;
+        // Staged bias (kBiasSmem): this warp's 32 rows, nvalid of them real.
+        // A key tile is staged when it lies inside [0, Nk) and the warp has a
+        // real row; the ragged last tile reads its bias directly.
+        const int64_t left = p.rows_per_group - wr0;
+        const int nvalid = left <= 0 ? 0 : left >= 32 ? 32 : static_cast<int>(left);
+        const uint32_t bbuf = smem_u32(smem + C::kBOff) + warp * (32 * 256);
+        auto staged = [&](int jj) { return nvalid > 0 && (kt0 + jj + 1) * kRows <= p.Nk; };
+        if constexpr (C::kBiasSmem)
+            if (n_t > 0 && staged(0)) bias_prefetch(bbuf, mrow, p.mask_kind, kt0 * kRows, nvalid, lane);
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t tS = tmem + lane_base + t * kRows;
         const uint32_t tO = tmem + lane_base + C::kOCol + t * D;
@@ -841,15 +857,18 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
             if (!warp_wait(&s_full[t], j & 1, abort_flag, p.status)) { ok = false; break; }
             tc_fence_after();
             const int key0 = (kt0 + j) * kRows;
-            if constexpr (MASK) {
+            if constexpr (MASK && !C::kBiasSmem) {
                 // Scores -> log2-domain logits with the bias, in place in TMEM
-                // one 32-key chunk at a time (few live registers); the rest of
-                // the tile then runs with scale 1 (sc below).
+                // one 32-key chunk at a time (few live registers), each chunk's
+                // bias requested one chunk ahead; the rest of the tile then
+                // runs with scale 1 (sc below).
                 const bool full = row_valid && key0 + kRows <= p.Nk;
+                BiasChunk bn;
+                bias_load(bn, mrow, p.mask_kind, key0, full);
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
-                    BiasChunk b;
-                    bias_load(b, mrow, p.mask_kind, key0 + 32 * c, full);
+                    const BiasChunk b = bn;
+                    if (c < 3) bias_load(bn, mrow, p.mask_kind, key0 + 32 * (c + 1), full);
                     uint32_t x[32];
                     tmem_ld32(tS + c * 32, x);
                     tmem_wait_ld();
@@ -870,6 +889,24 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
                 // S_t is in registers: the MMA warp may compute the next S_t.
                 tc_fence_before();
                 mbar_arrive(&s_free[t]);
+            }
+            if constexpr (C::kBiasSmem) {
+                // Scores -> log2-domain logits with the staged bias; then the
+                // next key tile's bias is requested into the same rows.
+                if (staged(j)) {
+                    cp_async_wait_all();
+                    __syncwarp();
+                    bias_fold_smem<BF16>(sr, bbuf, p.mask_kind, sl2, lane);
+                    __syncwarp();
+                } else {
+                    const BiasChunk none{};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        bias_apply<BF16>(sr[c], none, mrow, p.mask_kind, key0 + 32 * c, p.Nk, sl2,
+                                         false, row_valid);
+                }
+                if (j + 1 < n_t && staged(j + 1))
+                    bias_prefetch(bbuf, mrow, p.mask_kind, key0 + kRows, nvalid, lane);
             }
 
             const float sc = MASK ? 1.0f : sl2;   // scale still to apply to sr
@@ -946,6 +983,8 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
             tc_fence_before();
             mbar_arrive(&p_full[t]);
         }
+        // No bias copy may still be in flight when the CTA gives up its shared memory.
+        if constexpr (C::kBiasSmem) cp_async_wait_all();
 
         if (ok && warp_live && n_t > 0 && warp_wait(&o_full[t], 0, abort_flag, p.status)) {
             tc_fence_after();

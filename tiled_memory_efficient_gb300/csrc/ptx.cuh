@@ -148,6 +148,22 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared, cached in L2 only (both
+// addresses 16-byte aligned).  Completion: cp_async_wait_all in the issuing
+// thread, which then sees the data; other threads of the warp see it after a
+// __syncwarp that follows that wait.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src))
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05
 
 // Whole warp: allocate `ncols` TMEM columns, base address written to *dst.
@@ -559,7 +575,6 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 template <bool OUT_BF16, bool ADD = true>
 __device__ __forceinline__ uint32_t softmax_pair(uint32_t s0, uint32_t s1, uint64_t scale2,
                                                  uint64_t negm2, uint64_t& acc) {
-    uint32_t w;
     if constexpr (!ADD) {
         // the accumulator's first pair: acc = p
         float a, b;
@@ -574,6 +589,7 @@ __device__ __forceinline__ uint32_t softmax_pair(uint32_t s0, uint32_t s1, uint6
         acc = f2(a, b);
         return pack2<OUT_BF16>(a, b);
     } else if constexpr (OUT_BF16) {
+        uint32_t w;
         asm("{\n\t.reg .b64 x, p;\n\t.reg .f32 a, b;\n\t"
             "mov.b64 x, {%2, %3};\n\t"
             "fma.rn.f32x2 x, x, %4, %5;\n\t"
@@ -585,7 +601,9 @@ __device__ __forceinline__ uint32_t softmax_pair(uint32_t s0, uint32_t s1, uint6
             "cvt.rn.bf16x2.f32 %0, b, a;\n\t}"
             : "=r"(w), "+l"(acc)
             : "r"(s0), "r"(s1), "l"(scale2), "l"(negm2));
+        return w;
     } else {
+        uint32_t w;
         asm("{\n\t.reg .b64 x, p;\n\t.reg .f32 a, b;\n\t"
             "mov.b64 x, {%2, %3};\n\t"
             "fma.rn.f32x2 x, x, %4, %5;\n\t"
@@ -597,8 +615,8 @@ __device__ __forceinline__ uint32_t softmax_pair(uint32_t s0, uint32_t s1, uint6
             "cvt.rn.f16x2.f32 %0, b, a;\n\t}"
             : "=r"(w), "+l"(acc)
             : "r"(s0), "r"(s1), "l"(scale2), "l"(negm2));
+        return w;
     }
-    return w;
 }
 
 // The softmax term of a score s: p = 2^(s * scale - m) computed exactly as
