@@ -132,6 +132,20 @@ def test_all_true_padding_mask_is_the_unmasked_forward_bitwise(cuda_lib, causal)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_all_true_general_mask_d64_is_the_unmasked_forward_bitwise(cuda_lib, causal):
+    """At D=64 (fp16) a general boolean mask runs in the unmasked kernel's
+    split layout, its bias staged in shared memory, and only drops keys:
+    keeping every key must give the unmasked result bit for bit."""
+    x = inputs.make_custom(1, 6, 2, 300, 700, 64, F16, seed=17)
+    q, k, v = (x[n].cuda() for n in "qkv")
+    a = _lib.attn_fwd(q, k, v, causal=causal)
+    b = _lib.attn_fwd(q, k, v, causal=causal,
+                      mask=torch.ones((1, 6, 300, 700), dtype=torch.bool, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
 def test_sdpa_with_attn_mask(cuda_lib):
     x = inputs.make_custom(2, 4, 2, 200, 200, 64, F16, seed=14)
     mask = make_mask((2, 1, 1, 200), "padding", F16, seed=15, Nk=200)

@@ -206,6 +206,7 @@ int fwd_prepare(const void* q, const void* k, const void* v, void* out, float* l
     p->n_splits = 1;
     p->tiles_per_split = static_cast<int>(key_tiles(Nk));
     p->scale_log2 = scale * 1.4426950408889634f;
+    p->scale = scale;
     p->mask = nullptr;
     p->Hkv = Hkv;
     p->G = Hq / Hkv;

@@ -144,14 +144,27 @@ __device__ __forceinline__ void next_tile(int& pos, int& head, int Nq) {
 // (first row at head `head`, position `pos`, all of them real if rows_left
 // >= 32, else only rows below `rows_left`) runs down a column of the mask.
 // bias_load_column reads that column (raw 16-bit values or bytes; rows and
-// keys outside the problem get the neutral 0 / keep), bias_fold_column turns
-// the scores in x into log2-domain logits with it, in place.
+// keys outside the problem get the neutral 0 / keep); when the 32 rows lie in
+// one head the addresses are one stride apart.  bias_fold_column then turns
+// the scores in x, in place, into natural-log logits s * scale + b (additive;
+// the caller's softmax scale becomes log2 e) or leaves them raw / -inf
+// (boolean).
 __device__ __forceinline__ void bias_load_column(uint32_t (&r)[32], const BwdParams& p,
                                                  int64_t b_off, int head, int pos, int key,
                                                  int rows_left) {
     const uint8_t* base = static_cast<const uint8_t*>(p.mask);
     const bool add = p.mask_kind == 2;
+    const int esz = add ? 2 : 1;
     int64_t off = b_off + static_cast<int64_t>(head) * p.msh + static_cast<int64_t>(pos) * p.msq;
+    if (pos + 32 <= p.Nq && rows_left >= 32 && key < p.Nk) {
+        const uint8_t* e = base + (off + key) * esz;
+        const int64_t step = p.msq * esz;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            r[i] = add ? static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(e + i * step))
+                       : static_cast<uint32_t>(e[i * step]);
+        return;
+    }
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         uint32_t v = add ? 0u : 1u;
@@ -173,16 +186,20 @@ __device__ __forceinline__ void bias_load_column(uint32_t (&r)[32], const BwdPar
 
 template <bool BF16>
 __device__ __forceinline__ void bias_fold_column(uint32_t (&x)[32], const uint32_t (&r)[32],
-                                                 int kind, float sl2) {
-    constexpr float kL2e = 1.4426950408889634f;
+                                                 int kind, float scale) {
+    if (kind == 2) {
+        const uint64_t sc2 = f2(scale, scale);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        float t = __uint_as_float(x[i]) * sl2;
-        if (kind == 2)
-            t += half_to_float<BF16>(r[i]) * kL2e;
-        else if (r[i] == 0u)
-            t = -INFINITY;
-        x[i] = __float_as_uint(t);
+        for (int i = 0; i < 32; i += 2) {
+            const uint64_t t = ffma2(f2(__uint_as_float(x[i]), __uint_as_float(x[i + 1])), sc2,
+                                     f2(half_to_float<BF16>(r[i]), half_to_float<BF16>(r[i + 1])));
+            x[i] = __float_as_uint(f2lo(t));
+            x[i + 1] = __float_as_uint(f2hi(t));
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (r[i] == 0u) x[i] = __float_as_uint(-INFINITY);
     }
 }
 
@@ -399,7 +416,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         const uint32_t lb = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t tS = tmem + lb + 128 * hq + 32 * cc, tDP = tS + 64;
         const float sl2 = p.scale_log2;
-        const float sc = MASK ? 1.0f : sl2;   // scale still to apply to the scores read below
+        // scale still to apply to the scores read below: an additive bias
+        // leaves natural-log logits (log2 e), a boolean one raw scores
+        const float sc = (MASK && p.mask_kind == 2) ? kLog2e : sl2;
         const int64_t b_off = MASK ? static_cast<int64_t>(group / p.Hkv) * p.msb : 0;
         const int head0 = MASK ? (group % p.Hkv) * p.G : 0;
         int n = 0;
@@ -429,7 +448,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 tmem_ld32(tS, x);
                 tmem_wait_ld();
                 reg_fence(x);
-                bias_fold_column<BF16>(x, bcol, p.mask_kind, sl2);
+                bias_fold_column<BF16>(x, bcol, p.mask_kind, p.scale);
                 tmem_st32(tS, x);
                 tmem_wait_st();
             }

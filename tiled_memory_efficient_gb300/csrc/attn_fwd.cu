@@ -53,7 +53,9 @@ constexpr float kRescaleThreshold = 8.0f;
 template <int D, int MK = 0, bool BF16 = false, bool VPRE = false>
 struct FwdCfg {
     static constexpr int kTileBytes = kRows * D * 2;         // one 128 x D tile, 16-bit
-    static constexpr int kKStages = (D == 128) ? 2 : 4;   // D = 128: shared memory is full
+    // D = 128: shared memory is full.  A general mask at D = 64 (fp16) gives
+    // one K stage to its staged bias.
+    static constexpr int kKStages = (D == 128) ? 2 : (MK == 1 && !BF16) ? 3 : 4;
     static constexpr int kVStages = (D == 128) ? 3 : 4;   // D = 128: 225.5 KB in all
     static constexpr int kQOff = 0;
     static constexpr int kKOff = kQOff + 2 * kTileBytes;
@@ -74,12 +76,11 @@ struct FwdCfg {
     //  D=64:  the softmax is the bottleneck, so every row is split over two
     //         warps of 64 keys each: warps 0-15 softmax (Q tile (w/4)%2, key
     //         half w/8), warp 16 producer, warps 17/18 MMA issuers.
-    // (A general mask, MK = 1, keeps one thread per 128-key row at D = 64
-    // too: its bias loads need the registers the split layout does not have.
-    // A key-only mask, MK = 2, needs 16 bytes per lane and runs split.  bf16
-    // inputs keep one thread per row as well: their value-tile converters
-    // take the warps that layout leaves idle.)
-    static constexpr bool kSplit = (D == 64 && MK != 1 && !BF16);
+    // (Masks at D = 64 run split too: a key-only mask, MK = 2, with 16 keep
+    // bytes per lane; a general bias, MK = 1, staged in shared memory.  bf16
+    // inputs keep one thread per row: their value-tile converters take the
+    // warps that layout leaves idle.)
+    static constexpr bool kSplit = (D == 64 && !BF16);
     static constexpr int kSoftmaxWarps = kSplit ? 16 : 8;
     static constexpr int kProducerWarp = kSplit ? 16 : 11;
     static constexpr int kMmaWarp0 = kSplit ? 17 : 9;
@@ -96,9 +97,11 @@ struct FwdCfg {
     static constexpr int kXOff = kBarOff + 512;
     static constexpr int kXBytes = kSplit ? (4096 + 2048 + 2048) : 0;
     // A general mask at D = 64 stages the bias of the next key tile in shared
-    // memory while the softmax works on this one: 8 warps x 32 rows x 256
-    // bytes (a 16-bit additive bias; a boolean one uses half).  At D = 128
-    // shared memory has no room for it and each row reads its bias directly.
+    // memory while the softmax works on this one: 32 rows x 256 bytes for
+    // each of 8 warps (one thread per row), or 32 rows x 128 bytes (half a
+    // row) for each of 16 (split); 16-bit additive, a boolean one uses half.
+    // At D = 128 shared memory has no room for it and each row reads its
+    // bias directly.
     static constexpr bool kBiasSmem = (MK == 1 && D == 64);
     static constexpr int kBOff = kXOff + kXBytes;
     static constexpr int kBiasBytes = kBiasSmem ? 8 * 32 * 256 : 0;
@@ -239,8 +242,8 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
                     const __grid_constant__ CUtensorMap tmV,
                     const __grid_constant__ CUtensorMap tmV16, const FwdParams p) {
     using C = FwdCfg<D, MK, BF16, VPRE>;
-    constexpr bool MASK = MK == 1;      // general bias: the one-thread-per-row layout
-    constexpr bool KEYMASK = MK == 2;   // key-only keep-mask: the split layout
+    constexpr bool MASK = MK == 1;      // general bias
+    constexpr bool KEYMASK = MK == 2;   // key-only keep-mask (split layout)
     constexpr int KS = C::kKStages, VS = C::kVStages;
     constexpr int kProducerWarp = C::kProducerWarp;
     constexpr int kMmaWarp0 = C::kMmaWarp0;
@@ -593,6 +596,28 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
         const int64_t wr1 = min(wr0 + 31, p.rows_per_group - 1);
         const int warp_min_pos =
             (wr0 / p.Nq == wr1 / p.Nq) ? static_cast<int>(wr0 % p.Nq) : 0;
+        // General bias (MK = 1): this row's bias row (query head hkv*G +
+        // row/Nq of batch group/Hkv), staged one key tile ahead: this warp's
+        // 32 rows x 64 keys, nvalid rows real.  A half-tile is staged when its
+        // keys lie inside [0, Nk); the ragged one reads its bias directly.
+        // An additive bias turns the scores into natural-log logits s * scale
+        // + b, so the softmax scale below becomes log2(e).
+        const uint8_t* mrow = nullptr;
+        if constexpr (MASK) {
+            const int64_t hq = static_cast<int64_t>(group % p.Hkv) * p.G + row / p.Nq;
+            const int64_t bq = group / p.Hkv;
+            mrow = static_cast<const uint8_t*>(p.mask) +
+                   (bq * p.msb + hq * p.msh + pos * p.msq) * (p.mask_kind == 2 ? 2 : 1);
+        }
+        const int64_t wleft = p.rows_per_group - wr0;
+        const int nvalid = wleft <= 0 ? 0 : wleft >= 32 ? 32 : static_cast<int>(wleft);
+        const uint32_t bbuf = smem_u32(smem + C::kBOff) + warp * (32 * 128);
+        auto staged = [&](int jj) {
+            return nvalid > 0 && (kt0 + jj) * kRows + 64 * h + 64 <= p.Nk;
+        };
+        if constexpr (MASK)
+            if (n_t > 0 && staged(0))
+                bias_prefetch<64>(bbuf, mrow, p.mask_kind, kt0 * kRows + 64 * h, nvalid, lane);
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t tS = tmem + lane_base + t * kRows + 64 * h;
         const uint32_t tO = tmem + lane_base + C::kOCol + t * D;
@@ -606,7 +631,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
         const uint32_t xr_slot = x_slot + 6144;
         const uint32_t pair_bar = 1 + t * 4 + quad;  // named barrier of the warp pair
         uint32_t xbuf = 0;                           // 0 / 2048: buffer of key tile j
-        const float sl2 = p.scale_log2;
+        const float sl2 = (MASK && p.mask_kind == 2) ? 1.4426950408889634f : p.scale_log2;
 
         float m = -INFINITY;  // running max (log2 domain, scaled), same in both halves
         float l = 0.0f;       // this half's running sum of p
@@ -670,6 +695,18 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
             tc_fence_before();
             mbar_arrive(&s_free[t]);
 
+            if constexpr (MASK) {
+                if (staged(j)) {
+                    cp_async_wait_all();
+                    __syncwarp();
+                    bias_fold_smem64<BF16>(sr, bbuf, p.mask_kind, p.scale, lane);
+                    __syncwarp();
+                } else {
+                    bias_fold_direct64<BF16>(sr, mrow, p.mask_kind, key0, p.Nk, p.scale, row_valid);
+                }
+                if (j + 1 < n_t && staged(j + 1))
+                    bias_prefetch<64>(bbuf, mrow, p.mask_kind, key0 + kRows, nvalid, lane);
+            }
             if constexpr (KEYMASK) {
                 uint32_t mn = __vminu4(__vminu4(kcur.x, kcur.y), __vminu4(kcur.z, kcur.w));
                 mn = __vminu4(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
@@ -764,6 +801,8 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
             tc_fence_before();
             mbar_arrive(&p_full[t]);
         }
+        // No bias copy may still be in flight when the CTA gives up its shared memory.
+        if constexpr (MASK) cp_async_wait_all();
 
         if (n_t > 0 && warp_live) {
             warp_wait(&o_full[t], 0, abort_flag, p.status);
@@ -831,7 +870,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
         const uint32_t bbuf = smem_u32(smem + C::kBOff) + warp * (32 * 256);
         auto staged = [&](int jj) { return nvalid > 0 && (kt0 + jj + 1) * kRows <= p.Nk; };
         if constexpr (C::kBiasSmem)
-            if (n_t > 0 && staged(0)) bias_prefetch(bbuf, mrow, p.mask_kind, kt0 * kRows, nvalid, lane);
+            if (n_t > 0 && staged(0)) bias_prefetch<128>(bbuf, mrow, p.mask_kind, kt0 * kRows, nvalid, lane);
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t tS = tmem + lane_base + t * kRows;
         const uint32_t tO = tmem + lane_base + C::kOCol + t * D;
@@ -854,17 +893,19 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
                 warp_wait(&p_full[t], j & 1, abort_flag, p.status);
                 continue;
             }
+            const int key0 = (kt0 + j) * kRows;
+            // D = 128 with a general mask: the first bias chunk is requested
+            // before the wait for S, each later one a chunk ahead.
+            const bool bfull = MASK && row_valid && key0 + kRows <= p.Nk;
+            BiasChunk bn;
+            if constexpr (MASK && !C::kBiasSmem) bias_load(bn, mrow, p.mask_kind, key0, bfull);
             if (!warp_wait(&s_full[t], j & 1, abort_flag, p.status)) { ok = false; break; }
             tc_fence_after();
-            const int key0 = (kt0 + j) * kRows;
             if constexpr (MASK && !C::kBiasSmem) {
                 // Scores -> log2-domain logits with the bias, in place in TMEM
-                // one 32-key chunk at a time (few live registers), each chunk's
-                // bias requested one chunk ahead; the rest of the tile then
-                // runs with scale 1 (sc below).
-                const bool full = row_valid && key0 + kRows <= p.Nk;
-                BiasChunk bn;
-                bias_load(bn, mrow, p.mask_kind, key0, full);
+                // one 32-key chunk at a time (few live registers); the rest of
+                // the tile then runs with scale 1 (sc below).
+                const bool full = bfull;
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
                     const BiasChunk b = bn;
@@ -906,7 +947,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
                                          false, row_valid);
                 }
                 if (j + 1 < n_t && staged(j + 1))
-                    bias_prefetch(bbuf, mrow, p.mask_kind, key0 + kRows, nvalid, lane);
+                    bias_prefetch<128>(bbuf, mrow, p.mask_kind, key0 + kRows, nvalid, lane);
             }
 
             const float sc = MASK ? 1.0f : sl2;   // scale still to apply to sr

@@ -41,6 +41,7 @@ struct FwdParams {
     int n_splits;            // key ranges (1: no split)
     int tiles_per_split;     // 128-key tiles per range
     float scale_log2;        // scale * log2(e)
+    float scale;             // softmax scale (a general additive bias is added after it)
     // Optional attention bias (masked kernels only): element (b, h, i, j) at
     // mask + b*msb + h*msh + i*msq + j elements; kind 1: bytes, nonzero keeps
     // the key; kind 2: additive, 16-bit in the input dtype.

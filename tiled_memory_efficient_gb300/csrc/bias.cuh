@@ -115,42 +115,36 @@ __device__ __forceinline__ void bias_apply(uint32_t (&s)[32], const BiasChunk& b
     }
 }
 
-// Shared-memory staging of the bias of one 128-key tile for the 32 rows of a
-// warp, one row per lane.  Row r occupies row_bytes = 256 (additive, 16-bit)
-// or 128 (boolean bytes) at buf + r * row_bytes, its 16-byte chunk q stored at
-// chunk position q ^ (r & 7): the eight lanes of one quarter-warp read the
-// same chunk of eight consecutive rows from eight different bank groups.
+// Shared-memory staging of the bias of one key tile (KEYS = 128 keys, or the
+// 64 keys of one half of a 128-key tile) for the 32 rows of a warp, one row
+// per lane.  Row r occupies KEYS * 2 bytes at buf + r * KEYS * 2 (room for a
+// 16-bit additive bias; a boolean one uses the first half), its 16-byte chunk
+// q stored at chunk position q ^ (r & 7): the eight lanes of one quarter-warp
+// read the same chunk of eight consecutive rows from eight different bank
+// groups.
 //
-// bias_prefetch (warp-collective) issues the copies of the tile at key0 with
-// cp.async, two (additive) or four (boolean) whole rows per instruction, so
-// each instruction touches whole 128-byte lines.  row_ptr is the lane's own
-// bias row; rows r >= nvalid (1 <= nvalid <= 32) copy row nvalid - 1, so
-// every staged value is a real bias value.  The key tile must lie inside
-// [0, Nk).  Wait with cp_async_wait_all and then __syncwarp before reading.
+// bias_prefetch (warp-collective) issues the copies of the keys [key0, key0 +
+// KEYS) with cp.async, whole rows per instruction (a row's chunks on
+// consecutive lanes), so each instruction touches whole 64- or 128-byte
+// spans.  row_ptr is the lane's own bias row; rows r >= nvalid (1 <= nvalid
+// <= 32) copy row nvalid - 1, so every staged value is a real bias value.
+// The keys must lie inside [0, Nk).  Wait with cp_async_wait_all and then
+// __syncwarp before reading.
+template <int KEYS>
 __device__ __forceinline__ void bias_prefetch(uint32_t buf, const uint8_t* row_ptr, int kind,
                                               int key0, int nvalid, int lane) {
     const unsigned long long mine = reinterpret_cast<uintptr_t>(row_ptr);
-    if (kind == 2) {
-        const int q = lane & 15;
+    const int esz = kind == 2 ? 2 : 1;
+    const int cshift = kind == 2 ? (KEYS == 128 ? 4 : 3) : (KEYS == 128 ? 3 : 2);  // log2 chunks per row
+    const int q = lane & ((1 << cshift) - 1);
+    const int n_ins = 1 << cshift;   // instructions: 32 rows / (32 >> cshift) rows each
 #pragma unroll 2
-        for (int i = 0; i < 16; ++i) {
-            const int r = 2 * i + (lane >> 4);
-            const unsigned long long base = __shfl_sync(0xffffffffu, mine, min(2 * i + 1, nvalid - 1));
-            const unsigned long long base0 = __shfl_sync(0xffffffffu, mine, min(2 * i, nvalid - 1));
-            const uint8_t* src = reinterpret_cast<const uint8_t*>((lane >> 4) ? base : base0) +
-                                 2 * static_cast<int64_t>(key0) + 16 * q;
-            cp_async16(buf + r * 256 + ((q ^ (r & 7)) << 4), src);
-        }
-    } else {
-        const int q = lane & 7;
-#pragma unroll 2
-        for (int i = 0; i < 8; ++i) {
-            const int r = 4 * i + (lane >> 3);
-            const unsigned long long base =
-                __shfl_sync(0xffffffffu, mine, min(r, nvalid - 1));
-            const uint8_t* src = reinterpret_cast<const uint8_t*>(base) + key0 + 16 * q;
-            cp_async16(buf + r * 128 + ((q ^ (r & 7)) << 4), src);
-        }
+    for (int i = 0; i < n_ins; ++i) {
+        const int r = (i << (5 - cshift)) + (lane >> cshift);
+        const unsigned long long base = __shfl_sync(0xffffffffu, mine, min(r, nvalid - 1));
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(base) +
+                             static_cast<int64_t>(key0) * esz + 16 * q;
+        cp_async16(buf + r * (2 * KEYS) + ((q ^ (r & 7)) << 4), src);
     }
     cp_async_commit();
 }
@@ -162,7 +156,7 @@ template <bool BF16>
 __device__ __forceinline__ void bias_fold_smem(uint32_t (&s)[4][32], uint32_t buf, int kind,
                                                float sl2, int lane) {
     constexpr float kLog2e = 1.4426950408889634f;
-    const uint32_t rbase = buf + lane * (kind == 2 ? 256 : 128);
+    const uint32_t rbase = buf + lane * 256;
     const int sw = lane & 7;
     if (kind == 2) {
         const uint64_t sl22 = f2(sl2, sl2), l2e2 = f2(kLog2e, kLog2e);
@@ -200,6 +194,75 @@ __device__ __forceinline__ void bias_fold_smem(uint32_t (&s)[4][32], uint32_t bu
             }
         }
     }
+}
+
+// Split layout (each row's 128-key tile in two halves of 64 keys, one per
+// warp): the half's 64 scores become natural-log-domain logits u = s * scale
+// + b (additive; the softmax then takes 2^(u * log2 e - m)) or stay raw
+// scores / -inf (boolean; the softmax keeps its scale * log2 e).
+// bias_fold_smem64 reads the staged half-row (bias_prefetch<64>),
+// bias_fold_direct64 reads the bias row directly key by key (keys >= Nk and
+// unreal rows: no bias).  Both compute the same fused multiply-add.
+template <bool BF16>
+__device__ __forceinline__ void bias_fold_smem64(uint32_t (&s)[2][32], uint32_t buf, int kind,
+                                                 float scale, int lane) {
+    const uint32_t rbase = buf + lane * 128;
+    const int sw = lane & 7;
+    if (kind == 2) {
+        const uint64_t sc2 = f2(scale, scale);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            uint32_t w[4];
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                         : "r"(rbase + ((q ^ sw) << 4)));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int k = 8 * q + 2 * e;
+                uint32_t& a = s[k >> 5][k & 31];
+                uint32_t& b = s[k >> 5][(k & 31) + 1];
+                const uint64_t t =
+                    ffma2(f2(__uint_as_float(a), __uint_as_float(b)), sc2,
+                          f2(half_to_float<BF16>(w[e] & 0xffffu), half_to_float<BF16>(w[e] >> 16)));
+                a = __float_as_uint(f2lo(t));
+                b = __float_as_uint(f2hi(t));
+            }
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t w[4];
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                         : "r"(rbase + ((q ^ sw) << 4)));
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int k = 16 * q + i;
+                if (((w[i >> 2] >> (8 * (i & 3))) & 0xffu) == 0u)
+                    s[k >> 5][k & 31] = __float_as_uint(-INFINITY);
+            }
+        }
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void bias_fold_direct64(uint32_t (&s)[2][32], const uint8_t* row,
+                                                   int kind, int key0, int Nk, float scale,
+                                                   bool row_ok) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int key = key0 + 32 * c + i;
+            const bool in = row_ok && key < Nk;
+            if (kind == 2) {
+                const float b =
+                    in ? half_to_float<BF16>(reinterpret_cast<const uint16_t*>(row)[key]) : 0.0f;
+                s[c][i] = __float_as_uint(fmaf(__uint_as_float(s[c][i]), scale, b));
+            } else if (in && row[key] == 0) {
+                s[c][i] = __float_as_uint(-INFINITY);
+            }
+        }
 }
 
 }  // namespace tme
