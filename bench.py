@@ -236,6 +236,11 @@ def run_ours(args):
     if decode and bwd:
         raise SystemExit("the decode workload has no backward pass")
     splits = {n: _lib.num_splits(w.B, w.Hq, w.Hkv, w.queries(n), n, w.D) for n in seq}
+    # the unmasked forward goes through attn_fwd_ws (its workspace allocated
+    # here, outside the timed region); --plain times attn_fwd
+    use_ws = not (args.plain or bwd or decode or args.mask != "none")
+    ws_splits = {n: _lib.fwd_ws_splits(w.B, w.Hq, w.Hkv, n, n, w.D, w.causal) if use_ws else 1
+                 for n in seq}
     if args.mask != "none" and decode:
         raise SystemExit("--mask is for the prefill / training workloads")
     # inputs resident in HBM before the timed region
@@ -260,7 +265,7 @@ def run_ours(args):
         elif decode:
             extra = torch.empty(max(16, _lib.splitkv_workspace_size(
                 w.B, w.Hq, w.Hkv, w.queries(n), n, w.D, splits[n])), device=dev, dtype=torch.uint8)
-        elif args.ws:
+        elif use_ws:
             extra = torch.empty(max(16, _lib.fwd_workspace_size(w.B, w.Hq, w.Hkv, n, n, w.D,
                                                                w.dtype)),
                                 device=dev, dtype=torch.uint8)
@@ -309,7 +314,7 @@ def run_ours(args):
         elif decode:
             _lib.attn_fwd_splitkv(q, k, v, causal=w.causal, splits=splits[n], out=out, lse=lse,
                                   workspace=extra)
-        elif args.ws:
+        elif use_ws:
             _lib.attn_fwd_ws(q, k, v, causal=w.causal, out=out, lse=lse, workspace=extra)
         else:
             _lib.attn_fwd(q, k, v, causal=w.causal, out=out, lse=lse, mask=x["mask"])
@@ -399,7 +404,7 @@ def run_ours(args):
     dom = max(range(len(seq)), key=lambda i: ms_each[i])
     achieved = work[dom] / (ms_each[dom] * 1e-3) / scale
     peak = pk["hbm_gbs"] if decode else pk["bf16_tflops"]
-    traffic = traffic_for(args.config + ("_ws" if args.ws else ""), seq[dom])
+    traffic = traffic_for(args.config, seq[dom]) if (use_ws or decode or bwd) else None
     if bwd:
         traffic = None
     if decode:
@@ -408,7 +413,9 @@ def run_ours(args):
         peak_source = f"{pk['source']} HBM copy bandwidth"
     else:
         kernel = ("attn_bwd (stats + dK/dV + dQ kernels)" if bwd else
-                  "attn_fwd_ws (v_to_f16_kernel + attn_fwd_kernel)" if args.ws else "attn_fwd_kernel")
+                  "attn_fwd_kernel" if not use_ws else
+                  "attn_fwd_ws: " + ("v_to_f16_kernel + " if w.dtype == torch.bfloat16 else "") +
+                  "attn_fwd_kernel" + (" + splitkv_merge_kernel" if ws_splits[seq[dom]] > 1 else ""))
         peak_source = f"{pk['source']} bf16 dense (burst; fp16 runs at the same tensor rate)"
     roofline = {"bound": "hbm" if decode else "tensor", "achieved": round(achieved, 1),
                 "peak": peak, "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -497,8 +504,20 @@ def run_ours(args):
         sweep = [{"N": n, "ms": round(ms, 4), "tflops": round(f / (ms * 1e-3) / 1e12, 1),
                   "frac_of_peak": round(f / (ms * 1e-3) / 1e12 / peak, 4)}
                  for n, ms, f in zip(seq, ms_each, flops)]
-    launches_per_step = sum((2 if splits[n] > 1 else 1) if decode else (3 if bwd else 1)
-                            for n in seq) + 3 * len(d128) + 4 * len(bwdp)
+    def fwd_launches(wd, n, ws_call):
+        if not ws_call:
+            return 1
+        return (1 + (wd.dtype == torch.bfloat16) +
+                (_lib.fwd_ws_splits(wd.B, wd.Hq, wd.Hkv, n, n, wd.D, wd.causal) > 1))
+
+    def bwd_launches(wd, n):
+        return 3 + (_lib.bwd_splits(wd.B, wd.Hq, wd.Hkv, n, n, wd.D) > 1)
+
+    launches_per_step = (
+        sum((2 if splits[n] > 1 else 1) if decode else bwd_launches(w, n) if bwd else
+            fwd_launches(w, n, use_ws) for n in seq) +
+        sum(fwd_launches(wd, n, True) + 1 for wd, n, *_ in d128) +
+        sum(bwd_launches(wd, n) for wd, n, *_ in bwdp))
     bwd_rep = None
     if bwdp:
         pts = []
@@ -859,9 +878,10 @@ def main():
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
                     help="time the forward (default) or the backward")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--ws", action="store_true",
-                    help="time attn_fwd_ws (bf16: the value tensor converted to fp16 once per "
-                         "call, into a workspace) instead of attn_fwd")
+    ap.add_argument("--plain", action="store_true",
+                    help="time attn_fwd instead of attn_fwd_ws (the default for unmasked "
+                         "forwards: bf16 value tiles converted once per call into a workspace, "
+                         "unevenly filled grids cut into key ranges)")
     ap.add_argument("--no-d128", action="store_true",
                     help="leave the head-dim-128 target points out of the default sweep run")
     ap.add_argument("--mask", choices=["none", "padding", "additive"], default="none",

@@ -94,11 +94,20 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
  * other reads v and packs P as bf16.  The results agree with attn_fwd's to
  * rounding; this call runs about 20% faster at D = 128.
  *
+ * The workspace also lets this call even out the grid (both dtypes).  attn_fwd
+ * runs one CTA per SM-sized unit (KV group, pair of 128-row query tiles), so a
+ * grid of U units runs as ceil(U / SMs) waves.  When the last wave's units,
+ * cut into two key halves, fit in one wave (no causal mask, >= 8 key tiles),
+ * or when the whole grid is under one wave (every unit cut into ranges of >= 16
+ * key tiles), the cut units write fp32 partial results to the workspace and a
+ * second kernel merges them (the online-softmax identity of attn_fwd_splitkv).
+ * The rows of uncut units are attn_fwd's bit for bit (fp16); merged rows agree
+ * with them to rounding.
+ *
  * workspace: a 16-byte-aligned device buffer of at least
  * attn_fwd_workspace_size() bytes (ATTN_ERR_WORKSPACE if smaller, checked
  * before anything is launched); its contents on entry do not matter, and the
- * call writes it.  For fp16 inputs no workspace is needed (size 0; it may be
- * NULL) and the call is attn_fwd.
+ * call writes it.  When that size is 0 (fp16 with no cut) it may be NULL.
  */
 int attn_fwd_ws(const void* q, const void* k, const void* v, void* out, float* lse,
                 void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int Nq, int Nk,
@@ -106,10 +115,22 @@ int attn_fwd_ws(const void* q, const void* k, const void* v, void* out, float* l
 
 /*
  * Workspace bytes attn_fwd_ws needs: for bf16, B*Hkv*Nk*D*2 (the fp16 copy of
- * v) plus B*Hkv*ceil(Nk/128) flag bytes, each part padded to 256 bytes; 0 for
- * fp16 and for invalid sizes.  Host-only.
+ * v) plus B*Hkv*ceil(Nk/128) flag bytes; for a grid that is cut (above), S
+ * ranges times R rows of D + 1 fp32 values (the cut units' partial outputs and
+ * LSEs); each part padded to 256 bytes.  0 for invalid sizes.  The cut depends
+ * on the SM count of the current device (queried here; no cut without a
+ * device) and is planned for the non-causal case, which covers the causal
+ * one.  Host-only.
  */
 size_t attn_fwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int D, int dtype);
+
+/*
+ * Key ranges attn_fwd_ws cuts its cut units into for this shape and causal
+ * mode on the current device: 1 when the grid is not cut (one forward
+ * kernel, plus the value conversion for bf16), > 1 when a merge kernel
+ * follows.  0 for invalid sizes.  Host-only.
+ */
+int attn_fwd_ws_splits(int B, int Hq, int Hkv, int Nq, int Nk, int D, int causal);
 
 /*
  * Forward with an attention bias: the attn_mask argument of the SDPA call
@@ -188,6 +209,14 @@ int attn_fwd_num_splits(int B, int Hq, int Hkv, int Nq, int Nk, int D, int num_s
  * SM count (without one: the statistics alone).
  */
 size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int D, int dtype);
+
+/*
+ * The number S of query ranges attn_bwd cuts the dK/dV work into at these
+ * sizes on the current device, given the workspace attn_bwd_workspace_size()
+ * recommends: 1 (three kernels: statistics, dK/dV, dQ) or more (a fourth adds
+ * the ranges' partial sums).  0 for invalid sizes.  Host-only.
+ */
+int attn_bwd_splits(int B, int Hq, int Hkv, int Nq, int Nk, int D);
 
 /*
  * Backward of attn_fwd (forum post, "Other areas where this could be useful":

@@ -22,7 +22,8 @@ def test_header_declares_the_boundary():
                      "attn_strerror", "attn_selftest_timeout", "attn_version", "attn_fwd_splitkv",
                      "attn_fwd_splitkv_workspace_size", "attn_fwd_num_splits", "attn_fwd_masked",
                      "attn_bwd_masked", "ffn_forward", "ffn_check_chunking",
-                     "ffn_workspace_size", "attn_fwd_ws", "attn_fwd_workspace_size"):
+                     "ffn_workspace_size", "attn_fwd_ws", "attn_fwd_workspace_size",
+                     "attn_fwd_ws_splits", "attn_bwd_splits"):
         assert required in names
 
 
@@ -101,6 +102,12 @@ def test_fwd_ws_workspace_size_and_validation(lib):
     assert lib.attn_fwd_ws(*([P] * 5), P + 8, ws, *args) == 3      # misaligned workspace
     assert lib.attn_fwd_ws(*([P] * 5), P, ws - 1, *args) == 6      # too small
     assert lib.attn_fwd_ws(*([P] * 5), P, ws, 1, 2, 2, 128, 128, 96, 0.125, 0, 1, None) == 2
+    # plan queries: small grids whose ranges would be under 4 key tiles (or no
+    # device) are not cut; invalid sizes give 0
+    assert lib.attn_fwd_ws_splits(1, 2, 2, 300, 300, 64, 0) == 1
+    assert lib.attn_fwd_ws_splits(1, 3, 2, 300, 300, 64, 0) == 0
+    assert lib.attn_bwd_splits(1, 2, 2, 300, 300, 64) == 1
+    assert lib.attn_bwd_splits(1, 3, 2, 300, 300, 64) == 0
 
 
 def test_bwd_rejects_bottom_right(lib):

@@ -298,11 +298,86 @@ def test_value_tile_beyond_fp16_range_stays_bf16(cuda_lib, path):
 
 
 def test_ws_fp16_is_attn_fwd(cuda_lib):
+    """fp16 with a grid that is not cut: attn_fwd itself, no workspace."""
     x = inputs.make_custom(1, 2, 2, 300, 300, 64, F16, seed=43)
     assert _lib.fwd_workspace_size(1, 2, 2, 300, 300, 64, F16) == 0
     a = run_fwd(x, True)
     b = run_fwd_ws(x, True)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+# attn_fwd_ws also evens out the grid (one CTA per SM per unit of a KV group
+# and 256 query rows): the last wave's units are cut into two key halves when
+# the halves fit in one wave (no causal mask, >= 8 key tiles), and a grid under
+# one wave has every unit's keys cut into ranges of >= 16 key tiles; the cut
+# units' partials are merged by a second kernel.  The shapes below are cut on
+# a 152-SM GB300.
+
+CUT_SHAPES = [
+    # B, Hq, Hkv, Nq, Nk, D, dtype, causal
+    (1, 4, 4, 10240, 1000, 64, F16, False),    # 160 units: 152 whole, 8 in halves; ragged keys
+    (1, 8, 2, 5120, 1100, 64, F16, False),     # GQA 4:1, 9 key tiles: halves of 5 and 4
+    (1, 4, 4, 10240, 1000, 128, BF16, False),  # bf16 with the fp16 copy of V
+    (1, 2, 2, 1000, 8000, 64, F16, False),     # 8 units: 3 ranges of 21 key tiles (the last 21)
+    (1, 2, 2, 1000, 8000, 64, F16, "bottom_right"),  # causal: a range may hold no visible key
+    (2, 6, 2, 300, 4200, 128, BF16, "bottom_right"),  # GQA 3:1, 2 ranges of 17 and 16
+]
+
+
+def cut_plan(B, Hq, Hkv, Nq, Nk, causal, sms):
+    """(first output row of the cut units, ranges) as the library plans it."""
+    rows = Hq // Hkv * Nq
+    n_pairs = -(-rows // 256)
+    units = B * Hkv * n_pairs
+    tiles = -(-Nk // 128)
+    if units >= sms:
+        waves = -(-units // sms)
+        tail = units - (waves - 1) * sms
+        if causal or tiles < 8 or waves < 2 or 2 * tail > sms:
+            return None, 1
+        whole = units - tail
+        return (whole // n_pairs) * rows + (whole % n_pairs) * 256, 2
+    want = min(sms // units, tiles // 16, 256)
+    if want < 2:
+        return None, 1
+    tps = -(-tiles // want)
+    return 0, -(-tiles // tps)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,D,dtype,causal", CUT_SHAPES)
+def test_ws_cut_grid_every_row(cuda_lib, B, Hq, Hkv, Nq, Nk, D, dtype, causal):
+    """Every row against the oracle; the rows of whole units are attn_fwd's
+    bit for bit (fp16: the same kernel arithmetic), the merged rows agree
+    with the oracle at the usual bound."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    row0, splits = cut_plan(B, Hq, Hkv, Nq, Nk, bool(causal), sms)
+    if sms == 152:
+        assert splits > 1
+    ws = _lib.fwd_workspace_size(B, Hq, Hkv, Nq, Nk, D, dtype)
+    assert (ws > 0) == (splits > 1 or dtype == BF16)
+    x = inputs.make_custom(B, Hq, Hkv, Nq, Nk, D, dtype, seed=Nq + 3 * Nk + D)
+    check_ws(x, causal, f"cut grid {(B, Hq, Hkv, Nq, Nk, D, causal)}")
+    if dtype == F16 and row0 is not None:
+        a_o, a_l = run_fwd(x, causal)
+        b_o, b_l = run_fwd_ws(x, causal)
+        a_o, b_o = a_o.reshape(-1, D), b_o.reshape(-1, D)
+        a_l, b_l = a_l.reshape(-1), b_l.reshape(-1)
+        assert torch.equal(a_o[:row0], b_o[:row0]) and torch.equal(a_l[:row0], b_l[:row0])
+
+
+def test_ws_cut_workspace_is_checked(cuda_lib):
+    """A cut fp16 grid needs its workspace: a smaller one is refused before
+    anything runs."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms != 152:
+        pytest.skip("the cut shape is planned for 152 SMs")
+    ws = _lib.fwd_workspace_size(1, 4, 4, 10240, 1000, 64, F16)
+    assert ws > 0
+    x = inputs.make_custom(1, 4, 4, 10240, 1000, 64, F16, seed=5)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    small = torch.empty(ws - 256, device="cuda", dtype=torch.uint8)
+    with pytest.raises(_lib.AttnError):
+        _lib.attn_fwd_ws(q, k, v, workspace=small)
 
 
 @pytest.mark.parametrize("D,dtype", [(64, F16), (128, BF16)])

@@ -54,6 +54,8 @@ _SIGNATURES = {
     "attn_fwd_ws": ([_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _i, _i, _i, _i, _i, _i,
                      ctypes.c_float, _i, _i, _vp], _i),
     "attn_fwd_workspace_size": ([_i, _i, _i, _i, _i, _i, _i], ctypes.c_size_t),
+    "attn_fwd_ws_splits": ([_i, _i, _i, _i, _i, _i, _i], _i),
+    "attn_bwd_splits": ([_i, _i, _i, _i, _i, _i], _i),
     "attn_fwd_num_splits": ([_i, _i, _i, _i, _i, _i, _i], _i),
     "attn_bwd_workspace_size": ([_i, _i, _i, _i, _i, _i, _i], ctypes.c_size_t),
     "attn_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
@@ -231,17 +233,30 @@ def attn_fwd(q, k, v, causal=False, scale: float | None = None, out=None, lse=No
 
 
 def fwd_workspace_size(B, Hq, Hkv, Nq, Nk, D, dtype) -> int:
-    """Bytes of workspace attn_fwd_ws needs (0 for fp16)."""
+    """Bytes of workspace attn_fwd_ws needs on the current device (0: none)."""
     code = dtype if isinstance(dtype, int) else (ATTN_BF16 if str(dtype).endswith("bfloat16")
                                                  else ATTN_F16)
     return load().attn_fwd_workspace_size(B, Hq, Hkv, Nq, Nk, D, code)
 
 
+def fwd_ws_splits(B, Hq, Hkv, Nq, Nk, D, causal=False) -> int:
+    """Key ranges attn_fwd_ws cuts its cut units into on the current device
+    (1: the grid is not cut, no merge kernel)."""
+    return load().attn_fwd_ws_splits(B, Hq, Hkv, Nq, Nk, D, causal_code(causal))
+
+
+def bwd_splits(B, Hq, Hkv, Nq, Nk, D) -> int:
+    """Query ranges attn_bwd cuts the dK/dV work into with its recommended
+    workspace (1: no partial-sum kernel)."""
+    return load().attn_bwd_splits(B, Hq, Hkv, Nq, Nk, D)
+
+
 def attn_fwd_ws(q, k, v, causal=False, scale: float | None = None, out=None, lse=None,
                 workspace=None):
-    """attn_fwd through attn_fwd_ws: for bf16 inputs the value tiles are
-    converted to fp16 once, into a workspace (allocated here on q's device
-    when not given), instead of inside every CTA."""
+    """attn_fwd through attn_fwd_ws, with a workspace (allocated here on q's
+    device when not given): for bf16 inputs the value tiles are converted to
+    fp16 once into it, instead of inside every CTA, and grids that fill the
+    GPU unevenly cut some units' keys into ranges whose partials it holds."""
     import torch
     _check(q, k, v)
     B, Hq, Nq, D = q.shape

@@ -155,6 +155,78 @@ int effective_splits(int Nk, int requested) {
     return static_cast<int>((tiles + per - 1) / per);
 }
 
+// Launch plan of attn_fwd_ws: units [0, n_whole) run whole, the keys of the
+// rest are cut into `splits` ranges of `tps` key tiles (FwdParams).
+struct FwdPlan {
+    int64_t n_whole = 0;
+    int splits = 1;
+    int tps = 0;
+};
+
+// One CTA per SM (shared memory and the 512 TMEM columns), so a grid of U
+// equal units runs as ceil(U / SMs) waves.
+//  * Several waves: when the last wave's units, cut in two key halves, fit in
+//    one wave, they are cut (the last wave then takes about half as long).
+//    Only without the causal mask, whose units are laid out so that the last
+//    ones cover the last output rows; and with at least 8 key tiles.
+//  * Under one wave: every unit's keys are cut into as many ranges as fill
+//    the SMs, each of at least 16 key tiles (a range costs a CTA's fixed
+//    set-up and its share of the merge: two ranges of 4 key tiles made N =
+//    1024 (B = 1, H = 16, D = 64) 19% slower).
+FwdPlan fwd_plan(int B, int Hq, int Hkv, int Nq, int Nk, int causal) {
+    FwdPlan pl;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0) {
+        cudaGetLastError();   // leave no error behind on a machine without a device
+        return pl;
+    }
+    const int64_t rows = static_cast<int64_t>(Hq / Hkv) * Nq;
+    const int64_t units = static_cast<int64_t>(B) * Hkv * ((rows + 255) / 256);
+    const int64_t tiles = key_tiles(Nk);
+    if (units >= sms) {
+        if (causal != ATTN_CAUSAL_NONE || tiles < 8) return pl;
+        const int64_t waves = (units + sms - 1) / sms;
+        const int64_t tail = units - (waves - 1) * sms;
+        if (waves < 2 || 2 * tail > sms) return pl;
+        pl.n_whole = units - tail;
+        pl.splits = 2;
+        pl.tps = static_cast<int>((tiles + 1) / 2);
+        return pl;
+    }
+    int64_t want = sms / units;
+    if (want > tiles / 16) want = tiles / 16;
+    if (want > kMaxSplits) want = kMaxSplits;
+    if (want < 2) return pl;
+    pl.tps = static_cast<int>((tiles + want - 1) / want);
+    pl.splits = static_cast<int>((tiles + pl.tps - 1) / pl.tps);
+    if (pl.splits < 2) pl = FwdPlan{};
+    return pl;
+}
+
+// First output row and row count of the split units' partials.
+void plan_rows(const FwdPlan& pl, int B, int Hq, int Hkv, int Nq, int64_t* row0,
+               int64_t* nrows) {
+    const int64_t rows = static_cast<int64_t>(Hq / Hkv) * Nq;
+    const int64_t total = rows * B * Hkv;
+    const int64_t n_pairs = (rows + 255) / 256;
+    const int64_t first = (pl.n_whole / n_pairs) * rows + (pl.n_whole % n_pairs) * 256;
+    *row0 = pl.n_whole > 0 ? first : 0;
+    *nrows = total - *row0;
+}
+
+size_t pad256(size_t b) { return (b + 255) & ~size_t(255); }
+
+// Bytes of the split partials of a plan (0 without a split).
+size_t plan_bytes(const FwdPlan& pl, int B, int Hq, int Hkv, int Nq, int D) {
+    if (pl.splits < 2) return 0;
+    int64_t row0 = 0, nrows = 0;
+    plan_rows(pl, B, Hq, Hkv, Nq, &row0, &nrows);
+    return pad256(static_cast<size_t>(pl.splits) * nrows * D * sizeof(float)) +
+           pad256(static_cast<size_t>(pl.splits) * nrows * sizeof(float));
+}
+
 // Checks shared by the mask entry points: kind, strides, alignment of the
 // 16-byte vector loads of bias rows.
 int check_mask(const void* mask, int kind, long long sb, long long sh, long long sq) {
@@ -205,6 +277,9 @@ int fwd_prepare(const void* q, const void* k, const void* v, void* out, float* l
     p->n_pairs = static_cast<int>((rows + 255) / 256);
     p->n_splits = 1;
     p->tiles_per_split = static_cast<int>(key_tiles(Nk));
+    p->n_whole = 0;
+    p->part_row0 = 0;
+    p->part_rows = p->total_rows;
     p->scale_log2 = scale * 1.4426950408889634f;
     p->scale = scale;
     p->mask = nullptr;
@@ -232,42 +307,69 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, 
 extern "C" size_t attn_fwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int D,
                                           int dtype) {
     if (check_shape(B, Hq, Hkv, Nq, Nk, D, 1.0f, dtype) != ATTN_OK) return 0;
-    if (dtype != ATTN_BF16) return 0;
-    const size_t groups = static_cast<size_t>(B) * Hkv;
-    const size_t v_bytes = (groups * Nk * D * 2 + 255) & ~size_t(255);
-    const size_t f_bytes = (groups * static_cast<size_t>(key_tiles(Nk)) + 255) & ~size_t(255);
-    return v_bytes + f_bytes;
+    size_t bytes = 0;
+    if (dtype == ATTN_BF16) {
+        const size_t groups = static_cast<size_t>(B) * Hkv;
+        bytes = pad256(groups * Nk * D * 2) + pad256(groups * static_cast<size_t>(key_tiles(Nk)));
+    }
+    // The plan without the causal mask cuts at least as much as with it.
+    return bytes + plan_bytes(fwd_plan(B, Hq, Hkv, Nq, Nk, ATTN_CAUSAL_NONE), B, Hq, Hkv, Nq, D);
 }
 
 extern "C" int attn_fwd_ws(const void* q, const void* k, const void* v, void* out, float* lse,
                            void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
                            int Nq, int Nk, int D, float scale, int causal, int dtype,
                            void* stream) {
-    if (dtype != ATTN_BF16)
-        return attn_fwd(q, k, v, out, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype, stream);
     int rc = check_shape(B, Hq, Hkv, Nq, Nk, D, scale, dtype);
     if (rc != ATTN_OK) return rc;
+    const FwdPlan pl = fwd_plan(B, Hq, Hkv, Nq, Nk, causal);
+    const bool bf16 = dtype == ATTN_BF16;
     // Workspace checks come before any device call.
-    if (!workspace) return ATTN_ERR_INVALID;
-    if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
-    if (workspace_bytes < attn_fwd_workspace_size(B, Hq, Hkv, Nq, Nk, D, dtype))
-        return ATTN_ERR_WORKSPACE;
+    const size_t need = attn_fwd_workspace_size(B, Hq, Hkv, Nq, Nk, D, dtype);
+    if (need > 0) {
+        if (!workspace) return ATTN_ERR_INVALID;
+        if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
+        if (workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+    }
     CUtensorMap tmQ, tmK, tmV, tmV16;
     FwdParams p;
     rc = fwd_prepare(q, k, v, out, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype, &tmQ, &tmK,
                      &tmV, &p);
     if (rc != ATTN_OK) return rc;
-    const int64_t groups = static_cast<int64_t>(B) * Hkv;
-    const size_t v_bytes = (static_cast<size_t>(groups) * Nk * D * 2 + 255) & ~size_t(255);
-    uint8_t* flags = static_cast<uint8_t*>(workspace) + v_bytes;
-    if (make_map(&tmV16, workspace, false, D, Nk, groups) != ATTN_OK) return ATTN_ERR_CUDA;
-    p.vflags = flags;
-    p.n_ktiles = static_cast<int>(key_tiles(Nk));
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_v_to_f16(D, v, workspace, flags, groups, Nk, st);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const int64_t groups = static_cast<int64_t>(B) * Hkv;
+    size_t off = 0;
+    uint8_t* vflags = nullptr;
+    if (bf16) {
+        const size_t v_bytes = pad256(static_cast<size_t>(groups) * Nk * D * 2);
+        if (make_map(&tmV16, ws, false, D, Nk, groups) != ATTN_OK) return ATTN_ERR_CUDA;
+        vflags = ws + v_bytes;
+        p.vflags = vflags;
+        p.n_ktiles = static_cast<int>(key_tiles(Nk));
+        off = v_bytes + pad256(static_cast<size_t>(groups) * key_tiles(Nk));
+    }
+    if (pl.splits > 1) {
+        p.n_splits = pl.splits;
+        p.tiles_per_split = pl.tps;
+        p.n_whole = static_cast<int>(pl.n_whole);
+        plan_rows(pl, B, Hq, Hkv, Nq, &p.part_row0, &p.part_rows);
+        p.o_part = reinterpret_cast<float*>(ws + off);
+        p.lse_part = reinterpret_cast<float*>(
+            ws + off + pad256(static_cast<size_t>(pl.splits) * p.part_rows * D * sizeof(float)));
+    }
+    cudaError_t e = cudaSuccess;
+    if (bf16) e = launch_v_to_f16(D, v, ws, vflags, groups, Nk, st);
     if (e == cudaSuccess)
-        e = launch_fwd(D, true, causal != ATTN_CAUSAL_NONE, tmQ, tmK, tmV, p, st, &tmV16);
+        e = launch_fwd(D, bf16, causal != ATTN_CAUSAL_NONE, tmQ, tmK, tmV, p, st,
+                       bf16 ? &tmV16 : nullptr);
+    if (e == cudaSuccess && pl.splits > 1) e = launch_splitkv_merge(D, bf16, p, st);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+extern "C" int attn_fwd_ws_splits(int B, int Hq, int Hkv, int Nq, int Nk, int D, int causal) {
+    if (check_shape(B, Hq, Hkv, Nq, Nk, D, 1.0f, ATTN_F16) != ATTN_OK) return 0;
+    return fwd_plan(B, Hq, Hkv, Nq, Nk, causal).splits;
 }
 
 extern "C" int attn_fwd_masked(const void* q, const void* k, const void* v, void* out, float* lse,
@@ -413,6 +515,12 @@ int bwd_splits(int B, int Hq, int Hkv, int Nq, int Nk, int* tiles_per_split) {
 
 }  // namespace
 }  // namespace tme
+
+extern "C" int attn_bwd_splits(int B, int Hq, int Hkv, int Nq, int Nk, int D) {
+    if (check_shape(B, Hq, Hkv, Nq, Nk, D, 1.0f, ATTN_F16) != ATTN_OK) return 0;
+    int per = 0;
+    return bwd_splits(B, Hq, Hkv, Nq, Nk, &per);
+}
 
 extern "C" size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int D,
                                           int dtype) {

@@ -205,6 +205,10 @@ __device__ __forceinline__ void bias_fold_column(uint32_t (&x)[32], const uint32
 
 constexpr int kDqKStages = 3;  // dQ kernel: K ring (live from S_j to dQ_j)
 constexpr int kDqVStages = 2;  // dQ kernel: V ring (live until dP_j)
+// K stages of the dQ kernel: one fewer at D = 128 with a general mask (its
+// staged bias takes that stage's shared memory).
+template <int D, bool MASK>
+constexpr int dq_kstages() { return (MASK && D == 128) ? kDqKStages - 1 : kDqKStages; }
 
 template <int D>
 struct BwdCfg {
@@ -587,7 +591,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tmV, const BwdParams p) {
     using C = BwdCfg<D>;
     // K lives from S_j to dQ_j, V only until dP_j: separate rings, K deeper.
-    constexpr int TB = C::kTileBytes, KB = C::kKB, KS = kDqKStages, VS = kDqVStages;
+    // A general mask stages each warp's next 32 x 64 bias block in shared
+    // memory (8 warps x 4 KB); at D = 128 the K ring gives a stage for it.
+    constexpr int TB = C::kTileBytes, KB = C::kKB, VS = kDqVStages;
+    constexpr int KS = dq_kstages<D, MASK>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -595,7 +602,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sDO = sQ + TB;
     uint8_t* sK = sDO + TB;           // [KS]
     uint8_t* sV = sK + KS * TB;       // [VS]
-    float* sL = reinterpret_cast<float*>(sV + VS * TB);
+    uint8_t* sB = sV + VS * TB;       // [8 warps][32 rows][64 keys x 2 bytes] (MASK)
+    float* sL = reinterpret_cast<float*>(sB + (MASK ? 8 * 4096 : 0));
     float* sDl = sL + kRows;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sDl + kRows);
     uint64_t* q_full = bars;
@@ -749,7 +757,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t wr0 = row0 + quad * 32;
         const int64_t wr1 = min(wr0 + 31, p.rows_per_group - 1);
         const int warp_min_pos = (wr0 / p.Nq == wr1 / p.Nq) ? static_cast<int>(wr0 % p.Nq) : 0;
-        const float sc = MASK ? 1.0f : sl2;   // scale still to apply to the scores read below
+        // scale still to apply to the scores read below: an additive bias
+        // leaves natural-log logits (log2 e), a boolean one raw scores
+        const float sc = (MASK && p.mask_kind == 2) ? kLog2e : sl2;
         const uint64_t sl22 = f2(sc, sc), nl2 = f2(nl, nl), nd2 = f2(nd, nd);
         const uint32_t tDS = tmem + lb + 384;
         // This row's bias: query head hkv*G + row/Nq of batch group/Hkv.
@@ -760,33 +770,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             mrow = static_cast<const uint8_t*>(p.mask) +
                    (b * p.msb + h * p.msh + pos * p.msq) * (p.mask_kind == 2 ? 2 : 1);
         }
+        // Staged bias (MASK): this warp's 32 rows x the 64 keys of its half of
+        // each key tile, one tile ahead, nvalid rows real; a half-tile past
+        // Nk reads its bias directly.
+        const int64_t wleft = p.rows_per_group - wr0;
+        const int nvalid = wleft <= 0 ? 0 : wleft >= 32 ? 32 : static_cast<int>(wleft);
+        const uint32_t bbuf = smem_u32(sB) + warp * 4096;
+        auto staged = [&](int jj) { return nvalid > 0 && jj * kRows + 64 * hq + 64 <= p.Nk; };
+        if constexpr (MASK)
+            if (nkv > 0 && staged(0)) bias_prefetch<64>(bbuf, mrow, p.mask_kind, 64 * hq, nvalid, lane);
         for (int j = 0; j < nkv; ++j) {
             const int k0 = j * kRows;
-            // this half's bias, loaded before the wait for S (hides the latency)
-            BiasChunk b0, b1;
-            if constexpr (MASK) {
-                const int key = k0 + 2 * hq * 32;
-                bias_load(b0, mrow, p.mask_kind, key, row_ok && key + 32 <= p.Nk);
-                bias_load(b1, mrow, p.mask_kind, key + 32, row_ok && key + 64 <= p.Nk);
-            }
             warp_wait(s_full, j & 1, abort_flag, p.status);
             tc_fence_after();
-            if constexpr (MASK) {
-                // this half's scores -> logits with the bias, in place in TMEM
-#pragma unroll 1
-                for (int cc = 0; cc < 2; ++cc) {
-                    const int key = k0 + (2 * hq + cc) * 32;
-                    const bool full = row_ok && key + 32 <= p.Nk;
-                    uint32_t x[32];
-                    tmem_ld32(tS + (2 * hq + cc) * 32, x);
-                    tmem_wait_ld();
-                    reg_fence(x);
-                    bias_apply<BF16>(x, b0, mrow, p.mask_kind, key, p.Nk, sl2, full, row_ok);
-                    tmem_st32(tS + (2 * hq + cc) * 32, x);
-                    b0 = b1;
-                }
-                tmem_wait_st();
-            }
             const bool need_mask = (k0 + kRows > p.Nk) || (CAUSAL && k0 + kRows - 1 > warp_min_pos);
             uint32_t sv[2][32], dp[2][32];
 #pragma unroll
@@ -803,6 +799,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             // S_j and dP_j are in registers: the next S and dP may overwrite them.
             tc_fence_before();
             mbar_arrive(s_free);
+            if constexpr (MASK) {
+                // this half's scores -> logits with the bias; then the next
+                // key tile's bias is requested into the same rows
+                if (staged(j)) {
+                    cp_async_wait_all();
+                    __syncwarp();
+                    bias_fold_smem64<BF16>(sv, bbuf, p.mask_kind, p.scale, lane);
+                    __syncwarp();
+                } else {
+                    bias_fold_direct64<BF16>(sv, mrow, p.mask_kind, k0 + 64 * hq, p.Nk, p.scale,
+                                             row_ok);
+                }
+                if (j + 1 < nkv && staged(j + 1))
+                    bias_prefetch<64>(bbuf, mrow, p.mask_kind, k0 + kRows + 64 * hq, nvalid, lane);
+            }
             // dS columns still feed dQ += dS_{j-1} K_{j-1}.
             if (j > 0) {
                 warp_wait(dq_done, (j - 1) & 1, abort_flag, p.status);
@@ -833,6 +844,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(p_full);
         }
+        // No bias copy may still be in flight when the CTA gives up its shared memory.
+        if constexpr (MASK) cp_async_wait_all();
         const bool ok = *abort_flag == 0;
         if (nkv > 0) warp_wait(acc_full, 0, abort_flag, p.status);
         tc_fence_after();
@@ -866,9 +879,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 constexpr int dkdv_smem() { return 2 * BwdCfg<D>::kTileBytes + 4 * BwdCfg<D>::kTileBytes + 2 * 2 * kRows * 4 + 256 + 1024; }
-template <int D>
+template <int D, bool MASK>
 constexpr int dq_smem() {
-    return (2 + kDqKStages + kDqVStages) * BwdCfg<D>::kTileBytes + 2 * kRows * 4 + 256 + 1024;
+    return (2 + dq_kstages<D, MASK>() + kDqVStages) * BwdCfg<D>::kTileBytes +
+           (MASK ? 8 * 4096 : 0) + 2 * kRows * 4 + 256 + 1024;
 }
 
 // Sum of the kv_splits partial dV / dK (fp32, in range order) into dv / dk
@@ -924,7 +938,7 @@ cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
     }
     {
         auto kern = bwd_dq_kernel<D, BF16, CAUSAL, MASK>;
-        constexpr int smem = dq_smem<D>();
+        constexpr int smem = dq_smem<D, MASK>();
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         const long long ctas = static_cast<long long>(p.n_groups) * p.n_qtiles;

@@ -151,9 +151,9 @@ __device__ __forceinline__ int kv_tiles_for(int64_t row0, const FwdParams& p, bo
     return static_cast<int>((keys + kRows - 1) / kRows);
 }
 
-// Key tiles of [kt0, kt0 + tiles_per_split) below a tile's limit n_full.
-__device__ __forceinline__ int tiles_in_range(int n_full, int kt0, const FwdParams& p) {
-    const int end = n_full < kt0 + p.tiles_per_split ? n_full : kt0 + p.tiles_per_split;
+// Key tiles of [kt0, kt0 + tps) below a tile's limit n_full.
+__device__ __forceinline__ int tiles_in_range(int n_full, int kt0, int tps) {
+    const int end = n_full < kt0 + tps ? n_full : kt0 + tps;
     return end > kt0 ? end - kt0 : 0;
 }
 
@@ -161,14 +161,15 @@ __device__ __forceinline__ int tiles_in_range(int n_full, int kt0, const FwdPara
 // the 16-bit dtype, as two 32-byte stores: each lane writes whole 32-byte
 // sectors of its row (rows are D * 2 bytes apart and the 32 columns start at
 // a multiple of 64 bytes, so they are 32-byte aligned whenever out is; an out
-// that is only 16-byte aligned takes four 16-byte stores).  Split mode: the
-// same values in fp32 to this key range's partial arrays.
+// that is only 16-byte aligned takes four 16-byte stores).  A key range of
+// a split unit (split >= 0): the same values in fp32 to its partial arrays.
 template <int D, bool BF16>
 __device__ __forceinline__ void store_o32(const FwdParams& p, int split, int64_t grow, int c,
                                           const uint32_t (&o)[32], float inv_l) {
-    if (p.n_splits > 1) {
+    if (split >= 0) {
         float4* dst = reinterpret_cast<float4*>(
-            p.o_part + (static_cast<int64_t>(split) * p.total_rows + grow) * D + c * 32);
+            p.o_part + (static_cast<int64_t>(split) * p.part_rows + grow - p.part_row0) * D +
+            c * 32);
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
@@ -195,8 +196,8 @@ __device__ __forceinline__ void store_o32(const FwdParams& p, int split, int64_t
 }
 
 __device__ __forceinline__ void store_lse(const FwdParams& p, int split, int64_t grow, float v) {
-    if (p.n_splits > 1)
-        p.lse_part[static_cast<int64_t>(split) * p.total_rows + grow] = v;
+    if (split >= 0)
+        p.lse_part[static_cast<int64_t>(split) * p.part_rows + grow - p.part_row0] = v;
     else
         p.lse[grow] = v;
 }
@@ -286,12 +287,18 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
     // position k = m-1 .. 0 and, within one position, over every (group,
     // head), which is heaviest-first across the whole grid.  A general mask
     // without the causal mask walks the pairs position-major (below).
-    // Otherwise consecutive CTAs share a KV group (its K/V stay hot in L2),
-    // heaviest pair first within the group.  With split keys, the CTAs of one
-    // unit are adjacent and each takes the key tiles [kt0, kt0 +
-    // tiles_per_split).
-    const int split = static_cast<int>(blockIdx.x % p.n_splits);
-    const int unit = static_cast<int>(blockIdx.x / p.n_splits);
+    // Otherwise consecutive CTAs share a KV group (its K/V stay hot in L2):
+    // without the causal mask pairs ascending (so the units of the last CTAs
+    // cover the last rows of the output, contiguously), with it heaviest pair
+    // first within the group.  Units [0, n_whole) run whole; after them the
+    // CTAs of one split unit are adjacent and each takes the key tiles [kt0,
+    // kt0 + tiles_per_split) (split < 0: the whole unit).
+    int unit = static_cast<int>(blockIdx.x), split = -1;
+    if (p.n_splits > 1 && unit >= p.n_whole) {
+        const int c = unit - p.n_whole;
+        unit = p.n_whole + c / p.n_splits;
+        split = c % p.n_splits;
+    }
     int group, pair;
     if (CAUSAL && p.Nq % (2 * kRows) == 0) {
         const int m = p.Nq / (2 * kRows);        // pairs per head (n_pairs = G * m)
@@ -305,14 +312,18 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
         // one block of bias rows run together and share it through L2.
         group = unit % p.n_groups;
         pair = unit / p.n_groups;
+    } else if (!CAUSAL) {
+        group = unit / p.n_pairs;
+        pair = unit % p.n_pairs;
     } else {
         group = unit / p.n_pairs;
         pair = p.n_pairs - 1 - unit % p.n_pairs;
     }
     const int64_t row_base = static_cast<int64_t>(pair) * (2 * kRows);
-    const int kt0 = split * p.tiles_per_split;
-    int n0 = tiles_in_range(kv_tiles_for(row_base, p, CAUSAL), kt0, p);
-    int n1 = tiles_in_range(kv_tiles_for(row_base + kRows, p, CAUSAL), kt0, p);
+    const int kt0 = split >= 0 ? split * p.tiles_per_split : 0;
+    const int tps = split >= 0 ? p.tiles_per_split : 0x7fffffff - kt0;
+    int n0 = tiles_in_range(kv_tiles_for(row_base, p, CAUSAL), kt0, tps);
+    int n1 = tiles_in_range(kv_tiles_for(row_base + kRows, p, CAUSAL), kt0, tps);
     int nmax = n0 > n1 ? n0 : n1;
     // A boolean mask that depends on the key alone (one row of keep bytes for
     // the whole CTA, as a padding mask is) removes every key tile past its
@@ -830,7 +841,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
                 const float m_sub = (m == -INFINITY) ? 0.0f : m;
                 store_lse(p, split, grow, lt > 0.0f ? (m_sub + lg2_approx(lt)) * kLn2 : -INFINITY);
             }
-        } else if (p.n_splits > 1 && row_valid) {
+        } else if (split >= 0 && row_valid) {
             // No key of this range is visible to the tile: an empty partial.
             const int64_t grow = static_cast<int64_t>(group) * p.rows_per_group + row;
             const uint32_t z[32] = {};
@@ -1046,7 +1057,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
                 const float m_sub = (m == -INFINITY) ? 0.0f : m;
                 store_lse(p, split, grow, l > 0.0f ? (m_sub + lg2_approx(l)) * kLn2 : -INFINITY);
             }
-        } else if (n_t == 0 && p.n_splits > 1 && row_valid) {
+        } else if (n_t == 0 && split >= 0 && row_valid) {
             // No key of this range is visible to the tile: an empty partial.
             const int64_t grow = static_cast<int64_t>(group) * p.rows_per_group + row;
             const uint32_t z[32] = {};
@@ -1075,7 +1086,9 @@ cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
     // whichever device is current.
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const long long ctas = static_cast<long long>(p.n_groups) * p.n_pairs * p.n_splits;
+    const long long units = static_cast<long long>(p.n_groups) * p.n_pairs;
+    const long long ctas =
+        p.n_splits > 1 ? p.n_whole + (units - p.n_whole) * p.n_splits : units;
     return launch_kernel(kern, dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, stream,
                          tmQ, tmK, tmV, tmV16, p);
 }

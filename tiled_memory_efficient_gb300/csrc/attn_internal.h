@@ -21,10 +21,10 @@ inline cudaError_t launch_kernel(void (*kern)(Params...), dim3 grid, dim3 block,
 // Forward launch parameters (everything the kernel needs besides the three
 // tensor maps).  Row indices are "flattened": within KV group g of batch b the
 // G query heads that share that KV head form G*Nq consecutive rows, head-major.
-// With n_splits > 1 the keys are cut into n_splits ranges of tiles_per_split
-// 128-key tiles, one CTA per (group, pair of Q tiles, range); each CTA writes
-// its range's normalised partial output and LSE in fp32 to o_part / lse_part
-// ([n_splits][n_groups * rows_per_group][D] and [n_splits][...]) instead of
+// With n_splits > 1 the keys of the split units are cut into n_splits ranges
+// of tiles_per_split 128-key tiles, one CTA per (unit, range); each such CTA
+// writes its range's normalised partial output and LSE in fp32 to o_part /
+// lse_part ([n_splits][part_rows][D] and [n_splits][part_rows]) instead of
 // out / lse, and splitkv_merge combines them.
 struct FwdParams {
     void* out;               // [B, Hq, Nq, D] fp16/bf16
@@ -40,6 +40,13 @@ struct FwdParams {
     int n_pairs;             // ceil(rows_per_group / 256): CTAs per group and key range
     int n_splits;            // key ranges (1: no split)
     int tiles_per_split;     // 128-key tiles per range
+    // Units [0, n_whole) run whole (every key tile, output to out / lse); the
+    // CTAs after them take the n_splits key ranges of units n_whole, n_whole
+    // + 1, ...  Their partials hold rows [part_row0, part_row0 + part_rows) of
+    // the flattened output (those units' rows, contiguous): partial row
+    // grow - part_row0 of range s at index s * part_rows + grow - part_row0.
+    int n_whole;
+    int64_t part_row0, part_rows;
     float scale_log2;        // scale * log2(e)
     float scale;             // softmax scale (a general additive bias is added after it)
     // Optional attention bias (masked kernels only): element (b, h, i, j) at

@@ -8,8 +8,10 @@
 // output O_r and its log-sum-exp L_r.  Softmax over the union of the ranges is
 //     L = M + ln(sum_r e^(L_r - M)),   O = sum_r e^(L_r - L) O_r,
 // with M = max_r L_r (the same online-softmax identity the tiles use, applied
-// once per range).  This file combines the partials: one warp per output row,
-// fp32 throughout, the result rounded once to the output dtype.
+// once per range).  This file combines the partials: one warp per output row
+// of the split units (all rows, or the rows of the last units of a grid whose
+// first units ran whole), fp32 throughout, the result rounded once to the
+// output dtype.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -27,12 +29,14 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(kMergeWarps * 32)
     splitkv_merge_kernel(const FwdParams p) {
     constexpr int V = D / 32;  // columns per lane
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+    // partial row pr = output row part_row0 + pr
+    const int64_t pr = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+    const int64_t row = p.part_row0 + pr;
     const int lane = threadIdx.x & 31;
     // Launched as a programmatic dependent of the split kernel: wait here
     // until that grid has finished and its partials are visible.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (row >= p.total_rows) return;
+    if (pr >= p.part_rows) return;
 
     // Every lane holds the LSE of ranges lane, lane + 32, ...: the maximum and
     // the weights need no further loads, so all partial-output loads below
@@ -41,7 +45,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
         const int s = lane + 32 * u;
-        ls[u] = s < p.n_splits ? p.lse_part[static_cast<int64_t>(s) * p.total_rows + row]
+        ls[u] = s < p.n_splits ? p.lse_part[static_cast<int64_t>(s) * p.part_rows + pr]
                                : -INFINITY;
     }
     float M = ls[0];
@@ -62,8 +66,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
     float acc[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) acc[i] = 0.0f;
-    const float* src = p.o_part + row * D + lane * V;
-    const int64_t step = p.total_rows * D;   // one range further (kMaxSplits = 256 = 8 x 32)
+    const float* src = p.o_part + pr * D + lane * V;
+    const int64_t step = p.part_rows * D;   // one range further (kMaxSplits = 256 = 8 x 32)
 #pragma unroll
     for (int u = 0; u < 8; ++u) {   // ranges 32u .. 32u + 31, weight from lane s - 32u
         if (32 * u >= p.n_splits) break;
@@ -100,7 +104,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 }  // namespace
 
 cudaError_t launch_splitkv_merge(int D, bool bf16, const FwdParams& p, cudaStream_t stream) {
-    const long long blocks = (p.total_rows + kMergeWarps - 1) / kMergeWarps;
+    const long long blocks = (p.part_rows + kMergeWarps - 1) / kMergeWarps;
     // Programmatic dependent launch: the merge grid is set up while the split
     // kernel drains, and waits for it on the device (griddepcontrol.wait).
     cudaLaunchAttribute attr{};
