@@ -511,7 +511,7 @@ def run_ours(args):
                 (_lib.fwd_ws_splits(wd.B, wd.Hq, wd.Hkv, n, n, wd.D, wd.causal) > 1))
 
     def bwd_launches(wd, n):
-        return 3 + (_lib.bwd_splits(wd.B, wd.Hq, wd.Hkv, n, n, wd.D) > 1)
+        return 3 + (_lib.bwd_splits(wd.B, wd.Hq, wd.Hkv, n, n, wd.D, wd.causal) > 1)
 
     launches_per_step = (
         sum((2 if splits[n] > 1 else 1) if decode else bwd_launches(w, n) if bwd else

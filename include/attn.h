@@ -205,18 +205,21 @@ int attn_fwd_num_splits(int B, int Hq, int Hkv, int Nq, int Nk, int D, int num_s
  * 256), plus -- when B*Hkv*ceil(Nk/128) dK/dV CTAs would leave SMs of the
  * current device idle (small batches, GQA) -- fp32 partial sums of dK and dV
  * for the S query ranges the dK/dV work is cut into, 2 * S * B*Hkv*Nk*D * 4
- * bytes.  Returns 0 for invalid sizes.  Needs the current device only for its
+ * bytes (S of the causal plan, which covers the plain one: attn_bwd_splits).  Returns 0 for invalid sizes.  Needs the current device only for its
  * SM count (without one: the statistics alone).
  */
 size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int D, int dtype);
 
 /*
  * The number S of query ranges attn_bwd cuts the dK/dV work into at these
- * sizes on the current device, given the workspace attn_bwd_workspace_size()
- * recommends: 1 (three kernels: statistics, dK/dV, dQ) or more (a fourth adds
- * the ranges' partial sums).  0 for invalid sizes.  Host-only.
+ * sizes and causal mode on the current device, given the workspace
+ * attn_bwd_workspace_size() recommends: 1 (three kernels: statistics, dK/dV,
+ * dQ) or more (a fourth adds the ranges' partial sums).  Without the causal
+ * mask, as many ranges as fill one wave of CTAs; with it, enough that the
+ * CTAs of the first key tile (which meets every query tile) do no more than
+ * the average work per SM.  0 for invalid sizes.  Host-only.
  */
-int attn_bwd_splits(int B, int Hq, int Hkv, int Nq, int Nk, int D);
+int attn_bwd_splits(int B, int Hq, int Hkv, int Nq, int Nk, int D, int causal);
 
 /*
  * Backward of attn_fwd (forum post, "Other areas where this could be useful":

@@ -106,8 +106,8 @@ def test_fwd_ws_workspace_size_and_validation(lib):
     # device) are not cut; invalid sizes give 0
     assert lib.attn_fwd_ws_splits(1, 2, 2, 300, 300, 64, 0) == 1
     assert lib.attn_fwd_ws_splits(1, 3, 2, 300, 300, 64, 0) == 0
-    assert lib.attn_bwd_splits(1, 2, 2, 300, 300, 64) == 1
-    assert lib.attn_bwd_splits(1, 3, 2, 300, 300, 64) == 0
+    assert lib.attn_bwd_splits(1, 2, 2, 300, 300, 64, 1) == 1
+    assert lib.attn_bwd_splits(1, 3, 2, 300, 300, 64, 0) == 0
 
 
 def test_bwd_rejects_bottom_right(lib):

@@ -103,6 +103,20 @@ def test_backward_workspace_contents_do_not_matter(cuda_lib):
         assert torch.equal(a, b)
 
 
+def test_backward_range_plan(cuda_lib):
+    """dK/dV query ranges on a 152-SM GB300: without the causal mask as many as
+    fill one wave; with it enough that key tile 0's CTAs (which meet every
+    query tile) do no more than the average work per SM."""
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the plan below is for 152 SMs")
+    # GQA 14:2, D = 64: 2 KV groups x Nk / 128 key tiles
+    assert _lib.bwd_splits(1, 14, 2, 2048, 2048, 64, True) == 9
+    assert _lib.bwd_splits(1, 14, 2, 4096, 4096, 64, True) == 5
+    assert _lib.bwd_splits(1, 14, 2, 8192, 8192, 64, True) == 3
+    assert _lib.bwd_splits(1, 14, 2, 4096, 4096, 64, False) == 3
+    assert _lib.bwd_splits(2, 16, 16, 8192, 8192, 128, True) == 1   # 2048 key-tile CTAs
+
+
 def test_gqa_backward_split_every_head(cuda_lib):
     """GQA 14:2 at N = 2048 (causal, fp16): 2 KV heads x 16 key tiles are far
     fewer dK/dV CTAs than SMs, so the query tiles of each key tile are cut

@@ -55,7 +55,7 @@ _SIGNATURES = {
                      ctypes.c_float, _i, _i, _vp], _i),
     "attn_fwd_workspace_size": ([_i, _i, _i, _i, _i, _i, _i], ctypes.c_size_t),
     "attn_fwd_ws_splits": ([_i, _i, _i, _i, _i, _i, _i], _i),
-    "attn_bwd_splits": ([_i, _i, _i, _i, _i, _i], _i),
+    "attn_bwd_splits": ([_i, _i, _i, _i, _i, _i, _i], _i),
     "attn_fwd_num_splits": ([_i, _i, _i, _i, _i, _i, _i], _i),
     "attn_bwd_workspace_size": ([_i, _i, _i, _i, _i, _i, _i], ctypes.c_size_t),
     "attn_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
@@ -245,10 +245,10 @@ def fwd_ws_splits(B, Hq, Hkv, Nq, Nk, D, causal=False) -> int:
     return load().attn_fwd_ws_splits(B, Hq, Hkv, Nq, Nk, D, causal_code(causal))
 
 
-def bwd_splits(B, Hq, Hkv, Nq, Nk, D) -> int:
+def bwd_splits(B, Hq, Hkv, Nq, Nk, D, causal=False) -> int:
     """Query ranges attn_bwd cuts the dK/dV work into with its recommended
     workspace (1: no partial-sum kernel)."""
-    return load().attn_bwd_splits(B, Hq, Hkv, Nq, Nk, D)
+    return load().attn_bwd_splits(B, Hq, Hkv, Nq, Nk, D, causal_code(causal))
 
 
 def attn_fwd_ws(q, k, v, causal=False, scale: float | None = None, out=None, lse=None,

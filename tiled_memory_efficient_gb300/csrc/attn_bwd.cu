@@ -205,10 +205,10 @@ __device__ __forceinline__ void bias_fold_column(uint32_t (&x)[32], const uint32
 
 constexpr int kDqKStages = 3;  // dQ kernel: K ring (live from S_j to dQ_j)
 constexpr int kDqVStages = 2;  // dQ kernel: V ring (live until dP_j)
-// K stages of the dQ kernel: one fewer at D = 128 with a general mask (its
-// staged bias takes that stage's shared memory).
-template <int D, bool MASK>
-constexpr int dq_kstages() { return (MASK && D == 128) ? kDqKStages - 1 : kDqKStages; }
+// K stages of the dQ kernel: one fewer at D = 128 with a staged general mask
+// (its bias takes that stage's shared memory).
+template <int D, bool STAGE>
+constexpr int dq_kstages() { return (STAGE && D == 128) ? kDqKStages - 1 : kDqKStages; }
 
 template <int D>
 struct BwdCfg {
@@ -583,18 +583,22 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 // Warpgroup h owns key columns [64h, 64h+64).  dS has its own columns, so once
 // both warpgroups have read S_j and dP_j into registers (s_free) the tensor
 // core computes S_{j+1} and dP_{j+1} while the elementwise work on j runs.
-template <int D, bool BF16, bool CAUSAL, bool MASK>
+template <int D, bool BF16, bool CAUSAL, int MK>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmDO,
                   const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const BwdParams p) {
     using C = BwdCfg<D>;
+    // MK: 0 no mask, 1 a general bias, 2 a boolean mask that depends on the
+    // key alone (the same keep bytes for every row: read directly, served to
+    // the whole warp at once).
+    constexpr bool MASK = MK != 0, STAGE = MK == 1;
     // K lives from S_j to dQ_j, V only until dP_j: separate rings, K deeper.
     // A general mask stages each warp's next 32 x 64 bias block in shared
     // memory (8 warps x 4 KB); at D = 128 the K ring gives a stage for it.
     constexpr int TB = C::kTileBytes, KB = C::kKB, VS = kDqVStages;
-    constexpr int KS = dq_kstages<D, MASK>();
+    constexpr int KS = dq_kstages<D, STAGE>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -602,8 +606,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sDO = sQ + TB;
     uint8_t* sK = sDO + TB;           // [KS]
     uint8_t* sV = sK + KS * TB;       // [VS]
-    uint8_t* sB = sV + VS * TB;       // [8 warps][32 rows][64 keys x 2 bytes] (MASK)
-    float* sL = reinterpret_cast<float*>(sB + (MASK ? 8 * 4096 : 0));
+    uint8_t* sB = sV + VS * TB;       // [8 warps][32 rows][64 keys x 2 bytes] (STAGE)
+    float* sL = reinterpret_cast<float*>(sB + (STAGE ? 8 * 4096 : 0));
     float* sDl = sL + kRows;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sDl + kRows);
     uint64_t* q_full = bars;
@@ -776,8 +780,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t wleft = p.rows_per_group - wr0;
         const int nvalid = wleft <= 0 ? 0 : wleft >= 32 ? 32 : static_cast<int>(wleft);
         const uint32_t bbuf = smem_u32(sB) + warp * 4096;
-        auto staged = [&](int jj) { return nvalid > 0 && jj * kRows + 64 * hq + 64 <= p.Nk; };
-        if constexpr (MASK)
+        auto staged = [&](int jj) {
+            return STAGE && nvalid > 0 && jj * kRows + 64 * hq + 64 <= p.Nk;
+        };
+        if constexpr (STAGE)
             if (nkv > 0 && staged(0)) bias_prefetch<64>(bbuf, mrow, p.mask_kind, 64 * hq, nvalid, lane);
         for (int j = 0; j < nkv; ++j) {
             const int k0 = j * kRows;
@@ -845,7 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(p_full);
         }
         // No bias copy may still be in flight when the CTA gives up its shared memory.
-        if constexpr (MASK) cp_async_wait_all();
+        if constexpr (STAGE) cp_async_wait_all();
         const bool ok = *abort_flag == 0;
         if (nkv > 0) warp_wait(acc_full, 0, abort_flag, p.status);
         tc_fence_after();
@@ -879,10 +885,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 constexpr int dkdv_smem() { return 2 * BwdCfg<D>::kTileBytes + 4 * BwdCfg<D>::kTileBytes + 2 * 2 * kRows * 4 + 256 + 1024; }
-template <int D, bool MASK>
+template <int D, bool STAGE>
 constexpr int dq_smem() {
-    return (2 + dq_kstages<D, MASK>() + kDqVStages) * BwdCfg<D>::kTileBytes +
-           (MASK ? 8 * 4096 : 0) + 2 * kRows * 4 + 256 + 1024;
+    return (2 + dq_kstages<D, STAGE>() + kDqVStages) * BwdCfg<D>::kTileBytes +
+           (STAGE ? 8 * 4096 : 0) + 2 * kRows * 4 + 256 + 1024;
 }
 
 // Sum of the kv_splits partial dV / dK (fp32, in range order) into dv / dk
@@ -908,6 +914,18 @@ __global__ void __launch_bounds__(256) bwd_dkdv_reduce_kernel(const BwdParams p,
             make_uint4(pack2<BF16>(a.x * sc, a.y * sc), pack2<BF16>(a.z * sc, a.w * sc),
                        pack2<BF16>(b.x * sc, b.y * sc), pack2<BF16>(b.z * sc, b.w * sc));
     }
+}
+
+template <int D, bool BF16, bool CAUSAL, int MK>
+cudaError_t launch_dq(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                      const CUtensorMap& tmDO, const BwdParams& p, cudaStream_t stream) {
+    auto kern = bwd_dq_kernel<D, BF16, CAUSAL, MK>;
+    constexpr int smem = dq_smem<D, MK == 1>();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const long long ctas = static_cast<long long>(p.n_groups) * p.n_qtiles;
+    return launch_kernel(kern, dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, stream,
+                         tmQ, tmDO, tmK, tmV, p);
 }
 
 template <int D, bool BF16, bool CAUSAL, bool MASK>
@@ -936,17 +954,10 @@ cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
             if (e != cudaSuccess) return e;
         }
     }
-    {
-        auto kern = bwd_dq_kernel<D, BF16, CAUSAL, MASK>;
-        constexpr int smem = dq_smem<D, MASK>();
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        const long long ctas = static_cast<long long>(p.n_groups) * p.n_qtiles;
-        e = launch_kernel(kern, dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, stream,
-                          tmQ, tmDO, tmK, tmV, p);
-        if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
+    // dQ: a key-only boolean mask takes its own instantiation (no staging).
+    const bool key_only = MASK && p.mask_kind == 1 && p.msq == 0 && (p.msh == 0 || p.G == 1);
+    return key_only ? launch_dq<D, BF16, CAUSAL, MASK ? 2 : 0>(tmQ, tmK, tmV, tmDO, p, stream)
+                    : launch_dq<D, BF16, CAUSAL, MASK ? 1 : 0>(tmQ, tmK, tmV, tmDO, p, stream);
 }
 
 }  // namespace
