@@ -572,9 +572,10 @@ int bwd_run(const void* q, const void* k, const void* v, const void* out, const 
     int per = 0;
     int splits = bwd_splits(B, Hq, Hkv, Nq, Nk, causal != ATTN_CAUSAL_NONE, &per);
     if (splits > 1) {
-        const size_t per_split = bwd_split_bytes(B, Hkv, Nk, D, 2) / 2;   // both arrays, one range
+        // the largest count whose partial sums the rest of the workspace holds
         const size_t room = workspace_bytes - stats_bytes;
-        int fit = static_cast<int>(room / (per_split + 512));
+        int fit = splits;
+        while (fit > 1 && bwd_split_bytes(B, Hkv, Nk, D, fit) > room) --fit;
         if (fit < splits) {
             const int64_t nqt = (static_cast<int64_t>(Hq / Hkv) * Nq + 127) / 128;
             splits = fit;
