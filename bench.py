@@ -572,12 +572,28 @@ def run_ours(args):
         "clocks": clocks, "sweep": sweep, "d128": d128_rep, "bwd": bwd_rep,
         "wall_s_timed_region": round(t_wall, 3),
     }
+    if args.config == "sweep" and not bwd and args.mask == "none":
+        line["context"] = {
+            "source": "the pages' isolated-attention table (noflash-attention forum post, "
+                      "\"It's actually faster too!\"): one AMD MI50 (gfx906, 150 W), FP16, "
+                      "the pages' tiled PyTorch-matmul kernel; context only",
+            "per_N": [{"N": n, "ms": PAGES_MI50_MS[n],
+                       "tflops": round(w.flops_fwd(n) / (PAGES_MI50_MS[n] * 1e-3) / 1e12, 2),
+                       "ratio_here": round(PAGES_MI50_MS[n] / ms, 1)}
+                      for n, ms in zip(seq, ms_each) if n in PAGES_MI50_MS]}
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
 
 
 D128_POINTS = (("video_dit", 17600), ("video_dit", 75600), ("training", 8192))
+# The pages' own timings of this sweep: the noflash-attention forum post
+# (ai-navigate-news, section "It's actually faster too!", the isolated
+# attention table: B=1, H=16, D=64, FP16 on one AMD MI50 (gfx906) at a 150 W
+# limit, the pages' tiled PyTorch-matmul kernel), in ms.  Another machine and
+# another implementation: reported as context, never as the target.
+PAGES_MI50_MS = {256: 0.18, 512: 0.29, 1024: 0.85, 2048: 4.74, 4096: 17.93, 8192: 72.75,
+                 16384: 1325.69}
 BWD_POINTS = (("training", 8192), ("gqa_prefill", 4096))
 
 
