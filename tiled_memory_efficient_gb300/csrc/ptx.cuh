@@ -187,54 +187,6 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Warp-converged forms: the whole warp executes the call with warp-uniform
-// operands and one elected lane issues the instruction.  Keeping the issuing
-// loop converged lets the operands live in uniform registers, so one MMA can be
-// issued every few cycles instead of once per ~100.
-__device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                             uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .b32 lid;\n\t.reg .pred e, p;\n\t"
-        "elect.sync lid|e, 0xffffffff;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                             uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .b32 lid;\n\t.reg .pred e, p;\n\t"
-        "elect.sync lid|e, 0xffffffff;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // Groups of MMAs along K from one asm block with a single elect: the K-major
 // operands of a 128-byte-swizzled tile advance by 32 bytes (descriptor +2) per
 // K=16 step and by a 16 KiB block (+1024) every four steps.  `acc` selects
@@ -325,46 +277,11 @@ __device__ __forceinline__ void mma_ts_k64_split(uint32_t d, uint32_t a_lo, uint
         : "memory");
 }
 
-// As mma_ts_k128, but the 128 K values of A come from two TMEM column ranges:
-// steps 0-3 from a_lo (+8 per step), steps 4-7 from a_hi (+8 per step).
-__device__ __forceinline__ void mma_ts_k128_split(uint32_t d, uint32_t a_lo, uint32_t a_hi,
-                                                  uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .b32 lid, a1, a2, a3, a5, a6, a7;\n\t.reg .pred e, p, t;\n\t"
-        ".reg .b64 b1, b2, b3, b4, b5, b6, b7;\n\t"
-        "elect.sync lid|e, 0xffffffff;\n\t"
-        "setp.ne.b32 p, %5, 0;\n\t"
-        "setp.eq.b32 t, 0, 0;\n\t"
-        "add.s32 a1, %1, 8;\n\tadd.s32 a2, %1, 16;\n\tadd.s32 a3, %1, 24;\n\t"
-        "add.s32 a5, %2, 8;\n\tadd.s32 a6, %2, 16;\n\tadd.s32 a7, %2, 24;\n\t"
-        "add.s64 b1, %3, 128;\n\tadd.s64 b2, %3, 256;\n\tadd.s64 b3, %3, 384;\n\t"
-        "add.s64 b4, %3, 512;\n\tadd.s64 b5, %3, 640;\n\tadd.s64 b6, %3, 768;\n\t"
-        "add.s64 b7, %3, 896;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %3, %4, p;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %4, t;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %4, t;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %4, t;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], b4, %4, t;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], b5, %4, t;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], b6, %4, t;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a7], b7, %4, t;\n\t}" ::"r"(d),
-        "r"(a_lo), "r"(a_hi), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-
 __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
     asm volatile(
         "{\n\t.reg .b32 lid;\n\t.reg .pred e;\n\t"
         "elect.sync lid|e, 0xffffffff;\n\t"
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-
-// Arrive once on `bar` when every tcgen05 op this thread issued so far is done.
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
         : "memory");
 }
