@@ -655,8 +655,9 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
         // Key-padding mask: one row of keep bytes for the whole CTA (batch
         // group / Hkv; head group % Hkv when a KV group is one query head).
         // Lane l holds 16 of this half's 64 keep bytes (chunk l & 3), loaded
-        // one key tile ahead so the load never waits; the four chunks meet
-        // by shuffles.  A tile with no dropped key costs one minimum.
+        // before the wait for S (every warp of the CTA reads the same bytes,
+        // so they come from L1); the four chunks meet by shuffles.  A tile
+        // with no dropped key costs one minimum.
         const uint8_t* krow = nullptr;
         if constexpr (KEYMASK)
             krow = static_cast<const uint8_t*>(p.mask) + (group / p.Hkv) * p.msb +
@@ -668,9 +669,6 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
             if (jj < n_t && k0 + 64 <= p.Nk) return reinterpret_cast<const uint4*>(krow + k0)[lane & 3];
             return make_uint4(0u, 0u, 0u, 0u);
         };
-        uint4 knext = make_uint4(0u, 0u, 0u, 0u);
-        if constexpr (KEYMASK)
-            if (warp_live) knext = kload(0);
         // First key tile j whose half-tile (keys key0(j) .. key0(j) + 63,
         // key0(j) = (kt0 + j) * 128 + 64 h) needs a per-key mask: it reaches
         // past Nk, or (causal) past what this warp's first row may see.  Both
@@ -693,8 +691,8 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
                 continue;
             }
             const int key0 = (kt0 + j) * kRows + 64 * h;
-            uint4 kcur = knext;
-            if constexpr (KEYMASK) knext = kload(j + 1);
+            uint4 kcur = make_uint4(0u, 0u, 0u, 0u);
+            if constexpr (KEYMASK) kcur = kload(j);
             warp_wait(&s_full[t], j & 1, abort_flag, p.status);
             tc_fence_after();
             uint32_t sr[2][32];
