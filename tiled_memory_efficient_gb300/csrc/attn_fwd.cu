@@ -717,10 +717,13 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
                     bias_prefetch<64>(bbuf, mrow, p.mask_kind, key0 + kRows, nvalid, lane);
             }
             if constexpr (KEYMASK) {
-                uint32_t mn = __vminu4(__vminu4(kcur.x, kcur.y), __vminu4(kcur.z, kcur.w));
-                mn = __vminu4(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
-                mn = __vminu4(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
-                if (__vcmpeq4(mn, 0u) != 0u) {   // the same in every lane
+                // does any of this lane's 16 keep bytes equal 0?  (w - 0x01..01) &
+                // ~w & 0x80..80 is nonzero exactly when a byte of w is 0; the
+                // lanes' chunks together cover the half-tile's 64 bytes
+                auto zero_byte = [](uint32_t w) { return (w - 0x01010101u) & ~w & 0x80808080u; };
+                const uint32_t z =
+                    zero_byte(kcur.x) | zero_byte(kcur.y) | zero_byte(kcur.z) | zero_byte(kcur.w);
+                if (__any_sync(0xffffffffu, z != 0u)) {   // the same in every lane
                     if (key0 + 64 <= p.Nk) {
 #pragma unroll
                         for (int w = 0; w < 16; ++w) {
