@@ -13,7 +13,9 @@ length's time is the median of its launches over the timed steps; value =
 sum of algorithmic FLOPs / sum of those times.  The default run also times,
 in the same region and with their own events, the head-dim-128 points of the
 >= 60%-of-peak target (video-DiT at N = 17600 and 75600, the training forward
-at N = 8192) and reports them under "d128".  Prints ONE JSON line.
+at N = 8192) under "d128", the backward of the training and GQA-prefill
+workloads under "bwd", and the GQA causal prefill forward (N = 4096, 16384)
+under "gqa_prefill_fwd".  Prints ONE JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--config sweep|gqa_prefill|video_dit|training|tiny|gqa_decode]
@@ -275,8 +277,19 @@ def run_ours(args):
     # same region as the sweep with their own events; reported under "d128".
     d128 = []
     bwdp = []
+    gqap = []
     if (args.config == "sweep" and not bwd and args.mask == "none" and args.n is None
             and not args.no_d128):
+        for name, n in GQA_POINTS:
+            wd = inputs.WORKLOADS[name]
+            x = inputs.make_inputs(wd, n)
+            q, k, v = (x[m].to(dev) for m in ("q", "k", "v"))
+            ws = torch.empty(max(16, _lib.fwd_workspace_size(wd.B, wd.Hq, wd.Hkv, n, n, wd.D,
+                                                             wd.dtype)),
+                             device=dev, dtype=torch.uint8)
+            gqap.append((wd, n, q, k, v, torch.empty_like(q),
+                         torch.empty(q.shape[:3], device=dev, dtype=torch.float32), ws))
+            del x
         for name, n in D128_POINTS:
             wd = inputs.WORKLOADS[name]
             x = inputs.make_inputs(wd, n)
@@ -342,6 +355,9 @@ def run_ours(args):
             launch_d128(b)
             flush()
             launch_d128(b, plain=True)
+        for b in gqap:
+            flush()
+            launch_d128(b)
     rc = _lib.sync_status(dev)
     if rc != _lib.ATTN_OK:
         raise RuntimeError(f"device status after warm-up: {_lib.strerror(rc)}")
@@ -354,6 +370,8 @@ def run_ours(args):
              for _ in d128] for _ in range(args.steps)]
     ev_b = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
              for _ in bwdp] for _ in range(args.steps)]
+    ev_g = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in gqap] for _ in range(args.steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -379,6 +397,11 @@ def run_ours(args):
                 ev_p[s][i][0].record(stream)
                 launch_d128(b, plain=True)
                 ev_p[s][i][1].record(stream)
+            for i, b in enumerate(gqap):
+                flush()
+                ev_g[s][i][0].record(stream)
+                launch_d128(b)
+                ev_g[s][i][1].record(stream)
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall
     if dist:
@@ -517,6 +540,7 @@ def run_ours(args):
         sum((2 if splits[n] > 1 else 1) if decode else bwd_launches(w, n) if bwd else
             fwd_launches(w, n, use_ws) for n in seq) +
         sum(fwd_launches(wd, n, True) + 1 for wd, n, *_ in d128) +
+        sum(fwd_launches(wd, n, True) for wd, n, *_ in gqap) +
         sum(bwd_launches(wd, n) for wd, n, *_ in bwdp))
     bwd_rep = None
     if bwdp:
@@ -558,6 +582,20 @@ def run_ours(args):
                               "(same timed region)",
                     "points": pts,
                     "met": all(p_["frac_of_peak"] >= 0.6 for p_ in pts)}
+    gqa_rep = None
+    if gqap:
+        pts = []
+        for i, (wd, n, *_rest) in enumerate(gqap):
+            ms = statistics.median(ev_g[s_][i][0].elapsed_time(ev_g[s_][i][1])
+                                   for s_ in range(args.steps))
+            tf = wd.flops_fwd(n) / (ms * 1e-3) / 1e12
+            pts.append({"workload": wd.note, "N": n, "ms": round(ms, 4), "tflops": round(tf, 1),
+                        "frac_of_peak": round(tf / pk["bf16_tflops"], 4),
+                        "key_ranges": _lib.fwd_ws_splits(wd.B, wd.Hq, wd.Hkv, n, n, wd.D,
+                                                         wd.causal)})
+        gqa_rep = {"entry": "attn_fwd_ws (causal FLOPs: half of 4*B*Hq*N*N*D)",
+                   "timing": "median call time over the timed steps, CUDA events, L2 flushed "
+                             "before every call", "points": pts}
     metric = METRIC_DECODE if decode else (METRIC_BWD if bwd else METRIC)
     line = {
         "metric": metric, "value": round(value, 2), "unit": unit,
@@ -570,6 +608,7 @@ def run_ours(args):
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks, "sweep": sweep, "d128": d128_rep, "bwd": bwd_rep,
+        "gqa_prefill_fwd": gqa_rep,
         "wall_s_timed_region": round(t_wall, 3),
     }
     if args.config == "sweep" and not bwd and args.mask == "none":
@@ -595,6 +634,8 @@ D128_POINTS = (("video_dit", 17600), ("video_dit", 75600), ("training", 8192))
 PAGES_MI50_MS = {256: 0.18, 512: 0.29, 1024: 0.85, 2048: 4.74, 4096: 17.93, 8192: 72.75,
                  16384: 1325.69}
 BWD_POINTS = (("training", 8192), ("gqa_prefill", 4096))
+# the GQA causal prefill forward (Hq=14, Hkv=2, D=64 fp16), through attn_fwd_ws
+GQA_POINTS = (("gqa_prefill", 4096), ("gqa_prefill", 16384))
 
 
 def bench_config(w, seq, mask, world):
