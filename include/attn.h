@@ -96,10 +96,11 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
  *
  * The workspace also lets this call even out the grid (both dtypes).  attn_fwd
  * runs one CTA per SM-sized unit (KV group, pair of 128-row query tiles), so a
- * grid of U units runs as ceil(U / SMs) waves.  When the last wave's units,
- * cut into two key halves, fit in one wave (no causal mask, >= 8 key tiles),
- * or when the whole grid is under one wave (every unit cut into ranges of >= 16
- * key tiles), the cut units write fp32 partial results to the workspace and a
+ * grid of U units runs as ceil(U / SMs) waves.  When cutting the last wave's
+ * units into 2 to 4 key ranges shortens that wave by more than the extra CTAs
+ * and the merge cost (no causal mask, >= 8 key tiles; ranges of >= 4), or when
+ * the whole grid is under one wave (every unit cut into ranges of >= 16 key
+ * tiles), the cut units write fp32 partial results to the workspace and a
  * second kernel merges them (the online-softmax identity of attn_fwd_splitkv).
  * The rows of uncut units are attn_fwd's bit for bit (fp16); merged rows agree
  * with them to rounding.

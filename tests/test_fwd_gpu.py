@@ -307,8 +307,9 @@ def test_ws_fp16_is_attn_fwd(cuda_lib):
 
 
 # attn_fwd_ws also evens out the grid (one CTA per SM per unit of a KV group
-# and 256 query rows): the last wave's units are cut into two key halves when
-# the halves fit in one wave (no causal mask, >= 8 key tiles), and a grid under
+# and 256 query rows): the last wave's units are cut into 2 to 4 key ranges
+# when a model of the last wave's time says it pays (no causal mask, >= 8 key
+# tiles), and a grid under
 # one wave has every unit's keys cut into ranges of >= 16 key tiles; the cut
 # units' partials are merged by a second kernel.  The shapes below are cut on
 # a 152-SM GB300.
@@ -317,6 +318,7 @@ CUT_SHAPES = [
     # B, Hq, Hkv, Nq, Nk, D, dtype, causal
     (1, 4, 4, 10240, 1000, 64, F16, False),    # 160 units: 152 whole, 8 in halves; ragged keys
     (1, 8, 2, 5120, 1100, 64, F16, False),     # GQA 4:1, 9 key tiles: halves of 5 and 4
+    (1, 4, 4, 10240, 2048, 64, F16, False),    # 16 key tiles: the 8 tail units in quarters
     (1, 4, 4, 10240, 1000, 128, BF16, False),  # bf16 with the fp16 copy of V
     (1, 2, 2, 1000, 8000, 64, F16, False),     # 8 units: 3 ranges of 21 key tiles (the last 21)
     (1, 2, 2, 1000, 8000, 64, F16, "bottom_right"),  # causal: a range may hold no visible key
@@ -324,8 +326,11 @@ CUT_SHAPES = [
 ]
 
 
-def cut_plan(B, Hq, Hkv, Nq, Nk, causal, sms):
-    """(first output row of the cut units, ranges) as the library plans it."""
+def cut_plan(B, Hq, Hkv, Nq, Nk, D, causal, sms):
+    """(first output row of the cut units, ranges) as the library plans it:
+    a tail of several waves cut into S = 2..4 ranges when the model of the
+    last wave's time (rounds of 1/S of a unit, ~15 us per extra round, ~4 us
+    for the merge, ~1.1 / 2.2 us per key tile at D = 64 / 128) says it pays."""
     rows = Hq // Hkv * Nq
     n_pairs = -(-rows // 256)
     units = B * Hkv * n_pairs
@@ -333,10 +338,22 @@ def cut_plan(B, Hq, Hkv, Nq, Nk, causal, sms):
     if units >= sms:
         waves = -(-units // sms)
         tail = units - (waves - 1) * sms
-        if causal or tiles < 8 or waves < 2 or 2 * tail > sms:
+        if causal or tiles < 8 or waves < 2:
+            return None, 1
+        unit_us = tiles * (2.2 if D == 128 else 1.1)
+        best, best_s = 1.0, 1
+        for S in (2, 3, 4):
+            if tiles < 4 * S:
+                break
+            rounds = -(-tail * S // sms)
+            cost = rounds / S + (rounds - 1) * 15.0 / unit_us + 4.0 / unit_us
+            if cost < best - 0.02:
+                best, best_s = cost, S
+        if best_s < 2:
             return None, 1
         whole = units - tail
-        return (whole // n_pairs) * rows + (whole % n_pairs) * 256, 2
+        tps = -(-tiles // best_s)
+        return (whole // n_pairs) * rows + (whole % n_pairs) * 256, -(-tiles // tps)
     want = min(sms // units, tiles // 16, 256)
     if want < 2:
         return None, 1
@@ -350,7 +367,8 @@ def test_ws_cut_grid_every_row(cuda_lib, B, Hq, Hkv, Nq, Nk, D, dtype, causal):
     bit for bit (fp16: the same kernel arithmetic), the merged rows agree
     with the oracle at the usual bound."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    row0, splits = cut_plan(B, Hq, Hkv, Nq, Nk, bool(causal), sms)
+    row0, splits = cut_plan(B, Hq, Hkv, Nq, Nk, D, bool(causal), sms)
+    assert _lib.fwd_ws_splits(B, Hq, Hkv, Nq, Nk, D, causal) == splits
     if sms == 152:
         assert splits > 1
     ws = _lib.fwd_workspace_size(B, Hq, Hkv, Nq, Nk, D, dtype)

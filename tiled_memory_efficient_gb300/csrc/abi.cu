@@ -165,15 +165,21 @@ struct FwdPlan {
 
 // One CTA per SM (shared memory and the 512 TMEM columns), so a grid of U
 // equal units runs as ceil(U / SMs) waves.
-//  * Several waves: when the last wave's units, cut in two key halves, fit in
-//    one wave, they are cut (the last wave then takes about half as long).
-//    Only without the causal mask, whose units are laid out so that the last
-//    ones cover the last output rows; and with at least 8 key tiles.
+//  * Several waves (no causal mask, whose units are laid out so that the last
+//    ones cover the last output rows; at least 8 key tiles): the last wave's
+//    units are cut into S = 2, 3 or 4 key ranges (each of at least 4 key
+//    tiles) when that shortens the last wave: its pieces run in ceil(tail * S
+//    / SMs) rounds of 1/S of a unit, each round after the first costing ~15 us
+//    (CTA set-up, ramp, the extra partials) and the cut ~4 us of merge,
+//    against a unit of about 1.1 us (D = 64) or 2.2 us (D = 128) per key tile
+//    (measured: N = 8192 of the sweep, a tail of 56, gains 8% in halves; N =
+//    16384, a tail of 112, lost 1% in quarters; video-DiT N = 75600 gains 1-2%
+//    in quarters).  N = 4096 (104) is not cut.
 //  * Under one wave: every unit's keys are cut into as many ranges as fill
 //    the SMs, each of at least 16 key tiles (a range costs a CTA's fixed
 //    set-up and its share of the merge: two ranges of 4 key tiles made N =
 //    1024 (B = 1, H = 16, D = 64) 19% slower).
-FwdPlan fwd_plan(int B, int Hq, int Hkv, int Nq, int Nk, int causal) {
+FwdPlan fwd_plan(int B, int Hq, int Hkv, int Nq, int Nk, int causal, int D) {
     FwdPlan pl;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -189,10 +195,23 @@ FwdPlan fwd_plan(int B, int Hq, int Hkv, int Nq, int Nk, int causal) {
         if (causal != ATTN_CAUSAL_NONE || tiles < 8) return pl;
         const int64_t waves = (units + sms - 1) / sms;
         const int64_t tail = units - (waves - 1) * sms;
-        if (waves < 2 || 2 * tail > sms) return pl;
+        if (waves < 2) return pl;
+        const double unit_us = static_cast<double>(tiles) * (D == 128 ? 2.2 : 1.1);
+        const double fixed = 15.0 / unit_us, merge = 4.0 / unit_us;
+        double best = 1.0;
+        int best_s = 1;
+        for (int S = 2; S <= 4 && tiles >= 4 * S; ++S) {
+            const int64_t rounds = (tail * S + sms - 1) / sms;
+            const double cost = static_cast<double>(rounds) / S + (rounds - 1) * fixed + merge;
+            if (cost < best - 0.02) {
+                best = cost;
+                best_s = S;
+            }
+        }
+        if (best_s < 2) return pl;
         pl.n_whole = units - tail;
-        pl.splits = 2;
-        pl.tps = static_cast<int>((tiles + 1) / 2);
+        pl.tps = static_cast<int>((tiles + best_s - 1) / best_s);
+        pl.splits = static_cast<int>((tiles + pl.tps - 1) / pl.tps);
         return pl;
     }
     int64_t want = sms / units;
@@ -313,7 +332,7 @@ extern "C" size_t attn_fwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk
         bytes = pad256(groups * Nk * D * 2) + pad256(groups * static_cast<size_t>(key_tiles(Nk)));
     }
     // The plan without the causal mask cuts at least as much as with it.
-    return bytes + plan_bytes(fwd_plan(B, Hq, Hkv, Nq, Nk, ATTN_CAUSAL_NONE), B, Hq, Hkv, Nq, D);
+    return bytes + plan_bytes(fwd_plan(B, Hq, Hkv, Nq, Nk, ATTN_CAUSAL_NONE, D), B, Hq, Hkv, Nq, D);
 }
 
 extern "C" int attn_fwd_ws(const void* q, const void* k, const void* v, void* out, float* lse,
@@ -322,7 +341,7 @@ extern "C" int attn_fwd_ws(const void* q, const void* k, const void* v, void* ou
                            void* stream) {
     int rc = check_shape(B, Hq, Hkv, Nq, Nk, D, scale, dtype);
     if (rc != ATTN_OK) return rc;
-    const FwdPlan pl = fwd_plan(B, Hq, Hkv, Nq, Nk, causal);
+    const FwdPlan pl = fwd_plan(B, Hq, Hkv, Nq, Nk, causal, D);
     const bool bf16 = dtype == ATTN_BF16;
     // Workspace checks come before any device call.
     const size_t need = attn_fwd_workspace_size(B, Hq, Hkv, Nq, Nk, D, dtype);
@@ -369,7 +388,7 @@ extern "C" int attn_fwd_ws(const void* q, const void* k, const void* v, void* ou
 
 extern "C" int attn_fwd_ws_splits(int B, int Hq, int Hkv, int Nq, int Nk, int D, int causal) {
     if (check_shape(B, Hq, Hkv, Nq, Nk, D, 1.0f, ATTN_F16) != ATTN_OK) return 0;
-    return fwd_plan(B, Hq, Hkv, Nq, Nk, causal).splits;
+    return fwd_plan(B, Hq, Hkv, Nq, Nk, causal, D).splits;
 }
 
 extern "C" int attn_fwd_masked(const void* q, const void* k, const void* v, void* out, float* lse,
