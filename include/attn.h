@@ -127,11 +127,12 @@ size_t attn_fwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int D, in
 
 /*
  * Key ranges attn_fwd_ws cuts its cut units into for this shape and causal
- * mode on the current device: 1 when the grid is not cut (one forward
- * kernel, plus the value conversion for bf16), > 1 when a merge kernel
- * follows.  0 for invalid sizes.  Host-only.
+ * mode on a device of num_sms SMs (<= 0: the current device, as attn_fwd_ws
+ * does): 1 when the grid is not cut (one forward kernel, plus the value
+ * conversion for bf16), > 1 when a merge kernel follows.  0 for invalid
+ * sizes.  Host-only.
  */
-int attn_fwd_ws_splits(int B, int Hq, int Hkv, int Nq, int Nk, int D, int causal);
+int attn_fwd_ws_splits(int B, int Hq, int Hkv, int Nq, int Nk, int D, int causal, int num_sms);
 
 /*
  * Forward with an attention bias: the attn_mask argument of the SDPA call
@@ -213,14 +214,15 @@ size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int D, in
 
 /*
  * The number S of query ranges attn_bwd cuts the dK/dV work into at these
- * sizes and causal mode on the current device, given the workspace
+ * sizes and causal mode on a device of num_sms SMs (<= 0: the current one,
+ * as attn_bwd does), given the workspace
  * attn_bwd_workspace_size() recommends: 1 (three kernels: statistics, dK/dV,
  * dQ) or more (a fourth adds the ranges' partial sums).  Without the causal
  * mask, as many ranges as fill one wave of CTAs; with it, enough that the
  * CTAs of the first key tile (which meets every query tile) do no more than
  * the average work per SM.  0 for invalid sizes.  Host-only.
  */
-int attn_bwd_splits(int B, int Hq, int Hkv, int Nq, int Nk, int D, int causal);
+int attn_bwd_splits(int B, int Hq, int Hkv, int Nq, int Nk, int D, int causal, int num_sms);
 
 /*
  * Backward of attn_fwd (forum post, "Other areas where this could be useful":

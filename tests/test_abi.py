@@ -104,10 +104,31 @@ def test_fwd_ws_workspace_size_and_validation(lib):
     assert lib.attn_fwd_ws(*([P] * 5), P, ws, 1, 2, 2, 128, 128, 96, 0.125, 0, 1, None) == 2
     # plan queries: small grids whose ranges would be under 4 key tiles (or no
     # device) are not cut; invalid sizes give 0
-    assert lib.attn_fwd_ws_splits(1, 2, 2, 300, 300, 64, 0) == 1
-    assert lib.attn_fwd_ws_splits(1, 3, 2, 300, 300, 64, 0) == 0
-    assert lib.attn_bwd_splits(1, 2, 2, 300, 300, 64, 1) == 1
-    assert lib.attn_bwd_splits(1, 3, 2, 300, 300, 64, 0) == 0
+    assert lib.attn_fwd_ws_splits(1, 2, 2, 300, 300, 64, 0, 0) == 1
+    assert lib.attn_fwd_ws_splits(1, 3, 2, 300, 300, 64, 0, 152) == 0
+    assert lib.attn_bwd_splits(1, 2, 2, 300, 300, 64, 1, 0) == 1
+    assert lib.attn_bwd_splits(1, 3, 2, 300, 300, 64, 0, 152) == 0
+
+
+def test_launch_plans_for_152_sms(lib):
+    """The grid plans for a 152-SM GB300, computed on the host.
+    attn_fwd_ws: the last wave's units cut into 2..4 key ranges when a model
+    of that wave says it pays; a grid under one wave cut into ranges of >= 16
+    key tiles.  attn_bwd: dK/dV query ranges filling one wave, or (causal)
+    sized so key tile 0's CTAs do no more than the average work per SM."""
+    fwd = lambda B, Hq, Hkv, N, D, causal=0, Nk=None: lib.attn_fwd_ws_splits(
+        B, Hq, Hkv, N, Nk or N, D, causal, 152)
+    # the sweep (B=1, H=16, D=64): only N = 8192 (a last wave of 56 units) is cut
+    assert [fwd(1, 16, 16, n, 64) for n in (256, 1024, 2048, 4096, 8192, 16384)] == [1, 1, 1, 1, 2, 1]
+    assert fwd(1, 24, 24, 17600, 128) == 1 and fwd(1, 24, 24, 75600, 128) == 4   # video-DiT
+    assert fwd(2, 16, 16, 8192, 128, causal=1) == 1          # causal grids are not cut
+    assert fwd(1, 4, 4, 10240, 64, Nk=1000) == 2             # the parity cases of the cut
+    assert fwd(1, 4, 4, 10240, 64, Nk=2048) == 4
+    assert fwd(8, 14, 2, 1, 64, Nk=65536) == 9               # decode shape: 16 units, 512 key tiles
+    bwd = lambda B, Hq, Hkv, N, D, causal: lib.attn_bwd_splits(B, Hq, Hkv, N, N, D, causal, 152)
+    assert [bwd(1, 14, 2, n, 64, 1) for n in (2048, 4096, 8192, 16384)] == [9, 5, 3, 1]
+    assert bwd(1, 14, 2, 4096, 64, 0) == 3
+    assert bwd(2, 16, 16, 8192, 128, 1) == 1
 
 
 def test_bwd_rejects_bottom_right(lib):

@@ -54,8 +54,8 @@ _SIGNATURES = {
     "attn_fwd_ws": ([_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _i, _i, _i, _i, _i, _i,
                      ctypes.c_float, _i, _i, _vp], _i),
     "attn_fwd_workspace_size": ([_i, _i, _i, _i, _i, _i, _i], ctypes.c_size_t),
-    "attn_fwd_ws_splits": ([_i, _i, _i, _i, _i, _i, _i], _i),
-    "attn_bwd_splits": ([_i, _i, _i, _i, _i, _i, _i], _i),
+    "attn_fwd_ws_splits": ([_i, _i, _i, _i, _i, _i, _i, _i], _i),
+    "attn_bwd_splits": ([_i, _i, _i, _i, _i, _i, _i, _i], _i),
     "attn_fwd_num_splits": ([_i, _i, _i, _i, _i, _i, _i], _i),
     "attn_bwd_workspace_size": ([_i, _i, _i, _i, _i, _i, _i], ctypes.c_size_t),
     "attn_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
@@ -239,16 +239,17 @@ def fwd_workspace_size(B, Hq, Hkv, Nq, Nk, D, dtype) -> int:
     return load().attn_fwd_workspace_size(B, Hq, Hkv, Nq, Nk, D, code)
 
 
-def fwd_ws_splits(B, Hq, Hkv, Nq, Nk, D, causal=False) -> int:
-    """Key ranges attn_fwd_ws cuts its cut units into on the current device
-    (1: the grid is not cut, no merge kernel)."""
-    return load().attn_fwd_ws_splits(B, Hq, Hkv, Nq, Nk, D, causal_code(causal))
+def fwd_ws_splits(B, Hq, Hkv, Nq, Nk, D, causal=False, num_sms: int = 0) -> int:
+    """Key ranges attn_fwd_ws cuts its cut units into on a device of num_sms
+    SMs (0: the current device; 1: the grid is not cut, no merge kernel)."""
+    return load().attn_fwd_ws_splits(B, Hq, Hkv, Nq, Nk, D, causal_code(causal), num_sms)
 
 
-def bwd_splits(B, Hq, Hkv, Nq, Nk, D, causal=False) -> int:
+def bwd_splits(B, Hq, Hkv, Nq, Nk, D, causal=False, num_sms: int = 0) -> int:
     """Query ranges attn_bwd cuts the dK/dV work into with its recommended
-    workspace (1: no partial-sum kernel)."""
-    return load().attn_bwd_splits(B, Hq, Hkv, Nq, Nk, D, causal_code(causal))
+    workspace on a device of num_sms SMs (0: the current device; 1: no
+    partial-sum kernel)."""
+    return load().attn_bwd_splits(B, Hq, Hkv, Nq, Nk, D, causal_code(causal), num_sms)
 
 
 def attn_fwd_ws(q, k, v, causal=False, scale: float | None = None, out=None, lse=None,

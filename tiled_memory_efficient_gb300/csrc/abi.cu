@@ -155,6 +155,18 @@ int effective_splits(int Nk, int requested) {
     return static_cast<int>((tiles + per - 1) / per);
 }
 
+// SM count of the current device (0 without one, leaving no error behind).
+int device_sms() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0) {
+        cudaGetLastError();
+        return 0;
+    }
+    return sms;
+}
+
 // Launch plan of attn_fwd_ws: units [0, n_whole) run whole, the keys of the
 // rest are cut into `splits` ranges of `tps` key tiles (FwdParams).
 struct FwdPlan {
@@ -179,15 +191,10 @@ struct FwdPlan {
 //    the SMs, each of at least 16 key tiles (a range costs a CTA's fixed
 //    set-up and its share of the merge: two ranges of 4 key tiles made N =
 //    1024 (B = 1, H = 16, D = 64) 19% slower).
-FwdPlan fwd_plan(int B, int Hq, int Hkv, int Nq, int Nk, int causal, int D) {
+FwdPlan fwd_plan(int B, int Hq, int Hkv, int Nq, int Nk, int causal, int D, int sms = 0) {
     FwdPlan pl;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        sms <= 0) {
-        cudaGetLastError();   // leave no error behind on a machine without a device
-        return pl;
-    }
+    if (sms <= 0) sms = device_sms();
+    if (sms <= 0) return pl;
     const int64_t rows = static_cast<int64_t>(Hq / Hkv) * Nq;
     const int64_t units = static_cast<int64_t>(B) * Hkv * ((rows + 255) / 256);
     const int64_t tiles = key_tiles(Nk);
@@ -386,9 +393,10 @@ extern "C" int attn_fwd_ws(const void* q, const void* k, const void* v, void* ou
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-extern "C" int attn_fwd_ws_splits(int B, int Hq, int Hkv, int Nq, int Nk, int D, int causal) {
+extern "C" int attn_fwd_ws_splits(int B, int Hq, int Hkv, int Nq, int Nk, int D, int causal,
+                                  int num_sms) {
     if (check_shape(B, Hq, Hkv, Nq, Nk, D, 1.0f, ATTN_F16) != ATTN_OK) return 0;
-    return fwd_plan(B, Hq, Hkv, Nq, Nk, causal, D).splits;
+    return fwd_plan(B, Hq, Hkv, Nq, Nk, causal, D, num_sms).splits;
 }
 
 extern "C" int attn_fwd_masked(const void* q, const void* k, const void* v, void* out, float* lse,
@@ -518,17 +526,13 @@ namespace {
 // no more than the average work per SM (GQA 14:2, N = 4096: 5 ranges, 277 ->
 // 381 TFLOP/s against the one-wave rule).  At least 4 query tiles per range,
 // at most 32 ranges.
-int bwd_splits(int B, int Hq, int Hkv, int Nq, int Nk, bool causal, int* tiles_per_split) {
+int bwd_splits(int B, int Hq, int Hkv, int Nq, int Nk, bool causal, int* tiles_per_split,
+               int sms = 0) {
     const int64_t groups = static_cast<int64_t>(B) * Hkv;
     const int64_t n_qtiles = (static_cast<int64_t>(Hq / Hkv) * Nq + 127) / 128;
     *tiles_per_split = static_cast<int>(n_qtiles);
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        sms <= 0) {
-        cudaGetLastError();   // leave no error behind on a machine without a device
-        return 1;
-    }
+    if (sms <= 0) sms = device_sms();
+    if (sms <= 0) return 1;
     const int64_t units = groups * key_tiles(Nk);
     if (units >= sms) return 1;
     int64_t want = (sms + units - 1) / units;
@@ -549,10 +553,11 @@ int bwd_splits(int B, int Hq, int Hkv, int Nq, int Nk, bool causal, int* tiles_p
 }  // namespace
 }  // namespace tme
 
-extern "C" int attn_bwd_splits(int B, int Hq, int Hkv, int Nq, int Nk, int D, int causal) {
+extern "C" int attn_bwd_splits(int B, int Hq, int Hkv, int Nq, int Nk, int D, int causal,
+                               int num_sms) {
     if (check_shape(B, Hq, Hkv, Nq, Nk, D, 1.0f, ATTN_F16) != ATTN_OK) return 0;
     int per = 0;
-    return bwd_splits(B, Hq, Hkv, Nq, Nk, causal != ATTN_CAUSAL_NONE, &per);
+    return bwd_splits(B, Hq, Hkv, Nq, Nk, causal != ATTN_CAUSAL_NONE, &per, num_sms);
 }
 
 extern "C" size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int D,
