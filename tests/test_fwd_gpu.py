@@ -319,6 +319,7 @@ CUT_SHAPES = [
     (1, 4, 4, 10240, 1000, 64, F16, False),    # 160 units: 152 whole, 8 in halves; ragged keys
     (1, 8, 2, 5120, 1100, 64, F16, False),     # GQA 4:1, 9 key tiles: halves of 5 and 4
     (1, 4, 4, 10240, 2048, 64, F16, False),    # 16 key tiles: the 8 tail units in quarters
+    (1, 4, 4, 10100, 1000, 64, F16, False),    # heads of 10100 rows: the cut rows end mid-pair
     (1, 4, 4, 10240, 1000, 128, BF16, False),  # bf16 with the fp16 copy of V
     (1, 2, 2, 1000, 8000, 64, F16, False),     # 8 units: 3 ranges of 21 key tiles (the last 21)
     (1, 2, 2, 1000, 8000, 64, F16, "bottom_right"),  # causal: a range may hold no visible key
