@@ -150,8 +150,11 @@ int attn_fwd_ws_splits(int B, int Hq, int Hkv, int Nq, int Nk, int D, int causal
  * mask is read, never written, and must stay valid until the work completes.
  * Speed: at D = 64 a boolean mask that depends on the key alone (stride_q 0,
  * and stride_h 0 unless Hq == Hkv: a padding mask) runs in the unmasked
- * forward's layout, at most of its speed; any other mask takes a slower
- * general path (one thread per query row, the bias folded into the scores).
+ * forward's layout and skips key tiles past the last kept key; any other mask
+ * stages each key tile's bias in shared memory and folds it into the scores
+ * (D = 64 fp16: in the unmasked layout; bf16 D = 64: one thread per query
+ * row), at about half the unmasked speed; at D = 128 each row reads its bias
+ * directly.
  */
 int attn_fwd_masked(const void* q, const void* k, const void* v, void* out, float* lse,
                     const void* mask, int mask_kind, long long mask_stride_b,
