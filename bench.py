@@ -14,7 +14,7 @@ sum of algorithmic FLOPs / sum of those times.  The default run also times,
 in the same region and with their own events, the head-dim-128 points of the
 >= 60%-of-peak target (video-DiT at N = 17600 and 75600, the training forward
 at N = 8192) under "d128", the backward of the training and GQA-prefill
-workloads under "bwd", and the GQA causal prefill forward (N = 4096, 16384)
+workloads under "bwd", and the GQA causal prefill forward (N = 1024 .. 16384)
 under "gqa_prefill_fwd".  Prints ONE JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -592,7 +592,9 @@ def run_ours(args):
             pts.append({"workload": wd.note, "N": n, "ms": round(ms, 4), "tflops": round(tf, 1),
                         "frac_of_peak": round(tf / pk["bf16_tflops"], 4),
                         "key_ranges": _lib.fwd_ws_splits(wd.B, wd.Hq, wd.Hkv, n, n, wd.D,
-                                                         wd.causal)})
+                                                         wd.causal),
+                        "half_positions": _lib.fwd_half_positions(wd.B, wd.Hq, wd.Hkv, n, n,
+                                                                  wd.D, wd.causal, wd.dtype)})
         gqa_rep = {"entry": "attn_fwd_ws (causal FLOPs: half of 4*B*Hq*N*N*D)",
                    "timing": "median call time over the timed steps, CUDA events, L2 flushed "
                              "before every call", "points": pts}
@@ -635,7 +637,7 @@ PAGES_MI50_MS = {256: 0.18, 512: 0.29, 1024: 0.85, 2048: 4.74, 4096: 17.93, 8192
                  16384: 1325.69}
 BWD_POINTS = (("training", 8192), ("gqa_prefill", 4096))
 # the GQA causal prefill forward (Hq=14, Hkv=2, D=64 fp16), through attn_fwd_ws
-GQA_POINTS = (("gqa_prefill", 4096), ("gqa_prefill", 16384))
+GQA_POINTS = tuple(("gqa_prefill", n) for n in (1024, 2048, 4096, 8192, 16384))
 
 
 def bench_config(w, seq, mask, world):

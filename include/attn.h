@@ -135,6 +135,19 @@ size_t attn_fwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int D, in
 int attn_fwd_ws_splits(int B, int Hq, int Hkv, int Nq, int Nk, int D, int causal, int num_sms);
 
 /*
+ * Causal mask, D = 64, fp16, Nq a multiple of 256: how many of the heaviest
+ * 256-row pair positions of every head attn_fwd (and attn_fwd_ws, when it
+ * does not cut keys into ranges) runs as two CTAs per pair, one per 128-row
+ * Q tile, on a device of num_sms SMs (<= 0: the current device; 0 without
+ * one).  A pair's work grows with its position under the causal mask, and
+ * at short sequences the last pairs of each head outlast the average work
+ * per SM; the split changes no result bit.  0 for every other shape, -1 for
+ * invalid sizes or causal mode.  Host-only.
+ */
+int attn_fwd_half_positions(int B, int Hq, int Hkv, int Nq, int Nk, int D, int causal, int dtype,
+                            int num_sms);
+
+/*
  * Forward with an attention bias: the attn_mask argument of the SDPA call
  * that the forum post patches ("Other areas where this could be useful":
  * every SDPA call, e.g. from HuggingFace Transformers, which pass padding and

@@ -124,6 +124,39 @@ def test_workloads_sampled_rows(cuda_lib, name, n):
     print(f"{name} N={n}: rows={len(rows)} max|dO|={eo:.2e} max|dLSE|={el:.2e}")
 
 
+# The causal forward at short sequences runs the heaviest pair positions as
+# two one-tile CTAs per pair (attn_fwd_half_positions): the split changes which
+# CTA computes a row, not its arithmetic.  A key-only all-true mask (which
+# takes the same split-softmax layout without the split) must agree bit for
+# bit, and every row matches the oracle.
+
+HALF_SHAPES = [
+    # B, Hq, Hkv, Nq, Nk, causal
+    (1, 14, 2, 2048, 2048, True),            # the GQA prefill at N = 2048: 3 positions split
+    (1, 2, 2, 512, 512, True),               # one position split
+    (1, 2, 2, 512, 1000, "bottom_right"),    # Nk > Nq: every row sees 488 more keys
+    (2, 4, 2, 768, 768, True),               # B = 2, GQA 2:1, three pairs per head
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,causal", HALF_SHAPES)
+def test_half_pairs_every_row_and_bitwise(cuda_lib, B, Hq, Hkv, Nq, Nk, causal):
+    h = _lib.fwd_half_positions(B, Hq, Hkv, Nq, Nk, 64, causal, F16)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms == 152:
+        assert h > 0
+    x = inputs.make_custom(B, Hq, Hkv, Nq, Nk, 64, F16, seed=Nq + Nk + Hq)
+    check_full(x, causal, what=f"half pairs {(B, Hq, Hkv, Nq, Nk, causal)}")
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    a = _lib.attn_fwd(q, k, v, causal=causal)
+    b = _lib.attn_fwd(q, k, v, causal=causal,
+                      mask=torch.ones((B, 1, 1, Nk), dtype=torch.bool, device="cuda"))
+    c = _lib.attn_fwd_ws(q, k, v, causal=causal)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    assert torch.equal(a[0], c[0]) and torch.equal(a[1], c[1])
+
+
 def test_output_canaries_untouched(cuda_lib):
     B, Hq, Hkv, N, D = 1, 3, 3, 200, 64
     x = inputs.make_custom(B, Hq, Hkv, N, N, D, F16, seed=11)

@@ -55,6 +55,7 @@ _SIGNATURES = {
                      ctypes.c_float, _i, _i, _vp], _i),
     "attn_fwd_workspace_size": ([_i, _i, _i, _i, _i, _i, _i], ctypes.c_size_t),
     "attn_fwd_ws_splits": ([_i, _i, _i, _i, _i, _i, _i, _i], _i),
+    "attn_fwd_half_positions": ([_i, _i, _i, _i, _i, _i, _i, _i, _i], _i),
     "attn_bwd_splits": ([_i, _i, _i, _i, _i, _i, _i, _i], _i),
     "attn_fwd_num_splits": ([_i, _i, _i, _i, _i, _i, _i], _i),
     "attn_bwd_workspace_size": ([_i, _i, _i, _i, _i, _i, _i], ctypes.c_size_t),
@@ -243,6 +244,16 @@ def fwd_ws_splits(B, Hq, Hkv, Nq, Nk, D, causal=False, num_sms: int = 0) -> int:
     """Key ranges attn_fwd_ws cuts its cut units into on a device of num_sms
     SMs (0: the current device; 1: the grid is not cut, no merge kernel)."""
     return load().attn_fwd_ws_splits(B, Hq, Hkv, Nq, Nk, D, causal_code(causal), num_sms)
+
+
+def fwd_half_positions(B, Hq, Hkv, Nq, Nk, D, causal=True, dtype="float16",
+                       num_sms: int = 0) -> int:
+    """Heaviest pair positions per head that the causal forward runs as two
+    one-tile CTAs per pair (0: none; see attn_fwd_half_positions)."""
+    code = dtype if isinstance(dtype, int) else (ATTN_BF16 if str(dtype).endswith("bfloat16")
+                                                 else ATTN_F16)
+    return load().attn_fwd_half_positions(B, Hq, Hkv, Nq, Nk, D, causal_code(causal), code,
+                                          num_sms)
 
 
 def bwd_splits(B, Hq, Hkv, Nq, Nk, D, causal=False, num_sms: int = 0) -> int:

@@ -6,7 +6,10 @@
 
 #include <cmath>
 #include <cstdint>
+#include <functional>
 #include <mutex>
+#include <queue>
+#include <vector>
 
 #include "../../include/attn.h"
 #include "attn_internal.h"
@@ -244,6 +247,94 @@ void plan_rows(const FwdPlan& pl, int B, int Hq, int Hkv, int Nq, int64_t* row0,
 
 size_t pad256(size_t b) { return (b + 255) & ~size_t(255); }
 
+// Causal forward, D = 64 fp16, Nq a multiple of 256, no key ranges: how many
+// of the heaviest pair positions run as two CTAs per pair, one per Q tile
+// (FwdParams::n_half_pos).  Under the causal mask a pair's work grows with
+// its position, and the grid runs heaviest first, so at short sequences the
+// last pairs of each head outlast the average work per SM.  A one-tile CTA
+// runs its key tiles in kHalfTime of the pair's time (half the tensor work,
+// and each SM sub-partition runs two softmax warps instead of four); every
+// CTA costs kCtaTiles key-tile times more (set-up, first loads, last PV,
+// epilogue).  The plan simulates the hardware's in-order assignment of CTAs to
+// the first free SM for every count of split positions and keeps the
+// shortest, unless it saves under 2% (grids of more than 8 waves of pairs are
+// not split: the spread of their pairs no longer matters).  The constants are
+// fitted to GQA 14:2 prefill launches on a 152-SM GB300 (N = 1024 .. 16384,
+// 0 to all positions split; the fit is within 8% of every launch): split 2 /
+// 3 / 0 / 0 / 0 positions there, 18.4 -> 16.4 us at N = 1024 and 28.7 -> 22.5 us
+// at N = 2048; at N >= 8192 every split measured slower.
+constexpr double kHalfTime = 0.725;
+constexpr double kCtaTiles = 4.5;
+
+int plan_half_positions(int64_t heads, int Nq, int Nk, int causal, int sms) {
+    const int m = Nq / 256;
+    const int64_t off = causal == ATTN_CAUSAL_BOTTOM_RIGHT ? static_cast<int64_t>(Nk) - Nq : 0;
+    std::vector<double> t(m);   // key tiles of the later Q tile of the pair at position i from the top
+    for (int i = 0; i < m; ++i) {
+        int64_t keys = static_cast<int64_t>(m - 1 - i) * 256 + 256 + off;
+        if (keys > Nk) keys = Nk;
+        t[i] = keys <= 0 ? 0.0 : static_cast<double>((keys + 127) / 128);
+    }
+    double best = 0.0;
+    int best_h = 0;
+    for (int h = 0; h <= m; ++h) {
+        std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+        for (int s_ = 0; s_ < sms; ++s_) free_at.push(0.0);
+        double end = 0.0;
+        auto run = [&](double cost) {
+            const double t0 = free_at.top();
+            free_at.pop();
+            free_at.push(t0 + cost);
+            if (t0 + cost > end) end = t0 + cost;
+        };
+        for (int i = 0; i < m; ++i)
+            for (int64_t r = 0; r < heads; ++r) {
+                if (i < h) {
+                    run(kHalfTime * t[i] + kCtaTiles);
+                    run(kHalfTime * t[i] + kCtaTiles);
+                } else {
+                    run(t[i] + kCtaTiles);
+                }
+            }
+        if (h == 0 || end < 0.98 * best) {
+            best = end;
+            best_h = h;
+        }
+    }
+    return best_h;
+}
+
+// The plan above, remembered per shape (the simulation costs up to a few
+// hundred microseconds of host time, which a launch must not wait for).
+int half_positions(int B, int Hq, int Nq, int Nk, int causal, int D, int dtype, int sms) {
+    if (causal == ATTN_CAUSAL_NONE || D != 64 || dtype != ATTN_F16 || Nq % 256 != 0) return 0;
+    if (sms <= 0) sms = device_sms();
+    if (sms <= 0) return 0;
+    const int64_t heads = static_cast<int64_t>(B) * Hq;
+    if (heads * (Nq / 256) > 8LL * sms) return 0;
+    struct Entry {
+        int64_t heads;
+        int Nq, Nk, causal, sms, h;
+    };
+    static std::mutex mu;
+    static Entry cache[64];
+    static int n_cached = 0, next = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < n_cached; ++i) {
+            const Entry& e = cache[i];
+            if (e.heads == heads && e.Nq == Nq && e.Nk == Nk && e.causal == causal && e.sms == sms)
+                return e.h;
+        }
+    }
+    const int h = plan_half_positions(heads, Nq, Nk, causal, sms);
+    std::lock_guard<std::mutex> lock(mu);
+    cache[next] = Entry{heads, Nq, Nk, causal, sms, h};
+    next = (next + 1) % 64;
+    if (n_cached < 64) ++n_cached;
+    return h;
+}
+
 // Bytes of the split partials of a plan (0 without a split).
 size_t plan_bytes(const FwdPlan& pl, int B, int Hq, int Hkv, int Nq, int D) {
     if (pl.splits < 2) return 0;
@@ -325,6 +416,7 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, 
     const int rc = fwd_prepare(q, k, v, out, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, dtype,
                                &tmQ, &tmK, &tmV, &p);
     if (rc != ATTN_OK) return rc;
+    p.n_half_pos = half_positions(B, Hq, Nq, Nk, causal, D, dtype, 0);
     const cudaError_t e = launch_fwd(D, dtype == ATTN_BF16, causal != ATTN_CAUSAL_NONE, tmQ, tmK,
                                      tmV, p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -375,6 +467,7 @@ extern "C" int attn_fwd_ws(const void* q, const void* k, const void* v, void* ou
         p.n_ktiles = static_cast<int>(key_tiles(Nk));
         off = v_bytes + pad256(static_cast<size_t>(groups) * key_tiles(Nk));
     }
+    if (pl.splits == 1) p.n_half_pos = half_positions(B, Hq, Nq, Nk, causal, D, dtype, 0);
     if (pl.splits > 1) {
         p.n_splits = pl.splits;
         p.tiles_per_split = pl.tps;
@@ -391,6 +484,13 @@ extern "C" int attn_fwd_ws(const void* q, const void* k, const void* v, void* ou
                        bf16 ? &tmV16 : nullptr);
     if (e == cudaSuccess && pl.splits > 1) e = launch_splitkv_merge(D, bf16, p, st);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+extern "C" int attn_fwd_half_positions(int B, int Hq, int Hkv, int Nq, int Nk, int D,
+                                       int causal, int dtype, int num_sms) {
+    if (check_shape(B, Hq, Hkv, Nq, Nk, D, 1.0f, dtype) != ATTN_OK) return -1;
+    if (causal < ATTN_CAUSAL_NONE || causal > ATTN_CAUSAL_BOTTOM_RIGHT) return -1;
+    return half_positions(B, Hq, Nq, Nk, causal, D, dtype, num_sms);
 }
 
 extern "C" int attn_fwd_ws_splits(int B, int Hq, int Hkv, int Nq, int Nk, int D, int causal,

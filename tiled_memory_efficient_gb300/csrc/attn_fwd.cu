@@ -300,12 +300,26 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
         split = c % p.n_splits;
     }
     int group, pair;
+    int only = -1;   // >= 0: the one Q tile of the pair this CTA runs
     if (CAUSAL && p.Nq % (2 * kRows) == 0) {
         const int m = p.Nq / (2 * kRows);        // pairs per head (n_pairs = G * m)
         const int heads = p.n_groups * p.G;      // (group, head) combinations
-        const int r = unit % heads;
+        // The n_half_pos heaviest positions run as two CTAs per pair, one per
+        // Q tile (the later rows, which see one more key tile, first); the
+        // other positions follow, one CTA per pair.
+        const int n_half = 2 * heads * p.n_half_pos;
+        int pos, r;                              // position from the top, (group, head)
+        if (unit < n_half) {
+            pos = unit / (2 * heads);
+            r = (unit % (2 * heads)) >> 1;
+            only = 1 - (unit & 1);
+        } else {
+            const int u = unit - n_half + heads * p.n_half_pos;
+            pos = u / heads;
+            r = u % heads;
+        }
         group = r / p.G;
-        pair = (r % p.G) * m + (m - 1 - unit / heads);
+        pair = (r % p.G) * m + (m - 1 - pos);
     } else if (MASK && !CAUSAL) {
         // A general mask is often one bias for every head (and batch): with
         // the pairs walked position-major over the groups, the CTAs that read
@@ -324,6 +338,8 @@ __global__ void __launch_bounds__(FwdCfg<D, MK, BF16, VPRE>::kThreads, 1)
     const int tps = split >= 0 ? p.tiles_per_split : 0x7fffffff - kt0;
     int n0 = tiles_in_range(kv_tiles_for(row_base, p, CAUSAL), kt0, tps);
     int n1 = tiles_in_range(kv_tiles_for(row_base + kRows, p, CAUSAL), kt0, tps);
+    if (only == 0) n1 = 0;
+    if (only == 1) n0 = 0;
     int nmax = n0 > n1 ? n0 : n1;
     // A boolean mask that depends on the key alone (one row of keep bytes for
     // the whole CTA, as a padding mask is) removes every key tile past its
@@ -1089,7 +1105,8 @@ cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
     if (e != cudaSuccess) return e;
     const long long units = static_cast<long long>(p.n_groups) * p.n_pairs;
     const long long ctas =
-        p.n_splits > 1 ? p.n_whole + (units - p.n_whole) * p.n_splits : units;
+        (p.n_splits > 1 ? p.n_whole + (units - p.n_whole) * p.n_splits : units) +
+        static_cast<long long>(p.n_groups) * p.G * p.n_half_pos;
     return launch_kernel(kern, dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, stream,
                          tmQ, tmK, tmV, tmV16, p);
 }

@@ -60,6 +60,10 @@ struct FwdParams {
     // 128-key tile), 0 when the copy holds that tile.
     const uint8_t* vflags;
     int n_ktiles;            // ceil(Nk / 128)
+    // Causal mask with Nq % 256 == 0 and no key ranges (n_splits == 1): the
+    // n_half_pos heaviest pair positions of every head run as two CTAs per
+    // pair, one per Q tile (n_groups * G * n_half_pos more CTAs); 0: none.
+    int n_half_pos;
 };
 
 // Launches the forward kernel for one (D, dtype, causal) instantiation.
