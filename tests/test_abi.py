@@ -135,18 +135,18 @@ def test_half_positions_for_152_sms(lib):
     """The causal forward's one-tile CTAs (D=64 fp16, Nq % 256 == 0): the
     heaviest pair positions run as two CTAs when a simulation of the grid on
     152 SMs says it saves >= 2%.  The GQA prefill (B=1, 14:2) splits at N =
-    1024 and 2048 only."""
+    1024, 2048 and 4096 only."""
     half = lambda B, Hq, Hkv, N, D=64, causal=1, dtype=0, Nk=None, sms=152: \
         lib.attn_fwd_half_positions(B, Hq, Hkv, N, Nk or N, D, causal, dtype, sms)
-    assert [half(1, 14, 2, n) for n in (1024, 2048, 4096, 8192, 16384)] == [1, 3, 0, 0, 0]
-    assert half(1, 2, 2, 512) == 1 and half(1, 2, 2, 512, causal=2, Nk=1000) == 1
+    assert [half(1, 14, 2, n) for n in (1024, 2048, 4096, 8192, 16384)] == [2, 3, 1, 0, 0]
+    assert half(1, 2, 2, 512) == 1 and half(1, 2, 2, 512, causal=2, Nk=1000) == 2
     # shapes the split does not serve
     assert half(1, 14, 2, 1024, causal=0) == 0            # no causal mask
     assert half(1, 14, 2, 1024, dtype=1) == 0             # bf16: one thread per row
     assert half(1, 14, 2, 1024, D=128) == 0
     assert half(1, 14, 2, 1000) == 0                      # Nq not a multiple of 256
     assert half(2, 16, 16, 8192, D=128, dtype=1) == 0     # the training forward
-    assert half(1, 14, 2, 1024, sms=0) in (0, 1)          # current device (0 without one)
+    assert half(1, 14, 2, 1024, sms=0) in (0, 2)          # current device (0 without one)
     assert half(1, 14, 3, 1024) == -1                     # invalid sizes
     assert half(1, 14, 2, 1024, causal=3) == -1
 

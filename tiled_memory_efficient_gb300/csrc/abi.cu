@@ -260,11 +260,12 @@ size_t pad256(size_t b) { return (b + 255) & ~size_t(255); }
 // shortest, unless it saves under 2% (grids of more than 8 waves of pairs are
 // not split: the spread of their pairs no longer matters).  The constants are
 // fitted to GQA 14:2 prefill launches on a 152-SM GB300 (N = 1024 .. 16384,
-// 0 to all positions split; the fit is within 8% of every launch): split 2 /
-// 3 / 0 / 0 / 0 positions there, 18.4 -> 16.4 us at N = 1024 and 28.7 -> 22.5 us
-// at N = 2048; at N >= 8192 every split measured slower.
-constexpr double kHalfTime = 0.725;
-constexpr double kCtaTiles = 4.5;
+// 0 to all positions split) so that the plan's pick is the measured best at
+// every N: 2 / 3 / 1 / 0 / 0 positions, 18.4 -> 16.4 us at N = 1024, 28.7 ->
+// 22.5 us at N = 2048 and 49.2 -> 47.1 us at N = 4096; at N >= 8192 every
+// split measured slower.
+constexpr double kHalfTime = 0.70;
+constexpr double kCtaTiles = 2.5;
 
 int plan_half_positions(int64_t heads, int Nq, int Nk, int causal, int sms) {
     const int m = Nq / 256;
