@@ -232,8 +232,8 @@ size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int D, in
  * The number S of query ranges attn_bwd cuts the dK/dV work into at these
  * sizes and causal mode on a device of num_sms SMs (<= 0: the current one,
  * as attn_bwd does), given the workspace
- * attn_bwd_workspace_size() recommends: 1 (three kernels: statistics, dK/dV,
- * dQ) or more (a fourth adds the ranges' partial sums).  Without the causal
+ * attn_bwd_workspace_size() recommends: 1 (three kernels: statistics, dQ,
+ * dK/dV) or more (a fourth adds the ranges' partial sums).  Without the causal
  * mask, as many ranges as fill one wave of CTAs; with it, enough that the
  * CTAs of the first key tile (which meets every query tile) do no more than
  * the average work per SM.  0 for invalid sizes.  Host-only.

@@ -576,6 +576,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+    // Launched as a programmatic dependent of the dQ kernel (whose results it
+    // does not read): it does not end before dQ has, so whatever follows in the
+    // stream sees both.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- dQ
@@ -664,6 +668,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     if (key_only && nkv > 0) nkv = min(nkv, *key_lim);
+    // Launched as a programmatic dependent of the statistics kernel: its set-up
+    // above overlaps that kernel's end; nothing below runs before its results
+    // are complete.  Then the dK/dV kernel, which reads nothing this one
+    // writes, may start on the SMs this grid leaves idle once every CTA here
+    // has passed this point (so it, too, sees the statistics).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
 
     if (warp == kProducerWarp) {
         if (lane == 0) {
@@ -895,6 +906,9 @@ constexpr int dq_smem() {
 // in the input dtype (dK scaled): 8 consecutive elements per thread.
 template <bool BF16>
 __global__ void __launch_bounds__(256) bwd_dkdv_reduce_kernel(const BwdParams p, int64_t n8) {
+    // Launched as a programmatic dependent of the dK/dV kernel: wait for its
+    // partial sums (and, through its own wait, for the dQ kernel).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= n8) return;
     const int64_t stride = n8 * 8;   // elements per range
@@ -916,6 +930,25 @@ __global__ void __launch_bounds__(256) bwd_dkdv_reduce_kernel(const BwdParams p,
     }
 }
 
+// Launch as a programmatic dependent of the previous kernel in the stream:
+// the grid may start before that kernel has ended, and waits for it on the
+// device (griddepcontrol.wait) where it needs its results.
+template <typename Kern, typename... Args>
+cudaError_t launch_dependent(Kern kern, long long ctas, int threads, int smem,
+                             cudaStream_t stream, Args... args) {
+    cudaLaunchAttribute attr{};
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <int D, bool BF16, bool CAUSAL, int MK>
 cudaError_t launch_dq(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                       const CUtensorMap& tmDO, const BwdParams& p, cudaStream_t stream) {
@@ -924,8 +957,7 @@ cudaError_t launch_dq(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUte
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const long long ctas = static_cast<long long>(p.n_groups) * p.n_qtiles;
-    return launch_kernel(kern, dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, stream,
-                         tmQ, tmDO, tmK, tmV, p);
+    return launch_dependent(kern, ctas, kThreads, smem, stream, tmQ, tmDO, tmK, tmV, p);
 }
 
 template <int D, bool BF16, bool CAUSAL, bool MASK>
@@ -937,27 +969,32 @@ cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
         cudaError_t e = launch_kernel(bwd_stats_kernel<D, BF16>, dim3(blocks), dim3(256), 0, stream, p);
         if (e != cudaSuccess) return e;
     }
-    {
-        auto kern = bwd_dkdv_kernel<D, BF16, CAUSAL, MASK>;
-        constexpr int smem = dkdv_smem<D>();
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        const long long ctas = static_cast<long long>(p.n_groups) * p.n_ktiles * p.kv_splits;
-        e = launch_kernel(kern, dim3(static_cast<unsigned>(ctas)), dim3(kKvThreads), smem, stream,
-                          tmQ, tmDO, tmK, tmV, p);
-        if (e != cudaSuccess) return e;
-        if (p.kv_splits > 1) {
-            const int64_t n8 = static_cast<int64_t>(p.n_groups) * p.Nk * D / 8;
-            e = launch_kernel(bwd_dkdv_reduce_kernel<BF16>,
-                              dim3(static_cast<unsigned>((n8 + 255) / 256)), dim3(256), 0, stream,
-                              p, n8);
-            if (e != cudaSuccess) return e;
-        }
-    }
-    // dQ: a key-only boolean mask takes its own instantiation (no staging).
+    // Statistics, then dQ, then dK/dV, each a programmatic dependent of the
+    // one before: dQ sets up while the statistics kernel ends; dQ and dK/dV
+    // read the same inputs and statistics and write disjoint outputs, so
+    // dK/dV's CTAs take the SMs that dQ's last wave leaves idle (dK/dV waits
+    // for dQ only at its end); the partial sums' reduction sets up while
+    // dK/dV ends.  A key-only boolean mask takes its own dQ instantiation (no
+    // staging).
     const bool key_only = MASK && p.mask_kind == 1 && p.msq == 0 && (p.msh == 0 || p.G == 1);
-    return key_only ? launch_dq<D, BF16, CAUSAL, MASK ? 2 : 0>(tmQ, tmK, tmV, tmDO, p, stream)
-                    : launch_dq<D, BF16, CAUSAL, MASK ? 1 : 0>(tmQ, tmK, tmV, tmDO, p, stream);
+    {
+        const cudaError_t e =
+            key_only ? launch_dq<D, BF16, CAUSAL, MASK ? 2 : 0>(tmQ, tmK, tmV, tmDO, p, stream)
+                     : launch_dq<D, BF16, CAUSAL, MASK ? 1 : 0>(tmQ, tmK, tmV, tmDO, p, stream);
+        if (e != cudaSuccess) return e;
+    }
+    auto kern = bwd_dkdv_kernel<D, BF16, CAUSAL, MASK>;
+    constexpr int smem = dkdv_smem<D>();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const long long ctas = static_cast<long long>(p.n_groups) * p.n_ktiles * p.kv_splits;
+    e = launch_dependent(kern, ctas, kKvThreads, smem, stream, tmQ, tmDO, tmK, tmV, p);
+    if (e != cudaSuccess) return e;
+    if (p.kv_splits > 1) {
+        const int64_t n8 = static_cast<int64_t>(p.n_groups) * p.Nk * D / 8;
+        e = launch_dependent(bwd_dkdv_reduce_kernel<BF16>, (n8 + 255) / 256, 256, 0, stream, p, n8);
+    }
+    return e;
 }
 
 }  // namespace
