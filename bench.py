@@ -551,8 +551,9 @@ def run_ours(args):
             tf = 2.5 * wd.flops_fwd(n) / (ms * 1e-3) / 1e12
             pts.append({"workload": wd.note, "N": n, "ms": round(ms, 4), "tflops": round(tf, 1),
                         "frac_of_peak": round(tf / pk["bf16_tflops"], 4)})
-        bwd_rep = {"entry": "attn_bwd (statistics, dK/dV, dQ kernels; dK/dV partial sums and "
-                            "their reduction when the dK/dV grid is below one wave)",
+        bwd_rep = {"entry": "attn_bwd (statistics, dQ, dK/dV kernels, each a programmatic "
+                            "dependent of the one before; dK/dV partial sums and their "
+                            "reduction when the dK/dV grid is cut into query ranges)",
                    "flops": "5 products of the forward's size (2.5 x the forward's "
                             "4*B*Hq*Nq*Nk*D, halved under the causal mask)",
                    "timing": "median call time over the timed steps, CUDA events, L2 flushed "
