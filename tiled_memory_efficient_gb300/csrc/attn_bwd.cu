@@ -32,11 +32,15 @@ namespace tme {
 namespace {
 
 constexpr int kRows = 128;
-// dQ kernel: 8 elementwise warps (two warpgroups, each owning 64 of the 128
-// columns of a tile) + producer + MMA issuer.
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+// dQ kernel: EW elementwise warps (EW / 4 warpgroups, each owning 512 / EW of
+// the 128 columns of a tile) + producer (warp EW) + MMA issuer (warp EW + 1).
+// Without a mask 16 warps of 32 columns: four warps per SM sub-partition hide
+// more of the elementwise chain's latency than two; with one, 8 warps of 64
+// columns, the layout the bias staging is written for.
+template <int MK>
+constexpr int dq_ew() { return MK == 0 ? 16 : 8; }
+template <int MK>
+constexpr int dq_threads() { return (dq_ew<MK>() + 2) * 32; }
 // dK/dV kernel: 16 elementwise warps (warp w: key rows 32(w%4).., query half
 // (w/4)%2, 32-query chunk w/8 of that half) + producer + MMA issuer.
 constexpr int kKvThreads = 18 * 32;
@@ -584,11 +588,11 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 
 // ---------------------------------------------------------------- dQ
 // TMEM: S [0,128), dP [128,256), dQ [256,256+D), dS [384,448) (packed 16-bit).
-// Warpgroup h owns key columns [64h, 64h+64).  dS has its own columns, so once
-// both warpgroups have read S_j and dP_j into registers (s_free) the tensor
+// Warpgroup h owns key columns [32 CPW h, 32 CPW (h+1)).  dS has its own columns, so once
+// every warpgroup has read S_j and dP_j into registers (s_free) the tensor
 // core computes S_{j+1} and dP_{j+1} while the elementwise work on j runs.
 template <int D, bool BF16, bool CAUSAL, int MK>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(dq_threads<MK>(), 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmDO,
                   const __grid_constant__ CUtensorMap tmK,
@@ -603,6 +607,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // memory (8 warps x 4 KB); at D = 128 the K ring gives a stage for it.
     constexpr int TB = C::kTileBytes, KB = C::kKB, VS = kDqVStages;
     constexpr int KS = dq_kstages<D, STAGE>();
+    constexpr int EW = dq_ew<MK>();
+    constexpr int CPW = 128 / (EW / 4) / 32;   // 32-column chunks per elementwise warp
+    constexpr int kProducerWarp = EW, kMmaWarp = EW + 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -654,8 +661,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < KS; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
         for (int i = 0; i < VS; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 1); }
         mbar_init(s_full, 1);
-        mbar_init(s_free, 256);
-        mbar_init(p_full, 256);
+        mbar_init(s_free, EW * 32);
+        mbar_init(p_full, EW * 32);
         mbar_init(dq_done, 1);
         mbar_init(acc_full, 1);
         mbar_init(mma_done, 1);
@@ -755,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit_elect(mma_done);
         mbar_wait_bounded(mma_done, 0, p.status);
     } else {
-        const int hq = warp >> 2, quad = warp & 3;   // column half, TMEM lane quadrant
+        const int hq = warp >> 2, quad = warp & 3;   // column group, TMEM lane quadrant
         const int64_t row = row0 + quad * 32 + lane;
         const bool row_ok = row < p.rows_per_group;
         const int pos = static_cast<int>(row % p.Nq);
@@ -801,15 +808,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             warp_wait(s_full, j & 1, abort_flag, p.status);
             tc_fence_after();
             const bool need_mask = (k0 + kRows > p.Nk) || (CAUSAL && k0 + kRows - 1 > warp_min_pos);
-            uint32_t sv[2][32], dp[2][32];
+            uint32_t sv[CPW][32], dp[CPW][32];
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                tmem_ld32(tS + (2 * hq + cc) * 32, sv[cc]);
-                tmem_ld32(tDP + (2 * hq + cc) * 32, dp[cc]);
+            for (int cc = 0; cc < CPW; ++cc) {
+                tmem_ld32(tS + (CPW * hq + cc) * 32, sv[cc]);
+                tmem_ld32(tDP + (CPW * hq + cc) * 32, dp[cc]);
             }
             tmem_wait_ld();
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
+            for (int cc = 0; cc < CPW; ++cc) {
                 reg_fence(sv[cc]);
                 reg_fence(dp[cc]);
             }
@@ -837,8 +844,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
             }
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                const int c = 2 * hq + cc;   // 32-column chunk of the tile
+            for (int cc = 0; cc < CPW; ++cc) {
+                const int c = CPW * hq + cc;   // 32-column chunk of the tile
                 uint32_t dw[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
@@ -868,7 +875,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         uint16_t* dqp = static_cast<uint16_t*>(p.dq) + (static_cast<int64_t>(group) * p.rows_per_group + row) * D;
 #pragma unroll 1
-        for (int c = hq * (D / 64); c < (hq + 1) * (D / 64); ++c) {   // this half's columns
+        // this warpgroup's dQ columns: a contiguous half with 8 warps, every
+        // fourth 32-column chunk with 16
+        constexpr int kC0 = EW == 8 ? D / 64 : 1, kCStep = EW == 8 ? 1 : EW / 4;
+        for (int c = hq * kC0; c < (EW == 8 ? (hq + 1) * kC0 : D / 32); c += kCStep) {
             uint32_t a[32];
             tmem_ld32(tmem + lb + 256 + c * 32, a);
             tmem_wait_ld();
@@ -957,7 +967,7 @@ cudaError_t launch_dq(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUte
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const long long ctas = static_cast<long long>(p.n_groups) * p.n_qtiles;
-    return launch_dependent(kern, ctas, kThreads, smem, stream, tmQ, tmDO, tmK, tmV, p);
+    return launch_dependent(kern, ctas, dq_threads<MK>(), smem, stream, tmQ, tmDO, tmK, tmV, p);
 }
 
 template <int D, bool BF16, bool CAUSAL, bool MASK>
