@@ -34,11 +34,37 @@ namespace {
 constexpr int kRows = 128;
 // dQ kernel: EW elementwise warps (EW / 4 warpgroups, each owning 512 / EW of
 // the 128 columns of a tile) + producer (warp EW) + MMA issuer (warp EW + 1).
-// Without a mask 16 warps of 32 columns: four warps per SM sub-partition hide
-// more of the elementwise chain's latency than two; with one, 8 warps of 64
-// columns, the layout the bias staging is written for.
+// Without a mask, and with a key-only keep-mask (read directly), 16 warps of 32
+// columns: four warps per SM sub-partition hide more of the elementwise chain's
+// latency than two; with a general mask, 8 warps of 64 columns, the layout the
+// bias staging is written for.
 template <int MK>
-constexpr int dq_ew() { return MK == 0 ? 16 : 8; }
+constexpr int dq_ew() { return MK == 1 ? 8 : 16; }
+
+// Key-only keep bytes of the 32 keys from key0 (a multiple of 32): a dropped
+// key's score becomes -inf.  Whole 32-byte runs inside [0, Nk) are read as two
+// 16-byte vectors (every lane of the warp reads the same bytes) and skipped at
+// once when no byte is zero; the ragged end goes key by key (keys >= Nk are
+// masked later with the causal limit).
+__device__ __forceinline__ void keep_fold32(uint32_t (&s)[32], const uint8_t* row, int key0,
+                                            int Nk) {
+    if (key0 + 32 <= Nk) {
+        const uint4 a = reinterpret_cast<const uint4*>(row + key0)[0];
+        const uint4 b = reinterpret_cast<const uint4*>(row + key0)[1];
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        uint32_t z = 0u;   // (v - 0x01..01) & ~v & 0x80..80 is nonzero exactly when a byte of v is 0
+#pragma unroll
+        for (int i = 0; i < 8; ++i) z |= (w[i] - 0x01010101u) & ~w[i] & 0x80808080u;
+        if (z == 0u) return;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (((w[i >> 2] >> (8 * (i & 3))) & 0xffu) == 0u) s[i] = __float_as_uint(-INFINITY);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (key0 + i < Nk && row[key0 + i] == 0) s[i] = __float_as_uint(-INFINITY);
+    }
+}
 template <int MK>
 constexpr int dq_threads() { return (dq_ew<MK>() + 2) * 32; }
 // dK/dV kernel: 16 elementwise warps (warp w: key rows 32(w%4).., query half
@@ -823,7 +849,9 @@ __global__ void __launch_bounds__(dq_threads<MK>(), 1)
             // S_j and dP_j are in registers: the next S and dP may overwrite them.
             tc_fence_before();
             mbar_arrive(s_free);
-            if constexpr (MASK) {
+            if constexpr (MK == 2 && CPW == 1) {
+                keep_fold32(sv[0], mrow, k0 + 32 * hq, p.Nk);
+            } else if constexpr (MASK) {
                 // this half's scores -> logits with the bias; then the next
                 // key tile's bias is requested into the same rows
                 if (staged(j)) {
