@@ -34,12 +34,12 @@ namespace {
 constexpr int kRows = 128;
 // dQ kernel: EW elementwise warps (EW / 4 warpgroups, each owning 512 / EW of
 // the 128 columns of a tile) + producer (warp EW) + MMA issuer (warp EW + 1).
-// Without a mask, and with a key-only keep-mask (read directly), 16 warps of 32
-// columns: four warps per SM sub-partition hide more of the elementwise chain's
-// latency than two; with a general mask, 8 warps of 64 columns, the layout the
-// bias staging is written for.
-template <int MK>
-constexpr int dq_ew() { return MK == 1 ? 8 : 16; }
+// 16 warps of 32 columns (four warps per SM sub-partition hide more of the
+// elementwise chain's latency than two), except with a general mask at D = 128:
+// 8 warps of 64 columns there (measured faster with its staged bias and the
+// 2-deep K ring it leaves).
+template <int MK, int D>
+constexpr int dq_ew() { return (MK == 1 && D == 128) ? 8 : 16; }
 
 // Key-only keep bytes of the 32 keys from key0 (a multiple of 32): a dropped
 // key's score becomes -inf.  Whole 32-byte runs inside [0, Nk) are read as two
@@ -65,8 +65,8 @@ __device__ __forceinline__ void keep_fold32(uint32_t (&s)[32], const uint8_t* ro
             if (key0 + i < Nk && row[key0 + i] == 0) s[i] = __float_as_uint(-INFINITY);
     }
 }
-template <int MK>
-constexpr int dq_threads() { return (dq_ew<MK>() + 2) * 32; }
+template <int MK, int D>
+constexpr int dq_threads() { return (dq_ew<MK, D>() + 2) * 32; }
 // dK/dV kernel: 16 elementwise warps (warp w: key rows 32(w%4).., query half
 // (w/4)%2, 32-query chunk w/8 of that half) + producer + MMA issuer.
 constexpr int kKvThreads = 18 * 32;
@@ -612,13 +612,103 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// General bias, dQ layout: the next key tile's bias for a warp's 32 rows x 32
+// keys [key0, key0 + 32) (inside [0, Nk)), staged with cp.async, whole rows
+// per instruction (4 16-byte chunks per row for a 16-bit additive bias, 2 for
+// a boolean one).  Chunk q of row r sits at chunk position q ^ ((r >> 1) & 3)
+// (additive, 64-byte rows) or q ^ ((r >> 2) & 1) (boolean, 32-byte rows), so
+// the fold's reads (one row per lane, 16 bytes at a time) meet every bank once
+// per 8 lanes.  Rows r >= nvalid (1 <= nvalid <= 32) copy row nvalid - 1.
+// Wait with cp_async_wait_all and then __syncwarp before reading.
+__device__ __forceinline__ void bias_prefetch32(uint32_t buf, const uint8_t* row_ptr, int kind,
+                                                int key0, int nvalid, int lane) {
+    const unsigned long long mine = reinterpret_cast<uintptr_t>(row_ptr);
+    const bool add = kind == 2;
+    const int cshift = add ? 2 : 1;   // log2 chunks per row
+    const int q = lane & ((1 << cshift) - 1);
+    const int n_ins = add ? 4 : 2;    // 32 rows / (32 >> cshift) rows per instruction
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (i >= n_ins) break;
+        const int r = (i << (5 - cshift)) + (lane >> cshift);
+        const unsigned long long base = __shfl_sync(0xffffffffu, mine, min(r, nvalid - 1));
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(base) +
+                             static_cast<int64_t>(key0) * (add ? 2 : 1) + 16 * q;
+        const int slot = add ? (q ^ ((r >> 1) & 3)) : (q ^ ((r >> 2) & 1));
+        cp_async16(buf + r * (add ? 64 : 32) + (slot << 4), src);
+    }
+    cp_async_commit();
+}
+
+// This lane's staged 32 bias values folded into its 32 scores: natural-log
+// logits u = s * scale + b (additive) or raw scores / -inf (boolean), the
+// arithmetic of the forward's fold.
+template <bool BF16>
+__device__ __forceinline__ void bias_fold_smem32(uint32_t (&s)[32], uint32_t buf, int kind,
+                                                 float scale, int lane) {
+    if (kind == 2) {
+        const uint32_t rbase = buf + lane * 64;
+        const int sw = (lane >> 1) & 3;
+        const uint64_t sc2 = f2(scale, scale);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t w[4];
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                         : "r"(rbase + ((q ^ sw) << 4)));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int k = 8 * q + 2 * e;
+                const uint64_t t =
+                    ffma2(f2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), sc2,
+                          f2(half_to_float<BF16>(w[e] & 0xffffu), half_to_float<BF16>(w[e] >> 16)));
+                s[k] = __float_as_uint(f2lo(t));
+                s[k + 1] = __float_as_uint(f2hi(t));
+            }
+        }
+    } else {
+        const uint32_t rbase = buf + lane * 32;
+        const int sw = (lane >> 2) & 1;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            uint32_t w[4];
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                         : "r"(rbase + ((q ^ sw) << 4)));
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (((w[i >> 2] >> (8 * (i & 3))) & 0xffu) == 0u)
+                    s[16 * q + i] = __float_as_uint(-INFINITY);
+        }
+    }
+}
+
+// The same fold read from the bias row key by key (keys >= Nk and unreal rows:
+// no bias), for a key tile that reaches past Nk.
+template <bool BF16>
+__device__ __forceinline__ void bias_fold_direct32(uint32_t (&s)[32], const uint8_t* row, int kind,
+                                                   int key0, int Nk, float scale, bool row_ok) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int key = key0 + i;
+        const bool in = row_ok && key < Nk;
+        if (kind == 2) {
+            const float b =
+                in ? half_to_float<BF16>(reinterpret_cast<const uint16_t*>(row)[key]) : 0.0f;
+            s[i] = __float_as_uint(fmaf(__uint_as_float(s[i]), scale, b));
+        } else if (in && row[key] == 0) {
+            s[i] = __float_as_uint(-INFINITY);
+        }
+    }
+}
+
 // ---------------------------------------------------------------- dQ
 // TMEM: S [0,128), dP [128,256), dQ [256,256+D), dS [384,448) (packed 16-bit).
 // Warpgroup h owns key columns [32 CPW h, 32 CPW (h+1)).  dS has its own columns, so once
 // every warpgroup has read S_j and dP_j into registers (s_free) the tensor
 // core computes S_{j+1} and dP_{j+1} while the elementwise work on j runs.
 template <int D, bool BF16, bool CAUSAL, int MK>
-__global__ void __launch_bounds__(dq_threads<MK>(), 1)
+__global__ void __launch_bounds__(dq_threads<MK, D>(), 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmDO,
                   const __grid_constant__ CUtensorMap tmK,
@@ -633,7 +723,7 @@ __global__ void __launch_bounds__(dq_threads<MK>(), 1)
     // memory (8 warps x 4 KB); at D = 128 the K ring gives a stage for it.
     constexpr int TB = C::kTileBytes, KB = C::kKB, VS = kDqVStages;
     constexpr int KS = dq_kstages<D, STAGE>();
-    constexpr int EW = dq_ew<MK>();
+    constexpr int EW = dq_ew<MK, D>();
     constexpr int CPW = 128 / (EW / 4) / 32;   // 32-column chunks per elementwise warp
     constexpr int kProducerWarp = EW, kMmaWarp = EW + 1;
     extern __shared__ uint8_t smem_raw[];
@@ -818,17 +908,21 @@ __global__ void __launch_bounds__(dq_threads<MK>(), 1)
             mrow = static_cast<const uint8_t*>(p.mask) +
                    (b * p.msb + h * p.msh + pos * p.msq) * (p.mask_kind == 2 ? 2 : 1);
         }
-        // Staged bias (MASK): this warp's 32 rows x the 64 keys of its half of
-        // each key tile, one tile ahead, nvalid rows real; a half-tile past
-        // Nk reads its bias directly.
+        // Staged bias (MK = 1): this warp's 32 rows x the 32 CPW keys of its
+        // column group of each key tile, one tile ahead, nvalid rows real; a
+        // group past Nk reads its bias directly.
         const int64_t wleft = p.rows_per_group - wr0;
         const int nvalid = wleft <= 0 ? 0 : wleft >= 32 ? 32 : static_cast<int>(wleft);
-        const uint32_t bbuf = smem_u32(sB) + warp * 4096;
+        const uint32_t bbuf = smem_u32(sB) + warp * (CPW * 2048);
         auto staged = [&](int jj) {
-            return STAGE && nvalid > 0 && jj * kRows + 64 * hq + 64 <= p.Nk;
+            return STAGE && nvalid > 0 && jj * kRows + 32 * CPW * (hq + 1) <= p.Nk;
+        };
+        auto prefetch = [&](int key0) {
+            if constexpr (CPW == 2) bias_prefetch<64>(bbuf, mrow, p.mask_kind, key0, nvalid, lane);
+            else bias_prefetch32(bbuf, mrow, p.mask_kind, key0, nvalid, lane);
         };
         if constexpr (STAGE)
-            if (nkv > 0 && staged(0)) bias_prefetch<64>(bbuf, mrow, p.mask_kind, 64 * hq, nvalid, lane);
+            if (nkv > 0 && staged(0)) prefetch(32 * CPW * hq);
         for (int j = 0; j < nkv; ++j) {
             const int k0 = j * kRows;
             warp_wait(s_full, j & 1, abort_flag, p.status);
@@ -852,19 +946,23 @@ __global__ void __launch_bounds__(dq_threads<MK>(), 1)
             if constexpr (MK == 2 && CPW == 1) {
                 keep_fold32(sv[0], mrow, k0 + 32 * hq, p.Nk);
             } else if constexpr (MASK) {
-                // this half's scores -> logits with the bias; then the next
+                // this group's scores -> logits with the bias; then the next
                 // key tile's bias is requested into the same rows
                 if (staged(j)) {
                     cp_async_wait_all();
                     __syncwarp();
-                    bias_fold_smem64<BF16>(sv, bbuf, p.mask_kind, p.scale, lane);
+                    if constexpr (CPW == 2) bias_fold_smem64<BF16>(sv, bbuf, p.mask_kind, p.scale, lane);
+                    else bias_fold_smem32<BF16>(sv[0], bbuf, p.mask_kind, p.scale, lane);
                     __syncwarp();
                 } else {
-                    bias_fold_direct64<BF16>(sv, mrow, p.mask_kind, k0 + 64 * hq, p.Nk, p.scale,
-                                             row_ok);
+                    if constexpr (CPW == 2)
+                        bias_fold_direct64<BF16>(sv, mrow, p.mask_kind, k0 + 64 * hq, p.Nk, p.scale,
+                                                 row_ok);
+                    else
+                        bias_fold_direct32<BF16>(sv[0], mrow, p.mask_kind, k0 + 32 * hq, p.Nk,
+                                                 p.scale, row_ok);
                 }
-                if (j + 1 < nkv && staged(j + 1))
-                    bias_prefetch<64>(bbuf, mrow, p.mask_kind, k0 + kRows + 64 * hq, nvalid, lane);
+                if (j + 1 < nkv && staged(j + 1)) prefetch(k0 + kRows + 32 * CPW * hq);
             }
             // dS columns still feed dQ += dS_{j-1} K_{j-1}.
             if (j > 0) {
@@ -902,10 +1000,10 @@ __global__ void __launch_bounds__(dq_threads<MK>(), 1)
         if (nkv > 0) warp_wait(acc_full, 0, abort_flag, p.status);
         tc_fence_after();
         uint16_t* dqp = static_cast<uint16_t*>(p.dq) + (static_cast<int64_t>(group) * p.rows_per_group + row) * D;
-#pragma unroll 1
         // this warpgroup's dQ columns: a contiguous half with 8 warps, every
         // fourth 32-column chunk with 16
         constexpr int kC0 = EW == 8 ? D / 64 : 1, kCStep = EW == 8 ? 1 : EW / 4;
+#pragma unroll 1
         for (int c = hq * kC0; c < (EW == 8 ? (hq + 1) * kC0 : D / 32); c += kCStep) {
             uint32_t a[32];
             tmem_ld32(tmem + lb + 256 + c * 32, a);
@@ -995,7 +1093,7 @@ cudaError_t launch_dq(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUte
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const long long ctas = static_cast<long long>(p.n_groups) * p.n_qtiles;
-    return launch_dependent(kern, ctas, dq_threads<MK>(), smem, stream, tmQ, tmDO, tmK, tmV, p);
+    return launch_dependent(kern, ctas, dq_threads<MK, D>(), smem, stream, tmQ, tmDO, tmK, tmV, p);
 }
 
 template <int D, bool BF16, bool CAUSAL, bool MASK>
