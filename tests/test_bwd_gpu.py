@@ -88,6 +88,31 @@ def test_backward_deterministic(cuda_lib):
         assert torch.equal(a, b)
 
 
+def test_backward_chain_on_a_side_stream(cuda_lib):
+    """The backward's kernels are chained as programmatic dependent launches
+    (statistics, dQ, dK/dV, the reduction of the dK/dV ranges).  On a side
+    stream, two calls back to back and plain kernels reading the gradients
+    right after them (no host synchronisation in between) see exactly the
+    default-stream results."""
+    x = inputs.make_custom(1, 14, 2, 1024, 1024, 64, F16, seed=63, with_grad=True)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    out, lse = _lib.attn_fwd(q, k, v, causal=True)
+    ref = _lib.attn_bwd(q, k, v, out, do, lse, causal=True)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        a = _lib.attn_bwd(q, k, v, out, do, lse, causal=True)
+        b = _lib.attn_bwd(q, k, v, out, do, lse, causal=True)
+        doubled = [t * 2 for t in (*a, *b)]   # ordinary kernels right behind the chain
+    side.synchronize()
+    assert _lib.sync_status() == _lib.ATTN_OK
+    for r, ga, gb in zip(ref, a, b):
+        assert torch.equal(r, ga) and torch.equal(r, gb)
+    for d, r in zip(doubled, (*ref, *ref)):
+        assert torch.equal(d, r * 2)
+
+
 def test_backward_workspace_contents_do_not_matter(cuda_lib):
     x = inputs.make_custom(1, 2, 2, 300, 300, 64, F16, seed=22, with_grad=True)
     q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
