@@ -53,7 +53,7 @@ PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "fwd_traffic.json")
 
 
 def peaks():
-    """Measured denominators if the driver left MEASURED_PEAKS.json, else the fallback."""
+    """Measured denominators from MEASURED_PEAKS.json when it exists, else the fallback."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         try:
