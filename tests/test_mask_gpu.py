@@ -162,6 +162,12 @@ BWD_CASES = [
     (1, 4, 4, 257, 128, BF16, True, (1, 4, 257, 257), "additive"),
     (2, 6, 2, 200, 128, BF16, False, (2, 1, 200, 200), "bool"),
     (1, 14, 2, 90, 64, F16, True, (90, 90), "bool"),     # heads of 90 rows: tiles span heads
+    # D=64 dQ stages 32 keys of bias per warp (16 warps): an additive bias with
+    # a ragged last key tile and partly real warps; bf16 heads of 90 rows;
+    # a GQA padding mask under the causal mask (keep bytes 32 keys at a time)
+    (1, 4, 2, 300, 64, F16, False, (1, 4, 300, 300), "additive"),
+    (1, 6, 2, 90, 64, BF16, True, (1, 6, 90, 90), "additive"),
+    (2, 14, 2, 500, 64, F16, True, None, "padding"),
 ]
 
 
