@@ -151,6 +151,100 @@ def test_half_positions_for_152_sms(lib):
     assert half(1, 14, 2, 1024, causal=3) == -1
 
 
+def _model_cut(B, Hq, Hkv, Nq, Nk, D, causal, sms):
+    """Key ranges of attn_fwd_ws's grid, restated: several waves (no causal
+    mask, >= 8 key tiles) cut the last wave into S = 2..4 ranges when rounds / S
+    + (rounds - 1) * 15 us + 4 us of merge (in units of ~1.1 / 2.2 us per key
+    tile at D = 64 / 128) beats a whole unit by 2%; under one wave every unit
+    is cut into as many ranges of >= 16 key tiles as fill the SMs."""
+    rows = Hq // Hkv * Nq
+    units = B * Hkv * -(-rows // 256)
+    tiles = -(-Nk // 128)
+    if units >= sms:
+        if causal or tiles < 8:
+            return 1
+        waves = -(-units // sms)
+        tail = units - (waves - 1) * sms
+        if waves < 2:
+            return 1
+        unit_us = tiles * (2.2 if D == 128 else 1.1)
+        best, best_s = 1.0, 1
+        for S in (2, 3, 4):
+            if tiles < 4 * S:
+                break
+            rounds = -(-tail * S // sms)
+            cost = rounds / S + (rounds - 1) * 15.0 / unit_us + 4.0 / unit_us
+            if cost < best - 0.02:
+                best, best_s = cost, S
+        if best_s < 2:
+            return 1
+        tps = -(-tiles // best_s)
+        return -(-tiles // tps)
+    want = min(sms // units, tiles // 16, 256)
+    if want < 2:
+        return 1
+    tps = -(-tiles // want)
+    splits = -(-tiles // tps)
+    return splits if splits >= 2 else 1
+
+
+def _model_half(B, Hq, Nq, Nk, causal, sms, half=0.70, cta=2.5):
+    """Heaviest pair positions run as one-tile CTAs, restated: simulate the
+    grid's in-order assignment to the first free SM for each count h of split
+    positions (a one-tile CTA costs `half` of its pair's key tiles, every CTA
+    `cta` key tiles more) and keep the first h that beats the best so far by
+    2%; grids of more than 8 waves of pairs are not split."""
+    import heapq
+    if Nq % 256:
+        return 0
+    m, heads = Nq // 256, B * Hq
+    if heads * m > 8 * sms:
+        return 0
+    off = Nk - Nq if causal == 2 else 0
+    t = []
+    for i in range(m):
+        keys = min((m - 1 - i) * 256 + 256 + off, Nk)
+        t.append(0 if keys <= 0 else -(-keys // 128))
+    best, best_h = None, 0
+    for h in range(m + 1):
+        free = [0.0] * sms
+        end = 0.0
+        for i in range(m):
+            costs = [half * t[i] + cta] * 2 if i < h else [t[i] + cta]
+            for _ in range(heads):
+                for c in costs:
+                    t0 = heapq.heappop(free)
+                    heapq.heappush(free, t0 + c)
+                    end = max(end, t0 + c)
+        if best is None or end < 0.98 * best:
+            best, best_h = end, h
+    return best_h
+
+
+def test_fwd_plans_match_a_model(lib):
+    """Host-only: attn_fwd_ws's key ranges and the causal forward's one-tile
+    positions on a 152-SM device agree with an independent restatement of the
+    two plans over a grid of shapes."""
+    import itertools
+    n_cut = n_half = 0
+    for (B, Hq, Hkv), N, extra, D in itertools.product(
+            [(1, 16, 16), (1, 14, 2), (2, 4, 2), (1, 2, 2), (4, 24, 24)],
+            [256, 512, 1024, 2048, 4096, 8192, 10240, 16384], [0, 300], [64, 128]):
+        Nk = N + extra
+        for causal in (0, 1):
+            got = lib.attn_fwd_ws_splits(B, Hq, Hkv, N, Nk, D, causal, 152)
+            want = _model_cut(B, Hq, Hkv, N, Nk, D, causal, 152)
+            assert got == want, (B, Hq, Hkv, N, Nk, D, causal, got, want)
+            n_cut += got > 1
+        if D == 64 and N <= 4096:
+            for causal in (1, 2):
+                got = lib.attn_fwd_half_positions(B, Hq, Hkv, N, Nk, 64, causal, 0, 152)
+                want = _model_half(B, Hq, N, Nk, causal, 152)
+                assert got == want, (B, Hq, Hkv, N, Nk, causal, got, want)
+                n_half += got > 0
+    assert n_cut > 5 and n_half > 5   # the grid exercises both plans
+
+
 def test_bwd_rejects_bottom_right(lib):
     ws = lib.attn_bwd_workspace_size(1, 2, 2, 128, 256, 64, 0)
     assert lib.attn_bwd(*([P] * 9), P, ws, 1, 2, 2, 128, 256, 64, 0.125, 2, 0, None) == 2
