@@ -245,6 +245,44 @@ def test_fwd_plans_match_a_model(lib):
     assert n_cut > 5 and n_half > 5   # the grid exercises both plans
 
 
+def _model_bwd(B, Hq, Hkv, Nq, Nk, causal, sms):
+    """dK/dV query ranges, restated: none when the (group, key tile) CTAs fill
+    the SMs; otherwise enough ranges to fill one wave, or (causal) enough that
+    key tile 0's CTAs, which meet every query tile, do no more than the average
+    work per SM; at least 4 query tiles per range, at most 32 ranges."""
+    groups, ktiles = B * Hkv, -(-Nk // 128)
+    n_qtiles = -(-(Hq // Hkv) * Nq // 128)
+    units = groups * ktiles
+    if units >= sms:
+        return 1
+    want = -(-sms // units)
+    if causal:
+        tq = -(-Nq // 128)
+        total = sum(tq - kt for kt in range(min(ktiles, tq)))
+        if total > 0:
+            want = -(-tq * sms // (groups * total))
+    want = min(want, n_qtiles // 4, 32)
+    if want <= 1:
+        return 1
+    per = -(-n_qtiles // want)
+    return -(-n_qtiles // per)
+
+
+def test_bwd_plan_matches_a_model(lib):
+    """Host-only: attn_bwd's dK/dV query ranges on a 152-SM device agree with
+    an independent restatement of the plan over a grid of shapes."""
+    import itertools
+    cut = 0
+    for (B, Hq, Hkv), N, extra, causal in itertools.product(
+            [(1, 14, 2), (2, 16, 16), (1, 4, 4), (8, 8, 1), (1, 2, 2)],
+            [128, 512, 1024, 2048, 4096, 8192, 16384], [0, 700], (0, 1)):
+        got = lib.attn_bwd_splits(B, Hq, Hkv, N, N + extra, 64, causal, 152)
+        want = _model_bwd(B, Hq, Hkv, N, N + extra, causal, 152)
+        assert got == want, (B, Hq, Hkv, N, N + extra, causal, got, want)
+        cut += got > 1
+    assert cut > 10
+
+
 def test_bwd_rejects_bottom_right(lib):
     ws = lib.attn_bwd_workspace_size(1, 2, 2, 128, 256, 64, 0)
     assert lib.attn_bwd(*([P] * 9), P, ws, 1, 2, 2, 128, 256, 64, 0.125, 2, 0, None) == 2
